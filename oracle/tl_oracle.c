@@ -1,0 +1,230 @@
+/*
+ * tl_oracle.c -- CPU oracle for C = epilogue(op(A) . op(B)).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * do.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (the plain definition, written out):
+ *
+ *   C[i,j] = round_dtype( epi( sum_{k<K} x(opA[i,k]) * x(opB[k,j]) ) )
+ *
+ *   - opA[i,k] is A[i*lda+k], or A[k*lda+i] when trans_a; opB[k,j] is
+ *     B[k*ldb+j], or B[j*ldb+k] when trans_b.  This is T.gemm's transpose_A /
+ *     transpose_B reading: A is [M,K] (or [K,M]) and B is [K,N] (or [N,K])
+ *     ("TileLang core primitives" page, section 3.3 "T.gemm").
+ *   - x() decodes the exact value of an IEEE binary16 or bfloat16 bit pattern
+ *     (decoders below, written from the two formats' definitions).
+ *   - the sum runs over k = 0..K-1 in order, in IEEE binary64.  The pages fix the
+ *     accumulator at fp32 and the cast "at the end" ("TileLang: from tile dataflow
+ *     to controllable AI kernels", section "minimal but complete GEMM skeleton":
+ *     fp16 inputs, fp32 accumulation, converted back to the output dtype last);
+ *     the oracle accumulates in binary64, which is closer to the exact sum than
+ *     any fp32 order, so the GPU/oracle difference is the GPU's own rounding.
+ *   - epi is the identity, or ReLU = max(x, 0) applied to the accumulator before
+ *     the cast ("TileLang core primitives" page, section 3.8, where the epilogue
+ *     takes max(C, 0) on the fp32 accumulator tile; "NVIDIA backend codegen" page,
+ *     section 1, the GEMM+ReLU quickstart).  Negative sums give +0.
+ *   - round_dtype is round-to-nearest, ties-to-even, from binary64 straight to the
+ *     output format (same format as the inputs), with overflow to +-inf and
+ *     gradual underflow.
+ *
+ * Out-of-range elements of a partial tile do not exist here: the oracle sums over
+ * exactly K terms, which is what zero padding of partial tiles must reproduce
+ * ("TileLang core primitives" page, section 4.2: out-of-bounds source reads give
+ * the safe value 0, out-of-bounds destination stores are skipped).
+ *
+ * Parallelism: OpenMP over output rows only; the summation order of each C[i,j]
+ * is the same for every thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+
+/* ---- format decoders ---------------------------------------------------- */
+
+/* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double oracle_f16_to_f64(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 10) & 0x1F;
+  const int f = h & 0x3FF;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -24);                /* subnormal: f * 2^(1-15-10) */
+  } else if (e == 31) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(f + 1024), e - 25);    /* (1024+f) * 2^(e-15-10) */
+  }
+  return sign ? -v : v;
+}
+
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits. */
+double oracle_bf16_to_f64(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 7) & 0xFF;
+  const int f = h & 0x7F;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -133);               /* f * 2^(1-127-7) */
+  } else if (e == 255) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(f + 128), e - 134);    /* (128+f) * 2^(e-127-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* ---- round to nearest even, binary64 -> 16-bit format -------------------- */
+
+/*
+ * Generic RNE encoder for a binary format with `mant` fraction bits and minimum
+ * normal exponent `emin` (exponent bias = 1 - emin).  The value is scaled by
+ * its quantum q = 2^(max(E, emin) - mant), where E = floor(log2|v|); |v|/q is
+ * exact in binary64, and its integer rounding r (ties to even) is the
+ * significand.  The encoding (E - emin + 1) << mant + r - 2^mant carries into
+ * the exponent when r reaches 2^(mant+1), and equals r for subnormals.
+ */
+static uint16_t rne_encode(double v, int mant, int emin, uint32_t inf_bits,
+                           uint16_t qnan) {
+  if (isnan(v)) return qnan;
+  const uint16_t sign = signbit(v) ? 0x8000 : 0;
+  const double x = fabs(v);
+  if (isinf(x)) return (uint16_t)(sign | inf_bits);
+  if (x == 0.0) return sign;
+  int e2;
+  (void)frexp(x, &e2);          /* x = f * 2^e2, f in [0.5, 1) */
+  int E = e2 - 1;               /* floor(log2 x) */
+  if (E < emin) E = emin;       /* subnormal range shares the quantum of emin */
+  if (E > 2000) E = 2000;       /* far past overflow; keeps the shifts small */
+  const double q = ldexp(1.0, E - mant);
+  const double n = x / q;       /* exact: division by a power of two */
+  double r = floor(n);
+  const double frac = n - r;
+  if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  const uint32_t hidden = 1u << mant;
+  uint32_t bits;
+  if (r < (double)hidden) {
+    bits = (uint32_t)r;                                   /* subnormal or zero */
+  } else {
+    bits = ((uint32_t)(E - emin + 1) << mant) + (uint32_t)r - hidden;
+  }
+  if (bits >= inf_bits) bits = inf_bits;                  /* overflow -> inf */
+  return (uint16_t)(sign | bits);
+}
+
+uint16_t oracle_f64_to_f16(double v) { return rne_encode(v, 10, -14, 0x7C00, 0x7E00); }
+uint16_t oracle_f64_to_bf16(double v) { return rne_encode(v, 7, -126, 0x7F80, 0x7FC0); }
+
+/* ---- the GEMM ----------------------------------------------------------- */
+
+static double decode(uint16_t h, int dtype) {
+  return dtype == ORACLE_BF16 ? oracle_bf16_to_f64(h) : oracle_f16_to_f64(h);
+}
+
+static uint16_t encode(double v, int dtype) {
+  return dtype == ORACLE_BF16 ? oracle_f64_to_bf16(v) : oracle_f64_to_f16(v);
+}
+
+static double op_a(const uint16_t* A, int64_t lda, int trans_a, int64_t i, int64_t k,
+                   int dtype) {
+  return decode(trans_a ? A[k * lda + i] : A[i * lda + k], dtype);
+}
+
+static double op_b(const uint16_t* B, int64_t ldb, int trans_b, int64_t k, int64_t j,
+                   int dtype) {
+  return decode(trans_b ? B[j * ldb + k] : B[k * ldb + j], dtype);
+}
+
+/* The binary64 accumulator of one output element, k in order. */
+static double dot(const uint16_t* A, const uint16_t* B, int64_t K, int64_t lda,
+                  int64_t ldb, int dtype, int trans_a, int trans_b, int64_t i, int64_t j) {
+  double s = 0.0;
+  for (int64_t k = 0; k < K; ++k) {
+    s += op_a(A, lda, trans_a, i, k, dtype) * op_b(B, ldb, trans_b, k, j, dtype);
+  }
+  return s;
+}
+
+static double epilogue(double s, int relu) { return (relu && !(s > 0.0)) ? 0.0 : s; }
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/*
+ * Full product: C[i*ldc+j] for i<M, j<N, rounded to dtype.  If `sums` is not NULL
+ * it receives the binary64 accumulators after the epilogue (row-major, M x N).
+ * Returns 0, or -1 on an invalid argument.
+ */
+int oracle_gemm(const uint16_t* A, const uint16_t* B, uint16_t* C, double* sums,
+                int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                int dtype, int trans_a, int trans_b, int relu, int nthreads) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -1;
+  if (M == 0 || N == 0) return 0;
+  if (ldc < N) return -1;
+  if (K > 0) {
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? K : N)) return -1;
+  }
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      const double s = epilogue(dot(A, B, K, lda, ldb, dtype, trans_a, trans_b, i, j), relu);
+      if (C) C[i * ldc + j] = encode(s, dtype);
+      if (sums) sums[i * N + j] = s;
+    }
+  }
+  return 0;
+}
+
+/*
+ * Selected entries only: out[t] = C[rows[t], cols[t]] (rounded), and, if
+ * `sums` is not NULL, sums[t] = its binary64 accumulator after the epilogue.
+ */
+int oracle_gemm_entries(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N,
+                        int64_t K, int64_t lda, int64_t ldb, int dtype, int trans_a,
+                        int trans_b, int relu, const int64_t* rows, const int64_t* cols,
+                        int64_t count, uint16_t* out, double* sums, int nthreads) {
+  if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -1;
+  for (int64_t t = 0; t < count; ++t) {
+    if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+  }
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t t = 0; t < count; ++t) {
+    const double s =
+        epilogue(dot(A, B, K, lda, ldb, dtype, trans_a, trans_b, rows[t], cols[t]), relu);
+    if (out) out[t] = encode(s, dtype);
+    if (sums) sums[t] = s;
+  }
+  return 0;
+}
+
+/* Vector forms of the format conversions, for the pin tests. */
+void oracle_decode_array(const uint16_t* in, double* out, int64_t n, int dtype) {
+  for (int64_t t = 0; t < n; ++t) out[t] = decode(in[t], dtype);
+}
+
+void oracle_encode_array(const double* in, uint16_t* out, int64_t n, int dtype) {
+  for (int64_t t = 0; t < n; ++t) out[t] = encode(in[t], dtype);
+}

@@ -1,0 +1,33 @@
+"""Shared pytest setup: the ``gpu`` marker and import paths.
+
+Tests marked ``gpu`` need a CUDA device and the compiled library; everything else
+runs on a CPU-only machine.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def pytest_collection_modifyitems(config, items):
+    # A test marked gpu on a machine without a GPU is a configuration error for
+    # "-m gpu" runs; for default runs it is skipped.
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        has_gpu = False
+    if has_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)

@@ -1,0 +1,309 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test fixes one part of the oracle so that a plausible mistake (a dropped term,
+a wrong sign or index, a transposed operand, a wrong rounding rule) fails here:
+
+* format decoders: every one of the 65536 bit patterns against numpy's binary16
+  and torch's bfloat16 conversions;
+* the round-to-nearest-even encoders: exact values, every midpoint between
+  neighbours (ties go to the even significand), just-above/just-below midpoints,
+  overflow thresholds and subnormals, against numpy / torch conversions;
+* the GEMM: a hand-computed 2x2x2 case (tests/golden/hand_2x2x2.json), closed forms
+  (identity, permutation, all-ones giving K, rank-1 outer products, K = 1, ReLU
+  zeroing negatives, K = 0), exact integer products from numpy for all four
+  transpose combinations with padded leading dimensions, and exact rational sums
+  (fractions.Fraction) within the binary64 error bound.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f16_bits(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def bf16_bits_from_f32(x):
+    t = torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(bits):
+    t = torch.from_numpy(np.asarray(bits, dtype=np.uint16).view(np.int16).copy())
+    return t.view(torch.bfloat16).to(torch.float64).numpy()
+
+
+ALL = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+
+
+# ---------------------------------------------------------------- decoders ----
+
+def test_f16_decoder_all_patterns():
+    got = oracle.decode(ALL, oracle.F16)
+    want = ALL.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_bf16_decoder_all_patterns():
+    got = oracle.decode(ALL, oracle.BF16)
+    want = bf16_values(ALL)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+# ---------------------------------------------------------------- encoders ----
+
+def _finite_sorted_positive(dtype):
+    vals = oracle.decode(ALL, dtype)
+    return np.unique(np.abs(vals[np.isfinite(vals)]))    # +0 first, no -0
+
+
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+def test_encoder_roundtrips_every_finite_value(dtype):
+    vals = oracle.decode(ALL, dtype)
+    fin = np.isfinite(vals)
+    back = oracle.encode(vals[fin], dtype)
+    assert np.array_equal(back, ALL[fin])
+
+
+def test_f16_encoder_midpoints_ties_to_even_and_neighbours():
+    pos = _finite_sorted_positive(oracle.F16)
+    lo, hi = pos[:-1], pos[1:]
+    mid = (lo + hi) / 2.0                          # exact in binary64
+    got = oracle.encode(mid, oracle.F16)
+    lo_b, hi_b = oracle.encode(lo, oracle.F16), oracle.encode(hi, oracle.F16)
+    want = np.where(lo_b % 2 == 0, lo_b, hi_b)     # tie -> even significand
+    assert np.array_equal(got, want)
+    assert np.array_equal(got, f16_bits(mid))      # numpy agrees
+    eps = (hi - lo) * 2.0 ** -20
+    assert np.array_equal(oracle.encode(mid + eps, oracle.F16), hi_b)
+    assert np.array_equal(oracle.encode(mid - eps, oracle.F16), lo_b)
+    neg = oracle.encode(-mid, oracle.F16)
+    assert np.array_equal(neg, want | 0x8000)
+
+
+def test_bf16_encoder_midpoints_ties_to_even_and_neighbours():
+    pos = _finite_sorted_positive(oracle.BF16)
+    lo, hi = pos[:-1], pos[1:]
+    mid = (lo + hi) / 2.0                          # 9 significant bits: exact in fp32 too
+    got = oracle.encode(mid, oracle.BF16)
+    lo_b, hi_b = oracle.encode(lo, oracle.BF16), oracle.encode(hi, oracle.BF16)
+    want = np.where(lo_b % 2 == 0, lo_b, hi_b)
+    assert np.array_equal(got, want)
+    assert np.array_equal(got, bf16_bits_from_f32(mid))   # torch's fp32->bf16 agrees
+    eps = (hi - lo) * 2.0 ** -30                  # below fp32 resolution: binary64 only
+    assert np.array_equal(oracle.encode(mid + eps, oracle.BF16), hi_b)
+    assert np.array_equal(oracle.encode(mid - eps, oracle.BF16), lo_b)
+
+
+def test_encoders_random_values_against_libraries():
+    rng = np.random.default_rng(123)
+    x = rng.standard_normal(200000) * np.exp2(rng.integers(-30, 20, 200000))
+    assert np.array_equal(oracle.encode(x, oracle.F16), f16_bits(x))
+    x32 = (rng.standard_normal(200000) * np.exp2(rng.integers(-140, 130, 200000))).astype(
+        np.float32)
+    x32 = x32[np.isfinite(x32)]
+    assert np.array_equal(oracle.encode(x32.astype(np.float64), oracle.BF16),
+                          bf16_bits_from_f32(x32))
+
+
+def test_encoder_special_values():
+    E = oracle.encode
+    # fp16 overflow threshold: 65504 is the largest finite; 65520 ties to "65536" = inf
+    assert E(np.array([65504.0, 65519.99, 65520.0, 1e300]), oracle.F16).tolist() == \
+        [0x7BFF, 0x7BFF, 0x7C00, 0x7C00]
+    assert E(np.array([-65520.0]), oracle.F16)[0] == 0xFC00
+    # fp16 subnormals: 2^-24 is the smallest; half of it ties to 0, 3/4 of it rounds up
+    assert E(np.array([2.0 ** -24, 2.0 ** -25, 0.75 * 2.0 ** -24, 2.0 ** -14]),
+             oracle.F16).tolist() == [0x0001, 0x0000, 0x0001, 0x0400]
+    # bf16: largest finite (2 - 2^-7) 2^127; the midpoint to 2^128 ties to inf
+    big = (2.0 - 2.0 ** -7) * 2.0 ** 127
+    assert E(np.array([big, (2.0 - 2.0 ** -8) * 2.0 ** 127]), oracle.BF16).tolist() == \
+        [0x7F7F, 0x7F80]
+    assert E(np.array([2.0 ** -133, 2.0 ** -134, 2.0 ** -126]), oracle.BF16).tolist() == \
+        [0x0001, 0x0000, 0x0080]
+    assert E(np.array([0.0, -0.0, np.inf, -np.inf]), oracle.F16).tolist() == \
+        [0x0000, 0x8000, 0x7C00, 0xFC00]
+    assert (E(np.array([np.nan]), oracle.F16)[0] & 0x7C00) == 0x7C00
+    assert (E(np.array([np.nan]), oracle.F16)[0] & 0x03FF) != 0
+
+
+# -------------------------------------------------------------------- GEMM ----
+
+def _bits(values, dtype):
+    v = np.asarray(values, dtype=np.float64)
+    return f16_bits(v) if dtype == oracle.F16 else bf16_bits_from_f32(v.astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+@pytest.mark.parametrize("trans_b", [False, True])
+def test_hand_computed_2x2x2(dtype, trans_b):
+    g = json.load(open(os.path.join(GOLDEN, "hand_2x2x2.json")))
+    name = "f16" if dtype == oracle.F16 else "bf16"
+    A = _bits(g["A"], dtype)
+    Bm = np.asarray(g["B"])
+    B = _bits(Bm.T if trans_b else Bm, dtype)
+    for relu, key in ((False, "C_none_bits"), (True, "C_relu_bits")):
+        C = oracle.gemm(A, B, 2, 2, 2, dtype=dtype, trans_b=trans_b, relu=relu)
+        assert C.tolist() == g[key][name]
+
+
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+def test_identity_and_permutation(dtype):
+    rng = np.random.default_rng(5)
+    n, N = 37, 23
+    Bv = rng.uniform(-1, 1, (n, N))
+    B = _bits(Bv, dtype)
+    Bexact = oracle.decode(B, dtype)
+    I = _bits(np.eye(n), dtype)
+    C = oracle.gemm(I, B, n, N, n, dtype=dtype)
+    assert np.array_equal(C, B)                              # I.B = B exactly
+    C = oracle.gemm(I, B, n, N, n, dtype=dtype, relu=True)
+    want = _bits(np.maximum(Bexact, 0.0), dtype)
+    assert np.array_equal(C, want)                           # relu(B)
+    perm = rng.permutation(n)
+    P = _bits(np.eye(n)[perm], dtype)
+    C = oracle.gemm(P, B, n, N, n, dtype=dtype)
+    assert np.array_equal(C, B[perm])                        # rows of B permuted
+    # B = I on the right: A.I = A, with A transposed in storage as well
+    Av = _bits(rng.uniform(-1, 1, (N, n)), dtype)
+    C = oracle.gemm(Av.T.copy(), I, N, n, n, dtype=dtype, trans_a=True)
+    assert np.array_equal(C, Av)
+
+
+@pytest.mark.parametrize("K", [1, 7, 64, 4100])
+def test_all_ones_gives_k(K):
+    ones16 = _bits(np.ones((3, K)), oracle.F16)
+    C = oracle.gemm(ones16, ones16, 3, 3, K, dtype=oracle.F16, trans_b=True)
+    assert np.all(oracle.decode(C, oracle.F16) == float(K))       # fp16: K <= 4100 exact
+    onesbf = _bits(np.ones((3, K)), oracle.BF16)
+    C = oracle.gemm(onesbf, onesbf, 3, 3, K, dtype=oracle.BF16, trans_b=True)
+    want = {1: 1.0, 7: 7.0, 64: 64.0, 4100: 4096.0}[K]            # bf16 spacing 32 at 4096
+    assert np.all(oracle.decode(C, oracle.BF16) == want)
+
+
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+def test_rank1_and_relu_zeroing(dtype):
+    rng = np.random.default_rng(9)
+    M, N, K = 19, 21, 5
+    u = _bits(rng.uniform(-1, 1, M), dtype)
+    v = _bits(rng.uniform(-1, 1, N), dtype)
+    A = np.zeros((M, K), np.uint16)
+    A[:, 0] = u                              # A = u e0^T
+    B = np.zeros((K, N), np.uint16)
+    B[0, :] = v                              # B = e0 v^T
+    uv = np.outer(oracle.decode(u, dtype), oracle.decode(v, dtype))   # exact products
+    C = oracle.gemm(A, B, M, N, K, dtype=dtype)
+    assert np.array_equal(C, oracle.encode(uv, dtype))
+    assert np.array_equal(C, _bits(uv, dtype) if dtype == oracle.F16 else C)
+    C = oracle.gemm(A, B, M, N, K, dtype=dtype, relu=True)
+    assert np.array_equal(C, oracle.encode(np.maximum(uv, 0.0), dtype))
+    # all-negative products: relu gives +0 everywhere, no epilogue gives the product
+    An = _bits(-np.abs(rng.uniform(0.1, 1, (M, K))), dtype)
+    Bp = _bits(np.abs(rng.uniform(0.1, 1, (K, N))), dtype)
+    C = oracle.gemm(An, Bp, M, N, K, dtype=dtype, relu=True)
+    assert np.all(C == 0)
+    C = oracle.gemm(An, Bp, M, N, K, dtype=dtype)
+    assert np.all(oracle.decode(C, dtype) < 0)
+
+
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+def test_k1_single_rounding(dtype):
+    rng = np.random.default_rng(11)
+    a = _bits(rng.uniform(-1, 1, (8, 1)), dtype)
+    b = _bits(rng.uniform(-1, 1, (1, 9)), dtype)
+    prod = oracle.decode(a, dtype) @ oracle.decode(b, dtype)   # one exact product each
+    C = oracle.gemm(a, b, 8, 9, 1, dtype=dtype)
+    assert np.array_equal(C, oracle.encode(prod, dtype))
+    if dtype == oracle.F16:
+        assert np.array_equal(C, f16_bits(prod))
+
+
+def test_k0_gives_zero_and_degenerate_sizes():
+    A = np.zeros((4, 1), np.uint16)
+    C = oracle.gemm(A, A, 4, 3, 0, lda=1, ldb=3, dtype=oracle.F16, relu=True)
+    assert C.shape == (4, 3) and np.all(C == 0)
+    C = oracle.gemm(A, A, 0, 3, 5, lda=5, ldb=3, dtype=oracle.F16)
+    assert C.shape == (0, 3)
+
+
+@pytest.mark.parametrize("trans_a", [False, True])
+@pytest.mark.parametrize("trans_b", [False, True])
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+def test_integer_products_against_numpy(trans_a, trans_b, dtype):
+    """Small-integer operands: numpy's int64 product is exact; padded leading dims."""
+    rng = np.random.default_rng(17 + 2 * trans_a + trans_b)
+    M, N, K = 45, 29, 70
+    lo, hi = (-2, 3) if dtype == oracle.F16 else (-1, 2)
+    Ai = rng.integers(lo, hi, (M, K))
+    Bi = rng.integers(lo, hi, (K, N))
+    want = Ai @ Bi
+    pad = 3
+    As = Ai.T if trans_a else Ai
+    Bs = Bi.T if trans_b else Bi
+    Ast = np.zeros((As.shape[0], As.shape[1] + pad), np.int64)
+    Ast[:, :As.shape[1]] = As
+    Bst = np.zeros((Bs.shape[0], Bs.shape[1] + pad), np.int64)
+    Bst[:, :Bs.shape[1]] = Bs
+    Ab, Bb = _bits(Ast, dtype), _bits(Bst, dtype)
+    C = oracle.gemm(Ab, Bb, M, N, K, lda=Ast.shape[1], ldb=Bst.shape[1], ldc=N + 5,
+                    dtype=dtype, trans_a=trans_a, trans_b=trans_b)
+    assert np.array_equal(oracle.decode(C, dtype), want.astype(np.float64))
+    Cr = oracle.gemm(Ab, Bb, M, N, K, lda=Ast.shape[1], ldb=Bst.shape[1], dtype=dtype,
+                     trans_a=trans_a, trans_b=trans_b, relu=True)
+    assert np.array_equal(oracle.decode(Cr, dtype), np.maximum(want, 0).astype(np.float64))
+
+
+def test_exact_rational_sums_within_binary64_bound():
+    """Random fp16 operands: the oracle's binary64 sum is within K*2^-53*sum|terms| of the
+    exact rational sum, and its rounded output matches the correctly rounded exact sum
+    wherever the exact sum is not within that bound of a tie."""
+    rng = np.random.default_rng(21)
+    M, N, K = 6, 7, 33
+    A = _bits(rng.uniform(-1, 1, (M, K)), oracle.F16)
+    B = _bits(rng.uniform(-1, 1, (K, N)), oracle.F16)
+    Av, Bv = oracle.decode(A, oracle.F16), oracle.decode(B, oracle.F16)
+    C, S = oracle.gemm(A, B, M, N, K, dtype=oracle.F16, want_sums=True)
+    for i in range(M):
+        for j in range(N):
+            terms = [Fraction(float(Av[i, k])) * Fraction(float(Bv[k, j])) for k in range(K)]
+            exact = sum(terms, Fraction(0))
+            bound = K * 2.0 ** -53 * float(sum(abs(t) for t in terms))
+            assert abs(Fraction(float(S[i, j])) - exact) <= Fraction(bound)
+            assert C[i, j] == f16_bits(float(exact))
+
+
+def test_entries_match_full_product_and_threads_do_not_change_bits():
+    rng = np.random.default_rng(31)
+    M, N, K = 50, 40, 300
+    A = _bits(rng.uniform(-1, 1, (K, M)), oracle.BF16)
+    B = _bits(rng.uniform(-1, 1, (N, K)), oracle.BF16)
+    kw = dict(dtype=oracle.BF16, trans_a=True, trans_b=True, relu=True)
+    C1 = oracle.gemm(A, B, M, N, K, threads=1, **kw)
+    C4 = oracle.gemm(A, B, M, N, K, threads=4, **kw)
+    assert np.array_equal(C1, C4)
+    rows = rng.integers(0, M, 200)
+    cols = rng.integers(0, N, 200)
+    E = oracle.gemm_entries(A, B, M, N, K, rows, cols, **kw)
+    assert np.array_equal(E, C1[rows, cols])
+
+
+def test_rejects_bad_arguments():
+    A = np.zeros(16, np.uint16)
+    with pytest.raises(ValueError):
+        oracle.gemm(A, A, 4, 4, 4, lda=2)          # lda < K
+    with pytest.raises(ValueError):
+        oracle.gemm_entries(A, A, 4, 4, 4, [4], [0])   # row out of range

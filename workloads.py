@@ -1,0 +1,135 @@
+"""Seeded synthetic workloads for the tiled GEMM: shapes, layouts and input draws.
+
+This module only draws inputs; it holds none of the GEMM's arithmetic.  Both the
+CPU oracle's tests and the CUDA path's tests and benchmark take their inputs from
+here, so the two sides see bit-identical operands.
+
+Recipe (stated once, used everywhere): one CPU ``torch.Generator`` per workload,
+seeded with the workload's seed; A is drawn first, then B, each in fp32 in the
+shape of its *storage* (A is [M, K], or [K, M] when ``trans_a``; B is [K, N], or
+[N, K] when ``trans_b``), then converted to the 16-bit dtype by torch's
+round-to-nearest-even cast.  Distributions follow the workloads the GEMM is
+described with (the pages' quickstart GEMM at 1024^3 with fp16 operands and
+128x128x64 tiles in 3 stages; square bf16 GEMMs with a column-major B; a ragged
+shape that is a multiple of no tile; decode-like skinny products).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+F16 = 0
+BF16 = 1
+_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
+_NAME = {F16: "f16", BF16: "bf16"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype: int
+    trans_a: bool
+    trans_b: bool
+    relu: bool
+    dist_a: str            # "uniform" | "normal_over_sqrtk" | "normal"
+    dist_b: str
+    std_a: float = 1.0     # used by "normal"
+    std_b: float = 1.0
+    seed: int = 0
+    plan: tuple | None = None   # (BM, BN, BK, stages) when the workload fixes the tiling
+    description: str = ""
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPE[self.dtype]
+
+    @property
+    def dtype_name(self) -> str:
+        return _NAME[self.dtype]
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def bytes_moved(self) -> int:
+        """Algorithmic HBM bytes: read A and B once, write C once (2-byte elements)."""
+        return 2 * (self.M * self.K + self.K * self.N + self.M * self.N)
+
+    def a_shape(self) -> tuple[int, int]:
+        return (self.K, self.M) if self.trans_a else (self.M, self.K)
+
+    def b_shape(self) -> tuple[int, int]:
+        return (self.N, self.K) if self.trans_b else (self.K, self.N)
+
+
+def _draw(shape, dist: str, std: float, K: int, g: torch.Generator) -> torch.Tensor:
+    if dist == "uniform":
+        return torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "normal_over_sqrtk":
+        return torch.randn(shape, generator=g, dtype=torch.float32) / math.sqrt(K)
+    if dist == "normal":
+        return torch.randn(shape, generator=g, dtype=torch.float32) * std
+    if dist == "int_small":
+        # integers in [-2, 2]: every partial sum is an exact small integer in fp32
+        return torch.randint(-2, 3, shape, generator=g).to(torch.float32)
+    if dist == "int_unit":
+        # integers in [-1, 1]: exact in bf16 and in every fp32 partial sum
+        return torch.randint(-1, 2, shape, generator=g).to(torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def make_inputs(w: Workload, seed: int | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """CPU tensors (A, B) in storage layout and the workload's dtype; A drawn first."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    a = _draw(w.a_shape(), w.dist_a, w.std_a, w.K, g).to(w.torch_dtype)
+    b = _draw(w.b_shape(), w.dist_b, w.std_b, w.K, g).to(w.torch_dtype)
+    return a, b
+
+
+def integer_variant(w: Workload, M=None, N=None, K=None, seed=None) -> Workload:
+    """Same layout and dtype with small-integer entries, so that every fp32 partial sum
+    is exact and GPU and oracle must agree bit for bit."""
+    dist = "int_small" if w.dtype == F16 else "int_unit"
+    return dataclasses.replace(
+        w, name=w.name + "_int", M=M or w.M, N=N or w.N, K=K or w.K,
+        dist_a=dist, dist_b=dist, seed=w.seed if seed is None else seed)
+
+
+WORKLOADS: dict[str, Workload] = {}
+
+
+def _add(w: Workload) -> None:
+    WORKLOADS[w.name] = w
+
+
+_add(Workload("gemm_relu_256_f16", 256, 256, 256, F16, False, False, True,
+              "uniform", "uniform", seed=0,
+              description="GEMM+ReLU 256^3 fp16, A,B row-major U[-1,1]"))
+_add(Workload("gemm_relu_1024_f16_128x128x64s3", 1024, 1024, 1024, F16, False, False, True,
+              "uniform", "uniform", seed=1, plan=(128, 128, 64, 3),
+              description="GEMM+ReLU 1024^3 fp16 (quickstart size), tiles 128x128x64, "
+                          "3 stages, U[-1,1]"))
+_add(Workload("gemm_4096_bf16_tb", 4096, 4096, 4096, BF16, False, True, False,
+              "normal_over_sqrtk", "normal_over_sqrtk", seed=2,
+              description="GEMM 4096^3 bf16, B column-major, N(0,1)/sqrt(K)"))
+_add(Workload("gemm_8192_bf16_tb", 8192, 8192, 8192, BF16, False, True, False,
+              "normal_over_sqrtk", "normal_over_sqrtk", seed=3,
+              description="GEMM 8192^3 bf16, B column-major, N(0,1)/sqrt(K)"))
+_add(Workload("gemm_relu_3000x5000x4100_f16", 3000, 5000, 4100, F16, False, False, True,
+              "uniform", "uniform", seed=4,
+              description="ragged GEMM+ReLU 3000x5000x4100 fp16, U[-1,1]"))
+for _m, _seed in ((16, 5), (64, 6), (128, 7)):
+    _add(Workload(f"gemm_m{_m}_n8192_k8192_bf16", _m, 8192, 8192, BF16, False, True, False,
+                  "normal", "normal", std_a=1.0, std_b=0.02, seed=_seed,
+                  description=f"skinny decode-like GEMM M={_m}, N=K=8192 bf16, activations "
+                              "N(0,1), weights N(0,0.02) stored [N,K]"))
+
+# The benchmark's headline workload: the quickstart GEMM+ReLU.
+HEADLINE = "gemm_relu_1024_f16_128x128x64s3"
