@@ -1,0 +1,409 @@
+"""Benchmark of the tiled GEMM (+ReLU) on one GB300 per process.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl tl|reference] [--no-cpu-baseline] [--no-e2e]
+
+One step is one call of the C ABI (tl_gemm) on one seeded synthetic input set of
+the workload: the whole hot path (TMA producer, tcgen05 MMA, ReLU/cast epilogue,
+TMA store) in one persistent kernel launch.  Inputs are resident in HBM before the
+timed region.  Between timed steps the inputs rotate over enough independent sets
+that the working set exceeds twice the L2 cache, so every step reads its operands
+from HBM (or the operands alone are larger than L2).
+
+Prints ONE JSON line (rank 0): the metric (TFLOP/s), the roofline of the GEMM
+kernel against the measured peaks, the CPU oracle's rate on the host cores, the
+end-to-end rate from pinned host buffers, and the SM clocks seen during the run.
+
+With N > 1 (torchrun), every rank runs the same workload on its own GPU: the path
+has no exchange step, so the ranks are replicas (weak scaling) and only the timing
+barrier and the max-over-ranks reduction use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["tiled_gemm_gb300/csrc/gemm_kernel.cuh", "tiled_gemm_gb300/csrc/sm103_ptx.cuh",
+                  "tiled_gemm_gb300/csrc/tl_gemm.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = table.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def is_hbm_bound(w: workloads.Workload, peaks: dict) -> bool:
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return w.flops / w.bytes_moved < ridge
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="tl_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle ----
+
+def oracle_rate(w: workloads.Workload, a_cpu, b_cpu, budget_s: float, threads: int):
+    """Oracle TFLOP/s on whole-row slices of the workload, repeated for ~budget_s."""
+    import oracle
+    oracle.build()
+    rows = max(1, min(w.M, 8))
+    done_flops, elapsed, reps = 0, 0.0, 0
+    a_rows = a_cpu if w.trans_a else None
+    while elapsed < budget_s:
+        if w.trans_a:
+            sl_a, M_s = a_rows[:, :rows].contiguous(), rows
+            lda = rows
+        else:
+            sl_a, M_s = a_cpu[:rows].contiguous(), rows
+            lda = w.K
+        t0 = time.perf_counter()
+        oracle.gemm(sl_a, b_cpu, M_s, w.N, w.K, lda=lda, dtype=w.dtype, trans_a=w.trans_a,
+                    trans_b=w.trans_b, relu=w.relu, threads=threads)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done_flops += 2 * M_s * w.N * w.K
+        reps += 1
+        if dt < budget_s / 20 and rows < w.M:
+            rows = min(w.M, rows * 2)
+    return done_flops / elapsed / 1e12, elapsed, done_flops, rows, reps
+
+
+# ------------------------------------------------------------------ GPU arm ----
+
+def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
+    import numpy as np  # noqa: F401
+    import torch
+
+    import tiled_gemm_gb300 as tl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    a_cpu, b_cpu = workloads.make_inputs(w)
+    per_set = w.bytes_moved
+    rot = 1 if per_set >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / per_set))
+    sets = []
+    a0, b0 = a_cpu.to(dev), b_cpu.to(dev)
+    for i in range(rot):
+        a = a0 if i == 0 else a0.clone()
+        b = b0 if i == 0 else b0.clone()
+        c = torch.empty((w.M, w.N), dtype=w.torch_dtype, device=dev)
+        sets.append((a, b, c))
+    plan = None
+    if w.plan is not None:
+        bm, bn, bk, st = w.plan
+        plan = tl.plan_for(0, 0, 0, bm, bn, bk, st)
+    stream = torch.cuda.Stream(device=dev)
+    lda = w.M if w.trans_a else w.K
+    launches_per_step = 1 + int((lda * 2) % 16 != 0) + int(
+        ((w.K if w.trans_b else w.N) * 2) % 16 != 0)
+
+    def step(i):
+        a, b, c = sets[i % rot]
+        tl.gemm(a, b, trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, out=c, plan=plan,
+                stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+    status, word = tl.tl_device_status(reset=True)
+    if status != tl.TL_OK:
+        raise RuntimeError(f"device-side wait gave up during warm-up: {word:#x}")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            ev_s[i].record(stream)
+            step(args.warmup + i)
+            ev_e[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(ev_s, ev_e)]
+    status, word = tl.tl_device_status(reset=True)
+    if status != tl.TL_OK:
+        raise RuntimeError(f"device-side wait gave up in the timed region: {word:#x}")
+
+    max_ms = total_ms
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers --------------------
+    e2e = None
+    if not args.no_e2e:
+        a_h = a_cpu.pin_memory()
+        b_h = b_cpu.pin_memory()
+        c_h = torch.empty((w.M, w.N), dtype=w.torch_dtype).pin_memory()
+        a_d, b_d, c_d = sets[0]
+        e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            a_d.copy_(a_h, non_blocking=True)
+            b_d.copy_(b_h, non_blocking=True)
+            tl.gemm(a_d, b_d, trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, out=c_d,
+                    plan=plan, stream=stream)
+            c_h.copy_(c_d, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(e_steps):
+                e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(w.flops * e_steps * world / (e_ms * 1e-3) / 1e12, 3),
+               "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(a_cpu.numel() * 2 + b_cpu.numel() * 2),
+               "d2h_bytes_per_step": int(w.M * w.N * 2),
+               "steps": e_steps, "ms_per_step": round(e_ms / e_steps, 4)}
+
+    return {"total_ms": max_ms, "per_launch_ms": per_launch_ms, "clocks": clk, "e2e": e2e,
+            "rotation_sets": rot, "launches_per_step": launches_per_step,
+            "plan": tl.tl_gemm_plan(w.M, w.N, w.K, w.dtype, int(w.trans_a), int(w.trans_b),
+                                    torch.cuda.get_device_properties(dev).multi_processor_count)
+            .as_dict() if plan is None else
+            tl.tl_plan_complete(w.M, w.N, w.K, *w.plan, dtype=w.dtype).as_dict()}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="tl", choices=["tl", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    w = workloads.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks, peaks_src = load_peaks()
+    threads = os.cpu_count() or 1
+
+    config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype_name,
+              "trans_a": w.trans_a, "trans_b": w.trans_b,
+              "epilogue": "relu" if w.relu else "none", "inputs": w.description,
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        # The oracle on the host cores, rank 0 only: each step a bounded row slice.
+        if rank != 0:
+            return
+        a_cpu, b_cpu = workloads.make_inputs(w)
+        budget = max(0.5, 150.0 / (args.steps + args.warmup))
+        for _ in range(args.warmup):
+            oracle_rate(w, a_cpu, b_cpu, min(budget, 1.0), threads)
+        rates, times = [], []
+        for _ in range(args.steps):
+            r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, budget, threads)
+            rates.append(r)
+            times.append(el)
+        value = statistics.mean(rates)
+        line = {"metric": "GEMM+ReLU TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU",
+                "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 * statistics.mean(times), 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "impl": "reference", "config": config,
+                "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                                 "kind": "oracle",
+                                 "sample": f"row slices of up to {rows} of {w.M} rows per step, "
+                                           f"~{budget:.1f} s of CPU work per step"},
+                "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+
+    # The oracle's CPU baseline runs before any CUDA work of this process touches the
+    # GPU's clocks (rank 0, N = 1 only).
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        a_cpu, b_cpu = workloads.make_inputs(w)
+        r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, args.cpu_budget_s, threads)
+        cpu = {"value": round(r, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows), "
+                         f"{fl / 1e9:.2f} GFLOP in {el:.1f} s"}
+
+    res = run_tl(args, w, rank, world, dist)
+    total_ms = res["total_ms"]
+    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    per_launch = sorted(res["per_launch_ms"])
+    avg_launch_ms = statistics.mean(per_launch)
+    hbm = is_hbm_bound(w, peaks)
+    if hbm:
+        achieved = w.bytes_moved / (avg_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}
+    else:
+        achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]       # fp16 and bf16 share the dense tensor rate
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s"}
+    roof["frac"] = round(achieved / peak, 4)
+    roof["peak_source"] = f"{peaks_src} (burst)"
+    roof["traffic"] = load_traffic(w.name)
+    roof["kernel_ms"] = {"mean": round(avg_launch_ms, 5),
+                         "p10": round(per_launch[len(per_launch) // 10], 5),
+                         "median": round(per_launch[len(per_launch) // 2], 5),
+                         "p90": round(per_launch[(9 * len(per_launch)) // 10], 5)}
+    roof["algorithmic"] = {"flops_per_launch": w.flops, "bytes_per_launch": w.bytes_moved}
+    if rank != 0:
+        return
+    line = {"metric": "GEMM+ReLU TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU",
+            "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype_name, "data": "synthetic (seeded CPU generator)",
+            "config": dict(config, l2=(f"inputs rotate over {res['rotation_sets']} sets "
+                                       f"({res['rotation_sets'] * w.bytes_moved / 2**20:.0f} MiB "
+                                       "> 2x L2)") if res["rotation_sets"] > 1 else
+                           "operands larger than 2x L2"),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": res["e2e"],
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "clocks": res["clocks"], "plan": res["plan"],
+            "pct_of_nominal_2250": round(100 * value / world / 2250.0, 2)}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

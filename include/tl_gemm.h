@@ -1,0 +1,175 @@
+/*
+ * tl_gemm.h -- C ABI of the GB300 (sm_103a) tiled GEMM with a fused epilogue.
+ *
+ *   C = epi(op(A) . op(B)),  epi in {identity, ReLU},  fp16/bf16 in and out,
+ *   fp32 accumulation in Tensor Memory, round-to-nearest-even on the output.
+ *
+ * Sources of the semantics (the pages the operation is described on):
+ *   - The tiled GEMM itself: the quickstart kernel copies A and B tiles global ->
+ *     shared, multiplies them into an fp32 accumulator under a multi-stage
+ *     software pipeline, and copies the accumulator back to global ("TileLang: a
+ *     tile language one level below Triton", section "first kernel: GEMM";
+ *     "TileLang: from tile dataflow to controllable AI kernels", section "minimal
+ *     but complete GEMM skeleton": fp16 inputs, fp32 accumulation, cast to the
+ *     output dtype at the end).
+ *   - transpose_A / transpose_B: A is [M,K] or, transposed, [K,M]; B is [K,N] or,
+ *     transposed, [N,K] ("TileLang core primitives" page, section 3.3 "T.gemm").
+ *   - The ReLU epilogue max(x, 0) on the fp32 accumulator before the cast ("NVIDIA
+ *     backend codegen" page, section 1, the GEMM+ReLU quickstart; "TileLang core
+ *     primitives" page, section 3.8).
+ *   - Partial tiles: out-of-range source elements read as 0 and out-of-range
+ *     destination elements are never written ("TileLang core primitives" page,
+ *     section 4.2 "out of bounds and padding"; TMA zero fill, "NVIDIA backend
+ *     codegen" page, section 4.4.3).
+ *   - Argument checks at the ABI boundary, before any launch ("TileLang: from tile
+ *     dataflow to controllable AI kernels", section "automatically generated host
+ *     checks"), and explicit failure instead of a silent fallback ("NVIDIA backend
+ *     codegen" page, section 4.3.2).
+ *
+ * All pointers to matrices are DEVICE pointers of the current CUDA device.  The
+ * library never frees or retains caller memory.  Every call is asynchronous on
+ * `stream` (NULL = the legacy default stream) and returns once the work is
+ * enqueued.  The library holds only per-device caches of kernel attributes; it is
+ * safe to call from several host threads.
+ */
+#ifndef TL_GEMM_H
+#define TL_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, without requiring the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* tl_stream_t;
+
+typedef enum { TL_F16 = 0, TL_BF16 = 1 } tl_dtype;
+
+typedef enum { TL_EPI_NONE = 0, TL_EPI_RELU = 1 } tl_epilogue;
+
+typedef enum {
+  TL_OK = 0,
+  TL_ERR_INVALID_ARG = 1,  /* negative size, ld too small, bad enum, bad plan      */
+  TL_ERR_NULL_PTR = 2,     /* NULL matrix pointer with a non-empty extent          */
+  TL_ERR_ALIGNMENT = 3,    /* a matrix pointer not aligned to its 2-byte element   */
+  TL_ERR_UNSUPPORTED = 4,  /* valid request this build cannot run (no sm_103 GPU,  */
+                           /* size beyond the library's limits)                    */
+  TL_ERR_ALIAS = 5,        /* C overlaps A or B                                    */
+  TL_ERR_DEVICE = 6,       /* pointer not on the current device, CUDA query failed */
+  TL_ERR_LAUNCH = 7,       /* a kernel or an allocation failed to enqueue          */
+  TL_ERR_TIMEOUT = 8       /* a device-side wait ran out (read by tl_device_status)*/
+} tl_status;
+
+/*
+ * One execution plan: the tiling and scheduling the kernel runs with.
+ * tl_gemm_plan() fills it from (M, N, K, dtype, transposes) without touching a
+ * GPU; tl_gemm_with_plan() runs a given plan.
+ */
+typedef struct {
+  int32_t bm;            /* output rows per CTA tile (128)                          */
+  int32_t bn;            /* output columns per tile (64, 128 or 256)                */
+  int32_t bk;            /* K elements per pipeline stage (64: one 128-byte row)    */
+  int32_t stages;        /* depth of the shared-memory ring                         */
+  int32_t raster_group;  /* tile rows per L2 rasterisation group                    */
+  int32_t grid;          /* persistent CTAs launched (0 = one per SM, capped)       */
+  int64_t tiles_m, tiles_n, tiles, k_blocks;
+  int64_t ring_bytes;    /* stages * (bm*bk + bn*bk) * 2                            */
+  int64_t smem_bytes;    /* dynamic shared memory per CTA (ring + staging + bars)   */
+  int32_t tmem_cols;     /* Tensor Memory columns allocated (2 accumulators)        */
+  int32_t tx_bytes;      /* bytes one stage's TMA loads deliver (full boxes)        */
+  int32_t repack_a;      /* A is staged through a pitch-padded workspace            */
+  int32_t repack_b;      /* B likewise                                              */
+  int32_t tma_store;     /* C written by TMA bulk stores (else predicated stores)   */
+  int32_t reserved;
+  int64_t workspace_bytes; /* bytes of the stream-ordered repack workspace          */
+} tl_plan;
+
+/*
+ * C = epi(op(A) . op(B)).
+ *
+ *   A  device pointer; op(A)[i,k] = A[i*lda + k], or A[k*lda + i] if trans_a.
+ *   B  device pointer; op(B)[k,j] = B[k*ldb + j], or B[j*ldb + k] if trans_b.
+ *   C  device pointer; C[i*ldc + j] for 0 <= i < M, 0 <= j < N.  Nothing outside
+ *      that region is written.  C must not overlap A or B.
+ *   M, N, K >= 0.  M == 0 or N == 0: returns TL_OK, launches nothing.  K == 0:
+ *      C is filled with epi(0) = +0.
+ *   lda >= (trans_a ? M : K), ldb >= (trans_b ? K : N), ldc >= N (elements).
+ *   dtype: element type of A, B and C.  Accumulation is fp32; the output rounds
+ *      to nearest even.  epilogue: TL_EPI_NONE or TL_EPI_RELU (applied to the fp32
+ *      accumulator; negative values give +0).
+ *   stream: CUDA stream to enqueue on.
+ *
+ * Operands whose base or pitch is not 16-byte aligned (tensor-memory-access rule:
+ * the leading pitch in bytes must be a multiple of 16) are first copied on
+ * `stream` into a workspace with the pitch rounded up, allocated and freed with
+ * the stream-ordered allocator; an unaligned C is written by predicated stores.
+ *
+ * Errors are returned before anything is enqueued: TL_ERR_INVALID_ARG,
+ * TL_ERR_NULL_PTR, TL_ERR_ALIGNMENT, TL_ERR_ALIAS, TL_ERR_DEVICE,
+ * TL_ERR_UNSUPPORTED.  TL_ERR_LAUNCH means an enqueue failed.
+ */
+tl_status tl_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype, int trans_a,
+                  int trans_b, tl_epilogue epilogue, tl_stream_t stream);
+
+/*
+ * The plan tl_gemm() would run for this problem.  Host only: touches no GPU (the
+ * SM count is taken as `num_sms`, or 148 when num_sms <= 0).  Returns
+ * TL_ERR_INVALID_ARG for negative sizes or bad enums.  The resource figures follow
+ * the pages' shared-memory model S = stages * (BM*BK*s_A + BK*BN*s_B) + S_other
+ * ("TileLang: from tile dataflow to controllable AI kernels", section "more
+ * stages is not always better").
+ */
+tl_status tl_gemm_plan(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
+                       int trans_b, int num_sms, tl_plan* plan);
+
+/*
+ * Fill the derived fields of `plan` (tiles, k-blocks, ring/smem bytes, TMEM
+ * columns, tx bytes) from its bm/bn/bk/stages and the problem size.  Host only.
+ * Returns TL_ERR_INVALID_ARG when the tiling is not one the kernel supports
+ * (bm != 128, bn not in {64,128,256}, bk != 64, stages outside 2..8, or shared
+ * memory above the per-CTA limit).
+ */
+tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
+                           int trans_b, int num_sms, tl_plan* plan);
+
+/*
+ * tl_gemm() with an explicit plan (bm, bn, bk, stages, raster_group, grid are read;
+ * the rest is recomputed).  Used to run a workload at a fixed tiling, e.g. the
+ * pages' quickstart 128x128x64 with 3 stages.  Same arguments and errors as
+ * tl_gemm(), plus TL_ERR_INVALID_ARG for an unsupported plan.
+ */
+tl_status tl_gemm_with_plan(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype,
+                            int trans_a, int trans_b, tl_epilogue epilogue,
+                            const tl_plan* plan, tl_stream_t stream);
+
+/* Static, NUL-terminated name of a status code ("TL_OK", ...). */
+const char* tl_status_string(tl_status status);
+
+/*
+ * Outcome of the device-side bounded waits since the last reset, for the current
+ * device: TL_OK, or TL_ERR_TIMEOUT if some wait of some kernel gave up (the
+ * kernel then set this flag, drained its own copies, freed its Tensor Memory and
+ * returned; its output is undefined).  Synchronises the device.  If `reset` is
+ * non-zero the flag is cleared afterwards.  `detail`, if not NULL, receives the
+ * raw status word (role and wait site of the first timeout).
+ */
+tl_status tl_device_status(int reset, uint32_t* detail);
+
+/*
+ * Limit of every device-side wait, in nanoseconds, for kernels enqueued after this
+ * call (default 2e9).  Values are clamped to [1e5, 6e10].  Host only.
+ */
+void tl_set_wait_timeout_ns(uint64_t ns);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int tl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TL_GEMM_H */

@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+* The shared library loads and exports every function that include/tl_gemm.h
+  declares.
+* The host planner reproduces the pages' printed resource numbers for the
+  quickstart tiling (tests/golden/pages_resource_numbers.json): 16 KB per operand
+  tile, 64/96/128 KB of operand ring for 2/3/4 stages, B ring at offset 48 KB,
+  16 k-blocks at K = 1024, two such blocks per 228 KB SM.
+* Argument errors are returned before anything touches a device.
+"""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import tiled_gemm_gb300 as tl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tl_gemm.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "pages_resource_numbers.json")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tl_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    for required in ("tl_gemm", "tl_gemm_plan", "tl_gemm_with_plan", "tl_plan_complete",
+                     "tl_status_string", "tl_device_status", "tl_set_wait_timeout_ns",
+                     "tl_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(tl.LIBRARY._name)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_status_strings():
+    for code, name in enumerate(tl.STATUS_NAMES):
+        assert tl.tl_status_string(code) == name
+    assert tl.tl_status_string(99) == "TL_ERR_UNKNOWN"
+    assert tl.tl_version() >= 100
+
+
+def test_planner_reproduces_the_pages_resource_numbers():
+    g = json.load(open(GOLDEN))
+    bm, bn, bk = g["tile"]
+    for stages, ring in g["ring_bytes_by_stages"].items():
+        p = tl.tl_plan_complete(1024, 1024, 1024, bm, bn, bk, int(stages))
+        assert p.ring_bytes == ring
+        assert p.ring_bytes // int(stages) == 2 * g["bytes_per_operand_tile"]
+    p = tl.tl_plan_complete(1024, 1024, 1024, bm, bn, bk, 3)
+    assert p.k_blocks == g["k_blocks_at_k_1024"]
+    assert 3 * bm * bk * g["elem_bytes"] == g["b_ring_offset_bytes_3_stages"]
+    assert p.tx_bytes == 2 * g["bytes_per_operand_tile"]
+    assert g["smem_per_sm_bytes_h100"] // p.ring_bytes == g["blocks_per_sm_3_stages_h100"]
+    # the quickstart grid: ceil(N/128) x ceil(M/128) = 64 tiles
+    assert (p.tiles_m, p.tiles_n, p.tiles) == (8, 8, 64)
+
+
+@pytest.mark.parametrize("M,N,K", [(3000, 5000, 4100), (256, 256, 256), (16, 8192, 8192),
+                                   (8192, 8192, 8192), (1, 1, 1)])
+def test_plan_tiles_cover_the_output_exactly_once(M, N, K):
+    p = tl.tl_gemm_plan(M, N, K, num_sms=148)
+    assert p.tiles_m * p.bm >= M > (p.tiles_m - 1) * p.bm
+    assert p.tiles_n * p.bn >= N > (p.tiles_n - 1) * p.bn
+    assert p.k_blocks * p.bk >= K > (p.k_blocks - 1) * p.bk
+    assert p.tiles == p.tiles_m * p.tiles_n
+    assert 1 <= p.grid <= min(148, p.tiles)
+    assert p.smem_bytes <= 232448
+    assert p.tmem_cols in (128, 256, 512)
+    assert p.tx_bytes == (p.bm + p.bn) * p.bk * 2
+
+
+def test_every_supported_tiling_fits_shared_memory_and_others_are_rejected():
+    for bn, max_stages in ((64, 8), (128, 6), (256, 4)):
+        for stages in range(2, max_stages + 1):
+            p = tl.tl_plan_complete(4096, 4096, 4096, 128, bn, 64, stages)
+            assert p.smem_bytes <= 232448
+        if max_stages < 8:
+            with pytest.raises(tl.TLError):
+                tl.tl_plan_complete(4096, 4096, 4096, 128, bn, 64, max_stages + 1)
+    for bad in ((64, 128, 64, 3), (128, 96, 64, 3), (128, 128, 32, 3), (128, 128, 64, 1),
+                (128, 128, 64, 9)):
+        with pytest.raises(tl.TLError):
+            tl.tl_plan_complete(1024, 1024, 1024, *bad)
+
+
+def test_planner_rejects_bad_arguments():
+    with pytest.raises(tl.TLError):
+        tl.tl_gemm_plan(-1, 4, 4)
+    with pytest.raises(tl.TLError):
+        tl.tl_gemm_plan(4, 4, 4, dtype=7)
+    with pytest.raises(tl.TLError):
+        tl.tl_gemm_plan(4, 4, 4, trans_a=2)
+
+
+# Fake device addresses: every case below must be rejected before any CUDA call.
+A, B, C = 0x10000, 0x20000000, 0x40000000
+
+
+@pytest.mark.parametrize("args,code", [
+    ((A, B, C, -1, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_INVALID_ARG),
+    ((A, B, C, 4, 4, 4, 4, 4, 4, 2, 0, 0, 0), tl.TL_ERR_INVALID_ARG),      # dtype
+    ((A, B, C, 4, 4, 4, 4, 4, 4, 0, 0, 0, 5), tl.TL_ERR_INVALID_ARG),      # epilogue
+    ((A, B, C, 4, 4, 4, 4, 4, 4, 0, 3, 0, 0), tl.TL_ERR_INVALID_ARG),      # trans flag
+    ((A, B, C, 4, 4, 8, 7, 4, 4, 0, 0, 0, 0), tl.TL_ERR_INVALID_ARG),      # lda < K
+    ((A, B, C, 4, 5, 8, 8, 4, 5, 0, 0, 0, 0), tl.TL_ERR_INVALID_ARG),      # ldb < N
+    ((A, B, C, 4, 5, 8, 8, 5, 4, 0, 0, 0, 0), tl.TL_ERR_INVALID_ARG),      # ldc < N
+    ((A, B, C, 4, 4, 8, 3, 8, 4, 0, 1, 0, 0), tl.TL_ERR_INVALID_ARG),      # trans_a: lda < M
+    ((A, B, 0, 4, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_NULL_PTR),
+    ((0, B, C, 4, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_NULL_PTR),
+    ((A, 0, C, 4, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_NULL_PTR),
+    ((A + 1, B, C, 4, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_ALIGNMENT),
+    ((A, B, C + 1, 4, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_ALIGNMENT),
+    ((A, B, A + 8, 4, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_ALIAS),          # C inside A
+    ((A, B, B - 8, 4, 4, 4, 4, 4, 4, 0, 0, 0, 0), tl.TL_ERR_ALIAS),          # C runs into B
+])
+def test_argument_errors_before_any_device_work(args, code):
+    assert tl.tl_gemm(*args, None) == code
+
+
+def test_empty_outputs_are_a_no_op():
+    assert tl.tl_gemm(A, B, C, 0, 4, 4, 4, 4, 4, 0, 0, 0, 0, None) == tl.TL_OK
+    assert tl.tl_gemm(A, B, C, 4, 0, 4, 4, 0, 0, 0, 0, 0, 0, None) == tl.TL_OK
+    assert tl.tl_gemm(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == tl.TL_OK

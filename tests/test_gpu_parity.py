@@ -1,0 +1,235 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bars:
+* small-integer operands: bit-exact (every fp32 partial sum is an exact integer, so
+  the only rounding is the final round-to-nearest-even, identical on both sides);
+* random operands: |C - C_ref| <= 1e-2 + 1e-2 |C_ref| element by element;
+* full-size workloads: every element on the tile edges plus random entries against
+  the oracle computed one by one, and the canary guard band for coverage.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_gemm_gb300 as tl
+import workloads
+from gpu_helpers import (GuardedC, assert_bit_exact, assert_within_tolerance, oracle_full,
+                         run_tl, sample_indices, to_device_padded)
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16 = workloads.F16, workloads.BF16
+
+
+def _w(M, N, K, dtype, ta, tb, relu, dist, seed):
+    return workloads.Workload("t", M, N, K, dtype, ta, tb, relu, dist, dist, seed=seed)
+
+
+def _check_full(w, plan=None, exact=False, **kw):
+    a, b = workloads.make_inputs(w)
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu, plan=plan, **kw)
+    c.check_guards()
+    ref = oracle_full(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu)
+    if exact:
+        assert_bit_exact(got, ref)
+    return assert_within_tolerance(got, ref, w.dtype)
+
+
+# ------------------------------------------------------------- ragged, all layouts --
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("ta,tb", list(itertools.product([False, True], repeat=2)))
+@pytest.mark.parametrize("relu", [False, True])
+def test_ragged_all_transposes_integer_bit_exact(dtype, ta, tb, relu):
+    dist = "int_small" if dtype == F16 else "int_unit"
+    _check_full(_w(300, 520, 200, dtype, ta, tb, relu, dist, 3), exact=True)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("ta,tb", list(itertools.product([False, True], repeat=2)))
+def test_ragged_all_transposes_random_tolerance(dtype, ta, tb):
+    _check_full(_w(333, 777, 515, dtype, ta, tb, True, "uniform", 4))
+
+
+# ------------------------------------------------------------------ every tiling --
+
+PLANS = [(bn, s) for bn, smax in ((64, 8), (128, 6), (256, 4)) for s in range(2, smax + 1)]
+
+
+@pytest.mark.parametrize("bn,stages", PLANS)
+def test_every_tiling_integer_bit_exact(bn, stages):
+    plan = tl.plan_for(0, 0, 0, 128, bn, 64, stages, raster_group=3)
+    w = _w(128 * 3 + 17, bn * 2 + 40, 64 * 9 + 7, F16, False, bn == 128, True, "int_small",
+           bn + stages)
+    _check_full(w, plan=plan, exact=True)
+
+
+@pytest.mark.parametrize("grid", [1, 2, 7])
+def test_persistent_ctas_cover_every_tile_once(grid):
+    # fewer CTAs than tiles: each CTA walks several tiles and both accumulator buffers
+    plan = tl.plan_for(0, 0, 0, 128, 128, 64, 4, raster_group=2, grid=grid)
+    _check_full(_w(700, 900, 300, BF16, False, True, False, "int_unit", 30 + grid),
+                plan=plan, exact=True)
+
+
+# ------------------------------------------------------------------- tiny shapes --
+
+TINY = [1, 2, 3, 7, 16, 17, 63, 64, 65, 127, 128, 129]
+
+
+@pytest.mark.parametrize("M,N,K", [(m, n, k) for m, n, k in itertools.product(TINY, TINY, TINY)
+                                   if (m * 7 + n * 3 + k) % 23 == 0][:40] + [(1, 1, 1), (129, 129, 129)])
+def test_tiny_shapes(M, N, K):
+    _check_full(_w(M, N, K, F16, False, False, True, "int_small", M * 1000 + N * 10 + K),
+                exact=True)
+    _check_full(_w(M, N, K, BF16, True, True, False, "uniform", M + N + K))
+
+
+def test_k_zero_fills_zero_and_empty_outputs_are_untouched():
+    a = torch.zeros(4, 1, dtype=torch.float16)
+    got, c = run_tl(a, torch.zeros(1, 5, dtype=torch.float16), 4, 5, 0, F16, relu=True,
+                    lda=1, ldb=5, ldc=8)
+    c.check_guards()
+    assert np.all(got == 0)
+    c = GuardedC(1, 1, 1, torch.float16)
+    for M, N in ((0, 5), (5, 0)):
+        assert tl.tl_gemm(0, 0, c.ptr, M, N, 3, 3, max(N, 1), max(N, 1), F16, 0, 0, 0,
+                          0) == tl.TL_OK
+    torch.cuda.synchronize()
+    assert np.all(c.host_bits() == 0x7E55)
+
+
+# ------------------------------------------------ pitches the TMA unit cannot use --
+
+def test_unaligned_lda_is_repacked():
+    # lda = K = 4100 fp16 is 8200 bytes: not a multiple of 16
+    _check_full(_w(300, 264, 4100, F16, False, False, True, "int_small", 40), exact=True)
+
+
+def test_offset_operands_and_unaligned_c():
+    w = _w(200, 136, 300, BF16, False, True, True, "int_unit", 41)
+    a, b = workloads.make_inputs(w)
+    ref = oracle_full(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu)
+    # A and B start 2 bytes past alignment, C has an odd leading dimension and offset
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu,
+                    a_off=1, b_off=3, ldc=139, c_off=65)
+    c.check_guards()
+    assert_bit_exact(got, ref)
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu,
+                    lda=305, ldb=301)
+    c.check_guards()
+    assert_bit_exact(got, ref)
+
+
+# ------------------------------------------------------------------ the workloads --
+
+SMALL = ["gemm_relu_256_f16", "gemm_relu_1024_f16_128x128x64s3"]
+LARGE = ["gemm_4096_bf16_tb", "gemm_8192_bf16_tb", "gemm_relu_3000x5000x4100_f16",
+         "gemm_m16_n8192_k8192_bf16", "gemm_m64_n8192_k8192_bf16", "gemm_m128_n8192_k8192_bf16"]
+
+
+def _workload_plan(w):
+    if w.plan is None:
+        return None
+    bm, bn, bk, st = w.plan
+    return tl.plan_for(0, 0, 0, bm, bn, bk, st)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workloads_full_output(name):
+    w = workloads.WORKLOADS[name]
+    _check_full(w, plan=_workload_plan(w))
+    _check_full(workloads.integer_variant(w), plan=_workload_plan(w), exact=True)
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_large_workloads_sampled(name):
+    w = workloads.WORKLOADS[name]
+    a, b = workloads.make_inputs(w)
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu,
+                    plan=_workload_plan(w))
+    c.check_guards()
+    rng = np.random.default_rng(7)
+    rows, cols = sample_indices(w.M, w.N, 6000, rng)
+    ref = oracle.gemm_entries(a, b, w.M, w.N, w.K, rows, cols, dtype=w.dtype,
+                              trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu)
+    stats = assert_within_tolerance(got[rows, cols], ref, w.dtype)
+    # a tighter bound that follows from the arithmetic: two roundings of nearly equal
+    # sums differ by at most one unit in the last place of the output format, plus the
+    # fp32 accumulation error; relative to the output's scale this stays near 2^-7
+    refv = oracle.decode(ref, w.dtype)
+    scale = np.abs(refv).max()
+    assert stats["max_abs"] <= scale * 2.0 ** -6, (stats, scale)
+
+
+@pytest.mark.parametrize("name", ["gemm_8192_bf16_tb", "gemm_relu_3000x5000x4100_f16",
+                                  "gemm_m16_n8192_k8192_bf16"])
+def test_large_workloads_integer_sampled_bit_exact(name):
+    w = workloads.integer_variant(workloads.WORKLOADS[name])
+    a, b = workloads.make_inputs(w)
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu)
+    c.check_guards()
+    rng = np.random.default_rng(8)
+    rows, cols = sample_indices(w.M, w.N, 4000, rng)
+    ref = oracle.gemm_entries(a, b, w.M, w.N, w.K, rows, cols, dtype=w.dtype,
+                              trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu)
+    assert_bit_exact(got[rows, cols], ref)
+
+
+# ------------------------------------------------------------- streams and graphs --
+
+def test_repeated_calls_are_deterministic_and_stream_ordered():
+    w = _w(640, 768, 1000, BF16, False, True, True, "normal_over_sqrtk", 50)
+    a, b = workloads.make_inputs(w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got1, _ = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu, stream=s)
+        got2, _ = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu, stream=s)
+    assert np.array_equal(got1, got2)
+
+
+def test_graph_capture_and_replay():
+    w = _w(384, 512, 640, F16, False, False, True, "int_small", 51)
+    a, b = workloads.make_inputs(w)
+    ad, bd = a.cuda(), b.cuda()
+    out = torch.empty(w.M, w.N, dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tl.gemm(ad, bd, relu=True, out=out)       # first call sets kernel attributes
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    out.fill_(0)
+    with torch.cuda.graph(g, stream=s):
+        tl.gemm(ad, bd, relu=True, out=out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    ref = oracle_full(a, b, w.M, w.N, w.K, w.dtype, False, False, True)
+    assert_bit_exact(out.cpu().view(torch.int16).numpy().view(np.uint16), ref)
+
+
+# ------------------------------------------------------------------------ errors --
+
+def test_host_pointer_is_rejected():
+    a = torch.zeros(64, 64, dtype=torch.float16)          # CPU memory
+    c = GuardedC(64, 64, 64, torch.float16)
+    st = tl.tl_gemm(a.data_ptr(), a.data_ptr(), c.ptr, 64, 64, 64, 64, 64, 64, F16, 0, 0, 0, 0)
+    assert st == tl.TL_ERR_DEVICE
+
+
+def test_alias_is_rejected_on_device_buffers():
+    buf = torch.zeros(4096, dtype=torch.float16, device="cuda")
+    p = buf.data_ptr()
+    # A = [p, p + 512), B = [p + 2048, p + 2560): C at p + 256 overlaps A, at p + 2304 B
+    st = tl.tl_gemm(p, p + 2048, p + 256, 16, 16, 16, 16, 16, 16, F16, 0, 0, 0, 0)
+    assert st == tl.TL_ERR_ALIAS
+    st = tl.tl_gemm(p, p + 2048, p + 2304, 16, 16, 16, 16, 16, 16, F16, 0, 0, 0, 0)
+    assert st == tl.TL_ERR_ALIAS
+
+
+def test_device_status_clean_after_all_calls():
+    st, word = tl.tl_device_status(reset=False)
+    assert st == tl.TL_OK, f"bounded wait gave up: {word:#x}"

@@ -1,0 +1,212 @@
+"""Python binding of the tl_gemm C ABI (include/tl_gemm.h).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA library
+``_build/libtl_gemm.so`` (built by ``tiled_gemm_gb300.build``).  PyTorch supplies
+device memory and the current stream.  If the library is missing, importing the
+binding raises: there is no CPU or PyTorch fallback.
+
+Names follow the C ABI: ``tl_gemm``, ``tl_gemm_with_plan``, ``tl_gemm_plan``,
+``tl_plan_complete``, ``tl_status_string``, ``tl_device_status``,
+``tl_set_wait_timeout_ns``, ``tl_version``.  ``gemm`` is the tensor-level call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+TL_F16 = 0
+TL_BF16 = 1
+TL_EPI_NONE = 0
+TL_EPI_RELU = 1
+
+STATUS_NAMES = ["TL_OK", "TL_ERR_INVALID_ARG", "TL_ERR_NULL_PTR", "TL_ERR_ALIGNMENT",
+                "TL_ERR_UNSUPPORTED", "TL_ERR_ALIAS", "TL_ERR_DEVICE", "TL_ERR_LAUNCH",
+                "TL_ERR_TIMEOUT"]
+TL_OK = 0
+TL_ERR_INVALID_ARG = 1
+TL_ERR_NULL_PTR = 2
+TL_ERR_ALIGNMENT = 3
+TL_ERR_UNSUPPORTED = 4
+TL_ERR_ALIAS = 5
+TL_ERR_DEVICE = 6
+TL_ERR_LAUNCH = 7
+TL_ERR_TIMEOUT = 8
+
+
+class TLError(RuntimeError):
+    def __init__(self, status: int, what: str = "tl_gemm"):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{what} failed: {name}")
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``tl_plan``."""
+    _fields_ = [
+        ("bm", ctypes.c_int32), ("bn", ctypes.c_int32), ("bk", ctypes.c_int32),
+        ("stages", ctypes.c_int32), ("raster_group", ctypes.c_int32), ("grid", ctypes.c_int32),
+        ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64), ("tiles", ctypes.c_int64),
+        ("k_blocks", ctypes.c_int64), ("ring_bytes", ctypes.c_int64),
+        ("smem_bytes", ctypes.c_int64), ("tmem_cols", ctypes.c_int32),
+        ("tx_bytes", ctypes.c_int32), ("repack_a", ctypes.c_int32),
+        ("repack_b", ctypes.c_int32), ("tma_store", ctypes.c_int32),
+        ("reserved", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"tl_gemm CUDA library not built ({LIB_PATH} is missing); run "
+            "`python tiled_gemm_gb300/build.py` or __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i64, ci, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+    lib.tl_gemm.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, p]
+    lib.tl_gemm.restype = ci
+    lib.tl_gemm_with_plan.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci, ci,
+                                      ctypes.POINTER(Plan), p]
+    lib.tl_gemm_with_plan.restype = ci
+    lib.tl_gemm_plan.argtypes = [i64, i64, i64, ci, ci, ci, ci, ctypes.POINTER(Plan)]
+    lib.tl_gemm_plan.restype = ci
+    lib.tl_plan_complete.argtypes = [i64, i64, i64, ci, ci, ci, ci, ctypes.POINTER(Plan)]
+    lib.tl_plan_complete.restype = ci
+    lib.tl_status_string.argtypes = [ci]
+    lib.tl_status_string.restype = ctypes.c_char_p
+    lib.tl_device_status.argtypes = [ci, ctypes.POINTER(u32)]
+    lib.tl_device_status.restype = ci
+    lib.tl_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.tl_set_wait_timeout_ns.restype = None
+    lib.tl_version.argtypes = []
+    lib.tl_version.restype = ci
+    return lib
+
+
+_lib = _load()
+LIBRARY = _lib
+
+
+# ---- C-ABI names ---------------------------------------------------------------
+
+def tl_gemm(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+            dtype: int, trans_a: int, trans_b: int, epilogue: int, stream: int) -> int:
+    """Raw call with integer device pointers and a raw stream handle; returns tl_status."""
+    return _lib.tl_gemm(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b, epilogue,
+                        stream)
+
+
+def tl_gemm_with_plan(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                      ldc: int, dtype: int, trans_a: int, trans_b: int, epilogue: int,
+                      plan: Plan, stream: int) -> int:
+    return _lib.tl_gemm_with_plan(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b,
+                                  epilogue, ctypes.byref(plan), stream)
+
+
+def tl_gemm_plan(M: int, N: int, K: int, dtype: int = TL_F16, trans_a: int = 0,
+                 trans_b: int = 0, num_sms: int = 0) -> Plan:
+    pl = Plan()
+    st = _lib.tl_gemm_plan(M, N, K, dtype, trans_a, trans_b, num_sms, ctypes.byref(pl))
+    if st != TL_OK:
+        raise TLError(st, "tl_gemm_plan")
+    return pl
+
+
+def tl_plan_complete(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
+                     dtype: int = TL_F16, trans_a: int = 0, trans_b: int = 0,
+                     num_sms: int = 0, raster_group: int = 16, grid: int = 0) -> Plan:
+    pl = Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid)
+    st = _lib.tl_plan_complete(M, N, K, dtype, trans_a, trans_b, num_sms, ctypes.byref(pl))
+    if st != TL_OK:
+        raise TLError(st, "tl_plan_complete")
+    return pl
+
+
+def tl_status_string(status: int) -> str:
+    return _lib.tl_status_string(status).decode()
+
+
+def tl_device_status(reset: bool = False) -> tuple[int, int]:
+    """(tl_status, raw status word) of the device-side bounded waits; synchronises."""
+    word = ctypes.c_uint32(0)
+    st = _lib.tl_device_status(1 if reset else 0, ctypes.byref(word))
+    return st, word.value
+
+
+def tl_set_wait_timeout_ns(ns: int) -> None:
+    _lib.tl_set_wait_timeout_ns(int(ns))
+
+
+def tl_version() -> int:
+    return _lib.tl_version()
+
+
+# ---- tensor-level call ------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return TL_F16
+    if t.dtype == torch.bfloat16:
+        return TL_BF16
+    raise TypeError(f"tl_gemm supports float16 and bfloat16, got {t.dtype}")
+
+
+def _ld(t, name: str) -> int:
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.stride(1) != 1 and t.size(1) > 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    return max(t.stride(0), t.size(1), 1)
+
+
+def gemm(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool = False,
+         out=None, plan: Plan | None = None, stream=None):
+    """C = epi(op(a) . op(b)) on the current CUDA device.
+
+    ``a`` is [M, K] (or [K, M] with ``trans_a``), ``b`` is [K, N] (or [N, K] with
+    ``trans_b``); both row-major with unit inner stride, same dtype (fp16/bf16),
+    on the current device.  ``out`` (optional) is [M, N] of that dtype, unit inner
+    stride.  Runs on ``stream`` (a torch.cuda.Stream) or the current stream.
+    """
+    torch = _torch()
+    if not (a.is_cuda and b.is_cuda):
+        raise ValueError("a and b must be CUDA tensors")
+    if a.dtype != b.dtype:
+        raise TypeError("a and b must have the same dtype")
+    dt = _dtype_code(a)
+    M, K = (a.size(1), a.size(0)) if trans_a else (a.size(0), a.size(1))
+    Kb, N = (b.size(1), b.size(0)) if trans_b else (b.size(0), b.size(1))
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if out is None:
+        out = torch.empty((M, N), dtype=a.dtype, device=a.device)
+    elif tuple(out.shape) != (M, N) or out.dtype != a.dtype:
+        raise ValueError("out has the wrong shape or dtype")
+    lda, ldb, ldc = _ld(a, "a"), _ld(b, "b"), _ld(out, "out")
+    s = stream if stream is not None else torch.cuda.current_stream(a.device)
+    handle = s.cuda_stream
+    epi = TL_EPI_RELU if relu else TL_EPI_NONE
+    if plan is None:
+        st = tl_gemm(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc, dt,
+                     int(trans_a), int(trans_b), epi, handle)
+    else:
+        st = tl_gemm_with_plan(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, lda, ldb,
+                               ldc, dt, int(trans_a), int(trans_b), epi, plan, handle)
+    if st != TL_OK:
+        raise TLError(st)
+    return out
+
+
+def plan_for(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
+             raster_group: int = 16, grid: int = 0) -> Plan:
+    """A plan with a fixed tiling, to pass as ``gemm(..., plan=...)``."""
+    return Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid)

@@ -1,0 +1,453 @@
+// gemm_kernel.cuh -- the persistent, warp-specialised tiled GEMM for sm_103a.
+//
+// C[M,N] = epi(op(A)[M,K] . op(B)[K,N]), fp16/bf16 operands, fp32 accumulation in
+// Tensor Memory, epi in {identity, ReLU}, round-to-nearest-even on the way out.
+//
+// The pages' quickstart kernel tiles C into BM x BN blocks, copies A and B tiles
+// global -> shared for each BK slice of K under a multi-stage software pipeline,
+// multiplies them into an fp32 accumulator and copies the accumulator back
+// ("TileLang: a tile language one level below Triton", section "first kernel:
+// GEMM", and its generated-code excerpt: a producer that only issues TMA loads and
+// a consumer that only issues MMAs, handing stages over through full/empty
+// mbarrier pairs).  This kernel keeps that structure and maps it onto sm_103a:
+//
+//   warp 0 (one thread)  TMA producer: for every (tile, k-block) waits for a free
+//                        ring slot, arms its "full" barrier with the stage's byte
+//                        count and issues the A and B tile loads.  Boxes that run
+//                        past the matrix edge are zero-filled by the TMA unit, so
+//                        partial tiles add exact zeros ("TileLang core primitives"
+//                        page, section 4.2: out-of-range reads give the safe value 0).
+//   warp 1 (one thread)  tcgen05 MMA issuer: waits for a full slot, issues BK/16
+//                        MMAs of 128 x BN x 16 into a Tensor Memory accumulator
+//                        (overwrite on the tile's first step: the pages' clear_accum
+//                        = (k == 0)), and commits the slot back to the producer.
+//                        After a tile's last k-block it commits the accumulator to
+//                        the epilogue ("NVIDIA backend codegen" page, sections 3.4
+//                        and 4.6.1).  Warp 1 also owns the Tensor Memory allocation.
+//   warps 2-5            epilogue: Tensor Memory -> registers (tcgen05.ld), ReLU
+//                        (max(x, 0), "TileLang core primitives" page, section 3.8),
+//                        cast with round-to-nearest-even, swizzled shared staging,
+//                        then TMA bulk stores that skip rows/columns outside C.
+//
+// The accumulator is double-buffered in Tensor Memory (2 x BN columns), so the
+// epilogue of one tile overlaps the main loop of the next.  CTAs are persistent:
+// CTA b handles tiles b, b + grid, b + 2*grid, ... of a grouped raster order
+// (each tile exactly once, "TileLang: from tile dataflow to controllable AI
+// kernels", section "concurrency correctness").
+//
+// Every wait is bounded: after p.timeout_ns a waiter records TL timeout status,
+// raises a CTA-wide abort flag, and every role unwinds -- the producer waits for
+// its issued loads, the MMA thread commits and waits for its issued MMAs, the
+// epilogue waits for its bulk stores, and warp 1 frees Tensor Memory -- so a
+// failure returns an error status instead of hanging the GPU.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace tl {
+
+constexpr int kBM = 128;              // MMA M: one accumulator row per TMEM lane
+constexpr int kBK = 64;               // 64 x 2 B = one 128-byte swizzle row
+constexpr int kUmmaK = 16;            // K of one kind::f16 MMA
+constexpr int kThreads = 192;         // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr int kChunk = 64;            // epilogue columns per staging chunk (128 B)
+constexpr uint32_t kAStageBytes = kBM * kBK * 2;           // 16 KB
+constexpr uint32_t kStagingBytes = kEpiWarps * 2 * 32 * 128;  // 2 x (32 rows x 128 B) per warp
+constexpr uint32_t kMNChunkBytes = 64 * 128;               // one 64(MN) x 64(K) box
+
+// Status word layout (device global, first timeout wins):
+//   bits 0-7  tl_status (8 = timeout), bits 8-15 wait site, bits 16-31 blockIdx.x
+enum WaitSite : uint32_t {
+  kSiteProducerEmpty = 1,
+  kSiteMmaTmemEmpty = 2,
+  kSiteMmaFull = 3,
+  kSiteEpiTmemFull = 4,
+  kSiteDrain = 5,
+};
+
+struct GemmParams {
+  int32_t M, N, K;
+  int32_t tiles_m, tiles_n, num_tiles, k_blocks;
+  int32_t stages;
+  int32_t raster_group;
+  int32_t trans_a, trans_b;
+  int32_t bf16;
+  int32_t relu;
+  int32_t tma_store;        // 1: TMA bulk store of C; 0: predicated st.global
+  uint32_t idesc;
+  void* C;                  // used when tma_store == 0
+  int64_t ldc;
+  uint32_t* status;         // device status word (never NULL)
+  uint64_t timeout_ns;
+};
+
+template <int BN>
+__host__ __device__ constexpr uint32_t b_stage_bytes() {
+  return static_cast<uint32_t>(BN) * kBK * 2;
+}
+
+// Barrier block: full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done,
+// then the 4-byte Tensor Memory base slot and the 4-byte abort flag.
+__host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
+  return static_cast<uint32_t>(8 * (2 * stages + 5) + 8);
+}
+
+template <int BN>
+__host__ __device__ constexpr uint32_t smem_bytes_for(int stages) {
+  // +1024: the dynamic shared memory base is rounded up to 1024 B in the kernel
+  return 1024u + stages * (kAStageBytes + b_stage_bytes<BN>()) + kStagingBytes +
+         barrier_bytes(stages);
+}
+
+// Grouped raster order: walk `group` tile-rows top to bottom, then the next column.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group, int& mb,
+                                            int& nb) {
+  const int per_group = group * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * group;
+  const int rows = min(tiles_m - first_m, group);
+  const int r = t - g * per_group;
+  mb = first_m + r % rows;
+  nb = r / rows;
+}
+
+__device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32_t* abort_flag,
+                                               uint32_t site) {
+  *abort_flag = 1u;
+  const uint32_t word = 8u | (site << 8) | (static_cast<uint32_t>(blockIdx.x & 0xFFFF) << 16);
+  atomicCAS(status, 0u, word);
+}
+
+// Bounded wait for the phase with parity `parity` of barrier `bar`.  Returns false
+// on timeout or, when `abort_flag` is not NULL, once another role of this CTA has
+// raised it.  Drain waits (in-flight copies and MMAs at exit) pass NULL: they must
+// see their operations land even while the CTA is unwinding.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t* abort_flag, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 31u) == 0u) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16, int relu) {
+  if (relu) {
+    lo = lo > 0.0f ? lo : 0.0f;   // max(x, 0); -0 and NaN give +0
+    hi = hi > 0.0f ? hi : 0.0f;
+  }
+  if (bf16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tl_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
+  static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
+  constexpr uint32_t kBStage = b_stage_bytes<BN>();
+  constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;   // power of two for BN in {64,128,256}
+  constexpr uint32_t kTxBytes = kAStageBytes + kBStage;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const int S = p.stages;
+
+  const uint32_t sA = base;
+  const uint32_t sB = sA + S * kAStageBytes;
+  const uint32_t sC = sB + S * kBStage;
+  const uint32_t sBar = sC + kStagingBytes;
+  auto full_bar = [&](int s) { return sBar + 8u * s; };
+  auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
+  auto tfull_bar = [&](int a) { return sBar + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return sBar + 8u * (2 * S + 2 + a); };
+  const uint32_t done_bar = sBar + 8u * (2 * S + 4);
+  const uint32_t slot = sBar + 8u * (2 * S + 5);
+  volatile uint32_t* const tmem_slot_ptr =
+      reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
+  volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);    // one producer arrive + the TMA byte count
+      mbar_init(empty_bar(s), 1);   // one tcgen05.commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);            // one tcgen05.commit per tile
+      mbar_init(tempty_bar(a), kEpiWarps);   // one arrive per epilogue warp
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+    if (p.tma_store) tma_prefetch_map(&tmap_c);
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot_ptr;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      uint32_t issued = 0, issued_parity = 0;   // per-stage bit masks (S <= 8)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
+        const int m0 = mb * kBM;
+        const int n0 = nb * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, kTxBytes);
+          const int k0 = kb * kBK;
+          const uint32_t a_dst = sA + stage * kAStageBytes;
+          const uint32_t b_dst = sB + stage * kBStage;
+          if (!p.trans_a) {
+            tma_load_2d(a_dst, &tmap_a, fb, k0, m0);                 // box {64 K, 128 M}
+          } else {
+#pragma unroll
+            for (int c = 0; c < kBM / 64; ++c)                       // boxes {64 M, 64 K}
+              tma_load_2d(a_dst + c * kMNChunkBytes, &tmap_a, fb, m0 + 64 * c, k0);
+          }
+          if (p.trans_b) {
+            tma_load_2d(b_dst, &tmap_b, fb, k0, n0);                 // box {64 K, BN N}
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)                        // boxes {64 N, 64 K}
+              tma_load_2d(b_dst + c * kMNChunkBytes, &tmap_b, fb, n0 + 64 * c, k0);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every issued load must have landed before the CTA may exit.  In a normal run
+      // the MMA thread consumed them all and these waits return at once.
+      for (int s = 0; s < S; ++s) {
+        if (issued & (1u << s)) {
+          if (!wait_bounded(full_bar(s), (issued_parity >> s) & 1u, nullptr, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteDrain);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      const uint32_t a_lbo = p.trans_a ? kMNChunkBytes : 16u;
+      const uint32_t b_lbo = p.trans_b ? 16u : kMNChunkBytes;
+      const uint64_t a_desc0 = smem_desc_sw128(sA, a_lbo, 1024u);
+      const uint64_t b_desc0 = smem_desc_sw128(sB, b_lbo, 1024u);
+      // per-MMA K advance, in 16-byte descriptor units: K-major moves 16 elements
+      // (32 B) along the swizzled row; M/N-major moves 16 rows of 128 B.
+      const uint64_t a_kstep = p.trans_a ? (16u * 128u) >> 4 : 32u >> 4;
+      const uint64_t b_kstep = p.trans_b ? 32u >> 4 : (16u * 128u) >> 4;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+          record_timeout(p.status, abort_flag, kSiteMmaTmemEmpty);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t a_desc = a_desc0 + ((stage * kAStageBytes) >> 4);
+          const uint64_t b_desc = b_desc0 + ((stage * kBStage) >> 4);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            mma_f16_ss(d_tmem, a_desc + k * a_kstep, b_desc + k * b_kstep, p.idesc,
+                       (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty_bar(stage));   // frees the slot once these MMAs have read it
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));       // accumulator complete -> epilogue
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // No MMA may still run when Tensor Memory is freed.
+      mma_commit(done_bar);
+      if (!wait_bounded(done_bar, 0, nullptr, p.timeout_ns)) {
+        record_timeout(p.status, abort_flag, kSiteDrain);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue --
+    const int q = warp & 3;                // Tensor Memory lane quadrant of this warp
+    const int ew = warp - 2;               // staging-buffer owner index
+    uint32_t acc = 0, acc_phase = 0;
+    uint32_t sbuf = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
+      const int m0 = mb * kBM;
+      const int n0 = nb * BN;
+      const bool ready = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / kChunk; ++c) {
+        uint32_t v[64];
+        tmem_load_32cols(t_row + c * kChunk, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_load_32cols(t_row + c * kChunk + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_load_wait();
+        if (c == BN / kChunk - 1) {
+          // the whole accumulator is in registers: hand the buffer back to the MMA
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        uint32_t packed[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          packed[j] = pack2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), p.bf16,
+                            p.relu);
+        }
+        if (p.tma_store) {
+          const uint32_t buf = sC + (ew * 2 + sbuf) * 4096u;
+          if (lane == 0) bulk_wait_group_read<1>();   // the store two chunks ago has read buf
+          __syncwarp();
+          // row `lane` of the 32 x 64 staging box, 128-byte swizzle: 16-byte chunk j
+          // lands at chunk j ^ (row % 8)
+          const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t dst = row_addr + ((j ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                         "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
+                         "r"(packed[4 * j + 3])
+                         : "memory");
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0 && m0 + q * 32 < p.M && n0 + c * kChunk < p.N) {
+            tma_store_2d(&tmap_c, buf, n0 + c * kChunk, m0 + q * 32);   // clipped at M, N
+          }
+          if (lane == 0) bulk_commit_group();   // (an empty group keeps the count uniform)
+          sbuf ^= 1u;
+        } else {
+          const int row = m0 + q * 32 + lane;
+          if (row < p.M) {
+            uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
+            const int col0 = n0 + c * kChunk;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = col0 + 2 * j;
+              if (col < p.N) crow[col] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
+              if (col + 1 < p.N) crow[col + 1] = static_cast<uint16_t>(packed[j] >> 16);
+            }
+          }
+        }
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (p.tma_store && lane == 0) bulk_wait_group<0>();
+  }
+
+  // ------------------------------------------------------------------ teardown --
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// C = epi(0) for K == 0 (no Tensor Memory involved).
+__global__ void tl_fill_zero_kernel(uint16_t* C, int64_t M, int64_t N, int64_t ldc) {
+  const int64_t total = M * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N;
+    const int64_t c = i - r * N;
+    C[r * ldc + c] = 0;
+  }
+}
+
+// Copy a rows x cols matrix of 2-byte elements from pitch `sp` to pitch `dp`
+// (elements), used to give an operand a 16-byte-aligned pitch for the TMA unit.
+__global__ void tl_repack_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                 int64_t rows, int64_t cols, int64_t sp, int64_t dp) {
+  const bool wide = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 7u) == 0 &&
+                    (sp & 3) == 0 && (dp & 3) == 0 && (cols & 3) == 0;
+  if (wide) {
+    const int64_t units = cols >> 2;   // 8-byte units per row
+    const int64_t total = rows * units;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t r = i / units;
+      const int64_t u = i - r * units;
+      const uint2 v = *reinterpret_cast<const uint2*>(src + r * sp + 4 * u);
+      *reinterpret_cast<uint2*>(dst + r * dp + 4 * u) = v;
+    }
+  } else {
+    const int64_t total = rows * cols;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t r = i / cols;
+      const int64_t c = i - r * cols;
+      dst[r * dp + c] = src[r * sp + c];
+    }
+  }
+}
+
+}  // namespace tl
