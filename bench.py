@@ -80,7 +80,7 @@ def is_hbm_bound(w: workloads.Workload, peaks: dict) -> bool:
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    """nvidia-smi clock/throttle samples every 50 ms while the timed region runs."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -97,7 +97,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -197,18 +197,33 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
         tl.gemm(a, b, trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, out=c, plan=plan,
                 stream=stream)
 
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
+            if i == args.warmup - 2:
+                w0.record(stream)
             step(i)
+        w1.record(stream)
     torch.cuda.synchronize()
     status, word = tl.tl_device_status(reset=True)
     if status != tl.TL_OK:
         raise RuntimeError(f"device-side wait gave up during warm-up: {word:#x}")
+    if args.steps <= 0:
+        # default: enough steps for a timed region of ~1.5 s, so that the clock samples
+        # taken every 50 ms fall inside it
+        step_ms = max(w0.elapsed_time(w1) / 2.0, 1e-3)
+        args.steps = int(min(200000, max(50, math.ceil(1500.0 / step_ms))))
+        if dist is not None:
+            t = torch.tensor([args.steps], dtype=torch.int64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            args.steps = int(t.item())
 
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n_ev = min(args.steps, 2000)          # per-launch durations of the first n_ev steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     if dist is not None:
@@ -217,9 +232,11 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
     t_start.record(stream)
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            ev_s[i].record(stream)
+            if i < n_ev:
+                ev_s[i].record(stream)
             step(args.warmup + i)
-            ev_e[i].record(stream)
+            if i < n_ev:
+                ev_e[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -290,7 +307,8 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps; 0 (default) sizes the timed region to ~1.5 s")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="tl", choices=["tl", "reference"])
@@ -317,6 +335,8 @@ def main():
         # The oracle on the host cores, rank 0 only: each step a bounded row slice.
         if rank != 0:
             return
+        if args.steps <= 0:
+            args.steps = 10
         a_cpu, b_cpu = workloads.make_inputs(w)
         budget = max(0.5, 150.0 / (args.steps + args.warmup))
         for _ in range(args.warmup):

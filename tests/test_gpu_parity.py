@@ -67,6 +67,14 @@ def test_every_tiling_integer_bit_exact(bn, stages):
     _check_full(w, plan=plan, exact=True)
 
 
+@pytest.mark.parametrize("l2_prefetch", [0, 1, 3, 5, 100])
+@pytest.mark.parametrize("ta,tb", [(False, False), (True, True)])
+def test_l2_prefetch_distances(l2_prefetch, ta, tb):
+    plan = tl.plan_for(0, 0, 0, 128, 128, 64, 3, raster_group=4, l2_prefetch=l2_prefetch)
+    _check_full(_w(400, 700, 64 * 11 + 9, F16, ta, tb, True, "int_small", 60 + l2_prefetch),
+                plan=plan, exact=True)
+
+
 @pytest.mark.parametrize("grid", [1, 2, 7])
 def test_persistent_ctas_cover_every_tile_once(grid):
     # fewer CTAs than tiles: each CTA walks several tiles and both accumulator buffers

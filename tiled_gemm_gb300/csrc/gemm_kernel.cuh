@@ -11,9 +11,10 @@
 // a consumer that only issues MMAs, handing stages over through full/empty
 // mbarrier pairs).  This kernel keeps that structure and maps it onto sm_103a:
 //
-//   warp 0 (one thread)  TMA producer: for every (tile, k-block) waits for a free
-//                        ring slot, arms its "full" barrier with the stage's byte
-//                        count and issues the A and B tile loads.  Boxes that run
+//   warps 0, 6, 7        TMA producers (one thread each): for every (tile, k-block)
+//                        wait for a free ring slot, arm its "full" barrier with
+//                        their share of the stage's bytes and issue their share of
+//                        the A and B boxes (dealt round-robin).  Boxes that run
 //                        past the matrix edge are zero-filled by the TMA unit, so
 //                        partial tiles add exact zeros ("TileLang core primitives"
 //                        page, section 4.2: out-of-range reads give the safe value 0).
@@ -54,7 +55,8 @@ namespace tl {
 constexpr int kBM = 128;              // MMA M: one accumulator row per TMEM lane
 constexpr int kBK = 64;               // 64 x 2 B = one 128-byte swizzle row
 constexpr int kUmmaK = 16;            // K of one kind::f16 MMA
-constexpr int kThreads = 192;         // 6 warps
+constexpr int kThreads = 256;         // 8 warps: producers 0, 6, 7; MMA 1; epilogue 2-5
+constexpr int kProducers = 3;
 constexpr int kEpiWarps = 4;
 constexpr int kChunk = 64;            // epilogue columns per staging chunk (128 B)
 constexpr uint32_t kAStageBytes = kBM * kBK * 2;           // 16 KB
@@ -80,6 +82,7 @@ struct GemmParams {
   int32_t bf16;
   int32_t relu;
   int32_t tma_store;        // 1: TMA bulk store of C; 0: predicated st.global
+  int32_t l2_prefetch;      // k-blocks the producer prefetches into L2 ahead of the ring
   uint32_t idesc;
   void* C;                  // used when tma_store == 0
   int64_t ldc;
@@ -142,6 +145,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait for long waits: the thread sleeps in the barrier (suspend hint) and
+// backs off between polls, so a warp waiting out a main loop does not compete for
+// issue slots or the shared-memory pipe with the producer and MMA threads.
+__device__ __forceinline__ bool wait_bounded_sleep(uint32_t bar, uint32_t parity,
+                                                   volatile uint32_t* abort_flag,
+                                                   uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+    __nanosleep(64);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16, int relu) {
   if (relu) {
     lo = lo > 0.0f ? lo : 0.0f;   // max(x, 0); -0 and NaN give +0
@@ -163,7 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
   constexpr uint32_t kBStage = b_stage_bytes<BN>();
   constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;   // power of two for BN in {64,128,256}
-  constexpr uint32_t kTxBytes = kAStageBytes + kBStage;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -188,9 +206,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // TMA boxes of one stage: A as one K-major box {64 K, 128 M} or two M-major boxes
+  // {64 M, 64 K}; B as one K-major box {64 K, BN N} or BN/64 N-major boxes {64 N, 64 K}.
+  const int n_a_boxes = p.trans_a ? kBM / 64 : 1;
+  const int n_boxes = n_a_boxes + (p.trans_b ? 1 : BN / 64);
+  // Wide tiles are bound by shared-memory bandwidth, not by TMA issue: one producer.
+  const int n_producers = BN >= 256 ? 1 : min(kProducers, n_boxes);
+  auto box_bytes = [&](int j) -> uint32_t {
+    if (j < n_a_boxes) return p.trans_a ? kMNChunkBytes : kAStageBytes;
+    return p.trans_b ? kBStage : kMNChunkBytes;
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);    // one producer arrive + the TMA byte count
+      mbar_init(full_bar(s), n_producers);   // one arrive per producer + the TMA bytes
       mbar_init(empty_bar(s), 1);   // one tcgen05.commit
     }
     for (int a = 0; a < 2; ++a) {
@@ -215,18 +244,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      uint32_t issued = 0, issued_parity = 0;   // per-stage bit masks (S <= 8)
+  if (warp == 0 || warp >= 6) {
+    // ----------------------------------------------------------- producers --
+    // Issuing a TMA copy occupies the issuing thread for ~100 cycles, about as long
+    // as the MMAs of a narrow k-block take, so the stage's boxes are dealt round-robin
+    // to up to kProducers threads in different warps; each arms the stage's "full"
+    // barrier with its own byte count.
+    const int pi = warp == 0 ? 0 : warp - 5;           // producer index 0..2
+    if (lane == 0 && pi < n_producers) {
+      uint32_t issued = 0, issued_parity = 0;          // per-stage bit masks (S <= 8)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      uint32_t my_bytes = 0;
+      for (int j = pi; j < n_boxes; j += n_producers) my_bytes += box_bytes(j);
+      // the j-th box of k-block kb of tile (m0, n0): its smem slot and coordinates
+      auto issue_box = [&](int j, int kb, int m0, int n0, uint32_t a_dst, uint32_t b_dst,
+                           uint32_t fb, bool prefetch_only) {
+        const int k0 = kb * kBK;
+        const CUtensorMap* map;
+        uint32_t dst;
+        int x, y;
+        if (j < n_a_boxes) {
+          map = &tmap_a;
+          if (!p.trans_a) { dst = a_dst; x = k0; y = m0; }                   // {64 K, 128 M}
+          else { dst = a_dst + j * kMNChunkBytes; x = m0 + 64 * j; y = k0; }  // {64 M, 64 K}
+        } else {
+          const int c = j - n_a_boxes;
+          map = &tmap_b;
+          if (p.trans_b) { dst = b_dst; x = k0; y = n0; }                    // {64 K, BN N}
+          else { dst = b_dst + c * kMNChunkBytes; x = n0 + 64 * c; y = k0; }  // {64 N, 64 K}
+        }
+        if (prefetch_only) tma_prefetch_l2_2d(map, x, y);
+        else tma_load_2d(dst, map, fb, x, y);
+      };
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
         const int m0 = mb * kBM;
         const int n0 = nb * BN;
+        // Optional L2 prefetch up to l2_prefetch k-blocks ahead, at most two k-blocks
+        // per iteration so the ring keeps filling first.
+        int pf_next = S;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteProducerEmpty);
@@ -234,29 +293,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, kTxBytes);
-          const int k0 = kb * kBK;
+          mbar_arrive_expect_tx(fb, my_bytes);
           const uint32_t a_dst = sA + stage * kAStageBytes;
           const uint32_t b_dst = sB + stage * kBStage;
-          if (!p.trans_a) {
-            tma_load_2d(a_dst, &tmap_a, fb, k0, m0);                 // box {64 K, 128 M}
-          } else {
-#pragma unroll
-            for (int c = 0; c < kBM / 64; ++c)                       // boxes {64 M, 64 K}
-              tma_load_2d(a_dst + c * kMNChunkBytes, &tmap_a, fb, m0 + 64 * c, k0);
-          }
-          if (p.trans_b) {
-            tma_load_2d(b_dst, &tmap_b, fb, k0, n0);                 // box {64 K, BN N}
-          } else {
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)                        // boxes {64 N, 64 K}
-              tma_load_2d(b_dst + c * kMNChunkBytes, &tmap_b, fb, n0 + 64 * c, k0);
-          }
+          for (int j = pi; j < n_boxes; j += n_producers)
+            issue_box(j, kb, m0, n0, a_dst, b_dst, fb, false);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
+          }
+          for (int n = 0; n < 2 && p.l2_prefetch > 0 && pf_next < p.k_blocks &&
+                          pf_next <= kb + p.l2_prefetch;
+               ++n, ++pf_next) {
+            for (int j = pi; j < n_boxes; j += n_producers)
+              issue_box(j, pf_next, m0, n0, 0, 0, 0, true);
           }
         }
       }
@@ -323,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_timeout(p.status, abort_flag, kSiteDrain);
       }
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------- epilogue --
     const int q = warp & 3;                // Tensor Memory lane quadrant of this warp
     const int ew = warp - 2;               // staging-buffer owner index
@@ -334,8 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
       const int m0 = mb * kBM;
       const int n0 = nb * BN;
-      const bool ready = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
-      if (!__all_sync(0xFFFFFFFFu, ready)) {
+      // one lane waits (sleeping), the warp follows its verdict
+      bool ready = true;
+      if (lane == 0) ready = wait_bounded_sleep(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
+      __syncwarp();
+      if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
         if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
         break;
       }
@@ -398,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (p.tma_store && lane == 0) bulk_wait_group<0>();
+    // the staging buffers must stay valid until the bulk stores have read them; the
+    // global writes themselves complete before the grid is reported finished
+    if (p.tma_store && lane == 0) bulk_wait_group_read<0>();
   }
 
   // ------------------------------------------------------------------ teardown --
