@@ -68,17 +68,20 @@ typedef enum {
  * GPU; tl_gemm_with_plan() runs a given plan.
  */
 typedef struct {
-  int32_t bm;            /* output rows per CTA tile (128)                          */
-  int32_t bn;            /* output columns per tile (64, 128 or 256)                */
-  int32_t bk;            /* K elements per pipeline stage (64: one 128-byte row)    */
+  int32_t bm;            /* output rows per tile: 128 (one CTA) or 256 (a CTA pair   */
+                         /* in a 2-CTA cluster sharing each MMA, 128 rows each)     */
+  int32_t bn;            /* output columns per tile (64, 128, 256; pairs 128, 256)  */
+  int32_t bk;            /* K elements per pipeline stage: 64 or 128 (one or two    */
+                         /* 128-byte swizzle rows per matrix row)                   */
   int32_t stages;        /* depth of the shared-memory ring                         */
   int32_t raster_group;  /* tile rows per L2 rasterisation group                    */
-  int32_t grid;          /* persistent CTAs launched (0 = one per SM, capped)       */
+  int32_t grid;          /* persistent CTAs launched (0 = one per SM or SM pair,    */
+                         /* capped by the tiles and by the resident clusters)       */
   int64_t tiles_m, tiles_n, tiles, k_blocks;
-  int64_t ring_bytes;    /* stages * (bm*bk + bn*bk) * 2                            */
+  int64_t ring_bytes;    /* per CTA: stages * (128*bk + (bn/cg)*bk) * 2, cg = bm/128 */
   int64_t smem_bytes;    /* dynamic shared memory per CTA (ring + staging + bars)   */
-  int32_t tmem_cols;     /* Tensor Memory columns allocated (2 accumulators)        */
-  int32_t tx_bytes;      /* bytes one stage's TMA loads deliver (full boxes)        */
+  int32_t tmem_cols;     /* Tensor Memory columns allocated per CTA (2 accumulators)*/
+  int32_t tx_bytes;      /* bytes one stage's TMA loads deliver to one CTA          */
   int32_t repack_a;      /* A is staged through a pitch-padded workspace            */
   int32_t repack_b;      /* B likewise                                              */
   int32_t tma_store;     /* C written by TMA bulk stores (else predicated stores)   */
@@ -129,8 +132,8 @@ tl_status tl_gemm_plan(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int tran
  * Fill the derived fields of `plan` (tiles, k-blocks, ring/smem bytes, TMEM
  * columns, tx bytes) from its bm/bn/bk/stages and the problem size.  Host only.
  * Returns TL_ERR_INVALID_ARG when the tiling is not one the kernel supports
- * (bm != 128, bn not in {64,128,256}, bk != 64, stages outside 2..8, or shared
- * memory above the per-CTA limit).
+ * (bm = 128 with bn in {64,128,256}, or bm = 256 with bn in {128,256}; bk = 64
+ * or 128; stages 2..8; shared memory within the per-CTA limit).
  */
 tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
                            int trans_b, int num_sms, tl_plan* plan);
@@ -161,8 +164,10 @@ const char* tl_status_string(tl_status status);
 tl_status tl_device_status(int reset, uint32_t* detail);
 
 /*
- * Limit of every device-side wait, in nanoseconds, for kernels enqueued after this
- * call (default 2e9).  Values are clamped to [1e5, 6e10].  Host only.
+ * Limit of every device-side wait for kernels enqueued after this call, in
+ * nanoseconds at an SM clock of 4 GHz (default 1e9): the kernels count 4 SM cycles
+ * per nanosecond, so at the GPU's real clock (about 2 GHz) a wait gives up after
+ * two to four times this value.  Clamped to [1e5, 6e10].  Host only.
  */
 void tl_set_wait_timeout_ns(uint64_t ns);
 

@@ -73,22 +73,28 @@ def test_plan_tiles_cover_the_output_exactly_once(M, N, K):
     assert p.tiles_n * p.bn >= N > (p.tiles_n - 1) * p.bn
     assert p.k_blocks * p.bk >= K > (p.k_blocks - 1) * p.bk
     assert p.tiles == p.tiles_m * p.tiles_n
-    assert 1 <= p.grid <= min(148, p.tiles)
+    cg = p.bm // 128                       # CTAs per tile
+    assert 1 <= p.grid <= cg * min(148 // cg, p.tiles) and p.grid % cg == 0
     assert p.smem_bytes <= 232448
     assert p.tmem_cols in (128, 256, 512)
-    assert p.tx_bytes == (p.bm + p.bn) * p.bk * 2
+    assert p.tx_bytes == (128 + p.bn // cg) * p.bk * 2
 
 
 def test_every_supported_tiling_fits_shared_memory_and_others_are_rejected():
-    for bn, max_stages in ((64, 8), (128, 6), (256, 4)):
+    for bm, bn, bk, max_stages in ((128, 64, 64, 8), (128, 128, 64, 6), (128, 256, 64, 4),
+                                   (256, 128, 64, 8), (256, 256, 64, 6), (128, 64, 128, 4),
+                                   (128, 128, 128, 3), (128, 256, 128, 2), (256, 128, 128, 4),
+                                   (256, 256, 128, 3)):
         for stages in range(2, max_stages + 1):
-            p = tl.tl_plan_complete(4096, 4096, 4096, 128, bn, 64, stages)
+            p = tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, stages)
             assert p.smem_bytes <= 232448
+            assert p.grid % (bm // 128) == 0
+            assert p.ring_bytes == stages * (128 * bk + (bn // (bm // 128)) * bk) * 2
         if max_stages < 8:
             with pytest.raises(tl.TLError):
-                tl.tl_plan_complete(4096, 4096, 4096, 128, bn, 64, max_stages + 1)
+                tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, max_stages + 1)
     for bad in ((64, 128, 64, 3), (128, 96, 64, 3), (128, 128, 32, 3), (128, 128, 64, 1),
-                (128, 128, 64, 9)):
+                (128, 128, 64, 9), (256, 64, 64, 4), (512, 256, 64, 4), (128, 128, 256, 2)):
         with pytest.raises(tl.TLError):
             tl.tl_plan_complete(1024, 1024, 1024, *bad)
 

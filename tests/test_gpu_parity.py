@@ -56,15 +56,39 @@ def test_ragged_all_transposes_random_tolerance(dtype, ta, tb):
 
 # ------------------------------------------------------------------ every tiling --
 
-PLANS = [(bn, s) for bn, smax in ((64, 8), (128, 6), (256, 4)) for s in range(2, smax + 1)]
+# (bm, bn, bk, max stages): bm = 256 is a CTA pair sharing each MMA (cta_group::2);
+# bk = 128 stages hold two 64-element K chunks
+TILINGS = ((128, 64, 64, 8), (128, 128, 64, 6), (128, 256, 64, 4), (256, 128, 64, 8),
+           (256, 256, 64, 6), (128, 64, 128, 4), (128, 128, 128, 3), (128, 256, 128, 2),
+           (256, 128, 128, 4), (256, 256, 128, 3))
+PLANS = [(bm, bn, bk, s) for bm, bn, bk, smax in TILINGS for s in range(2, smax + 1)]
 
 
-@pytest.mark.parametrize("bn,stages", PLANS)
-def test_every_tiling_integer_bit_exact(bn, stages):
-    plan = tl.plan_for(0, 0, 0, 128, bn, 64, stages, raster_group=3)
-    w = _w(128 * 3 + 17, bn * 2 + 40, 64 * 9 + 7, F16, False, bn == 128, True, "int_small",
-           bn + stages)
+@pytest.mark.parametrize("bm,bn,bk,stages", PLANS)
+def test_every_tiling_integer_bit_exact(bm, bn, bk, stages):
+    # ragged K and N: 2-D boxes with zero fill at the edges
+    plan = tl.plan_for(0, 0, 0, bm, bn, bk, stages, raster_group=3)
+    w = _w(bm * 3 + 17, bn * 2 + 40, 64 * 9 + 7, F16, stages % 2 == 1, bn == 128, True,
+           "int_small", bm + bn + stages)
     _check_full(w, plan=plan, exact=True)
+
+
+@pytest.mark.parametrize("bm,bn,bk,stages", [p for p in PLANS if p[3] in (2, 3)])
+@pytest.mark.parametrize("ta,tb", list(itertools.product([False, True], repeat=2)))
+def test_every_tiling_aligned_shapes_bit_exact(bm, bn, bk, stages, ta, tb):
+    # M, N, K multiples of 64: the 3-D one-box-per-stage maps are used where they apply
+    plan = tl.plan_for(0, 0, 0, bm, bn, bk, stages, raster_group=2)
+    w = _w(bm * 2 + 64, bn * 2 + 64, 64 * 11, BF16, ta, tb, False, "int_unit",
+           bm + bn + bk + stages + 2 * ta + tb)
+    _check_full(w, plan=plan, exact=True)
+
+
+@pytest.mark.parametrize("bn,bk", [(128, 64), (256, 64), (128, 128), (256, 128)])
+@pytest.mark.parametrize("ta,tb", list(itertools.product([False, True], repeat=2)))
+def test_cta_pairs_all_transposes_random(bn, bk, ta, tb):
+    plan = tl.plan_for(0, 0, 0, 256, bn, bk, 3, raster_group=2)
+    _check_full(_w(700, 900, 515, BF16, ta, tb, False, "uniform", 70 + bn + bk), plan=plan)
+    _check_full(_w(768, 1024, 640, BF16, ta, tb, False, "uniform", 71 + bn + bk), plan=plan)
 
 
 @pytest.mark.parametrize("l2_prefetch", [0, 1, 3, 5, 100])
@@ -75,10 +99,11 @@ def test_l2_prefetch_distances(l2_prefetch, ta, tb):
                 plan=plan, exact=True)
 
 
-@pytest.mark.parametrize("grid", [1, 2, 7])
-def test_persistent_ctas_cover_every_tile_once(grid):
-    # fewer CTAs than tiles: each CTA walks several tiles and both accumulator buffers
-    plan = tl.plan_for(0, 0, 0, 128, 128, 64, 4, raster_group=2, grid=grid)
+@pytest.mark.parametrize("bm,grid", [(128, 1), (128, 2), (128, 7), (256, 2), (256, 6)])
+def test_persistent_ctas_cover_every_tile_once(bm, grid):
+    # fewer CTAs than tiles: each CTA (pair) walks several tiles and both accumulator
+    # buffers
+    plan = tl.plan_for(0, 0, 0, bm, 128, 64, 4, raster_group=2, grid=grid)
     _check_full(_w(700, 900, 300, BF16, False, True, False, "int_unit", 30 + grid),
                 plan=plan, exact=True)
 

@@ -53,15 +53,13 @@
 namespace tl {
 
 constexpr int kBM = 128;              // MMA M: one accumulator row per TMEM lane
-constexpr int kBK = 64;               // 64 x 2 B = one 128-byte swizzle row
+constexpr int kChunkK = 64;           // 64 x 2 B = one 128-byte swizzle row
 constexpr int kUmmaK = 16;            // K of one kind::f16 MMA
 constexpr int kThreads = 256;         // 8 warps: producers 0, 6, 7; MMA 1; epilogue 2-5
 constexpr int kProducers = 3;
 constexpr int kEpiWarps = 4;
 constexpr int kChunk = 64;            // epilogue columns per staging chunk (128 B)
-constexpr uint32_t kAStageBytes = kBM * kBK * 2;           // 16 KB
 constexpr uint32_t kStagingBytes = kEpiWarps * 2 * 32 * 128;  // 2 x (32 rows x 128 B) per warp
-constexpr uint32_t kMNChunkBytes = 64 * 128;               // one 64(MN) x 64(K) box
 
 // Status word layout (device global, first timeout wins):
 //   bits 0-7  tl_status (8 = timeout), bits 8-15 wait site, bits 16-31 blockIdx.x
@@ -83,6 +81,8 @@ struct GemmParams {
   int32_t relu;
   int32_t tma_store;        // 1: TMA bulk store of C; 0: predicated st.global
   int32_t l2_prefetch;      // k-blocks the producer prefetches into L2 ahead of the ring
+  int32_t a3d, b3d;         // operand map is the 3-D view {64, rows, chunks} (one box
+                            // per stage) instead of 2-D boxes of one 64-chunk each
   uint32_t idesc;
   void* C;                  // used when tma_store == 0
   int64_t ldc;
@@ -90,9 +90,15 @@ struct GemmParams {
   uint64_t timeout_ns;
 };
 
-template <int BN>
+// Shared memory of one stage in one CTA: A is 128 rows x BK, B is BN/CG columns x BK.
+template <int BK>
+__host__ __device__ constexpr uint32_t a_stage_bytes() {
+  return static_cast<uint32_t>(kBM) * BK * 2;
+}
+
+template <int BN, int CG, int BK>
 __host__ __device__ constexpr uint32_t b_stage_bytes() {
-  return static_cast<uint32_t>(BN) * kBK * 2;
+  return static_cast<uint32_t>(BN / CG) * BK * 2;
 }
 
 // Barrier block: full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done,
@@ -101,10 +107,10 @@ __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
   return static_cast<uint32_t>(8 * (2 * stages + 5) + 8);
 }
 
-template <int BN>
+template <int BN, int CG, int BK>
 __host__ __device__ constexpr uint32_t smem_bytes_for(int stages) {
   // +1024: the dynamic shared memory base is rounded up to 1024 B in the kernel
-  return 1024u + stages * (kAStageBytes + b_stage_bytes<BN>()) + kStagingBytes +
+  return 1024u + stages * (a_stage_bytes<BK>() + b_stage_bytes<BN, CG, BK>()) + kStagingBytes +
          barrier_bytes(stages);
 }
 
@@ -127,20 +133,34 @@ __device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32
   atomicCAS(status, 0u, word);
 }
 
+// One poll of a barrier phase; cluster scope when the arrivals may come from the
+// peer CTA of a pair.
+template <bool kCluster>
+__device__ __forceinline__ bool poll(uint32_t bar, uint32_t parity) {
+  return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 // Bounded wait for the phase with parity `parity` of barrier `bar`.  Returns false
 // on timeout or, when `abort_flag` is not NULL, once another role of this CTA has
 // raised it.  Drain waits (in-flight copies and MMAs at exit) pass NULL: they must
 // see their operations land even while the CTA is unwinding.
+//
+// The limit is kept in SM cycles (%clock64 is cheap to read; a %globaltimer read in
+// the poll loop delayed the wake-up of the pipeline threads by hundreds of cycles):
+// 4 cycles per nanosecond of limit, so the wait lasts at least the limit for any SM
+// clock up to 4 GHz.
+template <bool kCluster>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile uint32_t* abort_flag, uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  if (poll<kCluster>(bar, parity)) return true;
+  const uint64_t t0 = clock_cycles();
+  const uint64_t limit = timeout_ns * 4u;
   uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll<kCluster>(bar, parity)) return true;
     if ((++spins & 31u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (global_timer_ns() - t0 > timeout_ns) return false;
+      if (clock_cycles() - t0 > limit) return false;
     }
   }
 }
@@ -148,15 +168,19 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 // Bounded wait for long waits: the thread sleeps in the barrier (suspend hint) and
 // backs off between polls, so a warp waiting out a main loop does not compete for
 // issue slots or the shared-memory pipe with the producer and MMA threads.
+template <bool kCluster>
 __device__ __forceinline__ bool wait_bounded_sleep(uint32_t bar, uint32_t parity,
                                                    volatile uint32_t* abort_flag,
                                                    uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  if (poll<kCluster>(bar, parity)) return true;
+  const uint64_t t0 = clock_cycles();
+  const uint64_t limit = timeout_ns * 4u;
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    const bool ok = kCluster ? mbar_try_wait_sleep_cluster(bar, parity, 20000u)
+                             : mbar_try_wait_sleep(bar, parity, 20000u);
+    if (ok) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > timeout_ns) return false;
+    if (clock_cycles() - t0 > limit) return false;
     __nanosleep(64);
   }
 }
@@ -174,14 +198,33 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16, int relu
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int BN>
+// CG = 1: one CTA computes a 128 x BN tile.  CG = 2: a cluster of two CTAs on an SM
+// pair computes a 256 x BN tile with cta_group::2 MMAs issued by the even CTA; CTA r
+// holds rows [128 r, 128 r + 128) of A and columns [r BN/2, (r + 1) BN/2) of B, and
+// receives accumulator rows [128 r, 128 r + 128) x all BN columns in its Tensor Memory.
+// Each CTA's TMA copies complete on the even CTA's "full" barrier; the MMA commits are
+// multicast to both CTAs' "empty", "tmem_full" and "done" barriers; both CTAs'
+// epilogue warps release the accumulator on the even CTA's "tmem_empty" barrier.
+//
+// BK (64 or 128) is the K depth of one pipeline stage: 1 or 2 chunks of 64 elements,
+// each chunk one 128-byte swizzle row per matrix row.  Deeper stages halve the TMA
+// instructions and barrier hand-offs per byte: on GB300 one TMA instruction costs
+// the issuing thread a few hundred cycles whatever its box size.
+template <int BN, int CG, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     tl_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
-  constexpr uint32_t kBStage = b_stage_bytes<BN>();
-  constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;   // power of two for BN in {64,128,256}
+  static_assert(CG == 1 || (CG == 2 && BN >= 128), "pairs need BN/2 >= 64");
+  constexpr bool kPair = CG == 2;
+  static_assert(BK == 64 || BK == 128, "BK must be 64 or 128");
+  constexpr int kBnCta = BN / CG;                          // B columns this CTA loads
+  constexpr int kKChunks = BK / kChunkK;                   // 64-element K chunks per stage
+  constexpr uint32_t kAStageBytes = a_stage_bytes<BK>();
+  constexpr uint32_t kBStage = b_stage_bytes<BN, CG, BK>();
+  constexpr uint32_t kMNChunkBytes = 128u * BK;            // one 64(MN) x BK(K) chunk
+  constexpr uint32_t kTmemCols = 2 * BN;                   // two accumulators, power of 2
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -205,26 +248,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // position in the CTA pair
+  const bool leader = rank == 0;
+  const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+  const int n_clusters = static_cast<int>(gridDim.x) / CG;
 
-  // TMA boxes of one stage: A as one K-major box {64 K, 128 M} or two M-major boxes
-  // {64 M, 64 K}; B as one K-major box {64 K, BN N} or BN/64 N-major boxes {64 N, 64 K}.
-  const int n_a_boxes = p.trans_a ? kBM / 64 : 1;
-  const int n_boxes = n_a_boxes + (p.trans_b ? 1 : BN / 64);
-  // Wide tiles are bound by shared-memory bandwidth, not by TMA issue: one producer.
+  // TMA boxes of one stage in this CTA.  A: K-major, one 2-D box {64 K, 128 M} per
+  // K chunk, or M-major, one 2-D box {64 M, BK K} per 64-row chunk of M; or, with a
+  // 3-D map, the whole stage in one box.  B likewise with BN/CG columns.
+  const int n_a_boxes = p.a3d ? 1 : (p.trans_a ? kBM / 64 : kKChunks);
+  const int n_b_boxes = p.b3d ? 1 : (p.trans_b ? kKChunks : kBnCta / 64);
+  const int n_boxes = n_a_boxes + n_b_boxes;
+  // Wide tiles issue few boxes per stage: one producer.
   const int n_producers = BN >= 256 ? 1 : min(kProducers, n_boxes);
   auto box_bytes = [&](int j) -> uint32_t {
-    if (j < n_a_boxes) return p.trans_a ? kMNChunkBytes : kAStageBytes;
-    return p.trans_b ? kBStage : kMNChunkBytes;
+    if (j < n_a_boxes) return kAStageBytes / n_a_boxes;
+    return kBStage / n_b_boxes;
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), n_producers);   // one arrive per producer + the TMA bytes
-      mbar_init(empty_bar(s), 1);   // one tcgen05.commit
+      mbar_init(full_bar(s), n_producers);   // the even CTA's producers arrive + TMA bytes
+      mbar_init(empty_bar(s), 1);            // one tcgen05.commit
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);            // one tcgen05.commit per tile
-      mbar_init(tempty_bar(a), kEpiWarps);   // one arrive per epilogue warp
+      mbar_init(tfull_bar(a), 1);                 // one tcgen05.commit per tile
+      mbar_init(tempty_bar(a), kEpiWarps * CG);   // every epilogue warp of the pair
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0u;
@@ -236,11 +285,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.tma_store) tma_prefetch_map(&tmap_c);
   }
   if (warp == 1) {
-    tmem_alloc(slot, kTmemCols);
-    tmem_relinquish_alloc_permit();
+    if constexpr (kPair) {
+      tmem_alloc_pair(slot, kTmemCols);
+      tmem_relinquish_alloc_permit_pair();
+    } else {
+      tmem_alloc(slot, kTmemCols);
+      tmem_relinquish_alloc_permit();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();   // the peer's barriers exist before any use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
@@ -249,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Issuing a TMA copy occupies the issuing thread for ~100 cycles, about as long
     // as the MMAs of a narrow k-block take, so the stage's boxes are dealt round-robin
     // to up to kProducers threads in different warps; each arms the stage's "full"
-    // barrier with its own byte count.
+    // barrier with its own byte count (times CG: the peer's matching boxes complete
+    // on the same barrier).
     const int pi = warp == 0 ? 0 : warp - 5;           // producer index 0..2
     if (lane == 0 && pi < n_producers) {
       uint32_t issued = 0, issued_parity = 0;          // per-stage bit masks (S <= 8)
@@ -258,48 +314,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t my_bytes = 0;
       for (int j = pi; j < n_boxes; j += n_producers) my_bytes += box_bytes(j);
-      // the j-th box of k-block kb of tile (m0, n0): its smem slot and coordinates
-      auto issue_box = [&](int j, int kb, int m0, int n0, uint32_t a_dst, uint32_t b_dst,
+      // the j-th box of k-block kb: its shared-memory slot and coordinates
+      auto issue_box = [&](int j, int kb, int m0, int nb0, uint32_t a_dst, uint32_t b_dst,
                            uint32_t fb, bool prefetch_only) {
-        const int k0 = kb * kBK;
+        const int k0 = kb * BK;
         const CUtensorMap* map;
         uint32_t dst;
-        int x, y;
+        int x, y, z = -1;                              // z >= 0: a 3-D box
         if (j < n_a_boxes) {
           map = &tmap_a;
-          if (!p.trans_a) { dst = a_dst; x = k0; y = m0; }                   // {64 K, 128 M}
-          else { dst = a_dst + j * kMNChunkBytes; x = m0 + 64 * j; y = k0; }  // {64 M, 64 K}
+          dst = a_dst;
+          if (p.a3d) {
+            if (!p.trans_a) { x = 0; y = m0; z = kb * kKChunks; }            // {64, 128, chunks}
+            else { x = 0; y = k0; z = m0 / 64; }                              // {64, BK, 2}
+          } else if (!p.trans_a) {
+            dst += j * (kBM * 128u); x = k0 + 64 * j; y = m0;                 // {64 K, 128 M}
+          } else {
+            dst += j * kMNChunkBytes; x = m0 + 64 * j; y = k0;                // {64 M, BK K}
+          }
         } else {
           const int c = j - n_a_boxes;
           map = &tmap_b;
-          if (p.trans_b) { dst = b_dst; x = k0; y = n0; }                    // {64 K, BN N}
-          else { dst = b_dst + c * kMNChunkBytes; x = n0 + 64 * c; y = k0; }  // {64 N, 64 K}
+          dst = b_dst;
+          if (p.b3d) {
+            if (p.trans_b) { x = 0; y = nb0; z = kb * kKChunks; }            // {64, BN/CG, chunks}
+            else { x = 0; y = k0; z = nb0 / 64; }                             // {64, BK, chunks}
+          } else if (p.trans_b) {
+            dst += c * (kBnCta * 128u); x = k0 + 64 * c; y = nb0;             // {64 K, BN/CG N}
+          } else {
+            dst += c * kMNChunkBytes; x = nb0 + 64 * c; y = k0;               // {64 N, BK K}
+          }
         }
-        if (prefetch_only) tma_prefetch_l2_2d(map, x, y);
-        else tma_load_2d(dst, map, fb, x, y);
+        if (z >= 0) {
+          if (prefetch_only) tma_prefetch_l2_3d(map, x, y, z);
+          else if (kPair) tma_load_3d_pair(dst, map, fb, x, y, z);
+          else tma_load_3d(dst, map, fb, x, y, z);
+        } else {
+          if (prefetch_only) tma_prefetch_l2_2d(map, x, y);
+          else if (kPair) tma_load_2d_pair(dst, map, fb, x, y);
+          else tma_load_2d(dst, map, fb, x, y);
+        }
       };
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
         int mb, nb;
         tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
-        const int m0 = mb * kBM;
-        const int n0 = nb * BN;
+        const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;    // this CTA's A rows
+        const int nb0 = nb * BN + static_cast<int>(rank) * kBnCta;      // this CTA's B columns
         // Optional L2 prefetch up to l2_prefetch k-blocks ahead, at most two k-blocks
         // per iteration so the ring keeps filling first.
         int pf_next = S;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+          if (!wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteProducerEmpty);
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, my_bytes);
+          const uint32_t local_full = full_bar(stage);
+          if (leader) mbar_arrive_expect_tx(local_full, my_bytes * CG);
+          const uint32_t fb = kPair ? mapa_shared(local_full, 0) : local_full;
           const uint32_t a_dst = sA + stage * kAStageBytes;
           const uint32_t b_dst = sB + stage * kBStage;
           for (int j = pi; j < n_boxes; j += n_producers)
-            issue_box(j, kb, m0, n0, a_dst, b_dst, fb, false);
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            issue_box(j, kb, m0, nb0, a_dst, b_dst, fb, false);
+          if (leader) {
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -308,15 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                           pf_next <= kb + p.l2_prefetch;
                ++n, ++pf_next) {
             for (int j = pi; j < n_boxes; j += n_producers)
-              issue_box(j, pf_next, m0, n0, 0, 0, 0, true);
+              issue_box(j, pf_next, m0, nb0, 0, 0, 0, true);
           }
         }
       }
       // Every issued load must have landed before the CTA may exit.  In a normal run
-      // the MMA thread consumed them all and these waits return at once.
+      // the MMA thread consumed them all and these waits return at once.  (The even
+      // CTA's barriers also cover the odd CTA's loads of the same stages.)
       for (int s = 0; s < S; ++s) {
         if (issued & (1u << s)) {
-          if (!wait_bounded(full_bar(s), (issued_parity >> s) & 1u, nullptr, p.timeout_ns)) {
+          if (!wait_bounded<kPair>(full_bar(s), (issued_parity >> s) & 1u, nullptr,
+                                   p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteDrain);
           }
         }
@@ -324,28 +406,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       const uint32_t a_lbo = p.trans_a ? kMNChunkBytes : 16u;
       const uint32_t b_lbo = p.trans_b ? 16u : kMNChunkBytes;
       const uint64_t a_desc0 = smem_desc_sw128(sA, a_lbo, 1024u);
       const uint64_t b_desc0 = smem_desc_sw128(sB, b_lbo, 1024u);
-      // per-MMA K advance, in 16-byte descriptor units: K-major moves 16 elements
-      // (32 B) along the swizzled row; M/N-major moves 16 rows of 128 B.
-      const uint64_t a_kstep = p.trans_a ? (16u * 128u) >> 4 : 32u >> 4;
-      const uint64_t b_kstep = p.trans_b ? 32u >> 4 : (16u * 128u) >> 4;
+      // Start-address offset of MMA k-step k (16 elements of K) within a stage, in
+      // 16-byte descriptor units.  K-major: chunk k/4 of the stage, then 32 B along
+      // the swizzled row; M/N-major: 16 rows of 128 B per step.
+      auto k_off = [&](bool mn_major, uint32_t rows, int k) -> uint64_t {
+        return mn_major ? (static_cast<uint64_t>(k) * 16u * 128u) >> 4
+                        : (static_cast<uint64_t>(k / 4) * rows * 128u + (k % 4) * 32u) >> 4;
+      };
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+      for (int t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
+        if (!wait_bounded<kPair>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           record_timeout(p.status, abort_flag, kSiteMmaTmemEmpty);
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
+          if (!wait_bounded<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteMmaFull);
             ok = false;
             break;
@@ -354,24 +439,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a_desc = a_desc0 + ((stage * kAStageBytes) >> 4);
           const uint64_t b_desc = b_desc0 + ((stage * kBStage) >> 4);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            mma_f16_ss(d_tmem, a_desc + k * a_kstep, b_desc + k * b_kstep, p.idesc,
-                       (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BK / kUmmaK; ++k) {
+            const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
+            const uint64_t ad = a_desc + k_off(p.trans_a, kBM, k);
+            const uint64_t bd = b_desc + k_off(!p.trans_b, kBnCta, k);
+            if constexpr (kPair) mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, acc_in);
+            else mma_f16_ss(d_tmem, ad, bd, p.idesc, acc_in);
           }
-          mma_commit(empty_bar(stage));   // frees the slot once these MMAs have read it
+          // frees the slot (in both CTAs) once these MMAs have read it
+          if constexpr (kPair) mma_commit_pair(empty_bar(stage), 0x3);
+          else mma_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));       // accumulator complete -> epilogue
+        // accumulator complete -> epilogue(s)
+        if constexpr (kPair) mma_commit_pair(tfull_bar(acc), 0x3);
+        else mma_commit(tfull_bar(acc));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // No MMA may still run when Tensor Memory is freed.
-      mma_commit(done_bar);
-      if (!wait_bounded(done_bar, 0, nullptr, p.timeout_ns)) {
+      if constexpr (kPair) mma_commit_pair(done_bar, 0x3);
+      else mma_commit(done_bar);
+      if (!wait_bounded<kPair>(done_bar, 0, nullptr, p.timeout_ns)) {
+        record_timeout(p.status, abort_flag, kSiteDrain);
+      }
+    } else if (lane == 0 && kPair) {
+      // odd CTA of a pair: its Tensor Memory is written by the even CTA's MMAs
+      if (!wait_bounded<true>(done_bar, 0, nullptr, p.timeout_ns)) {
         record_timeout(p.status, abort_flag, kSiteDrain);
       }
     }
@@ -381,14 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;               // staging-buffer owner index
     uint32_t acc = 0, acc_phase = 0;
     uint32_t sbuf = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    for (int t = cluster_id; t < p.num_tiles; t += n_clusters) {
       int mb, nb;
       tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
-      const int m0 = mb * kBM;
+      const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;
       const int n0 = nb * BN;
       // one lane waits (sleeping), the warp follows its verdict
       bool ready = true;
-      if (lane == 0) ready = wait_bounded_sleep(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
+      if (lane == 0)
+        ready = wait_bounded_sleep<kPair>(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       __syncwarp();
       if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
         if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
@@ -406,7 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the whole accumulator is in registers: hand the buffer back to the MMA
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          if (lane == 0) {
+            if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            else mbar_arrive(tempty_bar(acc));
+          }
         }
         uint32_t packed[32];
 #pragma unroll
@@ -460,12 +562,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------------ teardown --
   __syncwarp();
+  if constexpr (kPair) {
+    // After a timeout the odd CTA cannot observe its own loads landing (they complete
+    // on the even CTA's barriers): give any copy still in flight time to finish.
+    if (*abort_flag) {
+      const uint64_t t0 = clock_cycles();
+      while (clock_cycles() - t0 < 800000ull) __nanosleep(1000);   // >= 200 us
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();   // no CTA leaves while its peer may touch it
   tc_fence_after_sync();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 

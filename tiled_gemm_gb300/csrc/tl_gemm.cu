@@ -31,7 +31,7 @@ constexpr int kDefaultSms = 148;
 
 __device__ uint32_t g_status_word;           // bounded-wait outcome, see tl_device_status
 
-std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -46,6 +46,8 @@ struct DeviceState {
   int smem_optin = 0;                        // max dynamic shared memory per CTA
   uint32_t* status = nullptr;
   std::atomic<uint32_t> attr_done{0};        // bit i: smem attribute set for kernel i
+  int max_units[12] = {};                      // resident CTAs (pairs) per kernel
+  std::mutex mu;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -117,17 +119,30 @@ tl_status check_device_pointer(const void* p, int dev) {
   return TL_OK;
 }
 
+// bm = 128: one CTA per 128 x bn tile.  bm = 256: a CTA pair (cluster of 2,
+// cta_group::2 MMAs) per 256 x bn tile, each CTA holding half of B's columns.
 bool plan_supported(const tl_plan& pl) {
-  return pl.bm == 128 && (pl.bn == 64 || pl.bn == 128 || pl.bn == 256) && pl.bk == 64 &&
-         pl.stages >= 2 && pl.stages <= 8 && pl.raster_group >= 1 && pl.grid >= 0;
+  const bool bn_ok = (pl.bm == 128 && (pl.bn == 64 || pl.bn == 128 || pl.bn == 256)) ||
+                     (pl.bm == 256 && (pl.bn == 128 || pl.bn == 256));
+  return bn_ok && (pl.bk == 64 || pl.bk == 128) && pl.stages >= 2 && pl.stages <= 8 &&
+         pl.raster_group >= 1 && pl.grid >= 0;
 }
 
-uint32_t smem_for(int bn, int stages) {
-  switch (bn) {
-    case 64: return tl::smem_bytes_for<64>(stages);
-    case 128: return tl::smem_bytes_for<128>(stages);
-    default: return tl::smem_bytes_for<256>(stages);
+template <int BK>
+uint32_t smem_for_bk(int bm, int bn, int stages) {
+  if (bm == 256) {
+    return bn == 128 ? tl::smem_bytes_for<128, 2, BK>(stages)
+                     : tl::smem_bytes_for<256, 2, BK>(stages);
   }
+  switch (bn) {
+    case 64: return tl::smem_bytes_for<64, 1, BK>(stages);
+    case 128: return tl::smem_bytes_for<128, 1, BK>(stages);
+    default: return tl::smem_bytes_for<256, 1, BK>(stages);
+  }
+}
+
+uint32_t smem_for(int bm, int bn, int bk, int stages) {
+  return bk == 128 ? smem_for_bk<128>(bm, bn, stages) : smem_for_bk<64>(bm, bn, stages);
 }
 
 tl_status validate_common(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
@@ -154,17 +169,21 @@ int default_prefetch(const tl_plan& pl) {
 tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* pl) {
   if (!plan_supported(*pl)) return TL_ERR_INVALID_ARG;
   const int sms = num_sms > 0 ? num_sms : kDefaultSms;
+  const int cg = pl->bm / 128;                       // CTAs per tile
   pl->tiles_m = ceil_div(M, pl->bm);
   pl->tiles_n = ceil_div(N, pl->bn);
   pl->tiles = pl->tiles_m * pl->tiles_n;
   pl->k_blocks = ceil_div(K, pl->bk);
-  pl->ring_bytes = static_cast<int64_t>(pl->stages) * (pl->bm * pl->bk + pl->bn * pl->bk) * 2;
-  pl->smem_bytes = smem_for(pl->bn, pl->stages);
+  // per CTA: 128 rows of A and bn/cg columns of B per stage
+  pl->ring_bytes = static_cast<int64_t>(pl->stages) * (128 * pl->bk + (pl->bn / cg) * pl->bk) * 2;
+  pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages);
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
   pl->tmem_cols = 2 * pl->bn;
-  pl->tx_bytes = (pl->bm + pl->bn) * pl->bk * 2;
-  const int64_t want = pl->grid > 0 ? pl->grid : sms;
-  pl->grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(want, pl->tiles)));
+  pl->tx_bytes = (128 + pl->bn / cg) * pl->bk * 2;
+  // grid in CTAs: a multiple of cg, one tile (pair) per SM (pair) at most
+  const int64_t want_units = pl->grid > 0 ? std::max<int64_t>(1, pl->grid / cg) : sms / cg;
+  pl->grid = static_cast<int32_t>(
+      cg * std::max<int64_t>(1, std::min<int64_t>(want_units, pl->tiles)));
   if (pl->tiles > (int64_t{1} << 31) - 1) return TL_ERR_UNSUPPORTED;
   if (pl->l2_prefetch < 0) pl->l2_prefetch = default_prefetch(*pl);
   if (pl->l2_prefetch > 1024) return TL_ERR_INVALID_ARG;
@@ -176,24 +195,35 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* p
 // smaller MMAs).  Depth fills the shared memory left after the staging buffers.
 void choose_tiling(int64_t M, int64_t N, int64_t K, int sms, tl_plan* pl) {
   (void)K;
-  // Relative time of one tile per unit of K, measured on GB300: a 128-wide tile runs
-  // at ~0.64 of the per-SM rate of a 256-wide one, a 64-wide one lower still.
-  struct Cand { int bn, stages; double tile_cost; };
-  const Cand cands[] = {{256, 4, 2.0}, {128, 6, 1.56}, {64, 8, 1.2}};
+  // Relative time of one tile per unit of K.  Shared memory (~128 B/clk per SM)
+  // carries both the TMA writes and the MMA operand reads, so a 1-CTA 128 x N tile
+  // needs 128 (128 + N) / N bytes per MMA cycle: 192 for N = 256, 256 for N = 128;
+  // a CTA pair sharing B halves that to 128 (128 + N/2) / N.  The figures below are
+  // that model, calibrated on GB300 (a 1-CTA 128-wide tile runs at ~0.64 of the
+  // per-SM rate of a 256-wide one).
+  struct Cand { int bm, bn, bk, stages; double tile_cost; };
+  const Cand cands[] = {{256, 256, 128, 3, 128.0}, {256, 256, 64, 6, 135.0},
+                        {256, 128, 128, 4, 100.0}, {128, 256, 64, 4, 192.0},
+                        {128, 128, 64, 6, 150.0},  {128, 64, 128, 4, 110.0},
+                        {128, 64, 64, 8, 115.0}};
+  constexpr int kCands = sizeof(cands) / sizeof(cands[0]);
   double best = 0.0;
-  int pick = 0;
-  for (int i = 0; i < 3; ++i) {
-    const int64_t tiles = ceil_div(M, 128) * ceil_div(N, cands[i].bn);
-    const int64_t waves = ceil_div(tiles, sms);
+  int pick = -1;
+  for (int i = 0; i < kCands; ++i) {
+    if (cands[i].bk == 128 && K < 1024) continue;   // deep stages pay off on long K loops
+    const int cg = cands[i].bm / 128;
+    if (cg == 2 && M <= 128) continue;            // the odd CTA would hold no rows of A
+    const int64_t tiles = ceil_div(M, cands[i].bm) * ceil_div(N, cands[i].bn);
+    const int64_t waves = ceil_div(tiles, std::max(1, sms / cg));
     const double cost = static_cast<double>(waves) * cands[i].tile_cost;
-    if (i == 0 || cost < best - 1e-9) {
+    if (pick < 0 || cost < best - 1e-9) {
       best = cost;
       pick = i;
     }
   }
-  pl->bm = 128;
+  pl->bm = cands[pick].bm;
   pl->bn = cands[pick].bn;
-  pl->bk = 64;
+  pl->bk = cands[pick].bk;
   pl->stages = cands[pick].stages;
   pl->raster_group = 16;
   pl->grid = 0;
@@ -202,32 +232,72 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int sms, tl_plan* pl) {
 
 
 
-template <int BN>
+template <int BN, int CG, int BK>
 tl_status launch_bn(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
                     const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
                     cudaStream_t stream) {
-  constexpr uint32_t bit = BN == 64 ? 1u : (BN == 128 ? 2u : 4u);
-  auto kern = tl::tl_gemm_kernel<BN>;
-  if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             st->smem_optin) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TL_ERR_LAUNCH;
-    }
-    st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
-  }
+  constexpr int kIdx = (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) + 6 * (BK == 128);
+  constexpr uint32_t bit = 1u << kIdx;
+  auto kern = tl::tl_gemm_kernel<BN, CG, BK>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+  cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(tl::kThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem_bytes);
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
+  if (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
+    std::lock_guard<std::mutex> lock(st->mu);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             st->smem_optin) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TL_ERR_LAUNCH;
+    }
+    // Pairs the device can keep resident at this shared-memory size: the persistent
+    // grid must not exceed it (clusters sit on SM pairs within one GPC).
+    int clusters = st->sms / CG;
+    if (CG == 2) {
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
+        clusters = n;
+      } else {
+        (void)cudaGetLastError();
+      }
+    }
+    st->max_units[kIdx] = clusters;
+    st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int64_t units = std::min<int64_t>(pl.grid / CG, st->max_units[kIdx]);
+  cfg.gridDim = dim3(static_cast<unsigned>(CG * std::max<int64_t>(1, units)));
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_LAUNCH;
   }
   return TL_OK;
+}
+
+template <int BK>
+tl_status launch_tiling(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
+                        const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
+                        cudaStream_t stream) {
+  if (pl.bm == 256) {
+    return pl.bn == 128 ? launch_bn<128, 2, BK>(st, pl, ta, tb, tc, prm, stream)
+                        : launch_bn<256, 2, BK>(st, pl, ta, tb, tc, prm, stream);
+  }
+  switch (pl.bn) {
+    case 64: return launch_bn<64, 1, BK>(st, pl, ta, tb, tc, prm, stream);
+    case 128: return launch_bn<128, 1, BK>(st, pl, ta, tb, tc, prm, stream);
+    default: return launch_bn<256, 1, BK>(st, pl, ta, tb, tc, prm, stream);
+  }
 }
 
 bool encode_2d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inner, uint64_t outer,
@@ -241,6 +311,27 @@ bool encode_2d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inne
   const CUtensorMapDataType dt =
       dtype == TL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A row-major [rows][ld] matrix whose contiguous extent `inner` is a multiple of 64,
+// viewed as the 3-D tensor {64, rows, inner/64} (element (i, r, c) at r*ld + 64c + i)
+// so that one box {64, box_rows, box_chunks} fetches several 64-element chunks of
+// every row.  Exact (no reads past `inner`) because the chunks tile `inner` exactly.
+bool encode_chunked_3d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inner,
+                       uint64_t rows, uint64_t ld_elems, uint32_t box_rows,
+                       uint32_t box_chunks) {
+  if (inner % 64 != 0) return false;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {64, rows, inner / 64};
+  const cuuint64_t strides[2] = {ld_elems * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == TL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -341,13 +432,30 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   }
   const bool tma_store = tma_ok(C, ldc);
 
+  // Operand maps.  One box per stage (a 3-D view) when the operand's contiguous extent
+  // is a multiple of 64 and the stage spans several 64-element chunks; otherwise 2-D
+  // boxes of one chunk each, whose out-of-range parts the TMA unit fills with zeros.
   CUtensorMap ta, tb, tc;
   std::memset(&tc, 0, sizeof(tc));
+  const int cg = pl.bm / 128;
+  const uint32_t bn_cta = static_cast<uint32_t>(pl.bn / cg);
+  const uint32_t kchunks = static_cast<uint32_t>(pl.bk / 64);
   bool enc_ok = true;
-  if (!trans_a) enc_ok &= encode_2d(&ta, dtype, a_use, K, M, lda_w, 64, 128);
-  else enc_ok &= encode_2d(&ta, dtype, a_use, M, K, lda_w, 64, 64);
-  if (trans_b) enc_ok &= encode_2d(&tb, dtype, b_use, K, N, ldb_w, 64, pl.bn);
-  else enc_ok &= encode_2d(&tb, dtype, b_use, N, K, ldb_w, 64, 64);
+  bool a3d = false, b3d = false;
+  if (!trans_a) {
+    a3d = kchunks > 1 && encode_chunked_3d(&ta, dtype, a_use, K, M, lda_w, 128, kchunks);
+    if (!a3d) enc_ok &= encode_2d(&ta, dtype, a_use, K, M, lda_w, 64, 128);
+  } else {
+    a3d = encode_chunked_3d(&ta, dtype, a_use, M, K, lda_w, pl.bk, 2);
+    if (!a3d) enc_ok &= encode_2d(&ta, dtype, a_use, M, K, lda_w, 64, pl.bk);
+  }
+  if (trans_b) {
+    b3d = kchunks > 1 && encode_chunked_3d(&tb, dtype, b_use, K, N, ldb_w, bn_cta, kchunks);
+    if (!b3d) enc_ok &= encode_2d(&tb, dtype, b_use, K, N, ldb_w, 64, bn_cta);
+  } else {
+    b3d = bn_cta > 64 && encode_chunked_3d(&tb, dtype, b_use, N, K, ldb_w, pl.bk, bn_cta / 64);
+    if (!b3d) enc_ok &= encode_2d(&tb, dtype, b_use, N, K, ldb_w, 64, pl.bk);
+  }
   if (tma_store) enc_ok &= encode_2d(&tc, dtype, C, N, M, ldc, 64, 32);
   if (!enc_ok) {
     if (ws) (void)cudaFreeAsync(ws, stream);
@@ -371,18 +479,17 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
   prm.tma_store = tma_store ? 1 : 0;
   prm.l2_prefetch = pl.l2_prefetch;
-  prm.idesc = tl::mma_idesc_f16(prm.bf16, trans_a ? 1u : 0u, trans_b ? 0u : 1u, 128u,
-                                static_cast<uint32_t>(pl.bn));
+  prm.a3d = a3d ? 1 : 0;
+  prm.b3d = b3d ? 1 : 0;
+  prm.idesc = tl::mma_idesc_f16(prm.bf16, trans_a ? 1u : 0u, trans_b ? 0u : 1u,
+                                static_cast<uint32_t>(pl.bm), static_cast<uint32_t>(pl.bn));
   prm.C = C;
   prm.ldc = ldc;
   prm.status = st->status;
   prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
 
-  switch (pl.bn) {
-    case 64: s = launch_bn<64>(st, pl, ta, tb, tc, prm, stream); break;
-    case 128: s = launch_bn<128>(st, pl, ta, tb, tc, prm, stream); break;
-    default: s = launch_bn<256>(st, pl, ta, tb, tc, prm, stream); break;
-  }
+  s = pl.bk == 128 ? launch_tiling<128>(st, pl, ta, tb, tc, prm, stream)
+                   : launch_tiling<64>(st, pl, ta, tb, tc, prm, stream);
   if (ws) {
     if (cudaFreeAsync(ws, stream) != cudaSuccess) {
       (void)cudaGetLastError();
