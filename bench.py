@@ -74,6 +74,21 @@ def load_traffic(workload: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Throughput of the whole job: every rank ran `steps` steps; the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
 def is_hbm_bound(w: workloads.Workload, peaks: dict) -> bool:
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     return w.flops / w.bytes_moved < ridge
@@ -214,10 +229,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
         # taken every 50 ms fall inside it
         step_ms = max(w0.elapsed_time(w1) / 2.0, 1e-3)
         args.steps = int(min(200000, max(50, math.ceil(1500.0 / step_ms))))
-        if dist is not None:
-            t = torch.tensor([args.steps], dtype=torch.int64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            args.steps = int(t.item())
+        args.steps = int(max_over_ranks(float(args.steps), dist, dev))
 
     # The timed steps run as CUDA-graph replays of consecutive tl_gemm calls (one call
     # per step, inputs rotating as in eager mode), so host-side launch cost does not
@@ -263,11 +275,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
     if status != tl.TL_OK:
         raise RuntimeError(f"device-side wait gave up in the timed region: {word:#x}")
 
-    max_ms = total_ms
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = max_over_ranks(total_ms, dist, dev)
 
     # ---- end to end through the public API with host buffers --------------------
     e2e = None
@@ -300,12 +308,8 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
                 e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(w.flops * e_steps * world / (e_ms * 1e-3) / 1e12, 3),
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        e2e = {"value": round(whole_job_tflops(w.flops, e_steps, world, e_ms), 3),
                "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(a_cpu.numel() * 2 + b_cpu.numel() * 2),
                "d2h_bytes_per_step": int(w.M * w.N * 2),
@@ -399,7 +403,7 @@ def main():
 
     res = run_tl(args, w, rank, world, dist)
     total_ms = res["total_ms"]
-    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(w.flops, args.steps, world, total_ms)
     avg_launch_ms = total_ms / args.steps        # back-to-back launches in the graph
     hbm = is_hbm_bound(w, peaks)
     if hbm:
