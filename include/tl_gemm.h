@@ -150,6 +150,43 @@ tl_status tl_gemm_with_plan(const void* A, const void* B, void* C, int64_t M, in
                             int trans_a, int trans_b, tl_epilogue epilogue,
                             const tl_plan* plan, tl_stream_t stream);
 
+/*
+ * tl_gemm() for callers that cannot allocate device memory.  (This entry point has
+ * no counterpart on the pages the GEMM is described on; it is a property of this
+ * library's C ABI.)
+ *
+ * Who needs it: tl_gemm() takes a temporary buffer from the stream-ordered
+ * allocator when A or B has a base or leading dimension the tensor-memory-access
+ * unit cannot address (not 16-byte aligned) and must first be copied with a padded
+ * pitch.  Some callers cannot allow that: a framework that owns all device memory
+ * through its own pool and must not see a second allocator fragment or exceed its
+ * budget; a serving process that has reserved nearly all HBM for its caches, where
+ * any extra allocation fails; a real-time loop that must not allocate after start-up.
+ * tl_gemm_noalloc() calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Instead it copies such operands into one fixed scratch array of
+ * tl_gemm_noalloc_scratch_bytes() bytes (32 MiB) that the library defines as device
+ * global memory: every GPU that loads the library holds it until the process exits.
+ *   - Same arguments, semantics and errors as tl_gemm(), plus TL_ERR_UNSUPPORTED
+ *     (returned before anything is enqueued) when the operands that need a copy do
+ *     not fit the array: rows * (pitch rounded up to 8 elements) * 2 bytes for A,
+ *     rounded up to 256 bytes, plus the same for B, must not exceed 32 MiB.
+ *     Operands that need no copy use no scratch and have no size limit.
+ *   - The first call on each device (that passes the argument checks) performs a
+ *     one-time set-up: it looks up the array's device address with that device
+ *     current.  Make that first call before any stream capture.
+ *   - Every call shares the one array, and it keeps whatever the last call left in
+ *     it (nothing read from it depends on that).  Calls whose work overlaps on the
+ *     GPU (different streams, or host threads enqueueing concurrently) race on the
+ *     array: serialise them, e.g. keep them on one stream.
+ */
+tl_status tl_gemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                          int64_t K, int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype,
+                          int trans_a, int trans_b, tl_epilogue epilogue, tl_stream_t stream);
+
+/* Size in bytes of the scratch array tl_gemm_noalloc() uses (33554432). */
+int64_t tl_gemm_noalloc_scratch_bytes(void);
+
 /* Static, NUL-terminated name of a status code ("TL_OK", ...). */
 const char* tl_status_string(tl_status status);
 

@@ -5,8 +5,8 @@ Argument marshalling only: every step of the GEMM runs in the CUDA library
 device memory and the current stream.  If the library is missing, importing the
 binding raises: there is no CPU or PyTorch fallback.
 
-Names follow the C ABI: ``tl_gemm``, ``tl_gemm_with_plan``, ``tl_gemm_plan``,
-``tl_plan_complete``, ``tl_status_string``, ``tl_device_status``,
+Names follow the C ABI: ``tl_gemm``, ``tl_gemm_with_plan``, ``tl_gemm_noalloc``,
+``tl_gemm_plan``, ``tl_plan_complete``, ``tl_status_string``, ``tl_device_status``,
 ``tl_set_wait_timeout_ns``, ``tl_version``.  ``gemm`` is the tensor-level call.
 """
 from __future__ import annotations
@@ -75,6 +75,10 @@ def _load() -> ctypes.CDLL:
     lib.tl_gemm_plan.restype = ci
     lib.tl_plan_complete.argtypes = [i64, i64, i64, ci, ci, ci, ci, ctypes.POINTER(Plan)]
     lib.tl_plan_complete.restype = ci
+    lib.tl_gemm_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, p]
+    lib.tl_gemm_noalloc.restype = ci
+    lib.tl_gemm_noalloc_scratch_bytes.argtypes = []
+    lib.tl_gemm_noalloc_scratch_bytes.restype = i64
     lib.tl_status_string.argtypes = [ci]
     lib.tl_status_string.restype = ctypes.c_char_p
     lib.tl_device_status.argtypes = [ci, ctypes.POINTER(u32)]
@@ -104,6 +108,20 @@ def tl_gemm_with_plan(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, 
                       plan: Plan, stream: int) -> int:
     return _lib.tl_gemm_with_plan(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b,
                                   epilogue, ctypes.byref(plan), stream)
+
+
+def tl_gemm_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                    ldc: int, dtype: int, trans_a: int, trans_b: int, epilogue: int,
+                    stream: int) -> int:
+    """tl_gemm for callers that cannot allocate device memory: operands that need a
+    padded copy go through the library's fixed 32 MiB device scratch array instead of
+    the stream-ordered allocator (see include/tl_gemm.h).  Returns tl_status."""
+    return _lib.tl_gemm_noalloc(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b,
+                                epilogue, stream)
+
+
+def tl_gemm_noalloc_scratch_bytes() -> int:
+    return _lib.tl_gemm_noalloc_scratch_bytes()
 
 
 def tl_gemm_plan(M: int, N: int, K: int, dtype: int = TL_F16, trans_a: int = 0,

@@ -340,9 +340,36 @@ int launch_blocks_for(int64_t elems) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(elems, 256 * 4), 4096)));
 }
 
+// ---- scratch for tl_gemm_noalloc -------------------------------------------------
+// Callers that cannot allocate get the repack workspace from this fixed array instead
+// of the stream-ordered allocator.  It exists on every device that loads the library,
+// for the life of the process.  Host code must not use the array's name as a device
+// address: its device address comes from cudaGetSymbolAddress, taken once per device
+// with that device current.
+constexpr int64_t kNoAllocScratchBytes = int64_t{32} << 20;   // 32 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocScratch {
+  std::once_flag once;
+  void* ptr = nullptr;
+};
+NoAllocScratch g_noalloc[kMaxDevices];
+
+void* noalloc_scratch(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  NoAllocScratch& e = g_noalloc[dev];
+  std::call_once(e.once, [&e] {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) e.ptr = p;
+    else (void)cudaGetLastError();
+  });
+  return e.ptr;
+}
+
 tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
               int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype, int trans_a, int trans_b,
-              tl_epilogue epilogue, const tl_plan* forced, cudaStream_t stream) {
+              tl_epilogue epilogue, const tl_plan* forced, cudaStream_t stream,
+              bool no_alloc = false) {
   tl_status s = validate_common(M, N, K, dtype, trans_a, trans_b);
   if (s != TL_OK) return s;
   if (epilogue != TL_EPI_NONE && epilogue != TL_EPI_RELU) return TL_ERR_INVALID_ARG;
@@ -367,6 +394,8 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   DeviceState* st = device_state(&dev);
   if (st == nullptr) return TL_ERR_DEVICE;
   if (!st->sm103) return TL_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (no_alloc && (scratch = noalloc_scratch(dev)) == nullptr) return TL_ERR_DEVICE;
   if ((s = check_device_pointer(C, dev)) != TL_OK) return s;
   if (K > 0) {
     if ((s = check_device_pointer(A, dev)) != TL_OK) return s;
@@ -407,11 +436,17 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   const void* b_use = B;
   if (ws_a + ws_b > 0) {
     const int64_t ws_a_rounded = ceil_div(ws_a, 256) * 256;
-    if (cudaMallocAsync(&ws, static_cast<size_t>(ws_a_rounded + ws_b), stream) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TL_ERR_LAUNCH;
+    uint8_t* w = nullptr;
+    if (no_alloc) {
+      if (ws_a_rounded + ws_b > kNoAllocScratchBytes) return TL_ERR_UNSUPPORTED;
+      w = static_cast<uint8_t*>(scratch);
+    } else {
+      if (cudaMallocAsync(&ws, static_cast<size_t>(ws_a_rounded + ws_b), stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TL_ERR_LAUNCH;
+      }
+      w = static_cast<uint8_t*>(ws);
     }
-    uint8_t* w = static_cast<uint8_t*>(ws);
     if (repack_a) {
       tl::tl_repack_kernel<<<launch_blocks_for(a_rows * a_cols), 256, 0, stream>>>(
           static_cast<const uint16_t*>(A), reinterpret_cast<uint16_t*>(w), a_rows, a_cols, lda,
@@ -426,7 +461,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
       b_use = wb;
     }
     if (cudaGetLastError() != cudaSuccess) {
-      (void)cudaFreeAsync(ws, stream);
+      if (ws) (void)cudaFreeAsync(ws, stream);
       return TL_ERR_LAUNCH;
     }
   }
@@ -541,6 +576,15 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
   plan->l2_prefetch = pf;
   return complete_plan(M, N, K, num_sms, plan);
 }
+
+tl_status tl_gemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                          int64_t K, int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype,
+                          int trans_a, int trans_b, tl_epilogue epilogue, tl_stream_t stream) {
+  return run(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b, epilogue, nullptr,
+             reinterpret_cast<cudaStream_t>(stream), /*no_alloc=*/true);
+}
+
+int64_t tl_gemm_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 const char* tl_status_string(tl_status status) {
   switch (status) {
