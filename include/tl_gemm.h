@@ -86,6 +86,9 @@ typedef struct {
   int32_t repack_b;      /* B likewise                                              */
   int32_t tma_store;     /* C written by TMA bulk stores (else predicated stores)   */
   int32_t l2_prefetch;   /* k-blocks prefetched into L2 ahead of the ring (0 = off) */
+  int32_t producers;     /* TMA producer threads taking turns by stage (1..3, at    */
+                         /* most `stages`; 0 = default)                             */
+  int32_t reserved;      /* zero                                                    */
   int64_t workspace_bytes; /* bytes of the stream-ordered repack workspace          */
 } tl_plan;
 
@@ -139,9 +142,9 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
                            int trans_b, int num_sms, tl_plan* plan);
 
 /*
- * tl_gemm() with an explicit plan (bm, bn, bk, stages, raster_group, grid and
- * l2_prefetch are read; the rest is recomputed; l2_prefetch < 0 selects the
- * default for the problem).  Used to run a workload at a fixed tiling, e.g. the
+ * tl_gemm() with an explicit plan (bm, bn, bk, stages, raster_group, grid,
+ * l2_prefetch and producers are read; the rest is recomputed; l2_prefetch < 0 and
+ * producers <= 0 select the defaults for the problem).  Used to run a workload at a fixed tiling, e.g. the
  * pages' quickstart 128x128x64 with 3 stages.  Same arguments and errors as
  * tl_gemm(), plus TL_ERR_INVALID_ARG for an unsupported plan.
  */

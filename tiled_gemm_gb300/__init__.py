@@ -52,11 +52,12 @@ class Plan(ctypes.Structure):
         ("smem_bytes", ctypes.c_int64), ("tmem_cols", ctypes.c_int32),
         ("tx_bytes", ctypes.c_int32), ("repack_a", ctypes.c_int32),
         ("repack_b", ctypes.c_int32), ("tma_store", ctypes.c_int32),
-        ("l2_prefetch", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("l2_prefetch", ctypes.c_int32), ("producers", ctypes.c_int32),
+        ("reserved", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
-        return {name: getattr(self, name) for name, _ in self._fields_}
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
 
 
 def _load() -> ctypes.CDLL:
@@ -136,9 +137,9 @@ def tl_gemm_plan(M: int, N: int, K: int, dtype: int = TL_F16, trans_a: int = 0,
 def tl_plan_complete(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
                      dtype: int = TL_F16, trans_a: int = 0, trans_b: int = 0,
                      num_sms: int = 0, raster_group: int = 16, grid: int = 0,
-                     l2_prefetch: int = -1) -> Plan:
+                     l2_prefetch: int = -1, producers: int = 0) -> Plan:
     pl = Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
-              l2_prefetch=l2_prefetch)
+              l2_prefetch=l2_prefetch, producers=producers)
     st = _lib.tl_plan_complete(M, N, K, dtype, trans_a, trans_b, num_sms, ctypes.byref(pl))
     if st != TL_OK:
         raise TLError(st, "tl_plan_complete")
@@ -227,8 +228,9 @@ def gemm(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool = Fal
 
 
 def plan_for(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
-             raster_group: int = 16, grid: int = 0, l2_prefetch: int = -1) -> Plan:
-    """A plan with a fixed tiling, to pass as ``gemm(..., plan=...)``; l2_prefetch < 0
-    takes the library's default for the problem."""
+             raster_group: int = 16, grid: int = 0, l2_prefetch: int = -1,
+             producers: int = 0) -> Plan:
+    """A plan with a fixed tiling, to pass as ``gemm(..., plan=...)``; l2_prefetch < 0 and
+    producers <= 0 take the library's defaults for the problem."""
     return Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
-                l2_prefetch=l2_prefetch)
+                l2_prefetch=l2_prefetch, producers=producers)

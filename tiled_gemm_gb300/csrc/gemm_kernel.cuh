@@ -11,10 +11,10 @@
 // a consumer that only issues MMAs, handing stages over through full/empty
 // mbarrier pairs).  This kernel keeps that structure and maps it onto sm_103a:
 //
-//   warps 0, 6, 7        TMA producers (one thread each): for every (tile, k-block)
-//                        wait for a free ring slot, arm its "full" barrier with
-//                        their share of the stage's bytes and issue their share of
-//                        the A and B boxes (dealt round-robin).  Boxes that run
+//   warps 0, 6, 7        TMA producers (one thread each), taking turns by stage: for
+//                        its (tile, k-block) iterations a producer waits for a free
+//                        ring slot, arms the slot's "full" barrier with the stage's
+//                        byte count and issues the A and B boxes.  Boxes that run
 //                        past the matrix edge are zero-filled by the TMA unit, so
 //                        partial tiles add exact zeros ("TileLang core primitives"
 //                        page, section 4.2: out-of-range reads give the safe value 0).
@@ -83,6 +83,7 @@ struct GemmParams {
   int32_t l2_prefetch;      // k-blocks the producer prefetches into L2 ahead of the ring
   int32_t a3d, b3d;         // operand map is the 3-D view {64, rows, chunks} (one box
                             // per stage) instead of 2-D boxes of one 64-chunk each
+  int32_t producers;        // producer threads taking turns by stage (1..3, <= stages)
   uint32_t idesc;
   void* C;                  // used when tma_store == 0
   int64_t ldc;
@@ -102,9 +103,10 @@ __host__ __device__ constexpr uint32_t b_stage_bytes() {
 }
 
 // Barrier block: full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done,
-// then the 4-byte Tensor Memory base slot and the 4-byte abort flag.
+// then the 4-byte Tensor Memory base slot, the 4-byte abort flag and, per stage, the
+// last lap at which a producer armed that stage (int32 x 8, -1 = never).
 __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
-  return static_cast<uint32_t>(8 * (2 * stages + 5) + 8);
+  return static_cast<uint32_t>(8 * (2 * stages + 5) + 8 + 32);
 }
 
 template <int BN, int CG, int BK>
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
+  volatile int32_t* const lap_armed = reinterpret_cast<volatile int32_t*>(tmem_slot_ptr + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -259,16 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_a_boxes = p.a3d ? 1 : (p.trans_a ? kBM / 64 : kKChunks);
   const int n_b_boxes = p.b3d ? 1 : (p.trans_b ? kKChunks : kBnCta / 64);
   const int n_boxes = n_a_boxes + n_b_boxes;
-  // Wide tiles issue few boxes per stage: one producer.
-  const int n_producers = BN >= 256 ? 1 : min(kProducers, n_boxes);
-  auto box_bytes = [&](int j) -> uint32_t {
-    if (j < n_a_boxes) return kAStageBytes / n_a_boxes;
-    return kBStage / n_b_boxes;
-  };
+  // producers take turns by stage (see below); at most one per ring slot
+  const int n_producers = min(kProducers, min(S, max(1, p.producers)));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), n_producers);   // the even CTA's producers arrive + TMA bytes
+      mbar_init(full_bar(s), 1);   // the producer of that iteration arrives + TMA bytes
       mbar_init(empty_bar(s), 1);            // one tcgen05.commit
     }
     for (int a = 0; a < 2; ++a) {
@@ -277,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0u;
+    for (int s = 0; s < 8; ++s) lap_armed[s] = -1;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -301,19 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp >= 6) {
     // ----------------------------------------------------------- producers --
-    // Issuing a TMA copy occupies the issuing thread for ~100 cycles, about as long
-    // as the MMAs of a narrow k-block take, so the stage's boxes are dealt round-robin
-    // to up to kProducers threads in different warps; each arms the stage's "full"
-    // barrier with its own byte count (times CG: the peer's matching boxes complete
-    // on the same barrier).
+    // One producer iteration (wait for a free slot, arm the stage's "full" barrier,
+    // issue its boxes) occupies the issuing thread for ~600 cycles, mostly barrier
+    // round trips, while further boxes in the same iteration cost ~100 each; several
+    // producer threads in different warps multiply the rate.  So up to kProducers
+    // threads take turns by stage: producer p issues every box of the iterations
+    // g = p, p + P, p + 2P, ... of this CTA's (tile, k-block) sequence, g in stage
+    // g mod S.  With P <= S the parity waits stay exact: before producer p reaches
+    // iteration g the MMA has consumed everything up to g - P - S, so a slot's
+    // barrier is never two phases behind its waiter.
     const int pi = warp == 0 ? 0 : warp - 5;           // producer index 0..2
     if (lane == 0 && pi < n_producers) {
-      uint32_t issued = 0, issued_parity = 0;          // per-stage bit masks (S <= 8)
-      int stage = 0;
-      uint32_t phase = 0;
       bool ok = true;
-      uint32_t my_bytes = 0;
-      for (int j = pi; j < n_boxes; j += n_producers) my_bytes += box_bytes(j);
       // the j-th box of k-block kb: its shared-memory slot and coordinates
       auto issue_box = [&](int j, int kb, int m0, int nb0, uint32_t a_dst, uint32_t b_dst,
                            uint32_t fb, bool prefetch_only) {
@@ -355,53 +354,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           else tma_load_2d(dst, map, fb, x, y);
         }
       };
-      for (int t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
+      // walk iterations g = pi, pi + P, ...: tile i = g / k_blocks, k-block g mod k_blocks
+      int i = 0, kb = pi;
+      while (kb >= p.k_blocks) { kb -= p.k_blocks; ++i; }
+      for (int g = pi; ok; g += n_producers) {
+        const int t = cluster_id + i * n_clusters;
+        if (t >= p.num_tiles) break;
         int mb, nb;
         tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
         const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;    // this CTA's A rows
         const int nb0 = nb * BN + static_cast<int>(rank) * kBnCta;      // this CTA's B columns
-        // Optional L2 prefetch up to l2_prefetch k-blocks ahead, at most two k-blocks
-        // per iteration so the ring keeps filling first.
-        int pf_next = S;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
-            record_timeout(p.status, abort_flag, kSiteProducerEmpty);
-            ok = false;
-            break;
-          }
-          const uint32_t local_full = full_bar(stage);
-          if (leader) mbar_arrive_expect_tx(local_full, my_bytes * CG);
-          const uint32_t fb = kPair ? mapa_shared(local_full, 0) : local_full;
-          const uint32_t a_dst = sA + stage * kAStageBytes;
-          const uint32_t b_dst = sB + stage * kBStage;
-          for (int j = pi; j < n_boxes; j += n_producers)
-            issue_box(j, kb, m0, nb0, a_dst, b_dst, fb, false);
-          if (leader) {
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          }
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          for (int n = 0; n < 2 && p.l2_prefetch > 0 && pf_next < p.k_blocks &&
-                          pf_next <= kb + p.l2_prefetch;
-               ++n, ++pf_next) {
-            for (int j = pi; j < n_boxes; j += n_producers)
-              issue_box(j, pf_next, m0, nb0, 0, 0, 0, true);
-          }
+        const int stage = g % S;
+        const uint32_t phase = static_cast<uint32_t>(g / S) & 1u;
+        if (!wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+          record_timeout(p.status, abort_flag, kSiteProducerEmpty);
+          ok = false;
+          break;
         }
-      }
-      // Every issued load must have landed before the CTA may exit.  In a normal run
-      // the MMA thread consumed them all and these waits return at once.  (The even
-      // CTA's barriers also cover the odd CTA's loads of the same stages.)
-      for (int s = 0; s < S; ++s) {
-        if (issued & (1u << s)) {
-          if (!wait_bounded<kPair>(full_bar(s), (issued_parity >> s) & 1u, nullptr,
-                                   p.timeout_ns)) {
-            record_timeout(p.status, abort_flag, kSiteDrain);
-          }
+        const uint32_t local_full = full_bar(stage);
+        if (leader) mbar_arrive_expect_tx(local_full, (kAStageBytes + kBStage) * CG);
+        const uint32_t fb = kPair ? mapa_shared(local_full, 0) : local_full;
+        const uint32_t a_dst = sA + stage * kAStageBytes;
+        const uint32_t b_dst = sB + stage * kBStage;
+        for (int j = 0; j < n_boxes; ++j) issue_box(j, kb, m0, nb0, a_dst, b_dst, fb, false);
+        if (leader) lap_armed[stage] = g / S;   // stage laps are armed in order
+        // optional L2 prefetch of the k-block l2_prefetch iterations ahead (same tile)
+        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < p.k_blocks) {
+          for (int j = 0; j < n_boxes; ++j)
+            issue_box(j, kb + p.l2_prefetch, m0, nb0, 0, 0, 0, true);
         }
+        kb += n_producers;
+        while (kb >= p.k_blocks) { kb -= p.k_blocks; ++i; }
       }
     }
   } else if (warp == 1) {
@@ -571,6 +554,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   tc_fence_before_sync();
+  __syncthreads();
+  // Every load a producer issued must have landed before the CTA may exit.  All roles
+  // are done, so the last armed lap of each stage is final and its phase parity is
+  // unambiguous.  In a normal run the MMA thread consumed every stage and these waits
+  // return at once.  (The even CTA's barriers also cover the odd CTA's loads.)
+  if (threadIdx.x == 0 && leader) {
+    for (int st = 0; st < S; ++st) {
+      const int lap = lap_armed[st];
+      if (lap >= 0 && !wait_bounded<kPair>(full_bar(st), static_cast<uint32_t>(lap) & 1u,
+                                           nullptr, p.timeout_ns)) {
+        record_timeout(p.status, abort_flag, kSiteDrain);
+      }
+    }
+  }
   __syncthreads();
   if constexpr (kPair) cluster_sync_all();   // no CTA leaves while its peer may touch it
   tc_fence_after_sync();

@@ -187,6 +187,10 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* p
   if (pl->tiles > (int64_t{1} << 31) - 1) return TL_ERR_UNSUPPORTED;
   if (pl->l2_prefetch < 0) pl->l2_prefetch = default_prefetch(*pl);
   if (pl->l2_prefetch > 1024) return TL_ERR_INVALID_ARG;
+  // producers take turns by stage: at most one per ring slot, at most three warps
+  const int max_prod = std::min(3, pl->stages);
+  pl->producers = pl->producers <= 0 ? max_prod : std::min(pl->producers, max_prod);
+  pl->reserved = 0;
   return TL_OK;
 }
 
@@ -418,6 +422,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     pl.raster_group = forced->raster_group > 0 ? forced->raster_group : 16;
     pl.grid = forced->grid;
     pl.l2_prefetch = forced->l2_prefetch;
+    pl.producers = forced->producers;
   } else {
     choose_tiling(M, N, K, st->sms, &pl);
   }
@@ -516,6 +521,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.l2_prefetch = pl.l2_prefetch;
   prm.a3d = a3d ? 1 : 0;
   prm.b3d = b3d ? 1 : 0;
+  prm.producers = pl.producers;
   prm.idesc = tl::mma_idesc_f16(prm.bf16, trans_a ? 1u : 0u, trans_b ? 0u : 1u,
                                 static_cast<uint32_t>(pl.bm), static_cast<uint32_t>(pl.bn));
   prm.C = C;
@@ -572,8 +578,10 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
   if (s != TL_OK) return s;
   if (plan->raster_group <= 0) plan->raster_group = 16;
   const int32_t pf = plan->l2_prefetch;
+  const int32_t prod = plan->producers;
   std::memset(&plan->tiles_m, 0, sizeof(tl_plan) - offsetof(tl_plan, tiles_m));
   plan->l2_prefetch = pf;
+  plan->producers = prod;
   return complete_plan(M, N, K, num_sms, plan);
 }
 
