@@ -88,8 +88,13 @@ typedef struct {
   int32_t l2_prefetch;   /* k-blocks prefetched into L2 ahead of the ring (0 = off) */
   int32_t producers;     /* TMA producer threads taking turns by stage (1..3, at    */
                          /* most `stages`; 0 = default)                             */
+  int32_t stream_k;      /* -1 off, 0 automatic, 1 on: the k-blocks of the last     */
+                         /* waves' tiles are split evenly over all CTAs (pairs)     */
+  int32_t dp_tiles;      /* tiles run whole before the split region                 */
   int32_t reserved;      /* zero                                                    */
-  int64_t workspace_bytes; /* bytes of the stream-ordered repack workspace          */
+  int64_t sk_iters;      /* k-block iterations split evenly (0: no split)           */
+  int64_t workspace_bytes; /* bytes of the stream-ordered workspace (repacked       */
+                         /* operands, stream-K partial sums and flags)              */
 } tl_plan;
 
 /*
@@ -111,6 +116,10 @@ typedef struct {
  * the leading pitch in bytes must be a multiple of 16) are first copied on
  * `stream` into a workspace with the pitch rounded up, allocated and freed with
  * the stream-ordered allocator; an unaligned C is written by predicated stores.
+ * When the tiles do not fill whole waves of the GPU, the k-blocks of the last
+ * waves are split evenly over all CTAs (stream-K); the fp32 partial sums of split
+ * tiles pass through the same kind of workspace and are added in a fixed order, so
+ * results are deterministic for a given plan and GPU.
  *
  * Errors are returned before anything is enqueued: TL_ERR_INVALID_ARG,
  * TL_ERR_NULL_PTR, TL_ERR_ALIGNMENT, TL_ERR_ALIAS, TL_ERR_DEVICE,
@@ -143,8 +152,9 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
 
 /*
  * tl_gemm() with an explicit plan (bm, bn, bk, stages, raster_group, grid,
- * l2_prefetch and producers are read; the rest is recomputed; l2_prefetch < 0 and
- * producers <= 0 select the defaults for the problem).  Used to run a workload at a fixed tiling, e.g. the
+ * l2_prefetch, producers and stream_k are read; the rest is recomputed;
+ * l2_prefetch < 0, producers <= 0 and stream_k = 0 select the defaults).  Used
+ * to run a workload at a fixed tiling, e.g. the
  * pages' quickstart 128x128x64 with 3 stages.  Same arguments and errors as
  * tl_gemm(), plus TL_ERR_INVALID_ARG for an unsupported plan.
  */

@@ -74,7 +74,15 @@ def test_plan_tiles_cover_the_output_exactly_once(M, N, K):
     assert p.k_blocks * p.bk >= K > (p.k_blocks - 1) * p.bk
     assert p.tiles == p.tiles_m * p.tiles_n
     cg = p.bm // 128                       # CTAs per tile
-    assert 1 <= p.grid <= cg * min(148 // cg, p.tiles) and p.grid % cg == 0
+    assert p.grid % cg == 0
+    if p.sk_iters == 0:                    # whole tiles only: one unit per tile at most
+        assert 1 <= p.grid <= cg * min(148 // cg, p.tiles)
+        assert p.dp_tiles == p.tiles
+    else:                                  # split: every unit takes a share
+        assert p.grid == cg * (148 // cg)
+        assert p.dp_tiles % (p.grid // cg) == 0
+        assert p.sk_iters == (p.tiles - p.dp_tiles) * p.k_blocks
+        assert p.workspace_bytes == p.grid * 128 * p.bn * 4 + p.grid * 4 * 8
     assert p.smem_bytes <= 232448
     assert p.tmem_cols in (128, 256, 512)
     assert p.tx_bytes == (128 + p.bn // cg) * p.bk * 2
@@ -97,6 +105,24 @@ def test_every_supported_tiling_fits_shared_memory_and_others_are_rejected():
                 (128, 128, 64, 9), (256, 64, 64, 4), (512, 256, 64, 4), (128, 128, 256, 2)):
         with pytest.raises(tl.TLError):
             tl.tl_plan_complete(1024, 1024, 1024, *bad)
+
+
+def test_stream_k_split_choices():
+    # short tiles stay whole (the fix-up would cost more than it saves), whole waves are
+    # never split, the ragged 3.2-wave shape is split, forcing works both ways
+    p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152)
+    assert (p.dp_tiles, p.sk_iters, p.grid) == (64, 0, 64)
+    p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, stream_k=1)
+    assert (p.dp_tiles, p.sk_iters, p.grid) == (0, 64 * 16, 152)
+    p = tl.tl_plan_complete(128 * 152, 128, 1024, 128, 128, 64, 3, num_sms=152)
+    assert p.sk_iters == 0 and p.tiles == 152
+    p = tl.tl_gemm_plan(3000, 5000, 4100, num_sms=152)
+    assert (p.bm, p.bn) == (256, 256) and p.dp_tiles == 2 * 76
+    assert p.sk_iters == (240 - 152) * p.k_blocks
+    p = tl.tl_plan_complete(4096, 4096, 4096, 256, 256, 128, 3, num_sms=152, stream_k=-1)
+    assert p.sk_iters == 0 and p.dp_tiles == 256
+    with pytest.raises(tl.TLError):
+        tl.tl_plan_complete(64, 64, 64, 128, 64, 64, 3, stream_k=2)
 
 
 def test_planner_rejects_bad_arguments():

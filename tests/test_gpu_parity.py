@@ -91,6 +91,52 @@ def test_cta_pairs_all_transposes_random(bn, bk, ta, tb):
     _check_full(_w(768, 1024, 640, BF16, ta, tb, False, "uniform", 71 + bn + bk), plan=plan)
 
 
+# stream-K: the k-blocks of the last waves split evenly over all units, partial sums
+# added by each split tile's finisher
+SPLIT_CASES = [
+    # bm, bn, bk, stages, M, N, K, grid
+    (128, 128, 64, 3, 1024, 1024, 1024, 0),      # quickstart tiling: 64 tiles over all SMs
+    (128, 64, 64, 4, 300, 520, 200, 0),          # short K: tiles split over many units
+    (128, 256, 64, 4, 1000, 900, 777, 0),        # ragged K: 2-D boxes
+    (256, 256, 128, 3, 2048, 2048, 1536, 0),     # pairs, 3-D boxes, DP waves then split
+    (256, 128, 64, 3, 700, 900, 515, 6),         # pairs, few units
+    (128, 64, 128, 4, 16, 8192, 2048, 0),        # skinny
+    (128, 128, 64, 3, 512, 512, 64, 0),          # one k-block: nothing to split
+]
+
+
+@pytest.mark.parametrize("bm,bn,bk,stages,M,N,K,grid", SPLIT_CASES)
+def test_stream_k_split_bit_exact(bm, bn, bk, stages, M, N, K, grid):
+    plan = tl.plan_for(0, 0, 0, bm, bn, bk, stages, raster_group=3, grid=grid, stream_k=1)
+    _check_full(_w(M, N, K, F16, False, bn == 128, True, "int_small", M + N + K + bm),
+                plan=plan, exact=True)
+    _check_full(_w(M, N, K, BF16, True, False, False, "uniform", M + N + K + bn), plan=plan)
+
+
+def test_stream_k_results_are_deterministic_and_replay_in_graphs():
+    w = _w(1024, 1024, 1024, F16, False, False, True, "uniform", 90)
+    a, b = workloads.make_inputs(w)
+    ad, bd = a.cuda(), b.cuda()
+    plan = tl.plan_for(0, 0, 0, 128, 128, 64, 3, stream_k=1)
+    outs = []
+    for _ in range(3):
+        outs.append(tl.gemm(ad, bd, relu=True, plan=plan).cpu())
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    out = torch.empty(1024, 1024, dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tl.gemm(ad, bd, relu=True, out=out, plan=plan, stream=s)
+    for _ in range(3):                      # replays reuse the launch's flags and token
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.cpu(), outs[0])
+    st, word = tl.tl_device_status(reset=True)
+    assert st == tl.TL_OK, hex(word)
+
+
 @pytest.mark.parametrize("l2_prefetch", [0, 1, 3, 5, 100])
 @pytest.mark.parametrize("ta,tb", [(False, False), (True, True)])
 def test_l2_prefetch_distances(l2_prefetch, ta, tb):

@@ -69,6 +69,7 @@ enum WaitSite : uint32_t {
   kSiteMmaFull = 3,
   kSiteEpiTmemFull = 4,
   kSiteDrain = 5,
+  kSiteStreamK = 6,
 };
 
 struct GemmParams {
@@ -84,6 +85,16 @@ struct GemmParams {
   int32_t a3d, b3d;         // operand map is the 3-D view {64, rows, chunks} (one box
                             // per stage) instead of 2-D boxes of one 64-chunk each
   int32_t producers;        // producer threads taking turns by stage (1..3, <= stages)
+  // Stream-K: tiles [0, dp_tiles) run whole, one per unit (CTA or CTA pair) in turn;
+  // the k-block iterations of tiles [dp_tiles, num_tiles), sk_iters of them, are split
+  // evenly over the units.  A unit that starts mid-tile stores that tile's partial sum
+  // (fp32) in its slot of sk_partials and raises its flags (sk_token); the unit that
+  // holds the tile's first k-block adds the partials in order and writes C.
+  int32_t dp_tiles;
+  int64_t sk_iters;
+  float* sk_partials;                 // [unit][cta][4 warps][BN cols][32 lanes]
+  unsigned long long* sk_flags;       // [unit][cta][4 warps]
+  unsigned long long sk_token;        // unique to this launch, never 0
   uint32_t idesc;
   void* C;                  // used when tma_store == 0
   int64_t ldc;
@@ -167,25 +178,41 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
-// Bounded wait for long waits: the thread sleeps in the barrier (suspend hint) and
-// backs off between polls, so a warp waiting out a main loop does not compete for
-// issue slots or the shared-memory pipe with the producer and MMA threads.
-template <bool kCluster>
-__device__ __forceinline__ bool wait_bounded_sleep(uint32_t bar, uint32_t parity,
-                                                   volatile uint32_t* abort_flag,
-                                                   uint64_t timeout_ns) {
-  if (poll<kCluster>(bar, parity)) return true;
-  const uint64_t t0 = clock_cycles();
-  const uint64_t limit = timeout_ns * 4u;
-  while (true) {
-    const bool ok = kCluster ? mbar_try_wait_sleep_cluster(bar, parity, 20000u)
-                             : mbar_try_wait_sleep(bar, parity, 20000u);
-    if (ok) return true;
-    if (*abort_flag) return false;
-    if (clock_cycles() - t0 > limit) return false;
-    __nanosleep(64);
-  }
+// The work of one unit (CTA or CTA pair): whole tiles u, u + U, ... below dp_tiles,
+// then its share [it, it_end) of the split iterations, cut at tile boundaries.  Every
+// role of the unit walks the same sequence.
+struct WorkItem {
+  int tile, k0, k1;   // k-blocks [k0, k1) of tile `tile`
+};
+
+__device__ __forceinline__ int64_t sk_begin(const GemmParams& p, int unit, int units) {
+  return static_cast<int64_t>(unit) * p.sk_iters / units;
 }
+
+struct WorkIter {
+  int next_dp, step, dp_end, kb;
+  int64_t it, it_end;
+  __device__ __forceinline__ WorkIter(const GemmParams& p, int unit, int units)
+      : next_dp(unit), step(units), dp_end(p.dp_tiles), kb(p.k_blocks),
+        it(sk_begin(p, unit, units)), it_end(sk_begin(p, unit + 1, units)) {}
+  __device__ __forceinline__ bool next(WorkItem& w) {
+    if (next_dp < dp_end) {
+      w = {next_dp, 0, kb};
+      next_dp += step;
+      return true;
+    }
+    if (it < it_end) {
+      const int t = static_cast<int>(it / kb);
+      const int k0 = static_cast<int>(it - static_cast<int64_t>(t) * kb);
+      const int64_t left = it_end - it;
+      const int k1 = left < static_cast<int64_t>(kb - k0) ? k0 + static_cast<int>(left) : kb;
+      w = {dp_end + t, k0, k1};
+      it += k1 - k0;
+      return true;
+    }
+    return false;
+  }
+};
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16, int relu) {
   if (relu) {
@@ -354,37 +381,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           else tma_load_2d(dst, map, fb, x, y);
         }
       };
-      // walk iterations g = pi, pi + P, ...: tile i = g / k_blocks, k-block g mod k_blocks
-      int i = 0, kb = pi;
-      while (kb >= p.k_blocks) { kb -= p.k_blocks; ++i; }
-      for (int g = pi; ok; g += n_producers) {
-        const int t = cluster_id + i * n_clusters;
-        if (t >= p.num_tiles) break;
+      // walk this unit's (tile, k-block) iterations g = 0, 1, ...; issue g = pi, pi + P, ...
+      WorkIter work(p, cluster_id, n_clusters);
+      WorkItem w;
+      int g = 0;
+      while (ok && work.next(w)) {
         int mb, nb;
-        tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
+        tile_coords(w.tile, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
         const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;    // this CTA's A rows
         const int nb0 = nb * BN + static_cast<int>(rank) * kBnCta;      // this CTA's B columns
-        const int stage = g % S;
-        const uint32_t phase = static_cast<uint32_t>(g / S) & 1u;
-        if (!wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
-          record_timeout(p.status, abort_flag, kSiteProducerEmpty);
-          ok = false;
-          break;
+        for (int kb = w.k0; kb < w.k1; ++kb, ++g) {
+          if (g % n_producers != pi) continue;
+          const int stage = g % S;
+          const uint32_t phase = static_cast<uint32_t>(g / S) & 1u;
+          if (!wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          const uint32_t local_full = full_bar(stage);
+          if (leader) mbar_arrive_expect_tx(local_full, (kAStageBytes + kBStage) * CG);
+          const uint32_t fb = kPair ? mapa_shared(local_full, 0) : local_full;
+          const uint32_t a_dst = sA + stage * kAStageBytes;
+          const uint32_t b_dst = sB + stage * kBStage;
+          for (int j = 0; j < n_boxes; ++j) issue_box(j, kb, m0, nb0, a_dst, b_dst, fb, false);
+          if (leader) lap_armed[stage] = g / S;   // stage laps are armed in order
+          // optional L2 prefetch of the k-block l2_prefetch iterations ahead (same item)
+          if (p.l2_prefetch > 0 && kb + p.l2_prefetch < w.k1) {
+            for (int j = 0; j < n_boxes; ++j)
+              issue_box(j, kb + p.l2_prefetch, m0, nb0, 0, 0, 0, true);
+          }
         }
-        const uint32_t local_full = full_bar(stage);
-        if (leader) mbar_arrive_expect_tx(local_full, (kAStageBytes + kBStage) * CG);
-        const uint32_t fb = kPair ? mapa_shared(local_full, 0) : local_full;
-        const uint32_t a_dst = sA + stage * kAStageBytes;
-        const uint32_t b_dst = sB + stage * kBStage;
-        for (int j = 0; j < n_boxes; ++j) issue_box(j, kb, m0, nb0, a_dst, b_dst, fb, false);
-        if (leader) lap_armed[stage] = g / S;   // stage laps are armed in order
-        // optional L2 prefetch of the k-block l2_prefetch iterations ahead (same tile)
-        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < p.k_blocks) {
-          for (int j = 0; j < n_boxes; ++j)
-            issue_box(j, kb + p.l2_prefetch, m0, nb0, 0, 0, 0, true);
-        }
-        kb += n_producers;
-        while (kb >= p.k_blocks) { kb -= p.k_blocks; ++i; }
       }
     }
   } else if (warp == 1) {
@@ -405,14 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
+      WorkIter work(p, cluster_id, n_clusters);
+      WorkItem w;
+      while (ok && work.next(w)) {
         if (!wait_bounded<kPair>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
           record_timeout(p.status, abort_flag, kSiteMmaTmemEmpty);
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!wait_bounded<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteMmaFull);
             ok = false;
@@ -423,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b_desc = b_desc0 + ((stage * kBStage) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / kUmmaK; ++k) {
-            const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
+            const uint32_t acc_in = (kb != w.k0 || k != 0) ? 1u : 0u;
             const uint64_t ad = a_desc + k_off(p.trans_a, kBM, k);
             const uint64_t bd = b_desc + k_off(!p.trans_b, kBnCta, k);
             if constexpr (kPair) mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, acc_in);
@@ -462,15 +491,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;               // staging-buffer owner index
     uint32_t acc = 0, acc_phase = 0;
     uint32_t sbuf = 0;
-    for (int t = cluster_id; t < p.num_tiles; t += n_clusters) {
+    WorkIter work(p, cluster_id, n_clusters);
+    WorkItem w;
+    while (work.next(w)) {
       int mb, nb;
-      tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
+      tile_coords(w.tile, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
       const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;
       const int n0 = nb * BN;
-      // one lane waits (sleeping), the warp follows its verdict
+      // Stream-K roles: a partial item that starts mid-tile stores its sum for the
+      // tile's finisher; an item that starts at k-block 0 but ends early is the
+      // finisher and adds the partials of units cluster_id + 1 .. v_end - 1.
+      const bool store_partial = w.k0 > 0;
+      int v_end = cluster_id + 1;
+      if (w.k0 == 0 && w.k1 < p.k_blocks) {
+        const int64_t tile_end = static_cast<int64_t>(w.tile - p.dp_tiles + 1) * p.k_blocks;
+        while (v_end < n_clusters && sk_begin(p, v_end, n_clusters) < tile_end) ++v_end;
+      }
+      const int slot_q = (static_cast<int>(rank) * 4 + q);     // this warp's slot in a unit
+      auto partial_at = [&](int unit, int col) -> float* {
+        return p.sk_partials +
+               ((static_cast<int64_t>(unit) * CG * 4 + slot_q) * BN + col) * 32 + lane;
+      };
+      auto flag_at = [&](int unit) -> unsigned long long* {
+        return p.sk_flags + static_cast<int64_t>(unit) * CG * 4 + slot_q;
+      };
+      // units with an empty share of the split store nothing
+      auto contributes = [&](int v) {
+        return sk_begin(p, v, n_clusters) < sk_begin(p, v + 1, n_clusters);
+      };
+      // contributors' partials must be stored before they are read
+      if (v_end > cluster_id + 1) {
+        bool ok_sk = true;
+        if (lane == 0) {
+          for (int v = cluster_id + 1; v < v_end && ok_sk; ++v) {
+            if (!contributes(v)) continue;
+            const uint64_t t0 = clock_cycles();
+            while (ld_acquire_gpu_u64(flag_at(v)) != p.sk_token) {
+              if (clock_cycles() - t0 > p.timeout_ns * 4u || *abort_flag) { ok_sk = false; break; }
+            }
+          }
+          if (!ok_sk && !*abort_flag) record_timeout(p.status, abort_flag, kSiteStreamK);
+        }
+        __syncwarp();
+        // every lane acquires the flags it relies on before reading the partials
+        for (int v = cluster_id + 1; v < v_end; ++v)
+          if (contributes(v)) (void)ld_acquire_gpu_u64(flag_at(v));
+      }
+      // one lane waits, the warp follows its verdict.  (A try_wait with a suspend-time
+      // hint was measured to wake microseconds after the phase completed: plain polls
+      // by one lane per warp cost less.)
       bool ready = true;
       if (lane == 0)
-        ready = wait_bounded_sleep<kPair>(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
+        ready = wait_bounded<kPair>(tfull_bar(acc), acc_phase, abort_flag, p.timeout_ns);
       __syncwarp();
       if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
         if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
@@ -492,6 +564,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
             else mbar_arrive(tempty_bar(acc));
           }
+        }
+        if (store_partial) {
+          // fp32 partial sum: for each column the warp's 32 lanes write 128 B
+#pragma unroll
+          for (int j = 0; j < 64; ++j) __stcg(partial_at(cluster_id, c * kChunk + j), __uint_as_float(v[j]));
+          continue;
+        }
+        // finisher: add the later k-blocks' partials, in unit order
+        for (int u2 = cluster_id + 1; u2 < v_end; ++u2) {
+          if (!contributes(u2)) continue;
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(partial_at(u2, c * kChunk + j)));
         }
         uint32_t packed[32];
 #pragma unroll
@@ -534,6 +619,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      }
+      if (store_partial) {
+        __threadfence();                  // this lane's partial is visible before the flag
+        __syncwarp();
+        if (lane == 0) st_release_gpu_u64(flag_at(cluster_id), p.sk_token);
+      } else if (v_end > cluster_id + 1) {
+        __syncwarp();                     // all lanes have read the partials: reset flags
+        if (lane == 0)
+          for (int u2 = cluster_id + 1; u2 < v_end; ++u2)
+            if (contributes(u2)) *flag_at(u2) = 0ull;
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;

@@ -56,22 +56,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, but lets the hardware suspend the thread for up to `hint_ns`
-// while the phase is incomplete (for waits expected to be long, e.g. the epilogue
-// waiting out a whole main loop): the waiting warp then takes no issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
-                                                    uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
 // SM cycle counter: cheap to read (unlike %globaltimer), used to bound waits.
 __device__ __forceinline__ uint64_t clock_cycles() {
   uint64_t c;
@@ -227,6 +211,18 @@ __device__ __forceinline__ void tmem_load_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------ global flags (gpu) --
+
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* addr, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* addr) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------- CTA pairs (cluster) --
 // A cluster of two CTAs on one SM pair shares each MMA (cta_group::2): the even CTA
 // issues it, each CTA supplies half of the operands from its own shared memory, and
@@ -265,19 +261,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_try_wait_sleep_cluster(uint32_t bar, uint32_t parity,
-                                                            uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }

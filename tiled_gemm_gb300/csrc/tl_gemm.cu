@@ -19,6 +19,7 @@
 #include <cstddef>
 #include <cstring>
 #include <mutex>
+#include <random>
 
 #include "gemm_kernel.cuh"
 #include "tl_gemm.h"
@@ -166,6 +167,48 @@ int default_prefetch(const tl_plan& pl) {
   return 0;
 }
 
+// Work split over `units` persistent units.  Whole waves of tiles run data-parallel;
+// when the tiles do not fill the last wave, the last full wave and the remainder are
+// split by k-block evenly over all units (stream-K) if that shortens the critical
+// path enough: data-parallel takes ceil(T/U) tile-lengths; the split takes (T_dp/U)
+// tile-lengths plus ceil(iterations/U) k-blocks plus the fix-up.  Measured on GB300
+// the fix-up (storing an fp32 partial tile, publishing it, the finisher reading it)
+// costs ~6,000 SM cycles, i.e. fixup_kb k-blocks of about max(600, MMA cycles) each --
+// so short tiles stay whole.  Under the power cap the split also raises the clock-
+// limited work, hence the 0.87 margin.
+void schedule(tl_plan* pl, int64_t units_avail, bool allow_split) {
+  const int cg = pl->bm / 128;
+  const int64_t units = std::max<int64_t>(1, units_avail);
+  const int64_t T = pl->tiles, KI = pl->k_blocks;
+  int64_t dp = T, iters = 0;
+  if (allow_split && pl->stream_k >= 0 && units > 1 && KI >= 2) {
+    const int64_t full = T / units, rem = T % units;
+    if (rem != 0 || pl->stream_k == 1) {
+      const int64_t dp_try = full >= 1 ? (full - 1) * units : 0;
+      const int64_t it = (T - dp_try) * KI;
+      const double mma_cycles = 128.0 * pl->bn * pl->bk / 4096.0;     // per SM and k-block
+      const double fixup_kb = 6000.0 / std::max(600.0, 1.1 * mma_cycles);
+      const double t_dp = static_cast<double>(ceil_div(T, units) * KI);
+      const double t_sk =
+          static_cast<double>((dp_try / units) * KI + ceil_div(it, units)) + fixup_kb;
+      if (pl->stream_k == 1 || t_sk < 0.87 * t_dp) {
+        dp = dp_try;
+        iters = it;
+      }
+    }
+  }
+  pl->dp_tiles = static_cast<int32_t>(dp);
+  pl->sk_iters = iters;
+  pl->grid = static_cast<int32_t>(cg * (iters > 0 ? units : std::min<int64_t>(units, T)));
+}
+
+// fp32 partial-sum slots (one 128 x bn tile per CTA) and ready flags (one per epilogue
+// warp of each CTA) for a split over grid / cg units.
+int64_t split_workspace_bytes(const tl_plan& pl) {
+  if (pl.sk_iters == 0) return 0;
+  return static_cast<int64_t>(pl.grid) * 128 * pl.bn * 4 + static_cast<int64_t>(pl.grid) * 4 * 8;
+}
+
 tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* pl) {
   if (!plan_supported(*pl)) return TL_ERR_INVALID_ARG;
   const int sms = num_sms > 0 ? num_sms : kDefaultSms;
@@ -180,17 +223,18 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* p
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
   pl->tmem_cols = 2 * pl->bn;
   pl->tx_bytes = (128 + pl->bn / cg) * pl->bk * 2;
-  // grid in CTAs: a multiple of cg, one tile (pair) per SM (pair) at most
-  const int64_t want_units = pl->grid > 0 ? std::max<int64_t>(1, pl->grid / cg) : sms / cg;
-  pl->grid = static_cast<int32_t>(
-      cg * std::max<int64_t>(1, std::min<int64_t>(want_units, pl->tiles)));
   if (pl->tiles > (int64_t{1} << 31) - 1) return TL_ERR_UNSUPPORTED;
+  if (pl->stream_k < -1 || pl->stream_k > 1) return TL_ERR_INVALID_ARG;
+  // grid in CTAs: a multiple of cg; one persistent unit (CTA or pair) per SM (pair)
+  const int64_t want_units = pl->grid > 0 ? std::max<int64_t>(1, pl->grid / cg) : sms / cg;
+  schedule(pl, want_units, true);
   if (pl->l2_prefetch < 0) pl->l2_prefetch = default_prefetch(*pl);
   if (pl->l2_prefetch > 1024) return TL_ERR_INVALID_ARG;
   // producers take turns by stage: at most one per ring slot, at most three warps
   const int max_prod = std::min(3, pl->stages);
   pl->producers = pl->producers <= 0 ? max_prod : std::min(pl->producers, max_prod);
   pl->reserved = 0;
+  pl->workspace_bytes = split_workspace_bytes(*pl);
   return TL_OK;
 }
 
@@ -237,51 +281,85 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int sms, tl_plan* pl) {
 
 
 template <int BN, int CG, int BK>
-tl_status launch_bn(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
-                    const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
-                    cudaStream_t stream) {
-  constexpr int kIdx = (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) + 6 * (BK == 128);
-  constexpr uint32_t bit = 1u << kIdx;
-  auto kern = tl::tl_gemm_kernel<BN, CG, BK>;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(tl::kThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem_bytes);
-  cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t smem,
+                   cudaStream_t stream) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->blockDim = dim3(tl::kThreads);
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = stream;
+  cfg->attrs = nullptr;
+  cfg->numAttrs = 0;
   if (CG == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
   }
-  if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
-    std::lock_guard<std::mutex> lock(st->mu);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             st->smem_optin) != cudaSuccess) {
+}
+
+// Once per device and kernel: allow the large dynamic shared memory, and find how many
+// units (CTAs, or CTA pairs) the device keeps resident at once -- the persistent grid
+// must not exceed it (pairs sit on SM pairs within one GPC).  Returns that count, or
+// -1 if the attribute could not be set.
+template <int BN, int CG, int BK>
+int prepare_kernel(DeviceState* st) {
+  constexpr int kIdx = (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) + 6 * (BK == 128);
+  constexpr uint32_t bit = 1u << kIdx;
+  if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
+  std::lock_guard<std::mutex> lock(st->mu);
+  if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
+  auto kern = tl::tl_gemm_kernel<BN, CG, BK>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           st->smem_optin) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  int units = st->sms / CG;
+  if (CG == 2) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    launch_config<BN, CG, BK>(&cfg, attr, static_cast<size_t>(st->smem_optin), nullptr);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
+      units = n;
+    } else {
       (void)cudaGetLastError();
-      return TL_ERR_LAUNCH;
     }
-    // Pairs the device can keep resident at this shared-memory size: the persistent
-    // grid must not exceed it (clusters sit on SM pairs within one GPC).
-    int clusters = st->sms / CG;
-    if (CG == 2) {
-      cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
-        clusters = n;
-      } else {
-        (void)cudaGetLastError();
-      }
-    }
-    st->max_units[kIdx] = clusters;
-    st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  const int64_t units = std::min<int64_t>(pl.grid / CG, st->max_units[kIdx]);
-  cfg.gridDim = dim3(static_cast<unsigned>(CG * std::max<int64_t>(1, units)));
+  st->max_units[kIdx] = units;
+  st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  return units;
+}
+
+template <int BK>
+int resident_units_bk(DeviceState* st, int bm, int bn) {
+  if (bm == 256) return bn == 128 ? prepare_kernel<128, 2, BK>(st) : prepare_kernel<256, 2, BK>(st);
+  switch (bn) {
+    case 64: return prepare_kernel<64, 1, BK>(st);
+    case 128: return prepare_kernel<128, 1, BK>(st);
+    default: return prepare_kernel<256, 1, BK>(st);
+  }
+}
+
+int resident_units(DeviceState* st, const tl_plan& pl) {
+  return pl.bk == 128 ? resident_units_bk<128>(st, pl.bm, pl.bn)
+                      : resident_units_bk<64>(st, pl.bm, pl.bn);
+}
+
+// Launch with exactly pl.grid CTAs: the work split in `prm` was computed for that grid.
+template <int BN, int CG, int BK>
+tl_status launch_bn(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
+                    const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
+                    cudaStream_t stream) {
+  if (prepare_kernel<BN, CG, BK>(st) < 0) return TL_ERR_LAUNCH;
+  auto kern = tl::tl_gemm_kernel<BN, CG, BK>;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  launch_config<BN, CG, BK>(&cfg, attr, static_cast<size_t>(pl.smem_bytes), stream);
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_LAUNCH;
@@ -342,6 +420,22 @@ bool encode_chunked_3d(CUtensorMap* map, tl_dtype dtype, const void* base, uint6
 
 int launch_blocks_for(int64_t elems) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(elems, 256 * 4), 4096)));
+}
+
+// Flags of split tiles hold a value unique to the launch that set them (and are reset
+// by their reader), so neither stale flags of earlier launches nor the replay of a
+// captured launch can satisfy a wait early.  Random start, then a 64-bit count.
+std::atomic<unsigned long long> g_split_token{0};
+std::once_flag g_split_token_once;
+
+unsigned long long next_split_token() {
+  std::call_once(g_split_token_once, [] {
+    std::random_device rd;
+    const unsigned long long seed = (static_cast<unsigned long long>(rd()) << 32) ^ rd();
+    g_split_token.store(seed | 1ull, std::memory_order_relaxed);
+  });
+  unsigned long long t = g_split_token.fetch_add(2, std::memory_order_relaxed);
+  return t == 0 ? 1ull : t;
 }
 
 // ---- scratch for tl_gemm_noalloc -------------------------------------------------
@@ -423,11 +517,24 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     pl.grid = forced->grid;
     pl.l2_prefetch = forced->l2_prefetch;
     pl.producers = forced->producers;
+    pl.stream_k = forced->stream_k;
   } else {
     choose_tiling(M, N, K, st->sms, &pl);
   }
   if ((s = complete_plan(M, N, K, st->sms, &pl)) != TL_OK) return s;
   if (pl.smem_bytes > st->smem_optin) return TL_ERR_INVALID_ARG;
+  // Re-split over the units this device really keeps resident (CTA pairs: the cluster
+  // occupancy can be below SMs / 2).  Callers that cannot allocate get whole tiles only:
+  // the split needs a workspace for partial sums.
+  const int resident = resident_units(st, pl);
+  if (resident <= 0) return TL_ERR_LAUNCH;
+  {
+    const int cg = pl.bm / 128;
+    const int64_t want_units = forced && forced->grid > 0 ? std::max(1, forced->grid / cg)
+                                                           : st->sms / cg;
+    schedule(&pl, std::min<int64_t>(want_units, resident), !no_alloc);
+  }
+  const int64_t ws_split = split_workspace_bytes(pl);
 
   // Operands the TMA unit cannot address directly go through a padded copy.
   const bool repack_a = !tma_ok(A, lda);
@@ -439,18 +546,28 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   void* ws = nullptr;
   const void* a_use = A;
   const void* b_use = B;
-  if (ws_a + ws_b > 0) {
+  float* sk_partials = nullptr;
+  unsigned long long* sk_flags = nullptr;
+  if (ws_a + ws_b + ws_split > 0) {
     const int64_t ws_a_rounded = ceil_div(ws_a, 256) * 256;
+    const int64_t ws_b_rounded = ceil_div(ws_b, 256) * 256;
     uint8_t* w = nullptr;
     if (no_alloc) {
       if (ws_a_rounded + ws_b > kNoAllocScratchBytes) return TL_ERR_UNSUPPORTED;
       w = static_cast<uint8_t*>(scratch);
     } else {
-      if (cudaMallocAsync(&ws, static_cast<size_t>(ws_a_rounded + ws_b), stream) != cudaSuccess) {
+      if (cudaMallocAsync(&ws, static_cast<size_t>(ws_a_rounded + ws_b_rounded + ws_split),
+                          stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return TL_ERR_LAUNCH;
       }
       w = static_cast<uint8_t*>(ws);
+    }
+    if (ws_split > 0) {
+      uint8_t* split = w + ws_a_rounded + ws_b_rounded;
+      sk_partials = reinterpret_cast<float*>(split);
+      sk_flags = reinterpret_cast<unsigned long long*>(
+          split + static_cast<int64_t>(pl.grid) * 128 * pl.bn * 4);
     }
     if (repack_a) {
       tl::tl_repack_kernel<<<launch_blocks_for(a_rows * a_cols), 256, 0, stream>>>(
@@ -522,6 +639,11 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.a3d = a3d ? 1 : 0;
   prm.b3d = b3d ? 1 : 0;
   prm.producers = pl.producers;
+  prm.dp_tiles = pl.dp_tiles;
+  prm.sk_iters = pl.sk_iters;
+  prm.sk_partials = sk_partials;
+  prm.sk_flags = sk_flags;
+  prm.sk_token = next_split_token();
   prm.idesc = tl::mma_idesc_f16(prm.bf16, trans_a ? 1u : 0u, trans_b ? 0u : 1u,
                                 static_cast<uint32_t>(pl.bm), static_cast<uint32_t>(pl.bn));
   prm.C = C;
@@ -579,9 +701,11 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
   if (plan->raster_group <= 0) plan->raster_group = 16;
   const int32_t pf = plan->l2_prefetch;
   const int32_t prod = plan->producers;
+  const int32_t sk = plan->stream_k;
   std::memset(&plan->tiles_m, 0, sizeof(tl_plan) - offsetof(tl_plan, tiles_m));
   plan->l2_prefetch = pf;
   plan->producers = prod;
+  plan->stream_k = sk;
   return complete_plan(M, N, K, num_sms, plan);
 }
 
