@@ -70,7 +70,8 @@ typedef enum {
 typedef struct {
   int32_t bm;            /* output rows per tile: 128 (one CTA) or 256 (a CTA pair   */
                          /* in a 2-CTA cluster sharing each MMA, 128 rows each)     */
-  int32_t bn;            /* output columns per tile (64, 128, 256; pairs 128, 256)  */
+  int32_t bn;            /* output columns per tile (64, 128, 256; pairs 128, 256;  */
+                         /* 16 or 32 with bk 128 when the kernel's B is K-major)    */
   int32_t bk;            /* K elements per pipeline stage: 64 or 128 (one or two    */
                          /* 128-byte swizzle rows per matrix row)                   */
   int32_t stages;        /* depth of the shared-memory ring                         */
@@ -80,18 +81,23 @@ typedef struct {
   int64_t tiles_m, tiles_n, tiles, k_blocks;
   int64_t ring_bytes;    /* per CTA: stages * (128*bk + (bn/cg)*bk) * 2, cg = bm/128 */
   int64_t smem_bytes;    /* dynamic shared memory per CTA (ring + staging + bars)   */
-  int32_t tmem_cols;     /* Tensor Memory columns allocated per CTA (2 accumulators)*/
+  int32_t tmem_cols;     /* Tensor Memory columns allocated per CTA (2 accumulators,*/
+                         /* at least 32)                                            */
   int32_t tx_bytes;      /* bytes one stage's TMA loads deliver to one CTA          */
-  int32_t repack_a;      /* A is staged through a pitch-padded workspace            */
-  int32_t repack_b;      /* B likewise                                              */
-  int32_t tma_store;     /* C written by TMA bulk stores (else predicated stores)   */
+  int32_t repack_a;      /* A is staged through a pitch-padded workspace (plans     */
+  int32_t repack_b;      /* from tl_gemm_plan assume aligned operands: 0)           */
+  int32_t tma_store;     /* C written by TMA bulk stores when C is 16-byte aligned  */
+                         /* (else predicated stores)                                */
   int32_t l2_prefetch;   /* k-blocks prefetched into L2 ahead of the ring (0 = off) */
   int32_t producers;     /* TMA producer threads taking turns by stage (1..3, at    */
                          /* most `stages`; 0 = default)                             */
   int32_t stream_k;      /* -1 off, 0 automatic, 1 on: the k-blocks of the last     */
                          /* waves' tiles are split evenly over all CTAs (pairs)     */
   int32_t dp_tiles;      /* tiles run whole before the split region                 */
-  int32_t reserved;      /* zero                                                    */
+  int32_t swap_ab;       /* 1: the kernel computes C^T = op(B)^T . op(A)^T (the     */
+                         /* skinny-M plan: N on the MMA's 128 rows, M <= bn on its  */
+                         /* narrow side) and writes it transposed into C; tiles_m,  */
+                         /* tiles_n then count tiles of C^T.  0: C directly.        */
   int64_t sk_iters;      /* k-block iterations split evenly (0: no split)           */
   int64_t workspace_bytes; /* bytes of the stream-ordered workspace (repacked       */
                          /* operands, stream-K partial sums and flags)              */

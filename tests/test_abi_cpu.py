@@ -69,8 +69,9 @@ def test_planner_reproduces_the_pages_resource_numbers():
                                    (8192, 8192, 8192), (1, 1, 1)])
 def test_plan_tiles_cover_the_output_exactly_once(M, N, K):
     p = tl.tl_gemm_plan(M, N, K, num_sms=148)
-    assert p.tiles_m * p.bm >= M > (p.tiles_m - 1) * p.bm
-    assert p.tiles_n * p.bn >= N > (p.tiles_n - 1) * p.bn
+    rows, cols = (N, M) if p.swap_ab else (M, N)    # swap_ab: tiles of C^T
+    assert p.tiles_m * p.bm >= rows > (p.tiles_m - 1) * p.bm
+    assert p.tiles_n * p.bn >= cols > (p.tiles_n - 1) * p.bn
     assert p.k_blocks * p.bk >= K > (p.k_blocks - 1) * p.bk
     assert p.tiles == p.tiles_m * p.tiles_n
     cg = p.bm // 128                       # CTAs per tile
@@ -84,7 +85,7 @@ def test_plan_tiles_cover_the_output_exactly_once(M, N, K):
         assert p.sk_iters == (p.tiles - p.dp_tiles) * p.k_blocks
         assert p.workspace_bytes == p.grid * 128 * p.bn * 4 + p.grid * 4 * 8
     assert p.smem_bytes <= 232448
-    assert p.tmem_cols in (128, 256, 512)
+    assert p.tmem_cols == max(32, 2 * p.bn) and p.tmem_cols in (32, 64, 128, 256, 512)
     assert p.tx_bytes == (128 + p.bn // cg) * p.bk * 2
 
 
@@ -92,17 +93,18 @@ def test_every_supported_tiling_fits_shared_memory_and_others_are_rejected():
     for bm, bn, bk, max_stages in ((128, 64, 64, 8), (128, 128, 64, 6), (128, 256, 64, 4),
                                    (256, 128, 64, 8), (256, 256, 64, 6), (128, 64, 128, 4),
                                    (128, 128, 128, 3), (128, 256, 128, 2), (256, 128, 128, 4),
-                                   (256, 256, 128, 3)):
+                                   (256, 256, 128, 3), (128, 16, 128, 6), (128, 32, 128, 5)):
         for stages in range(2, max_stages + 1):
-            p = tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, stages)
+            p = tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, stages, trans_b=1)
             assert p.smem_bytes <= 232448
             assert p.grid % (bm // 128) == 0
             assert p.ring_bytes == stages * (128 * bk + (bn // (bm // 128)) * bk) * 2
         if max_stages < 8:
             with pytest.raises(tl.TLError):
-                tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, max_stages + 1)
+                tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, max_stages + 1, trans_b=1)
     for bad in ((64, 128, 64, 3), (128, 96, 64, 3), (128, 128, 32, 3), (128, 128, 64, 1),
-                (128, 128, 64, 9), (256, 64, 64, 4), (512, 256, 64, 4), (128, 128, 256, 2)):
+                (128, 128, 64, 9), (256, 64, 64, 4), (512, 256, 64, 4), (128, 128, 256, 2),
+                (128, 16, 64, 4), (128, 32, 64, 4), (256, 32, 128, 4), (128, 8, 128, 4)):
         with pytest.raises(tl.TLError):
             tl.tl_plan_complete(1024, 1024, 1024, *bad)
 
@@ -123,6 +125,31 @@ def test_stream_k_split_choices():
     assert p.sk_iters == 0 and p.dp_tiles == 256
     with pytest.raises(tl.TLError):
         tl.tl_plan_complete(64, 64, 64, 128, 64, 64, 3, stream_k=2)
+
+
+def test_skinny_products_swap_operands():
+    # M <= 32 against long N and K: the kernel runs on C^T with M as the MMA's N,
+    # the 64 tiles of 128 rows of C^T split by k-block over all SMs
+    for M, bn, stages in ((1, 16, 6), (16, 16, 6), (17, 32, 5), (32, 32, 5)):
+        p = tl.tl_gemm_plan(M, 8192, 8192, dtype=tl.TL_BF16, trans_b=1, num_sms=152)
+        assert p.swap_ab == 1 and (p.bm, p.bn, p.bk, p.stages) == (128, bn, 128, stages)
+        assert (p.tiles_m, p.tiles_n, p.k_blocks) == (64, 1, 64)
+        assert p.dp_tiles == 0 and p.sk_iters == 64 * 64 and p.grid == 152
+        assert p.tma_store == 0 and p.tx_bytes == (128 + bn) * 128 * 2
+    # wider M, an M-major A, short N or K: the direct form
+    assert tl.tl_gemm_plan(64, 8192, 8192, trans_b=1).swap_ab == 0
+    assert tl.tl_gemm_plan(16, 8192, 8192, trans_a=1).swap_ab == 0
+    assert tl.tl_gemm_plan(16, 1024, 8192).swap_ab == 0
+    assert tl.tl_gemm_plan(16, 8192, 512).swap_ab == 0
+    # narrow tiles need the kernel's B operand K-major
+    tl.tl_plan_complete(4096, 4096, 4096, 128, 16, 128, 4, trans_b=1)
+    with pytest.raises(tl.TLError):
+        tl.tl_plan_complete(4096, 4096, 4096, 128, 16, 128, 4, trans_b=0)
+    tl.tl_plan_complete(16, 4096, 4096, 128, 16, 128, 4, trans_a=0, swap_ab=1)
+    with pytest.raises(tl.TLError):
+        tl.tl_plan_complete(16, 4096, 4096, 128, 16, 128, 4, trans_a=1, swap_ab=1)
+    with pytest.raises(tl.TLError):
+        tl.tl_plan_complete(16, 4096, 4096, 128, 64, 128, 4, swap_ab=2)
 
 
 def test_planner_rejects_bad_arguments():

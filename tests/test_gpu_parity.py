@@ -113,6 +113,39 @@ def test_stream_k_split_bit_exact(bm, bn, bk, stages, M, N, K, grid):
     _check_full(_w(M, N, K, BF16, True, False, False, "uniform", M + N + K + bn), plan=plan)
 
 
+# Skinny products on C^T (swap_ab): the kernel's rows are N, its narrow columns M, and
+# it writes C transposed with plain stores.  Narrow tiles (bn 16, 32) need A K-major.
+SWAP_CASES = [
+    # bn, stages, M, N, K, trans_a, trans_b, stream_k
+    (16, 6, 1, 1000, 1100, False, True, 1),       # one row of C, ragged N and K
+    (16, 6, 16, 2100, 1024, False, False, 1),     # M-major B (the kernel's A)
+    (16, 4, 7, 300, 777, False, True, -1),        # whole tiles, ragged K tail
+    (32, 5, 17, 1300, 2000, False, True, 1),
+    (32, 3, 32, 129, 130, False, False, -1),
+    (64, 4, 64, 2000, 1500, True, True, 1),       # M-major A needs 64-wide boxes
+    (64, 4, 50, 700, 300, True, False, -1),
+    (128, 3, 128, 1500, 2100, False, True, 1),
+    (128, 3, 100, 333, 1000, True, True, 0),
+]
+
+
+@pytest.mark.parametrize("bn,stages,M,N,K,ta,tb,sk", SWAP_CASES)
+def test_swapped_operands_for_skinny_products(bn, stages, M, N, K, ta, tb, sk):
+    plan = tl.plan_for(0, 0, 0, 128, bn, 128, stages, raster_group=4, stream_k=sk, swap_ab=1)
+    _check_full(_w(M, N, K, F16, ta, tb, True, "int_small", M + N + K + bn),
+                plan=plan, exact=True)
+    _check_full(_w(M, N, K, BF16, ta, tb, False, "uniform", M + N + K + 3), plan=plan)
+
+
+@pytest.mark.parametrize("bn,stages", [(16, 6), (32, 5)])
+def test_narrow_tiles_without_swap(bn, stages):
+    # N itself narrow: bn 16/32 tiles of C with a K-major B (trans_b)
+    plan = tl.plan_for(0, 0, 0, 128, bn, 128, stages, raster_group=2)
+    _check_full(_w(700, bn + 5, 900, BF16, False, True, True, "int_unit", 71 + bn),
+                plan=plan, exact=True)
+    _check_full(_w(300, bn - 3, 1300, F16, True, True, False, "uniform", 72 + bn), plan=plan)
+
+
 def test_stream_k_results_are_deterministic_and_replay_in_graphs():
     w = _w(1024, 1024, 1024, F16, False, False, True, "uniform", 90)
     a, b = workloads.make_inputs(w)

@@ -54,12 +54,12 @@ class Plan(ctypes.Structure):
         ("repack_b", ctypes.c_int32), ("tma_store", ctypes.c_int32),
         ("l2_prefetch", ctypes.c_int32), ("producers", ctypes.c_int32),
         ("stream_k", ctypes.c_int32), ("dp_tiles", ctypes.c_int32),
-        ("reserved", ctypes.c_int32), ("sk_iters", ctypes.c_int64),
+        ("swap_ab", ctypes.c_int32), ("sk_iters", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
-        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 def _load() -> ctypes.CDLL:
@@ -139,9 +139,10 @@ def tl_gemm_plan(M: int, N: int, K: int, dtype: int = TL_F16, trans_a: int = 0,
 def tl_plan_complete(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
                      dtype: int = TL_F16, trans_a: int = 0, trans_b: int = 0,
                      num_sms: int = 0, raster_group: int = 16, grid: int = 0,
-                     l2_prefetch: int = -1, producers: int = 0, stream_k: int = 0) -> Plan:
+                     l2_prefetch: int = -1, producers: int = 0, stream_k: int = 0,
+                     swap_ab: int = 0) -> Plan:
     pl = Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
-              l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k)
+              l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k, swap_ab=swap_ab)
     st = _lib.tl_plan_complete(M, N, K, dtype, trans_a, trans_b, num_sms, ctypes.byref(pl))
     if st != TL_OK:
         raise TLError(st, "tl_plan_complete")
@@ -231,9 +232,11 @@ def gemm(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool = Fal
 
 def plan_for(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
              raster_group: int = 16, grid: int = 0, l2_prefetch: int = -1,
-             producers: int = 0, stream_k: int = 0) -> Plan:
+             producers: int = 0, stream_k: int = 0, swap_ab: int = 0) -> Plan:
     """A plan with a fixed tiling, to pass as ``gemm(..., plan=...)``; l2_prefetch < 0,
     producers <= 0 and stream_k = 0 take the library's defaults for the problem
-    (stream_k -1 forces whole tiles only, 1 forces the split of the last waves)."""
+    (stream_k -1 forces whole tiles only, 1 forces the split of the last waves);
+    swap_ab = 1 runs the kernel on C^T = op(B)^T op(A)^T (bm x bn tiles of C^T)."""
     return Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
-                l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k)
+                l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k,
+                swap_ab=swap_ab)

@@ -61,6 +61,13 @@ constexpr int kEpiWarps = 4;
 constexpr int kChunk = 64;            // epilogue columns per staging chunk (128 B)
 constexpr uint32_t kStagingBytes = kEpiWarps * 2 * 32 * 128;  // 2 x (32 rows x 128 B) per warp
 
+// Shared staging for the TMA store of C: 64-column chunks, so tiles narrower than 64
+// columns (which write C with plain stores) need none.
+template <int BN>
+__host__ __device__ constexpr uint32_t staging_bytes() {
+  return BN >= kChunk ? kStagingBytes : 0u;
+}
+
 // Status word layout (device global, first timeout wins):
 //   bits 0-7  tl_status (8 = timeout), bits 8-15 wait site, bits 16-31 blockIdx.x
 enum WaitSite : uint32_t {
@@ -81,6 +88,8 @@ struct GemmParams {
   int32_t bf16;
   int32_t relu;
   int32_t tma_store;        // 1: TMA bulk store of C; 0: predicated st.global
+  int32_t c_trans;          // 1: the kernel computes C^T (operands swapped by the host):
+                            // its element (i, j) goes to C[j * ldc + i], plain stores
   int32_t l2_prefetch;      // k-blocks the producer prefetches into L2 ahead of the ring
   int32_t a3d, b3d;         // operand map is the 3-D view {64, rows, chunks} (one box
                             // per stage) instead of 2-D boxes of one 64-chunk each
@@ -123,8 +132,8 @@ __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
 template <int BN, int CG, int BK>
 __host__ __device__ constexpr uint32_t smem_bytes_for(int stages) {
   // +1024: the dynamic shared memory base is rounded up to 1024 B in the kernel
-  return 1024u + stages * (a_stage_bytes<BK>() + b_stage_bytes<BN, CG, BK>()) + kStagingBytes +
-         barrier_bytes(stages);
+  return 1024u + stages * (a_stage_bytes<BK>() + b_stage_bytes<BN, CG, BK>()) +
+         staging_bytes<BN>() + barrier_bytes(stages);
 }
 
 // Grouped raster order: walk `group` tile-rows top to bottom, then the next column.
@@ -244,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tl_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
-  static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
+  static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128 || BN == 256,
+                "BN must be 16, 32, 64, 128 or 256");
   static_assert(CG == 1 || (CG == 2 && BN >= 128), "pairs need BN/2 >= 64");
   constexpr bool kPair = CG == 2;
   static_assert(BK == 64 || BK == 128, "BK must be 64 or 128");
@@ -253,7 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kAStageBytes = a_stage_bytes<BK>();
   constexpr uint32_t kBStage = b_stage_bytes<BN, CG, BK>();
   constexpr uint32_t kMNChunkBytes = 128u * BK;            // one 64(MN) x BK(K) chunk
-  constexpr uint32_t kTmemCols = 2 * BN;                   // two accumulators, power of 2
+  constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;   // two accumulators; the
+                                                               // allocation unit is 32
+  // Epilogue columns per step: one 128-byte staging row, or the whole tile when it is
+  // narrower (then K-major B only: a 64-wide M/N-major box would not fit the tile).
+  constexpr int kEC = BN < kChunk ? BN : kChunk;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -264,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sA = base;
   const uint32_t sB = sA + S * kAStageBytes;
   const uint32_t sC = sB + S * kBStage;
-  const uint32_t sBar = sC + kStagingBytes;
+  const uint32_t sBar = sC + staging_bytes<BN>();
   auto full_bar = [&](int s) { return sBar + 8u * s; };
   auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
   auto tfull_bar = [&](int a) { return sBar + 8u * (2 * S + a); };
@@ -551,12 +565,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / kChunk; ++c) {
-        uint32_t v[64];
-        tmem_load_32cols(t_row + c * kChunk, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_load_32cols(t_row + c * kChunk + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      for (int c = 0; c < BN / kEC; ++c) {
+        uint32_t v[kEC];
+        if constexpr (kEC == 16) {
+          tmem_load_16cols(t_row + c * kEC, v);
+        } else {
+#pragma unroll
+          for (int h = 0; h < kEC / 32; ++h)
+            tmem_load_32cols(t_row + c * kEC + 32 * h,
+                             *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+        }
         tmem_load_wait();
-        if (c == BN / kChunk - 1) {
+        if (c == BN / kEC - 1) {
           // the whole accumulator is in registers: hand the buffer back to the MMA
           tc_fence_before_sync();
           __syncwarp();
@@ -568,51 +588,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (store_partial) {
           // fp32 partial sum: for each column the warp's 32 lanes write 128 B
 #pragma unroll
-          for (int j = 0; j < 64; ++j) __stcg(partial_at(cluster_id, c * kChunk + j), __uint_as_float(v[j]));
+          for (int j = 0; j < kEC; ++j)
+            __stcg(partial_at(cluster_id, c * kEC + j), __uint_as_float(v[j]));
           continue;
         }
         // finisher: add the later k-blocks' partials, in unit order
         for (int u2 = cluster_id + 1; u2 < v_end; ++u2) {
           if (!contributes(u2)) continue;
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
-            v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(partial_at(u2, c * kChunk + j)));
+          for (int j = 0; j < kEC; ++j)
+            v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(partial_at(u2, c * kEC + j)));
         }
-        uint32_t packed[32];
+        uint32_t packed[kEC / 2];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < kEC / 2; ++j) {
           packed[j] = pack2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), p.bf16,
                             p.relu);
         }
-        if (p.tma_store) {
-          const uint32_t buf = sC + (ew * 2 + sbuf) * 4096u;
-          if (lane == 0) bulk_wait_group_read<1>();   // the store two chunks ago has read buf
-          __syncwarp();
-          // row `lane` of the 32 x 64 staging box, 128-byte swizzle: 16-byte chunk j
-          // lands at chunk j ^ (row % 8)
-          const uint32_t row_addr = buf + lane * 128u;
+        const int row = m0 + q * 32 + lane;      // this lane's row of the kernel's tile
+        const int col0 = n0 + c * kEC;
+        if (p.c_trans) {
+          // The kernel computed C^T: its row `row` is column `row` of C, and each of
+          // its columns is a row of C that the warp's 32 lanes write as 64 contiguous
+          // bytes.
+          if (row < p.M) {
+            uint16_t* ccol = reinterpret_cast<uint16_t*>(p.C) + row;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t dst = row_addr + ((j ^ (lane & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                         "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
-                         "r"(packed[4 * j + 3])
-                         : "memory");
+            for (int j = 0; j < kEC / 2; ++j) {
+              const int col = col0 + 2 * j;
+              if (col < p.N) ccol[static_cast<int64_t>(col) * p.ldc] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
+              if (col + 1 < p.N) ccol[static_cast<int64_t>(col + 1) * p.ldc] = static_cast<uint16_t>(packed[j] >> 16);
+            }
           }
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0 && m0 + q * 32 < p.M && n0 + c * kChunk < p.N) {
-            tma_store_2d(&tmap_c, buf, n0 + c * kChunk, m0 + q * 32);   // clipped at M, N
+        } else if (kEC == kChunk && p.tma_store) {
+          if constexpr (kEC == kChunk) {
+            const uint32_t buf = sC + (ew * 2 + sbuf) * 4096u;
+            if (lane == 0) bulk_wait_group_read<1>();   // the store two chunks ago has read buf
+            __syncwarp();
+            // row `lane` of the 32 x 64 staging box, 128-byte swizzle: 16-byte chunk j
+            // lands at chunk j ^ (row % 8)
+            const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t dst = row_addr + ((j ^ (lane & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                           "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
+                           "r"(packed[4 * j + 3])
+                           : "memory");
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && m0 + q * 32 < p.M && col0 < p.N) {
+              tma_store_2d(&tmap_c, buf, col0, m0 + q * 32);   // clipped at M, N
+            }
+            if (lane == 0) bulk_commit_group();   // (an empty group keeps the count uniform)
+            sbuf ^= 1u;
           }
-          if (lane == 0) bulk_commit_group();   // (an empty group keeps the count uniform)
-          sbuf ^= 1u;
         } else {
-          const int row = m0 + q * 32 + lane;
           if (row < p.M) {
             uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
-            const int col0 = n0 + c * kChunk;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < kEC / 2; ++j) {
               const int col = col0 + 2 * j;
               if (col < p.N) crow[col] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
               if (col + 1 < p.N) crow[col + 1] = static_cast<uint16_t>(packed[j] >> 16);

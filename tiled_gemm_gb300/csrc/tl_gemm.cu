@@ -47,7 +47,7 @@ struct DeviceState {
   int smem_optin = 0;                        // max dynamic shared memory per CTA
   uint32_t* status = nullptr;
   std::atomic<uint32_t> attr_done{0};        // bit i: smem attribute set for kernel i
-  int max_units[12] = {};                      // resident CTAs (pairs) per kernel
+  int max_units[16] = {};                    // resident CTAs (pairs) per kernel
   std::mutex mu;
 };
 
@@ -122,11 +122,21 @@ tl_status check_device_pointer(const void* p, int dev) {
 
 // bm = 128: one CTA per 128 x bn tile.  bm = 256: a CTA pair (cluster of 2,
 // cta_group::2 MMAs) per 256 x bn tile, each CTA holding half of B's columns.
+// Narrow tiles (bn 16 or 32, for skinny products) come with 128-deep stages only.
 bool plan_supported(const tl_plan& pl) {
-  const bool bn_ok = (pl.bm == 128 && (pl.bn == 64 || pl.bn == 128 || pl.bn == 256)) ||
+  const bool narrow = pl.bm == 128 && (pl.bn == 16 || pl.bn == 32) && pl.bk == 128;
+  const bool bn_ok = narrow ||
+                     (pl.bm == 128 && (pl.bn == 64 || pl.bn == 128 || pl.bn == 256)) ||
                      (pl.bm == 256 && (pl.bn == 128 || pl.bn == 256));
   return bn_ok && (pl.bk == 64 || pl.bk == 128) && pl.stages >= 2 && pl.stages <= 8 &&
-         pl.raster_group >= 1 && pl.grid >= 0;
+         pl.raster_group >= 1 && pl.grid >= 0 && (pl.swap_ab == 0 || pl.swap_ab == 1);
+}
+
+// Narrow tiles read B in 64-element K chunks of bn rows: the kernel's B operand must
+// be K-major.  With swap_ab the kernel's B is A, K-major when A is not transposed.
+bool narrow_ok(const tl_plan& pl, int trans_a, int trans_b) {
+  if (pl.bn >= 64) return true;
+  return pl.swap_ab ? trans_a == 0 : trans_b == 1;
 }
 
 template <int BK>
@@ -134,6 +144,10 @@ uint32_t smem_for_bk(int bm, int bn, int stages) {
   if (bm == 256) {
     return bn == 128 ? tl::smem_bytes_for<128, 2, BK>(stages)
                      : tl::smem_bytes_for<256, 2, BK>(stages);
+  }
+  if constexpr (BK == 128) {
+    if (bn == 16) return tl::smem_bytes_for<16, 1, BK>(stages);
+    if (bn == 32) return tl::smem_bytes_for<32, 1, BK>(stages);
   }
   switch (bn) {
     case 64: return tl::smem_bytes_for<64, 1, BK>(stages);
@@ -209,10 +223,12 @@ int64_t split_workspace_bytes(const tl_plan& pl) {
   return static_cast<int64_t>(pl.grid) * 128 * pl.bn * 4 + static_cast<int64_t>(pl.grid) * 4 * 8;
 }
 
-tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* pl) {
-  if (!plan_supported(*pl)) return TL_ERR_INVALID_ARG;
+tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, int num_sms,
+                        tl_plan* pl) {
+  if (!plan_supported(*pl) || !narrow_ok(*pl, trans_a, trans_b)) return TL_ERR_INVALID_ARG;
   const int sms = num_sms > 0 ? num_sms : kDefaultSms;
   const int cg = pl->bm / 128;                       // CTAs per tile
+  if (pl->swap_ab) std::swap(M, N);                  // the kernel computes C^T
   pl->tiles_m = ceil_div(M, pl->bm);
   pl->tiles_n = ceil_div(N, pl->bn);
   pl->tiles = pl->tiles_m * pl->tiles_n;
@@ -221,7 +237,9 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* p
   pl->ring_bytes = static_cast<int64_t>(pl->stages) * (128 * pl->bk + (pl->bn / cg) * pl->bk) * 2;
   pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages);
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
-  pl->tmem_cols = 2 * pl->bn;
+  pl->tmem_cols = std::max(32, 2 * pl->bn);
+  pl->tma_store = (!pl->swap_ab && pl->bn >= 64) ? 1 : 0;   // for a 16-byte aligned C
+  pl->repack_a = pl->repack_b = 0;                            // ditto for A and B
   pl->tx_bytes = (128 + pl->bn / cg) * pl->bk * 2;
   if (pl->tiles > (int64_t{1} << 31) - 1) return TL_ERR_UNSUPPORTED;
   if (pl->stream_k < -1 || pl->stream_k > 1) return TL_ERR_INVALID_ARG;
@@ -233,7 +251,6 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* p
   // producers take turns by stage: at most one per ring slot, at most three warps
   const int max_prod = std::min(3, pl->stages);
   pl->producers = pl->producers <= 0 ? max_prod : std::min(pl->producers, max_prod);
-  pl->reserved = 0;
   pl->workspace_bytes = split_workspace_bytes(*pl);
   return TL_OK;
 }
@@ -241,8 +258,28 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int num_sms, tl_plan* p
 // Choose BN and the ring depth: fewest waves of tiles over the SMs, weighted by the
 // per-tile cost of each width (narrower tiles re-read A more often and issue
 // smaller MMAs).  Depth fills the shared memory left after the staging buffers.
-void choose_tiling(int64_t M, int64_t N, int64_t K, int sms, tl_plan* pl) {
-  (void)K;
+void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int sms, tl_plan* pl) {
+  pl->raster_group = 16;
+  pl->grid = 0;
+  pl->l2_prefetch = -1;
+  pl->swap_ab = 0;
+  // Very skinny products (M <= 32 rows against a long N and K) stream B from memory
+  // once and are bound by that stream.  Computing C^T = op(B)^T op(A)^T puts N on
+  // the MMA's 128 rows and M on its narrow N side, so each stage carries 32 KB of B
+  // instead of 16 KB beside a mostly empty 128-row tile of A; the 128-row tiles of
+  // C^T are then split by k-block over all SMs (stream-K), with small fp32 partials.
+  // Measured on GB300 at N = K = 8192 this gains ~7 % at M = 16, while at M = 64 and
+  // 128 the split's fix-up costs more than it saves (128 x 64 tiles stay faster).
+  // An M-major A (trans_a) cannot feed boxes narrower than 64, so it keeps the
+  // direct form.
+  if (M <= 32 && !trans_a && N >= 2048 && K >= 1024) {
+    pl->bm = 128;
+    pl->bn = M <= 16 ? 16 : 32;
+    pl->bk = 128;
+    pl->stages = pl->bn == 16 ? 6 : 5;
+    pl->swap_ab = 1;
+    return;
+  }
   // Relative time of one tile per unit of K.  Shared memory (~128 B/clk per SM)
   // carries both the TMA writes and the MMA operand reads, so a 1-CTA 128 x N tile
   // needs 128 (128 + N) / N bytes per MMA cycle: 192 for N = 256, 256 for N = 128;
@@ -273,9 +310,6 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int sms, tl_plan* pl) {
   pl->bn = cands[pick].bn;
   pl->bk = cands[pick].bk;
   pl->stages = cands[pick].stages;
-  pl->raster_group = 16;
-  pl->grid = 0;
-  pl->l2_prefetch = -1;
 }
 
 
@@ -305,7 +339,8 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
 // -1 if the attribute could not be set.
 template <int BN, int CG, int BK>
 int prepare_kernel(DeviceState* st) {
-  constexpr int kIdx = (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) + 6 * (BK == 128);
+  constexpr int kIdx = BN < 64 ? 12 + (BN == 32)
+                               : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) + 6 * (BK == 128);
   constexpr uint32_t bit = 1u << kIdx;
   if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
   std::lock_guard<std::mutex> lock(st->mu);
@@ -337,6 +372,10 @@ int prepare_kernel(DeviceState* st) {
 template <int BK>
 int resident_units_bk(DeviceState* st, int bm, int bn) {
   if (bm == 256) return bn == 128 ? prepare_kernel<128, 2, BK>(st) : prepare_kernel<256, 2, BK>(st);
+  if constexpr (BK == 128) {
+    if (bn == 16) return prepare_kernel<16, 1, BK>(st);
+    if (bn == 32) return prepare_kernel<32, 1, BK>(st);
+  }
   switch (bn) {
     case 64: return prepare_kernel<64, 1, BK>(st);
     case 128: return prepare_kernel<128, 1, BK>(st);
@@ -374,6 +413,10 @@ tl_status launch_tiling(DeviceState* st, const tl_plan& pl, const CUtensorMap& t
   if (pl.bm == 256) {
     return pl.bn == 128 ? launch_bn<128, 2, BK>(st, pl, ta, tb, tc, prm, stream)
                         : launch_bn<256, 2, BK>(st, pl, ta, tb, tc, prm, stream);
+  }
+  if constexpr (BK == 128) {
+    if (pl.bn == 16) return launch_bn<16, 1, BK>(st, pl, ta, tb, tc, prm, stream);
+    if (pl.bn == 32) return launch_bn<32, 1, BK>(st, pl, ta, tb, tc, prm, stream);
   }
   switch (pl.bn) {
     case 64: return launch_bn<64, 1, BK>(st, pl, ta, tb, tc, prm, stream);
@@ -518,10 +561,11 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     pl.l2_prefetch = forced->l2_prefetch;
     pl.producers = forced->producers;
     pl.stream_k = forced->stream_k;
+    pl.swap_ab = forced->swap_ab;
   } else {
-    choose_tiling(M, N, K, st->sms, &pl);
+    choose_tiling(M, N, K, trans_a, st->sms, &pl);
   }
-  if ((s = complete_plan(M, N, K, st->sms, &pl)) != TL_OK) return s;
+  if ((s = complete_plan(M, N, K, trans_a, trans_b, st->sms, &pl)) != TL_OK) return s;
   if (pl.smem_bytes > st->smem_optin) return TL_ERR_INVALID_ARG;
   // Re-split over the units this device really keeps resident (CTA pairs: the cluster
   // occupancy can be below SMs / 2).  Callers that cannot allocate get whole tiles only:
@@ -587,7 +631,18 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
       return TL_ERR_LAUNCH;
     }
   }
-  const bool tma_store = tma_ok(C, ldc);
+  // The kernel's operands: (A, B) as given, or (B, A) with their transposes flipped
+  // when it computes C^T = op(B)^T op(A)^T.
+  struct Operand {
+    const void* ptr;
+    int64_t ld;
+    int trans;
+  };
+  const bool swap = pl.swap_ab != 0;
+  const int64_t kM = swap ? N : M, kN = swap ? M : N;
+  const Operand ka = swap ? Operand{b_use, ldb_w, !trans_b} : Operand{a_use, lda_w, trans_a};
+  const Operand kb = swap ? Operand{a_use, lda_w, !trans_a} : Operand{b_use, ldb_w, trans_b};
+  const bool tma_store = !swap && pl.bn >= 64 && tma_ok(C, ldc);
 
   // Operand maps.  One box per stage (a 3-D view) when the operand's contiguous extent
   // is a multiple of 64 and the stage spans several 64-element chunks; otherwise 2-D
@@ -599,19 +654,19 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   const uint32_t kchunks = static_cast<uint32_t>(pl.bk / 64);
   bool enc_ok = true;
   bool a3d = false, b3d = false;
-  if (!trans_a) {
-    a3d = kchunks > 1 && encode_chunked_3d(&ta, dtype, a_use, K, M, lda_w, 128, kchunks);
-    if (!a3d) enc_ok &= encode_2d(&ta, dtype, a_use, K, M, lda_w, 64, 128);
+  if (!ka.trans) {
+    a3d = kchunks > 1 && encode_chunked_3d(&ta, dtype, ka.ptr, K, kM, ka.ld, 128, kchunks);
+    if (!a3d) enc_ok &= encode_2d(&ta, dtype, ka.ptr, K, kM, ka.ld, 64, 128);
   } else {
-    a3d = encode_chunked_3d(&ta, dtype, a_use, M, K, lda_w, pl.bk, 2);
-    if (!a3d) enc_ok &= encode_2d(&ta, dtype, a_use, M, K, lda_w, 64, pl.bk);
+    a3d = encode_chunked_3d(&ta, dtype, ka.ptr, kM, K, ka.ld, pl.bk, 2);
+    if (!a3d) enc_ok &= encode_2d(&ta, dtype, ka.ptr, kM, K, ka.ld, 64, pl.bk);
   }
-  if (trans_b) {
-    b3d = kchunks > 1 && encode_chunked_3d(&tb, dtype, b_use, K, N, ldb_w, bn_cta, kchunks);
-    if (!b3d) enc_ok &= encode_2d(&tb, dtype, b_use, K, N, ldb_w, 64, bn_cta);
+  if (kb.trans) {
+    b3d = kchunks > 1 && encode_chunked_3d(&tb, dtype, kb.ptr, K, kN, kb.ld, bn_cta, kchunks);
+    if (!b3d) enc_ok &= encode_2d(&tb, dtype, kb.ptr, K, kN, kb.ld, 64, bn_cta);
   } else {
-    b3d = bn_cta > 64 && encode_chunked_3d(&tb, dtype, b_use, N, K, ldb_w, pl.bk, bn_cta / 64);
-    if (!b3d) enc_ok &= encode_2d(&tb, dtype, b_use, N, K, ldb_w, 64, pl.bk);
+    b3d = bn_cta > 64 && encode_chunked_3d(&tb, dtype, kb.ptr, kN, K, kb.ld, pl.bk, bn_cta / 64);
+    if (!b3d) enc_ok &= encode_2d(&tb, dtype, kb.ptr, kN, K, kb.ld, 64, pl.bk);
   }
   if (tma_store) enc_ok &= encode_2d(&tc, dtype, C, N, M, ldc, 64, 32);
   if (!enc_ok) {
@@ -621,8 +676,8 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
 
   tl::GemmParams prm;
   std::memset(&prm, 0, sizeof(prm));
-  prm.M = static_cast<int32_t>(M);
-  prm.N = static_cast<int32_t>(N);
+  prm.M = static_cast<int32_t>(kM);
+  prm.N = static_cast<int32_t>(kN);
   prm.K = static_cast<int32_t>(K);
   prm.tiles_m = static_cast<int32_t>(pl.tiles_m);
   prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
@@ -630,11 +685,12 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
   prm.stages = pl.stages;
   prm.raster_group = pl.raster_group;
-  prm.trans_a = trans_a;
-  prm.trans_b = trans_b;
+  prm.trans_a = ka.trans;
+  prm.trans_b = kb.trans;
   prm.bf16 = dtype == TL_BF16 ? 1 : 0;
   prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
   prm.tma_store = tma_store ? 1 : 0;
+  prm.c_trans = swap ? 1 : 0;
   prm.l2_prefetch = pl.l2_prefetch;
   prm.a3d = a3d ? 1 : 0;
   prm.b3d = b3d ? 1 : 0;
@@ -644,7 +700,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.sk_partials = sk_partials;
   prm.sk_flags = sk_flags;
   prm.sk_token = next_split_token();
-  prm.idesc = tl::mma_idesc_f16(prm.bf16, trans_a ? 1u : 0u, trans_b ? 0u : 1u,
+  prm.idesc = tl::mma_idesc_f16(prm.bf16, ka.trans ? 1u : 0u, kb.trans ? 0u : 1u,
                                 static_cast<uint32_t>(pl.bm), static_cast<uint32_t>(pl.bn));
   prm.C = C;
   prm.ldc = ldc;
@@ -689,8 +745,8 @@ tl_status tl_gemm_plan(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int tran
   if (s != TL_OK) return s;
   std::memset(plan, 0, sizeof(*plan));
   const int sms = num_sms > 0 ? num_sms : kDefaultSms;
-  choose_tiling(M, N, K, sms, plan);
-  return complete_plan(M, N, K, sms, plan);
+  choose_tiling(M, N, K, trans_a, sms, plan);
+  return complete_plan(M, N, K, trans_a, trans_b, sms, plan);
 }
 
 tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
@@ -702,11 +758,13 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
   const int32_t pf = plan->l2_prefetch;
   const int32_t prod = plan->producers;
   const int32_t sk = plan->stream_k;
+  const int32_t swap = plan->swap_ab;
   std::memset(&plan->tiles_m, 0, sizeof(tl_plan) - offsetof(tl_plan, tiles_m));
   plan->l2_prefetch = pf;
   plan->producers = prod;
   plan->stream_k = sk;
-  return complete_plan(M, N, K, num_sms, plan);
+  plan->swap_ab = swap;
+  return complete_plan(M, N, K, trans_a, trans_b, num_sms, plan);
 }
 
 tl_status tl_gemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
