@@ -269,6 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // narrower (then K-major B only: a 64-wide M/N-major box would not fit the tile).
   constexpr int kEC = BN < kChunk ? BN : kChunk;
 
+  // The next kernel in the stream may start its set-up now (it waits for this grid to
+  // complete before it touches global memory, see grid_dependency_wait below).
+  grid_launch_dependents();
+  if (threadIdx.x == 64) {   // an epilogue warp, idle during set-up: fetch the maps early
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+    if (p.tma_store) tma_prefetch_map(&tmap_c);   // (else the map is left unencoded)
+  }
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -320,11 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 8; ++s) lap_armed[s] = -1;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_map(&tmap_a);
-    tma_prefetch_map(&tmap_b);
-    if (p.tma_store) tma_prefetch_map(&tmap_c);
-  }
   if (warp == 1) {
     if constexpr (kPair) {
       tmem_alloc_pair(slot, kTmemCols);
@@ -339,6 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (kPair) cluster_sync_all();   // the peer's barriers exist before any use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot_ptr;
+  // Everything above touched only this CTA's shared and Tensor Memory.  The operands,
+  // C and the split workspace may still be in use by the previous kernel of the
+  // stream: every role passes grid_dependency_wait() before its first global access
+  // and before its first bounded wait (so a long previous kernel cannot run down a
+  // wait's limit).  The producers first work out their first box.
 
   if (warp == 0 || warp >= 6) {
     // ----------------------------------------------------------- producers --
@@ -404,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords(w.tile, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
         const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;    // this CTA's A rows
         const int nb0 = nb * BN + static_cast<int>(rank) * kBnCta;      // this CTA's B columns
+        if (g == 0) grid_dependency_wait();
         for (int kb = w.k0; kb < w.k1; ++kb, ++g) {
           if (g % n_producers != pi) continue;
           const int stage = g % S;
@@ -430,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer --
+    grid_dependency_wait();
     if (lane == 0 && leader) {
       const uint32_t a_lbo = p.trans_a ? kMNChunkBytes : 16u;
       const uint32_t b_lbo = p.trans_b ? 16u : kMNChunkBytes;
@@ -501,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------- epilogue --
+    grid_dependency_wait();
     const int q = warp & 3;                // Tensor Memory lane quadrant of this warp
     const int ew = warp - 2;               // staging-buffer owner index
     uint32_t acc = 0, acc_phase = 0;

@@ -29,6 +29,19 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 
 // Makes the initialised barriers visible to the async proxy (TMA, tcgen05).
+// ------------------------------------------------ programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel in the stream is still running, once every CTA of that kernel
+// has signalled launch_dependents (or exited).  wait blocks until the previous
+// grid has completed and its memory operations are visible.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

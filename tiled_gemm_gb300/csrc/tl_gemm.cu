@@ -314,6 +314,11 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int sms, tl_pla
 
 
 
+// Launch attributes: a cluster of two for CTA pairs, and programmatic stream
+// serialization, which lets the kernel start its set-up (barriers, Tensor Memory,
+// descriptor prefetch) while the previous kernel of the stream finishes; the kernel
+// waits for that kernel's completion (griddepcontrol.wait) before it reads or
+// writes global memory.  attr must hold 2 entries.
 template <int BN, int CG, int BK>
 void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t smem,
                    cudaStream_t stream) {
@@ -321,16 +326,19 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
   cfg->blockDim = dim3(tl::kThreads);
   cfg->dynamicSmemBytes = smem;
   cfg->stream = stream;
-  cfg->attrs = nullptr;
-  cfg->numAttrs = 0;
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
   if (CG == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg->attrs = attr;
-    cfg->numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
+  cfg->attrs = attr;
+  cfg->numAttrs = n;
 }
 
 // Once per device and kernel: allow the large dynamic shared memory, and find how many
@@ -354,7 +362,7 @@ int prepare_kernel(DeviceState* st) {
   int units = st->sms / CG;
   if (CG == 2) {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     launch_config<BN, CG, BK>(&cfg, attr, static_cast<size_t>(st->smem_optin), nullptr);
     cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
     int n = 0;
@@ -396,7 +404,7 @@ tl_status launch_bn(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
   if (prepare_kernel<BN, CG, BK>(st) < 0) return TL_ERR_LAUNCH;
   auto kern = tl::tl_gemm_kernel<BN, CG, BK>;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   launch_config<BN, CG, BK>(&cfg, attr, static_cast<size_t>(pl.smem_bytes), stream);
   cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm) != cudaSuccess) {
