@@ -146,6 +146,17 @@ def test_narrow_tiles_without_swap(bn, stages):
     _check_full(_w(300, bn - 3, 1300, F16, True, True, False, "uniform", 72 + bn), plan=plan)
 
 
+@pytest.mark.parametrize("bm,bn,bk,stages", [(128, 64, 64, 4), (128, 256, 128, 2),
+                                             (256, 128, 64, 3), (256, 256, 128, 3)])
+def test_plain_stores_instead_of_tma_stores(bm, bn, bk, stages):
+    # tma_store = -1: C from registers, 16-byte vectors for whole chunks, scalars at the
+    # ragged right edge
+    plan = tl.plan_for(0, 0, 0, bm, bn, bk, stages, raster_group=3, tma_store=-1)
+    _check_full(_w(333, 64 * 7 + 40, 700, F16, False, True, True, "int_small", bm + bn + 5),
+                plan=plan, exact=True)
+    _check_full(_w(512, 512, 256, BF16, True, False, False, "uniform", bm + bn + 6), plan=plan)
+
+
 def test_stream_k_results_are_deterministic_and_replay_in_graphs():
     w = _w(1024, 1024, 1024, F16, False, False, True, "uniform", 90)
     a, b = workloads.make_inputs(w)

@@ -232,11 +232,13 @@ def gemm(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool = Fal
 
 def plan_for(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
              raster_group: int = 16, grid: int = 0, l2_prefetch: int = -1,
-             producers: int = 0, stream_k: int = 0, swap_ab: int = 0) -> Plan:
+             producers: int = 0, stream_k: int = 0, swap_ab: int = 0,
+             tma_store: int = 0) -> Plan:
     """A plan with a fixed tiling, to pass as ``gemm(..., plan=...)``; l2_prefetch < 0,
     producers <= 0 and stream_k = 0 take the library's defaults for the problem
     (stream_k -1 forces whole tiles only, 1 forces the split of the last waves);
-    swap_ab = 1 runs the kernel on C^T = op(B)^T op(A)^T (bm x bn tiles of C^T)."""
+    swap_ab = 1 runs the kernel on C^T = op(B)^T op(A)^T (bm x bn tiles of C^T);
+    tma_store = -1 writes C with plain stores instead of TMA bulk stores."""
     return Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
                 l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k,
-                swap_ab=swap_ab)
+                swap_ab=swap_ab, tma_store=tma_store)

@@ -90,6 +90,8 @@ struct GemmParams {
   int32_t tma_store;        // 1: TMA bulk store of C; 0: predicated st.global
   int32_t c_trans;          // 1: the kernel computes C^T (operands swapped by the host):
                             // its element (i, j) goes to C[j * ldc + i], plain stores
+  int32_t c_vec;            // 1: C's base and pitch are 16-byte aligned: plain stores of
+                            // a full chunk go out as 16-byte vectors
   int32_t l2_prefetch;      // k-blocks the producer prefetches into L2 ahead of the ring
   int32_t a3d, b3d;         // operand map is the 3-D view {64, rows, chunks} (one box
                             // per stage) instead of 2-D boxes of one 64-chunk each
@@ -656,9 +658,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) bulk_commit_group();   // (an empty group keeps the count uniform)
             sbuf ^= 1u;
           }
-        } else {
-          if (row < p.M) {
-            uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
+        } else if (row < p.M) {
+          uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
+          if (p.c_vec && col0 + kEC <= p.N) {
+            // the lane's kEC values are 2 kEC contiguous bytes of its row of C
+            uint4* dst = reinterpret_cast<uint4*>(crow + col0);
+#pragma unroll
+            for (int j = 0; j < kEC / 8; ++j)
+              dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                  packed[4 * j + 3]);
+          } else {
 #pragma unroll
             for (int j = 0; j < kEC / 2; ++j) {
               const int col = col0 + 2 * j;

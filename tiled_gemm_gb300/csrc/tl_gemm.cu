@@ -650,7 +650,11 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   const int64_t kM = swap ? N : M, kN = swap ? M : N;
   const Operand ka = swap ? Operand{b_use, ldb_w, !trans_b} : Operand{a_use, lda_w, trans_a};
   const Operand kb = swap ? Operand{a_use, lda_w, !trans_a} : Operand{b_use, ldb_w, trans_b};
-  const bool tma_store = !swap && pl.bn >= 64 && tma_ok(C, ldc);
+  // C by TMA bulk stores from a swizzled staging buffer, or by plain stores from
+  // registers (16-byte vectors when C is aligned).  A forced plan with tma_store = -1
+  // asks for plain stores.
+  const bool c_aligned = tma_ok(C, ldc);
+  const bool tma_store = !swap && pl.bn >= 64 && c_aligned && !(forced && forced->tma_store < 0);
 
   // Operand maps.  One box per stage (a 3-D view) when the operand's contiguous extent
   // is a multiple of 64 and the stage spans several 64-element chunks; otherwise 2-D
@@ -699,6 +703,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
   prm.tma_store = tma_store ? 1 : 0;
   prm.c_trans = swap ? 1 : 0;
+  prm.c_vec = c_aligned ? 1 : 0;
   prm.l2_prefetch = pl.l2_prefetch;
   prm.a3d = a3d ? 1 : 0;
   prm.b3d = b3d ? 1 : 0;
