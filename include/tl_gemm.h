@@ -227,6 +227,17 @@ tl_status tl_device_status(int reset, uint32_t* detail);
  */
 void tl_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * Test hook for the failure-detection path; not for production use.  mode 1: every
+ * GEMM kernel launched afterwards has its MMA thread wait first on a barrier that
+ * nothing arrives on, as if its operands never came.  The wait runs out after the
+ * limit set by tl_set_wait_timeout_ns(); the kernel then records TL_ERR_TIMEOUT with
+ * wait site 7 in the device status word, every role unwinds (issued loads land,
+ * Tensor Memory is freed) and the kernel returns with C unwritten.  mode 0 (the
+ * default) turns it off.  No compute fault, trap or unbounded wait is involved.
+ */
+void tl_debug_set_stall(int mode);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int tl_version(void);
 

@@ -88,6 +88,8 @@ def _load() -> ctypes.CDLL:
     lib.tl_device_status.restype = ci
     lib.tl_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.tl_set_wait_timeout_ns.restype = None
+    lib.tl_debug_set_stall.argtypes = [ci]
+    lib.tl_debug_set_stall.restype = None
     lib.tl_version.argtypes = []
     lib.tl_version.restype = ci
     return lib
@@ -162,6 +164,12 @@ def tl_device_status(reset: bool = False) -> tuple[int, int]:
 
 def tl_set_wait_timeout_ns(ns: int) -> None:
     _lib.tl_set_wait_timeout_ns(int(ns))
+
+
+def tl_debug_set_stall(mode: int) -> None:
+    """Test hook: 1 makes the following launches' MMA thread wait on a barrier that
+    nothing arrives on, so the bounded wait runs out (TL_ERR_TIMEOUT, site 7); 0 = off."""
+    _lib.tl_debug_set_stall(int(mode))
 
 
 def tl_version() -> int:

@@ -77,6 +77,7 @@ enum WaitSite : uint32_t {
   kSiteEpiTmemFull = 4,
   kSiteDrain = 5,
   kSiteStreamK = 6,
+  kSiteInjected = 7,    // the test hook's wait that nothing ends (GemmParams::stall)
 };
 
 struct GemmParams {
@@ -111,6 +112,8 @@ struct GemmParams {
   int64_t ldc;
   uint32_t* status;         // device status word (never NULL)
   uint64_t timeout_ns;
+  int32_t stall;            // test hook: 1 = the MMA thread first waits on a barrier that
+                            // nothing arrives on, so the wait runs out and every role unwinds
 };
 
 // Shared memory of one stage in one CTA: A is 128 rows x BK, B is BN/CG columns x BK.
@@ -459,6 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
+      if (p.stall) {
+        // Nothing arrives on "done" before the MMA thread itself commits to it below, so
+        // this wait can only run out: the timeout and unwind path under test.
+        if (!wait_bounded<kPair>(done_bar, 0, abort_flag, p.timeout_ns))
+          record_timeout(p.status, abort_flag, kSiteInjected);
+        ok = false;
+      }
       WorkIter work(p, cluster_id, n_clusters);
       WorkItem w;
       while (ok && work.next(w)) {

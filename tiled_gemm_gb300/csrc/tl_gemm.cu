@@ -33,6 +33,7 @@ constexpr int kDefaultSms = 148;
 __device__ uint32_t g_status_word;           // bounded-wait outcome, see tl_device_status
 
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_stall{0};                 // test hook, see tl_debug_set_stall
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -719,6 +720,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.ldc = ldc;
   prm.status = st->status;
   prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  prm.stall = g_stall.load(std::memory_order_relaxed);
 
   s = pl.bk == 128 ? launch_tiling<128>(st, pl, ta, tb, tc, prm, stream)
                    : launch_tiling<64>(st, pl, ta, tb, tc, prm, stream);
@@ -821,6 +823,8 @@ void tl_set_wait_timeout_ns(uint64_t ns) {
   ns = std::max<uint64_t>(100000ull, std::min<uint64_t>(ns, 60000000000ull));
   g_timeout_ns.store(ns, std::memory_order_relaxed);
 }
+
+void tl_debug_set_stall(int mode) { g_stall.store(mode == 1 ? 1 : 0, std::memory_order_relaxed); }
 
 int tl_version(void) { return 100; }
 
