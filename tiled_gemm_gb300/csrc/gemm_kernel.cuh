@@ -228,17 +228,41 @@ struct WorkIter {
   }
 };
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16, int relu) {
-  if (relu) {
+template <bool kBf16, bool kRelu>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kRelu) {
     lo = lo > 0.0f ? lo : 0.0f;   // max(x, 0); -0 and NaN give +0
     hi = hi > 0.0f ? hi : 0.0f;
   }
-  if (bf16) {
+  if constexpr (kBf16) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
   }
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Epilogue + cast of 2n fp32 values into n packed pairs.  The output type and the
+// ReLU are template arguments so that the unrolled loop carries no branches (chosen
+// once per chunk by pack_chunk; per-element branches on runtime flags cost the
+// epilogue ~600 cycles per 64-column chunk in branch resolution).
+template <int n, bool kBf16, bool kRelu>
+__device__ __forceinline__ void pack_n(const uint32_t* v, uint32_t* packed) {
+#pragma unroll
+  for (int j = 0; j < n; ++j)
+    packed[j] = pack2<kBf16, kRelu>(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+}
+
+template <int n>
+__device__ __forceinline__ void pack_chunk(const uint32_t* v, uint32_t* packed, int bf16, int relu) {
+  if (bf16) {
+    if (relu) pack_n<n, true, true>(v, packed);
+    else pack_n<n, true, false>(v, packed);
+  } else {
+    if (relu) pack_n<n, false, true>(v, packed);
+    else pack_n<n, false, false>(v, packed);
+  }
 }
 
 // CG = 1: one CTA computes a 128 x BN tile.  CG = 2: a cluster of two CTAs on an SM
@@ -624,11 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(partial_at(u2, c * kEC + j)));
         }
         uint32_t packed[kEC / 2];
-#pragma unroll
-        for (int j = 0; j < kEC / 2; ++j) {
-          packed[j] = pack2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), p.bf16,
-                            p.relu);
-        }
+        pack_chunk<kEC / 2>(v, packed, p.bf16, p.relu);
         const int row = m0 + q * 32 + lane;      // this lane's row of the kernel's tile
         const int col0 = n0 + c * kEC;
         if (p.c_trans) {
