@@ -467,14 +467,15 @@ def main():
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}
     else:
         achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
-        # fp16 and bf16 share the dense tensor rate.  A timed region longer than a
-        # second of back-to-back GEMMs runs under the power cap: sustained figure.
-        long_run = total_ms > 1000.0
-        peak = peaks["bf16_tflops_sustained" if long_run else "bf16_tflops"]
+        # fp16 and bf16 share the dense tensor rate.  The sustained figure (cuBLAS
+        # looping under the power cap) applies when the timed region ran under the
+        # power cap (sw_power_cap seen in the clock samples); otherwise the burst one.
+        capped = "sw_power_cap" in ((res.get("clocks") or {}).get("reasons") or [])
+        peak = peaks["bf16_tflops_sustained" if capped else "bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s"}
     roof["frac"] = round(achieved / peak, 4)
-    roof["peak_source"] = (f"{peaks_src} ({'sustained' if not hbm and total_ms > 1000.0 else 'burst' if not hbm else 'copy'})")
+    roof["peak_source"] = (f"{peaks_src} ({'copy' if hbm else 'sustained, power cap seen' if capped else 'burst'})")
     if not hbm:
         roof["frac_of_burst"] = round(achieved / peaks["bf16_tflops"], 4)
     roof["traffic"] = load_traffic(w.name)

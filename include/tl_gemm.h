@@ -29,8 +29,16 @@
  * All pointers to matrices are DEVICE pointers of the current CUDA device.  The
  * library never frees or retains caller memory.  Every call is asynchronous on
  * `stream` (NULL = the legacy default stream) and returns once the work is
- * enqueued.  The library holds only per-device caches of kernel attributes; it is
- * safe to call from several host threads.
+ * enqueued.  The library holds only per-device caches of kernel attributes and a
+ * bounded host-side cache of encoded tensor-map descriptors (each a pure function of
+ * a buffer's address, extents and pitch, so a stale entry is never wrong); it is
+ * safe to call from several host threads.  The GEMM kernel is launched with
+ * programmatic stream serialization and signals at its start that dependents may
+ * launch: it does its own set-up while the previous kernel of the stream finishes,
+ * and waits for that kernel before touching memory.  A kernel of the caller that is
+ * itself launched with programmatic serialization after a GEMM may therefore start
+ * before the GEMM ends, and must wait for it (cudaGridDependencySynchronize) before
+ * using C, as CUDA requires of such kernels; ordinary launches are unaffected.
  */
 #ifndef TL_GEMM_H
 #define TL_GEMM_H
@@ -158,8 +166,9 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
 
 /*
  * tl_gemm() with an explicit plan (bm, bn, bk, stages, raster_group, grid,
- * l2_prefetch, producers and stream_k are read; the rest is recomputed;
- * l2_prefetch < 0, producers <= 0 and stream_k = 0 select the defaults).  Used
+ * l2_prefetch, producers, stream_k and swap_ab are read, and tma_store = -1 asks
+ * for plain stores of C; the rest is recomputed; l2_prefetch < 0, producers <= 0
+ * and stream_k = 0 select the defaults).  Used
  * to run a workload at a fixed tiling, e.g. the
  * pages' quickstart 128x128x64 with 3 stages.  Same arguments and errors as
  * tl_gemm(), plus TL_ERR_INVALID_ARG for an unsupported plan.

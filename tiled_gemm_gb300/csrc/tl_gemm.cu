@@ -20,6 +20,7 @@
 #include <cstring>
 #include <mutex>
 #include <random>
+#include <unordered_map>
 
 #include "gemm_kernel.cuh"
 #include "tl_gemm.h"
@@ -434,19 +435,78 @@ tl_status launch_tiling(DeviceState* st, const tl_plan& pl, const CUtensorMap& t
   }
 }
 
-bool encode_2d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
+// ---- tensor-map descriptors --------------------------------------------------------
+// A CUtensorMap is a pure function of (element type, rank, base address, extents,
+// strides, box), so encoded maps are cached on that key: repeated calls on the same
+// buffers skip cuTensorMapEncodeTiled.  The cache is bounded (cleared when full) and
+// shared by all threads under a mutex.
+struct MapKey {
+  uint64_t base;
+  uint64_t dims[3];
+  uint64_t stride0, stride1;
+  uint32_t box[3];
+  uint32_t dtype_rank;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = 1469598103934665603ull;                     // FNV-1a over the key bytes
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+
+constexpr size_t kMapCacheMax = 4096;
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash>* g_maps = nullptr;
+
+bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* base,
+                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));                        // padding bytes take part
+  key.base = reinterpret_cast<uint64_t>(base);
+  for (uint32_t i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  key.stride0 = strides[0];
+  key.stride1 = rank > 2 ? strides[1] : 0;
+  key.dtype_rank = static_cast<uint32_t>(dtype) * 8u + rank;
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (g_maps != nullptr) {
+      auto it = g_maps->find(key);
+      if (it != g_maps->end()) {
+        *map = it->second;
+        return true;
+      }
+    }
+  }
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == TL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  if (g_maps == nullptr) g_maps = new std::unordered_map<MapKey, CUtensorMap, MapKeyHash>();
+  if (g_maps->size() >= kMapCacheMax) g_maps->clear();
+  (*g_maps)[key] = *map;
+  return true;
+}
+
+bool encode_2d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {ld_elems * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      dtype == TL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(map, dtype, 2, base, dims, strides, box);
 }
 
 // A row-major [rows][ld] matrix whose contiguous extent `inner` is a multiple of 64,
@@ -457,17 +517,10 @@ bool encode_chunked_3d(CUtensorMap* map, tl_dtype dtype, const void* base, uint6
                        uint64_t rows, uint64_t ld_elems, uint32_t box_rows,
                        uint32_t box_chunks) {
   if (inner % 64 != 0) return false;
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
   const cuuint64_t dims[3] = {64, rows, inner / 64};
   const cuuint64_t strides[2] = {ld_elems * 2, 128};
   const cuuint32_t box[3] = {64, box_rows, box_chunks};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt =
-      dtype == TL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(map, dtype, 3, base, dims, strides, box);
 }
 
 int launch_blocks_for(int64_t elems) {
