@@ -20,7 +20,10 @@ encoder against numpy/torch's own conversions over all 65536 bit patterns and al
 midpoints; the GEMM against closed forms (identity, permutation, all-ones = K,
 rank-1, K = 1, ReLU zeroing), exact integer products from numpy, exact rational
 sums (fractions.Fraction) within the binary64 error bound, and a hand-computed
-2x2x2 case.
+2x2x2 case.  The FP8 forms (E4M3 / E5M2 operands, one product scale alpha) are
+pinned the same way: both decoders against torch's float8 conversions over all 256
+codes plus the formats' defining values, and the FP8 product against closed forms
+and exact integer products.
 """
 from __future__ import annotations
 
@@ -38,6 +41,8 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 F16 = 0
 BF16 = 1
+E4M3 = 2
+E5M2 = 3
 
 _lib = None
 _lock = threading.Lock()
@@ -75,6 +80,14 @@ def _load():
         lib.oracle_decode_array.restype = None
         lib.oracle_encode_array.argtypes = [p, p, i64, ci]
         lib.oracle_encode_array.restype = None
+        lib.oracle_gemm_fp8.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci,
+                                         ci, ci, ctypes.c_double, ci, ci]
+        lib.oracle_gemm_fp8.restype = ci
+        lib.oracle_gemm_fp8_entries.argtypes = [p, p, i64, i64, i64, i64, i64, ci, ci, ci, ci,
+                                                ci, ctypes.c_double, ci, p, p, i64, p, p, ci]
+        lib.oracle_gemm_fp8_entries.restype = ci
+        lib.oracle_decode8_array.argtypes = [p, p, i64, ci]
+        lib.oracle_decode8_array.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ci
         _lib = lib
@@ -168,4 +181,73 @@ def gemm_entries(A, B, M: int, N: int, K: int, rows, cols, *, lda: int | None = 
                                      _ptr(sums) if sums is not None else None, threads)
     if rc != 0:
         raise ValueError("oracle_gemm_entries rejected its arguments")
+    return (out, sums) if want_sums else out
+
+
+# ---- FP8 operands -----------------------------------------------------------------
+
+def _as_u8(x) -> np.ndarray:
+    """Accept a numpy uint8 array or a CPU torch float8/uint8 tensor; return raw codes."""
+    if isinstance(x, np.ndarray):
+        if x.dtype == np.uint8:
+            return np.ascontiguousarray(x)
+        raise TypeError(f"expected uint8 codes, got {x.dtype}")
+    import torch  # CPU-side helper only
+    if not isinstance(x, torch.Tensor) or x.element_size() != 1:
+        raise TypeError("expected an 8-bit tensor or uint8 code array")
+    t = x.detach().to("cpu").contiguous()
+    return t.view(torch.uint8).numpy()
+
+
+def decode8(codes: np.ndarray, fmt: int) -> np.ndarray:
+    """Exact binary64 value of each E4M3 (fmt 2) or E5M2 (fmt 3) code."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _load().oracle_decode8_array(_ptr(codes), _ptr(out), codes.size, fmt)
+    return out
+
+
+def gemm_fp8(A, B, M: int, N: int, K: int, *, a_fmt: int = E4M3, b_fmt: int = E4M3,
+             out_dtype: int = BF16, alpha: float = 1.0, lda: int | None = None,
+             ldb: int | None = None, ldc: int | None = None, trans_a: bool = False,
+             trans_b: bool = False, relu: bool = False, threads: int = 0,
+             want_sums: bool = False):
+    """C = round_out(epi(alpha * op(A) . op(B))) from 8-bit operands; uint16 bits (M, N)."""
+    a = _as_u8(A).reshape(-1)
+    b = _as_u8(B).reshape(-1)
+    lda = lda if lda is not None else (M if trans_a else K)
+    ldb = ldb if ldb is not None else (K if trans_b else N)
+    ldc = ldc if ldc is not None else N
+    c = np.zeros((M, ldc), dtype=np.uint16)
+    sums = np.zeros((M, N), dtype=np.float64) if want_sums else None
+    rc = _load().oracle_gemm_fp8(_ptr(a), _ptr(b), _ptr(c),
+                                 _ptr(sums) if sums is not None else None,
+                                 M, N, K, lda, ldb, ldc, a_fmt, b_fmt, out_dtype,
+                                 int(trans_a), int(trans_b), float(alpha), int(relu), threads)
+    if rc != 0:
+        raise ValueError("oracle_gemm_fp8 rejected its arguments")
+    c = c[:, :N]
+    return (c, sums) if want_sums else c
+
+
+def gemm_fp8_entries(A, B, M: int, N: int, K: int, rows, cols, *, a_fmt: int = E4M3,
+                     b_fmt: int = E4M3, out_dtype: int = BF16, alpha: float = 1.0,
+                     lda: int | None = None, ldb: int | None = None, trans_a: bool = False,
+                     trans_b: bool = False, relu: bool = False, threads: int = 0,
+                     want_sums: bool = False):
+    """Selected entries of the FP8 product, computed one by one."""
+    a = _as_u8(A).reshape(-1)
+    b = _as_u8(B).reshape(-1)
+    lda = lda if lda is not None else (M if trans_a else K)
+    ldb = ldb if ldb is not None else (K if trans_b else N)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    cidx = np.ascontiguousarray(cols, dtype=np.int64)
+    out = np.zeros(r.shape, dtype=np.uint16)
+    sums = np.zeros(r.shape, dtype=np.float64) if want_sums else None
+    rc = _load().oracle_gemm_fp8_entries(_ptr(a), _ptr(b), M, N, K, lda, ldb, a_fmt, b_fmt,
+                                         out_dtype, int(trans_a), int(trans_b), float(alpha),
+                                         int(relu), _ptr(r), _ptr(cidx), r.size, _ptr(out),
+                                         _ptr(sums) if sums is not None else None, threads)
+    if rc != 0:
+        raise ValueError("oracle_gemm_fp8_entries rejected its arguments")
     return (out, sums) if want_sums else out

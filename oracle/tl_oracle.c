@@ -45,7 +45,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2, ORACLE_E5M2 = 3 };
 
 /* ---- format decoders ---------------------------------------------------- */
 
@@ -77,6 +77,41 @@ double oracle_bf16_to_f64(uint16_t h) {
     v = f ? NAN : INFINITY;
   } else {
     v = ldexp((double)(f + 128), e - 134);    /* (128+f) * 2^(e-127-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* 8-bit E4M3 ("fn" variant: finite only): 1 sign, 4 exponent (bias 7), 3 fraction
+ * bits; exponent 15 with fraction 7 is NaN, every other code is finite, so the
+ * largest magnitude is 1.75 * 2^8 = 448.  Subnormals: f * 2^(1-7-3). */
+double oracle_e4m3_to_f64(uint8_t h) {
+  const int sign = (h >> 7) & 1;
+  const int e = (h >> 3) & 0xF;
+  const int f = h & 0x7;
+  double v;
+  if (e == 15 && f == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f, -9);
+  } else {
+    v = ldexp((double)(f + 8), e - 10);       /* (8+f) * 2^(e-7-3) */
+  }
+  return sign ? -v : v;
+}
+
+/* 8-bit E5M2: 1 sign, 5 exponent (bias 15), 2 fraction bits, IEEE-style: exponent
+ * 31 is infinity (fraction 0) or NaN; largest finite 1.75 * 2^15 = 57344. */
+double oracle_e5m2_to_f64(uint8_t h) {
+  const int sign = (h >> 7) & 1;
+  const int e = (h >> 2) & 0x1F;
+  const int f = h & 0x3;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -16);                /* f * 2^(1-15-2) */
+  } else if (e == 31) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(f + 4), e - 17);       /* (4+f) * 2^(e-15-2) */
   }
   return sign ? -v : v;
 }
@@ -218,6 +253,89 @@ int oracle_gemm_entries(const uint16_t* A, const uint16_t* B, int64_t M, int64_t
     if (sums) sums[t] = s;
   }
   return 0;
+}
+
+/* ---- the FP8 GEMM ------------------------------------------------------------
+ *
+ *   C[i,j] = round_out( epi( alpha * sum_{k<K} x_a(opA[i,k]) * x_b(opB[k,j]) ) )
+ *
+ * A and B hold 8-bit codes of E4M3 or E5M2 (each operand its own format), decoded
+ * exactly; the sum runs over k in order in binary64 and is multiplied by the
+ * per-product scale alpha (binary64) before the epilogue and the cast to the
+ * 16-bit output format.  This is the plain definition of a low-precision GEMM with
+ * one scale for the whole product: the pages' block-scaled form shares one
+ * exponent among 32 consecutive K elements ("NVIDIA backend codegen" page,
+ * section 4.6.3; "TileLang: a tile language one level below Triton", block-scaled
+ * MMA); with every block scale equal, it reduces to this.
+ */
+static double decode8(uint8_t h, int type) {
+  return type == ORACLE_E5M2 ? oracle_e5m2_to_f64(h) : oracle_e4m3_to_f64(h);
+}
+
+static double dot8(const uint8_t* A, const uint8_t* B, int64_t K, int64_t lda, int64_t ldb,
+                   int a_type, int b_type, int trans_a, int trans_b, int64_t i, int64_t j) {
+  double s = 0.0;
+  for (int64_t k = 0; k < K; ++k) {
+    const double a = decode8(trans_a ? A[k * lda + i] : A[i * lda + k], a_type);
+    const double b = decode8(trans_b ? B[j * ldb + k] : B[k * ldb + j], b_type);
+    s += a * b;
+  }
+  return s;
+}
+
+static int fp8_args_ok(int a_type, int b_type, int out_dtype) {
+  return (a_type == ORACLE_E4M3 || a_type == ORACLE_E5M2) &&
+         (b_type == ORACLE_E4M3 || b_type == ORACLE_E5M2) &&
+         (out_dtype == ORACLE_F16 || out_dtype == ORACLE_BF16);
+}
+
+int oracle_gemm_fp8(const uint8_t* A, const uint8_t* B, uint16_t* C, double* sums,
+                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                    int a_type, int b_type, int out_dtype, int trans_a, int trans_b,
+                    double alpha, int relu, int nthreads) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  if (!fp8_args_ok(a_type, b_type, out_dtype)) return -1;
+  if (M == 0 || N == 0) return 0;
+  if (ldc < N) return -1;
+  if (K > 0) {
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? K : N)) return -1;
+  }
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      const double s = epilogue(
+          alpha * dot8(A, B, K, lda, ldb, a_type, b_type, trans_a, trans_b, i, j), relu);
+      if (C) C[i * ldc + j] = encode(s, out_dtype);
+      if (sums) sums[i * N + j] = s;
+    }
+  }
+  return 0;
+}
+
+int oracle_gemm_fp8_entries(const uint8_t* A, const uint8_t* B, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int a_type, int b_type, int out_dtype,
+                            int trans_a, int trans_b, double alpha, int relu,
+                            const int64_t* rows, const int64_t* cols, int64_t count,
+                            uint16_t* out, double* sums, int nthreads) {
+  if (!fp8_args_ok(a_type, b_type, out_dtype)) return -1;
+  for (int64_t t = 0; t < count; ++t) {
+    if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+  }
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t t = 0; t < count; ++t) {
+    const double s = epilogue(alpha * dot8(A, B, K, lda, ldb, a_type, b_type, trans_a, trans_b,
+                                           rows[t], cols[t]),
+                              relu);
+    if (out) out[t] = encode(s, out_dtype);
+    if (sums) sums[t] = s;
+  }
+  return 0;
+}
+
+void oracle_decode8_array(const uint8_t* in, double* out, int64_t n, int type) {
+  for (int64_t t = 0; t < n; ++t) out[t] = decode8(in[t], type);
 }
 
 /* Vector forms of the format conversions, for the pin tests. */

@@ -307,3 +307,106 @@ def test_rejects_bad_arguments():
         oracle.gemm(A, A, 4, 4, 4, lda=2)          # lda < K
     with pytest.raises(ValueError):
         oracle.gemm_entries(A, A, 4, 4, 4, [4], [0])   # row out of range
+
+
+# ---- FP8 operands (E4M3 / E5M2) ------------------------------------------------------
+
+FP8_TORCH = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
+
+
+def _codes8(values, fmt):
+    """8-bit codes of `values` via torch's own float8 conversion (exact when representable)."""
+    t = torch.as_tensor(np.asarray(values, dtype=np.float32)).to(FP8_TORCH[fmt])
+    return t.view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_fp8_decoders_all_codes_against_torch(fmt):
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.decode8(codes, fmt)
+    ref = torch.from_numpy(codes).view(FP8_TORCH[fmt]).to(torch.float64).numpy()
+    same = (mine == ref) | (np.isnan(mine) & np.isnan(ref))
+    assert same.all()
+
+
+def test_fp8_defining_values():
+    """The formats' definitions: E4M3 (bias 7, finite only, NaN = S.1111.111) and E5M2
+    (bias 15, IEEE-style infinities)."""
+    d4 = lambda c: float(oracle.decode8(np.array([c], np.uint8), oracle.E4M3)[0])
+    d5 = lambda c: float(oracle.decode8(np.array([c], np.uint8), oracle.E5M2)[0])
+    assert d4(0x38) == 1.0 and d4(0x40) == 2.0 and d4(0xB8) == -1.0
+    assert d4(0x7E) == 448.0                       # 1.75 * 2^8, the largest
+    assert d4(0x01) == 2.0 ** -9                   # smallest subnormal
+    assert d4(0x08) == 2.0 ** -6                   # smallest normal
+    assert np.isnan(d4(0x7F)) and np.isnan(d4(0xFF))
+    assert d4(0x78) == 256.0                       # exponent 15 is finite here
+    assert d5(0x3C) == 1.0 and d5(0x7B) == 57344.0
+    assert d5(0x7C) == np.inf and d5(0xFC) == -np.inf and np.isnan(d5(0x7D))
+    assert d5(0x01) == 2.0 ** -16 and d5(0x04) == 2.0 ** -14
+
+
+@pytest.mark.parametrize("out_dtype", [oracle.F16, oracle.BF16])
+def test_fp8_identity_and_power_of_two_scale(out_dtype):
+    """A = I (E4M3 ones) against E5M2 values: C = alpha * B exactly (every E4M3/E5M2
+    value times a power of two in range is exact in fp16 and bf16)."""
+    rng = np.random.default_rng(41)
+    K = N = 24
+    Bv = oracle.decode8(rng.integers(0, 256, (K, N)).astype(np.uint8), oracle.E5M2)
+    Bv = np.where(np.isfinite(Bv) & (np.abs(Bv) <= 4096), Bv, 1.5)
+    B = _codes8(Bv, oracle.E5M2)
+    A = _codes8(np.eye(K), oracle.E4M3)
+    for alpha in (1.0, 0.25, 4.0):
+        C = oracle.gemm_fp8(A, B, K, N, K, a_fmt=oracle.E4M3, b_fmt=oracle.E5M2,
+                            out_dtype=out_dtype, alpha=alpha)
+        assert np.array_equal(oracle.decode(C, out_dtype), alpha * Bv)
+
+
+@pytest.mark.parametrize("trans_a", [False, True])
+@pytest.mark.parametrize("trans_b", [False, True])
+def test_fp8_integer_products_against_numpy(trans_a, trans_b):
+    """Small integers are exact in both formats; numpy's int64 product is the exact sum;
+    mixed formats, padded leading dimensions, ReLU."""
+    rng = np.random.default_rng(43 + 2 * trans_a + trans_b)
+    M, N, K = 37, 29, 90
+    Ai = rng.integers(-4, 5, (M, K))
+    Bi = rng.integers(-3, 4, (K, N))
+    want = Ai @ Bi
+    pad = 5
+    As = Ai.T if trans_a else Ai
+    Bs = Bi.T if trans_b else Bi
+    Ast = np.zeros((As.shape[0], As.shape[1] + pad), np.int64)
+    Ast[:, :As.shape[1]] = As
+    Bst = np.zeros((Bs.shape[0], Bs.shape[1] + pad), np.int64)
+    Bst[:, :Bs.shape[1]] = Bs
+    A8, B8 = _codes8(Ast, oracle.E4M3), _codes8(Bst, oracle.E5M2)
+    kw = dict(a_fmt=oracle.E4M3, b_fmt=oracle.E5M2, out_dtype=oracle.F16,
+              lda=Ast.shape[1], ldb=Bst.shape[1], trans_a=trans_a, trans_b=trans_b)
+    C = oracle.gemm_fp8(A8, B8, M, N, K, ldc=N + 3, **kw)
+    assert np.array_equal(oracle.decode(C, oracle.F16), want.astype(np.float64))
+    Cr = oracle.gemm_fp8(A8, B8, M, N, K, relu=True, alpha=0.5, **kw)
+    assert np.array_equal(oracle.decode(Cr, oracle.F16),
+                          np.maximum(0.5 * want, 0).astype(np.float64))
+
+
+def test_fp8_exact_rational_sums_and_entries():
+    """Random E4M3 operands: the binary64 sum times alpha is within the binary64 bound of
+    the exact rational value and rounds like it; sampled entries equal the full product."""
+    rng = np.random.default_rng(47)
+    M, N, K = 5, 6, 41
+    A = _codes8(rng.uniform(-3, 3, (M, K)), oracle.E4M3)
+    B = _codes8(rng.uniform(-3, 3, (N, K)), oracle.E4M3)
+    Av, Bv = oracle.decode8(A, oracle.E4M3), oracle.decode8(B, oracle.E4M3)
+    alpha = 0.3
+    C, S = oracle.gemm_fp8(A, B, M, N, K, trans_b=True, alpha=alpha, out_dtype=oracle.F16,
+                           want_sums=True)
+    for i in range(M):
+        for j in range(N):
+            terms = [Fraction(float(Av[i, k])) * Fraction(float(Bv[j, k])) for k in range(K)]
+            exact = Fraction(alpha) * sum(terms, Fraction(0))
+            bound = (K + 1) * 2.0 ** -53 * alpha * float(sum(abs(t) for t in terms))
+            assert abs(Fraction(float(S[i, j])) - exact) <= Fraction(bound)
+            assert C[i, j] == f16_bits(float(exact))
+    rows, cols = rng.integers(0, M, 30), rng.integers(0, N, 30)
+    E = oracle.gemm_fp8_entries(A, B, M, N, K, rows, cols, trans_b=True, alpha=alpha,
+                                out_dtype=oracle.F16)
+    assert np.array_equal(E, C[rows, cols])
