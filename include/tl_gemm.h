@@ -53,7 +53,11 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st* tl_stream_t;
 
-typedef enum { TL_F16 = 0, TL_BF16 = 1 } tl_dtype;
+/* Element types.  fp16 and bf16 are operand and output types of tl_gemm(); the
+ * 8-bit E4M3 ("fn": finite only, bias 7, largest 448) and E5M2 (bias 15, with
+ * infinities) are operand types of tl_gemm_fp8() only, whose output is fp16 or bf16.
+ * The planning functions accept all four (8-bit: plans for tl_gemm_fp8). */
+typedef enum { TL_F16 = 0, TL_BF16 = 1, TL_E4M3 = 2, TL_E5M2 = 3 } tl_dtype;
 
 typedef enum { TL_EPI_NONE = 0, TL_EPI_RELU = 1 } tl_epilogue;
 
@@ -177,6 +181,37 @@ tl_status tl_gemm_with_plan(const void* A, const void* B, void* C, int64_t M, in
                             int64_t K, int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype,
                             int trans_a, int trans_b, tl_epilogue epilogue,
                             const tl_plan* plan, tl_stream_t stream);
+
+/*
+ * C = epi(alpha * op(A) . op(B)) with 8-bit floating-point operands.  (The pages'
+ * Blackwell GEMM also runs on low-precision operands: "NVIDIA backend codegen"
+ * page, section 4.6.3, and the block-scaled MMA of "TileLang: a tile language one
+ * level below Triton", where 32 consecutive K elements share one exponent; this
+ * entry point takes one scale for the whole product, which is that form with every
+ * block scale equal.)
+ *
+ *   A, B     device pointers to 8-bit codes: A of format a_type, B of b_type (each
+ *            TL_E4M3 or TL_E5M2; the two may differ).  op(A) and op(B) as in
+ *            tl_gemm(); lda, ldb, ldc in elements (bytes for A and B).
+ *   C        device pointer to c_type elements (TL_F16 or TL_BF16), written as in
+ *            tl_gemm(); C must not overlap A or B.
+ *   alpha    finite fp32 scale applied to the fp32 accumulator before the epilogue
+ *            (ReLU on alpha * sum) and the round-to-nearest-even cast.
+ *   plan     NULL for the planner's choice (tl_gemm_plan with dtype = a_type gives
+ *            it), or a plan whose bk is 128 or 256 (K elements per stage: one or two
+ *            128-byte chunks) and bn >= 64; with B N-major (trans_b = 0) each CTA's
+ *            share of the tile's columns (bn, or bn/2 for pairs) must be a multiple
+ *            of 128.  No operand swap.
+ * Operands whose base or pitch is not 16-byte aligned are copied to a padded pitch
+ * as in tl_gemm() (stream-ordered workspace).  Accumulation is fp32 in Tensor
+ * Memory; each product of two 8-bit values is exact in it.  Errors as tl_gemm(),
+ * plus TL_ERR_INVALID_ARG for a non-8-bit operand type, a non-16-bit c_type, a
+ * non-finite alpha or an unsupported plan.
+ */
+tl_status tl_gemm_fp8(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, tl_dtype a_type, tl_dtype b_type,
+                      tl_dtype c_type, int trans_a, int trans_b, float alpha,
+                      tl_epilogue epilogue, const tl_plan* plan, tl_stream_t stream);
 
 /*
  * tl_gemm() for callers that cannot allocate device memory.  (This entry point has

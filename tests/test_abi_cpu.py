@@ -190,3 +190,33 @@ def test_empty_outputs_are_a_no_op():
     assert tl.tl_gemm(A, B, C, 0, 4, 4, 4, 4, 4, 0, 0, 0, 0, None) == tl.TL_OK
     assert tl.tl_gemm(A, B, C, 4, 0, 4, 4, 0, 0, 0, 0, 0, 0, None) == tl.TL_OK
     assert tl.tl_gemm(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == tl.TL_OK
+
+
+def test_fp8_plans():
+    # 8-bit operands: the same tiles with twice the K elements per stage (the same bytes)
+    for M, N, K, tb in ((8192, 8192, 8192, 1), (4096, 4096, 4096, 0), (1000, 72, 2049, 1),
+                        (16, 8192, 8192, 1), (3000, 5000, 4100, 0)):
+        p = tl.tl_gemm_plan(M, N, K, dtype=tl.TL_E4M3, trans_b=tb, num_sms=152)
+        cg = p.bm // 128
+        assert p.bk in (128, 256) and p.swap_ab == 0 and p.bn >= 64
+        assert p.ring_bytes == p.stages * (128 * p.bk + (p.bn // cg) * p.bk)
+        assert p.tx_bytes == (128 + p.bn // cg) * p.bk
+        assert p.smem_bytes <= 232448
+        if not tb:
+            assert (p.bn // cg) % 128 == 0
+    big = tl.tl_gemm_plan(8192, 8192, 8192, dtype=tl.TL_E5M2, trans_b=1, num_sms=152)
+    assert (big.bm, big.bn, big.bk, big.stages) == (256, 256, 256, 3)
+    for bm, bn, bk, smax in ((128, 64, 128, 8), (128, 256, 256, 2), (256, 256, 256, 3),
+                             (256, 128, 128, 8)):
+        tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, smax, dtype=tl.TL_E4M3, trans_b=1)
+        with pytest.raises(tl.TLError):
+            tl.tl_plan_complete(4096, 4096, 4096, bm, bn, bk, smax + 1, dtype=tl.TL_E4M3,
+                                trans_b=1)
+    for bad in ((128, 128, 64, 3), (128, 32, 128, 4), (128, 128, 512, 2)):
+        with pytest.raises(tl.TLError):
+            tl.tl_plan_complete(1024, 1024, 1024, *bad, dtype=tl.TL_E4M3, trans_b=1)
+    # an N-major B needs 128-column boxes per CTA
+    tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 128, 4, dtype=tl.TL_E4M3, trans_b=0)
+    for bm, bn in ((128, 64), (256, 128)):
+        with pytest.raises(tl.TLError):
+            tl.tl_plan_complete(1024, 1024, 1024, bm, bn, 128, 4, dtype=tl.TL_E4M3, trans_b=0)

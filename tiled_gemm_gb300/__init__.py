@@ -18,6 +18,8 @@ from .build import LIB_PATH
 
 TL_F16 = 0
 TL_BF16 = 1
+TL_E4M3 = 2
+TL_E5M2 = 3
 TL_EPI_NONE = 0
 TL_EPI_RELU = 1
 
@@ -78,6 +80,9 @@ def _load() -> ctypes.CDLL:
     lib.tl_gemm_plan.restype = ci
     lib.tl_plan_complete.argtypes = [i64, i64, i64, ci, ci, ci, ci, ctypes.POINTER(Plan)]
     lib.tl_plan_complete.restype = ci
+    lib.tl_gemm_fp8.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, ci,
+                                ctypes.c_float, ci, ctypes.POINTER(Plan), p]
+    lib.tl_gemm_fp8.restype = ci
     lib.tl_gemm_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, p]
     lib.tl_gemm_noalloc.restype = ci
     lib.tl_gemm_noalloc_scratch_bytes.argtypes = []
@@ -113,6 +118,15 @@ def tl_gemm_with_plan(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, 
                       plan: Plan, stream: int) -> int:
     return _lib.tl_gemm_with_plan(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b,
                                   epilogue, ctypes.byref(plan), stream)
+
+
+def tl_gemm_fp8(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                a_type: int, b_type: int, c_type: int, trans_a: int, trans_b: int, alpha: float,
+                epilogue: int, plan: Plan | None, stream: int) -> int:
+    """Raw FP8 call (8-bit operand codes, fp16/bf16 output); returns tl_status."""
+    return _lib.tl_gemm_fp8(A, B, C, M, N, K, lda, ldb, ldc, a_type, b_type, c_type, trans_a,
+                            trans_b, float(alpha), epilogue,
+                            ctypes.byref(plan) if plan is not None else None, stream)
 
 
 def tl_gemm_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
@@ -250,3 +264,45 @@ def plan_for(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
     return Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
                 l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k,
                 swap_ab=swap_ab, tma_store=tma_store)
+
+
+def _fp8_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float8_e4m3fn:
+        return TL_E4M3
+    if t.dtype == torch.float8_e5m2:
+        return TL_E5M2
+    raise TypeError(f"gemm_fp8 takes float8_e4m3fn / float8_e5m2 operands, got {t.dtype}")
+
+
+def gemm_fp8(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool = False,
+             alpha: float = 1.0, out_dtype=None, out=None, plan: Plan | None = None,
+             stream=None):
+    """C = epi(alpha * op(a) . op(b)) with 8-bit float operands, on the current device.
+
+    ``a`` and ``b`` are torch.float8_e4m3fn or torch.float8_e5m2 tensors (the two may
+    differ), laid out as for ``gemm``; the output is ``out_dtype`` (torch.bfloat16 by
+    default, or torch.float16), or ``out``'s dtype when ``out`` is given.
+    """
+    torch = _torch()
+    if not (a.is_cuda and b.is_cuda):
+        raise ValueError("a and b must be CUDA tensors")
+    at, bt = _fp8_code(a), _fp8_code(b)
+    M, K = (a.size(1), a.size(0)) if trans_a else (a.size(0), a.size(1))
+    Kb, N = (b.size(1), b.size(0)) if trans_b else (b.size(0), b.size(1))
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if out is None:
+        odt = out_dtype if out_dtype is not None else torch.bfloat16
+        out = torch.empty((M, N), dtype=odt, device=a.device)
+    elif tuple(out.shape) != (M, N):
+        raise ValueError("out has the wrong shape")
+    ct = _dtype_code(out)
+    lda, ldb, ldc = _ld(a, "a"), _ld(b, "b"), _ld(out, "out")
+    s = stream if stream is not None else torch.cuda.current_stream(a.device)
+    st = tl_gemm_fp8(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc, at, bt,
+                     ct, int(trans_a), int(trans_b), alpha,
+                     TL_EPI_RELU if relu else TL_EPI_NONE, plan, s.cuda_stream)
+    if st != TL_OK:
+        raise TLError(st, "tl_gemm_fp8")
+    return out

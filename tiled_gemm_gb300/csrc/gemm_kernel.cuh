@@ -53,8 +53,11 @@
 namespace tl {
 
 constexpr int kBM = 128;              // MMA M: one accumulator row per TMEM lane
-constexpr int kChunkK = 64;           // 64 x 2 B = one 128-byte swizzle row
-constexpr int kUmmaK = 16;            // K of one kind::f16 MMA
+// A pipeline stage holds, per matrix row, BK elements of K in 128-byte chunks (one
+// swizzle row each): 64 elements of a 16-bit type or 128 of an 8-bit one.  One MMA
+// consumes 32 bytes of K per row: K = 16 (kind::f16) or 32 (kind::f8f6f4).
+constexpr int kChunkBytes = 128;
+constexpr int kMmaKBytes = 32;
 constexpr int kThreads = 256;         // 8 warps: producers 0, 6, 7; MMA 1; epilogue 2-5
 constexpr int kProducers = 3;
 constexpr int kEpiWarps = 4;
@@ -86,11 +89,13 @@ struct GemmParams {
   int32_t stages;
   int32_t raster_group;
   int32_t trans_a, trans_b;
-  int32_t bf16;
+  int32_t bf16;             // output type (and kind::f16 inputs) is bf16, else fp16
   int32_t relu;
   int32_t tma_store;        // 1: TMA bulk store of C; 0: predicated st.global
   int32_t c_trans;          // 1: the kernel computes C^T (operands swapped by the host):
                             // its element (i, j) goes to C[j * ldc + i], plain stores
+  int32_t scale;            // 1: multiply the accumulator by alpha before the epilogue
+  float alpha;
   int32_t c_vec;            // 1: C's base and pitch are 16-byte aligned: plain stores of
                             // a full chunk go out as 16-byte vectors
   int32_t l2_prefetch;      // k-blocks the producer prefetches into L2 ahead of the ring
@@ -116,15 +121,16 @@ struct GemmParams {
                             // nothing arrives on, so the wait runs out and every role unwinds
 };
 
-// Shared memory of one stage in one CTA: A is 128 rows x BK, B is BN/CG columns x BK.
-template <int BK>
+// Shared memory of one stage in one CTA: A is 128 rows x BK, B is BN/CG columns x BK,
+// elements of EB bytes.
+template <int BK, int EB = 2>
 __host__ __device__ constexpr uint32_t a_stage_bytes() {
-  return static_cast<uint32_t>(kBM) * BK * 2;
+  return static_cast<uint32_t>(kBM) * BK * EB;
 }
 
-template <int BN, int CG, int BK>
+template <int BN, int CG, int BK, int EB = 2>
 __host__ __device__ constexpr uint32_t b_stage_bytes() {
-  return static_cast<uint32_t>(BN / CG) * BK * 2;
+  return static_cast<uint32_t>(BN / CG) * BK * EB;
 }
 
 // Barrier block: full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done,
@@ -134,10 +140,10 @@ __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
   return static_cast<uint32_t>(8 * (2 * stages + 5) + 8 + 32);
 }
 
-template <int BN, int CG, int BK>
+template <int BN, int CG, int BK, int EB = 2>
 __host__ __device__ constexpr uint32_t smem_bytes_for(int stages) {
   // +1024: the dynamic shared memory base is rounded up to 1024 B in the kernel
-  return 1024u + stages * (a_stage_bytes<BK>() + b_stage_bytes<BN, CG, BK>()) +
+  return 1024u + stages * (a_stage_bytes<BK, EB>() + b_stage_bytes<BN, CG, BK, EB>()) +
          staging_bytes<BN>() + barrier_bytes(stages);
 }
 
@@ -273,11 +279,12 @@ __device__ __forceinline__ void pack_chunk(const uint32_t* v, uint32_t* packed, 
 // multicast to both CTAs' "empty", "tmem_full" and "done" barriers; both CTAs'
 // epilogue warps release the accumulator on the even CTA's "tmem_empty" barrier.
 //
-// BK (64 or 128) is the K depth of one pipeline stage: 1 or 2 chunks of 64 elements,
-// each chunk one 128-byte swizzle row per matrix row.  Deeper stages halve the TMA
-// instructions and barrier hand-offs per byte: on GB300 one TMA instruction costs
-// the issuing thread a few hundred cycles whatever its box size.
-template <int BN, int CG, int BK>
+// BK is the K depth of one pipeline stage: 1 or 2 chunks of 128 bytes per matrix row
+// (each one swizzle row), i.e. 64 or 128 elements of fp16/bf16 (EB = 2) and 128 or 256
+// of E4M3/E5M2 (EB = 1, kind::f8f6f4 MMAs).  Deeper stages halve the TMA instructions
+// and barrier hand-offs per byte: on GB300 one TMA instruction costs the issuing
+// thread a few hundred cycles whatever its box size.
+template <int BN, int CG, int BK, int EB = 2>
 __global__ void __launch_bounds__(kThreads, 1)
     tl_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
@@ -286,12 +293,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 "BN must be 16, 32, 64, 128 or 256");
   static_assert(CG == 1 || (CG == 2 && BN >= 128), "pairs need BN/2 >= 64");
   constexpr bool kPair = CG == 2;
-  static_assert(BK == 64 || BK == 128, "BK must be 64 or 128");
+  static_assert(EB == 1 || EB == 2, "1- or 2-byte elements");
+  static_assert(BK * EB == 128 || BK * EB == 256, "one or two 128-byte chunks per stage");
+  static_assert(EB == 2 || BN >= 64, "8-bit operands: BN >= 64");
+  constexpr int kChunkElems = kChunkBytes / EB;            // K (or MN) elements per chunk
+  constexpr int kMmaK = kMmaKBytes / EB;                   // K elements of one MMA
   constexpr int kBnCta = BN / CG;                          // B columns this CTA loads
-  constexpr int kKChunks = BK / kChunkK;                   // 64-element K chunks per stage
-  constexpr uint32_t kAStageBytes = a_stage_bytes<BK>();
-  constexpr uint32_t kBStage = b_stage_bytes<BN, CG, BK>();
-  constexpr uint32_t kMNChunkBytes = 128u * BK;            // one 64(MN) x BK(K) chunk
+  constexpr int kKChunks = BK / kChunkElems;               // 128-byte K chunks per stage
+  constexpr uint32_t kAStageBytes = a_stage_bytes<BK, EB>();
+  constexpr uint32_t kBStage = b_stage_bytes<BN, CG, BK, EB>();
+  constexpr uint32_t kMNChunkBytes = 128u * BK;            // one 128-byte(MN) x BK(K) chunk
   constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;   // two accumulators; the
                                                                // allocation unit is 32
   // Epilogue columns per step: one 128-byte staging row, or the whole tile when it is
@@ -335,11 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cluster_id = static_cast<int>(blockIdx.x) / CG;
   const int n_clusters = static_cast<int>(gridDim.x) / CG;
 
-  // TMA boxes of one stage in this CTA.  A: K-major, one 2-D box {64 K, 128 M} per
-  // K chunk, or M-major, one 2-D box {64 M, BK K} per 64-row chunk of M; or, with a
-  // 3-D map, the whole stage in one box.  B likewise with BN/CG columns.
-  const int n_a_boxes = p.a3d ? 1 : (p.trans_a ? kBM / 64 : kKChunks);
-  const int n_b_boxes = p.b3d ? 1 : (p.trans_b ? kKChunks : kBnCta / 64);
+  // TMA boxes of one stage in this CTA (a chunk is kChunkElems = 128 bytes wide).
+  // A: K-major, one 2-D box {chunk K, 128 M} per K chunk, or M-major, one 2-D box
+  // {chunk M, BK K} per chunk of M; or, with a 3-D map, the whole stage in one box.
+  // B likewise with BN/CG columns.
+  const int n_a_boxes = p.a3d ? 1 : (p.trans_a ? kBM / kChunkElems : kKChunks);
+  const int n_b_boxes = p.b3d ? 1 : (p.trans_b ? kKChunks : kBnCta / kChunkElems);
   const int n_boxes = n_a_boxes + n_b_boxes;
   // producers take turns by stage (see below); at most one per ring slot
   const int n_producers = min(kProducers, min(S, max(1, p.producers)));
@@ -403,24 +415,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           map = &tmap_a;
           dst = a_dst;
           if (p.a3d) {
-            if (!p.trans_a) { x = 0; y = m0; z = kb * kKChunks; }            // {64, 128, chunks}
-            else { x = 0; y = k0; z = m0 / 64; }                              // {64, BK, 2}
+            if (!p.trans_a) { x = 0; y = m0; z = kb * kKChunks; }           // {chunk, 128, chunks}
+            else { x = 0; y = k0; z = m0 / kChunkElems; }                     // {chunk, BK, 128/chunk}
           } else if (!p.trans_a) {
-            dst += j * (kBM * 128u); x = k0 + 64 * j; y = m0;                 // {64 K, 128 M}
+            dst += j * (kBM * 128u); x = k0 + kChunkElems * j; y = m0;        // {chunk K, 128 M}
           } else {
-            dst += j * kMNChunkBytes; x = m0 + 64 * j; y = k0;                // {64 M, BK K}
+            dst += j * kMNChunkBytes; x = m0 + kChunkElems * j; y = k0;       // {chunk M, BK K}
           }
         } else {
           const int c = j - n_a_boxes;
           map = &tmap_b;
           dst = b_dst;
           if (p.b3d) {
-            if (p.trans_b) { x = 0; y = nb0; z = kb * kKChunks; }            // {64, BN/CG, chunks}
-            else { x = 0; y = k0; z = nb0 / 64; }                             // {64, BK, chunks}
+            if (p.trans_b) { x = 0; y = nb0; z = kb * kKChunks; }           // {chunk, BN/CG, chunks}
+            else { x = 0; y = k0; z = nb0 / kChunkElems; }                    // {chunk, BK, chunks}
           } else if (p.trans_b) {
-            dst += c * (kBnCta * 128u); x = k0 + 64 * c; y = nb0;             // {64 K, BN/CG N}
+            dst += c * (kBnCta * 128u); x = k0 + kChunkElems * c; y = nb0;    // {chunk K, BN/CG N}
           } else {
-            dst += c * kMNChunkBytes; x = nb0 + 64 * c; y = k0;               // {64 N, BK K}
+            dst += c * kMNChunkBytes; x = nb0 + kChunkElems * c; y = k0;      // {chunk N, BK K}
           }
         }
         if (z >= 0) {
@@ -475,11 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b_lbo = p.trans_b ? 16u : kMNChunkBytes;
       const uint64_t a_desc0 = smem_desc_sw128(sA, a_lbo, 1024u);
       const uint64_t b_desc0 = smem_desc_sw128(sB, b_lbo, 1024u);
-      // Start-address offset of MMA k-step k (16 elements of K) within a stage, in
-      // 16-byte descriptor units.  K-major: chunk k/4 of the stage, then 32 B along
-      // the swizzled row; M/N-major: 16 rows of 128 B per step.
+      // Start-address offset of MMA k-step k (kMmaK elements = 32 bytes of K) within
+      // a stage, in 16-byte descriptor units.  K-major: chunk k/4 of the stage, then
+      // 32 B along the swizzled row; M/N-major: kMmaK rows of 128 B per step.
       auto k_off = [&](bool mn_major, uint32_t rows, int k) -> uint64_t {
-        return mn_major ? (static_cast<uint64_t>(k) * 16u * 128u) >> 4
+        return mn_major ? (static_cast<uint64_t>(k) * kMmaK * 128u) >> 4
                         : (static_cast<uint64_t>(k / 4) * rows * 128u + (k % 4) * 32u) >> 4;
       };
       int stage = 0;
@@ -512,12 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a_desc = a_desc0 + ((stage * kAStageBytes) >> 4);
           const uint64_t b_desc = b_desc0 + ((stage * kBStage) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / kUmmaK; ++k) {
+          for (int k = 0; k < BK / kMmaK; ++k) {
             const uint32_t acc_in = (kb != w.k0 || k != 0) ? 1u : 0u;
             const uint64_t ad = a_desc + k_off(p.trans_a, kBM, k);
             const uint64_t bd = b_desc + k_off(!p.trans_b, kBnCta, k);
-            if constexpr (kPair) mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, acc_in);
-            else mma_f16_ss(d_tmem, ad, bd, p.idesc, acc_in);
+            if constexpr (EB == 1) {
+              if constexpr (kPair) mma_f8_ss_pair(d_tmem, ad, bd, p.idesc, acc_in);
+              else mma_f8_ss(d_tmem, ad, bd, p.idesc, acc_in);
+            } else {
+              if constexpr (kPair) mma_f16_ss_pair(d_tmem, ad, bd, p.idesc, acc_in);
+              else mma_f16_ss(d_tmem, ad, bd, p.idesc, acc_in);
+            }
           }
           // frees the slot (in both CTAs) once these MMAs have read it
           if constexpr (kPair) mma_commit_pair(empty_bar(stage), 0x3);
@@ -647,6 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kEC; ++j)
             v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(partial_at(u2, c * kEC + j)));
         }
+        if (p.scale) {
+#pragma unroll
+          for (int j = 0; j < kEC; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * p.alpha);
+        }
         uint32_t packed[kEC / 2];
         pack_chunk<kEC / 2>(v, packed, p.bf16, p.relu);
         const int row = m0 + q * 32 + lane;      // this lane's row of the kernel's tile
@@ -771,21 +792,23 @@ __global__ void tl_fill_zero_kernel(uint16_t* C, int64_t M, int64_t N, int64_t l
   }
 }
 
-// Copy a rows x cols matrix of 2-byte elements from pitch `sp` to pitch `dp`
+// Copy a rows x cols matrix of 1- or 2-byte elements from pitch `sp` to pitch `dp`
 // (elements), used to give an operand a 16-byte-aligned pitch for the TMA unit.
-__global__ void tl_repack_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                                 int64_t rows, int64_t cols, int64_t sp, int64_t dp) {
+template <typename T>
+__global__ void tl_repack_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows,
+                                 int64_t cols, int64_t sp, int64_t dp) {
+  constexpr int64_t kPer = 8 / sizeof(T);           // elements per 8-byte unit
   const bool wide = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 7u) == 0 &&
-                    (sp & 3) == 0 && (dp & 3) == 0 && (cols & 3) == 0;
+                    (sp % kPer) == 0 && (dp % kPer) == 0 && (cols % kPer) == 0;
   if (wide) {
-    const int64_t units = cols >> 2;   // 8-byte units per row
+    const int64_t units = cols / kPer;               // 8-byte units per row
     const int64_t total = rows * units;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
       const int64_t r = i / units;
       const int64_t u = i - r * units;
-      const uint2 v = *reinterpret_cast<const uint2*>(src + r * sp + 4 * u);
-      *reinterpret_cast<uint2*>(dst + r * dp + 4 * u) = v;
+      const uint2 v = *reinterpret_cast<const uint2*>(src + r * sp + kPer * u);
+      *reinterpret_cast<uint2*>(dst + r * dp + kPer * u) = v;
     }
   } else {
     const int64_t total = rows * cols;

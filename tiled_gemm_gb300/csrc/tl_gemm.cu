@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstddef>
@@ -49,7 +50,7 @@ struct DeviceState {
   int smem_optin = 0;                        // max dynamic shared memory per CTA
   uint32_t* status = nullptr;
   std::atomic<uint32_t> attr_done{0};        // bit i: smem attribute set for kernel i
-  int max_units[16] = {};                    // resident CTAs (pairs) per kernel
+  int max_units[32] = {};                    // resident CTAs (pairs) per kernel
   std::mutex mu;
 };
 
@@ -97,14 +98,29 @@ DeviceState* device_state(int* dev_out) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-bool tma_ok(const void* p, int64_t ld) {
-  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * 2) & 15) == 0;
+bool is_fp8(tl_dtype t) { return t == TL_E4M3 || t == TL_E5M2; }
+int elem_bytes(tl_dtype t) { return is_fp8(t) ? 1 : 2; }
+
+// The element types of one call: operands of `eb` bytes in formats a_fmt / b_fmt (the
+// MMA's format codes), output `out` (fp16 or bf16), and the product scale alpha.
+struct Types {
+  int eb;
+  tl_dtype a_type, b_type, out;
+  float alpha;
+  bool scale;
+};
+
+Types types_16(tl_dtype dtype) { return Types{2, dtype, dtype, dtype, 1.0f, false}; }
+
+bool tma_ok(const void* p, int64_t ld, int eb = 2) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * eb) & 15) == 0;
 }
 
 // Byte extent [lo, hi) touched by a rows x cols matrix with leading dimension ld.
-void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, uintptr_t* lo, uintptr_t* hi) {
+void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, uintptr_t* lo, uintptr_t* hi,
+            int eb = 2) {
   *lo = reinterpret_cast<uintptr_t>(p);
-  *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2);
+  *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * eb);
 }
 
 bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
@@ -125,7 +141,15 @@ tl_status check_device_pointer(const void* p, int dev) {
 // bm = 128: one CTA per 128 x bn tile.  bm = 256: a CTA pair (cluster of 2,
 // cta_group::2 MMAs) per 256 x bn tile, each CTA holding half of B's columns.
 // Narrow tiles (bn 16 or 32, for skinny products) come with 128-deep stages only.
-bool plan_supported(const tl_plan& pl) {
+// 8-bit operands (eb = 1): bk 128 or 256 (one or two 128-byte chunks), bn >= 64, no
+// operand swap.
+bool plan_supported(const tl_plan& pl, int eb = 2) {
+  if (eb == 1) {
+    const bool bn8 = (pl.bm == 128 && (pl.bn == 64 || pl.bn == 128 || pl.bn == 256)) ||
+                     (pl.bm == 256 && (pl.bn == 128 || pl.bn == 256));
+    return bn8 && (pl.bk == 128 || pl.bk == 256) && pl.stages >= 2 && pl.stages <= 8 &&
+           pl.raster_group >= 1 && pl.grid >= 0 && pl.swap_ab == 0;
+  }
   const bool narrow = pl.bm == 128 && (pl.bn == 16 || pl.bn == 32) && pl.bk == 128;
   const bool bn_ok = narrow ||
                      (pl.bm == 128 && (pl.bn == 64 || pl.bn == 128 || pl.bn == 256)) ||
@@ -136,36 +160,42 @@ bool plan_supported(const tl_plan& pl) {
 
 // Narrow tiles read B in 64-element K chunks of bn rows: the kernel's B operand must
 // be K-major.  With swap_ab the kernel's B is A, K-major when A is not transposed.
-bool narrow_ok(const tl_plan& pl, int trans_a, int trans_b) {
+// 8-bit operands: an N-major B is read in boxes 128 elements wide, so each CTA's share
+// of the tile's columns (bn / cg) must be a multiple of 128.
+bool narrow_ok(const tl_plan& pl, int trans_a, int trans_b, int eb = 2) {
+  if (eb == 1) return trans_b == 1 || (pl.bn / (pl.bm / 128)) % 128 == 0;
   if (pl.bn >= 64) return true;
   return pl.swap_ab ? trans_a == 0 : trans_b == 1;
 }
 
-template <int BK>
+template <int BK, int EB>
 uint32_t smem_for_bk(int bm, int bn, int stages) {
   if (bm == 256) {
-    return bn == 128 ? tl::smem_bytes_for<128, 2, BK>(stages)
-                     : tl::smem_bytes_for<256, 2, BK>(stages);
+    return bn == 128 ? tl::smem_bytes_for<128, 2, BK, EB>(stages)
+                     : tl::smem_bytes_for<256, 2, BK, EB>(stages);
   }
-  if constexpr (BK == 128) {
+  if constexpr (BK == 128 && EB == 2) {
     if (bn == 16) return tl::smem_bytes_for<16, 1, BK>(stages);
     if (bn == 32) return tl::smem_bytes_for<32, 1, BK>(stages);
   }
   switch (bn) {
-    case 64: return tl::smem_bytes_for<64, 1, BK>(stages);
-    case 128: return tl::smem_bytes_for<128, 1, BK>(stages);
-    default: return tl::smem_bytes_for<256, 1, BK>(stages);
+    case 64: return tl::smem_bytes_for<64, 1, BK, EB>(stages);
+    case 128: return tl::smem_bytes_for<128, 1, BK, EB>(stages);
+    default: return tl::smem_bytes_for<256, 1, BK, EB>(stages);
   }
 }
 
-uint32_t smem_for(int bm, int bn, int bk, int stages) {
-  return bk == 128 ? smem_for_bk<128>(bm, bn, stages) : smem_for_bk<64>(bm, bn, stages);
+uint32_t smem_for(int bm, int bn, int bk, int stages, int eb = 2) {
+  if (eb == 1) {
+    return bk == 256 ? smem_for_bk<256, 1>(bm, bn, stages) : smem_for_bk<128, 1>(bm, bn, stages);
+  }
+  return bk == 128 ? smem_for_bk<128, 2>(bm, bn, stages) : smem_for_bk<64, 2>(bm, bn, stages);
 }
 
 tl_status validate_common(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
                           int trans_b) {
   if (M < 0 || N < 0 || K < 0) return TL_ERR_INVALID_ARG;
-  if (dtype != TL_F16 && dtype != TL_BF16) return TL_ERR_INVALID_ARG;
+  if (dtype != TL_F16 && dtype != TL_BF16 && !is_fp8(dtype)) return TL_ERR_INVALID_ARG;
   if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return TL_ERR_INVALID_ARG;
   // coordinates and tile counts are 32-bit inside the kernel
   if (M > (int64_t{1} << 31) - 256 || N > (int64_t{1} << 31) - 256 ||
@@ -192,7 +222,7 @@ int default_prefetch(const tl_plan& pl) {
 // costs ~6,000 SM cycles, i.e. fixup_kb k-blocks of about max(600, MMA cycles) each --
 // so short tiles stay whole.  Under the power cap the split also raises the clock-
 // limited work, hence the 0.87 margin.
-void schedule(tl_plan* pl, int64_t units_avail, bool allow_split) {
+void schedule(tl_plan* pl, int64_t units_avail, bool allow_split, int eb = 2) {
   const int cg = pl->bm / 128;
   const int64_t units = std::max<int64_t>(1, units_avail);
   const int64_t T = pl->tiles, KI = pl->k_blocks;
@@ -202,7 +232,8 @@ void schedule(tl_plan* pl, int64_t units_avail, bool allow_split) {
     if (rem != 0 || pl->stream_k == 1) {
       const int64_t dp_try = full >= 1 ? (full - 1) * units : 0;
       const int64_t it = (T - dp_try) * KI;
-      const double mma_cycles = 128.0 * pl->bn * pl->bk / 4096.0;     // per SM and k-block
+      // per SM and k-block: 32 bytes of K per MMA step, bn/256 x 128 cycles each
+      const double mma_cycles = static_cast<double>(pl->bn) * pl->bk * eb / 64.0;
       const double fixup_kb = 6000.0 / std::max(600.0, 1.1 * mma_cycles);
       const double t_dp = static_cast<double>(ceil_div(T, units) * KI);
       const double t_sk =
@@ -226,8 +257,8 @@ int64_t split_workspace_bytes(const tl_plan& pl) {
 }
 
 tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, int num_sms,
-                        tl_plan* pl) {
-  if (!plan_supported(*pl) || !narrow_ok(*pl, trans_a, trans_b)) return TL_ERR_INVALID_ARG;
+                        tl_plan* pl, int eb = 2) {
+  if (!plan_supported(*pl, eb) || !narrow_ok(*pl, trans_a, trans_b, eb)) return TL_ERR_INVALID_ARG;
   const int sms = num_sms > 0 ? num_sms : kDefaultSms;
   const int cg = pl->bm / 128;                       // CTAs per tile
   if (pl->swap_ab) std::swap(M, N);                  // the kernel computes C^T
@@ -236,18 +267,19 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_
   pl->tiles = pl->tiles_m * pl->tiles_n;
   pl->k_blocks = ceil_div(K, pl->bk);
   // per CTA: 128 rows of A and bn/cg columns of B per stage
-  pl->ring_bytes = static_cast<int64_t>(pl->stages) * (128 * pl->bk + (pl->bn / cg) * pl->bk) * 2;
-  pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages);
+  pl->ring_bytes =
+      static_cast<int64_t>(pl->stages) * (128 * pl->bk + (pl->bn / cg) * pl->bk) * eb;
+  pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages, eb);
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
   pl->tmem_cols = std::max(32, 2 * pl->bn);
   pl->tma_store = (!pl->swap_ab && pl->bn >= 64) ? 1 : 0;   // for a 16-byte aligned C
   pl->repack_a = pl->repack_b = 0;                            // ditto for A and B
-  pl->tx_bytes = (128 + pl->bn / cg) * pl->bk * 2;
+  pl->tx_bytes = (128 + pl->bn / cg) * pl->bk * eb;
   if (pl->tiles > (int64_t{1} << 31) - 1) return TL_ERR_UNSUPPORTED;
   if (pl->stream_k < -1 || pl->stream_k > 1) return TL_ERR_INVALID_ARG;
   // grid in CTAs: a multiple of cg; one persistent unit (CTA or pair) per SM (pair)
   const int64_t want_units = pl->grid > 0 ? std::max<int64_t>(1, pl->grid / cg) : sms / cg;
-  schedule(pl, want_units, true);
+  schedule(pl, want_units, true, eb);
   if (pl->l2_prefetch < 0) pl->l2_prefetch = default_prefetch(*pl);
   if (pl->l2_prefetch > 1024) return TL_ERR_INVALID_ARG;
   // producers take turns by stage: at most one per ring slot, at most three warps
@@ -260,7 +292,8 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_
 // Choose BN and the ring depth: fewest waves of tiles over the SMs, weighted by the
 // per-tile cost of each width (narrower tiles re-read A more often and issue
 // smaller MMAs).  Depth fills the shared memory left after the staging buffers.
-void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int sms, tl_plan* pl) {
+void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, int sms,
+                   tl_plan* pl, int eb = 2) {
   pl->raster_group = 16;
   pl->grid = 0;
   pl->l2_prefetch = -1;
@@ -274,7 +307,7 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int sms, tl_pla
   // 128 the split's fix-up costs more than it saves (128 x 64 tiles stay faster).
   // An M-major A (trans_a) cannot feed boxes narrower than 64, so it keeps the
   // direct form.
-  if (M <= 32 && !trans_a && N >= 2048 && K >= 1024) {
+  if (eb == 2 && M <= 32 && !trans_a && N >= 2048 && K >= 1024) {
     pl->bm = 128;
     pl->bn = M <= 16 ? 16 : 32;
     pl->bk = 128;
@@ -296,10 +329,13 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int sms, tl_pla
   constexpr int kCands = sizeof(cands) / sizeof(cands[0]);
   double best = 0.0;
   int pick = -1;
+  // 8-bit operands: the same tiles with twice the K elements per stage (the same bytes).
   for (int i = 0; i < kCands; ++i) {
-    if (cands[i].bk == 128 && K < 1024) continue;   // deep stages pay off on long K loops
+    const int bk = cands[i].bk * (eb == 1 ? 2 : 1);
+    if (bk * eb == 256 && K < 1024 * (eb == 1 ? 2 : 1)) continue;   // deep stages: long K
     const int cg = cands[i].bm / 128;
     if (cg == 2 && M <= 128) continue;            // the odd CTA would hold no rows of A
+    if (eb == 1 && !trans_b && (cands[i].bn / cg) % 128 != 0) continue;   // 128-wide N boxes
     const int64_t tiles = ceil_div(M, cands[i].bm) * ceil_div(N, cands[i].bn);
     const int64_t waves = ceil_div(tiles, std::max(1, sms / cg));
     const double cost = static_cast<double>(waves) * cands[i].tile_cost;
@@ -310,7 +346,7 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int sms, tl_pla
   }
   pl->bm = cands[pick].bm;
   pl->bn = cands[pick].bn;
-  pl->bk = cands[pick].bk;
+  pl->bk = cands[pick].bk * (eb == 1 ? 2 : 1);
   pl->stages = cands[pick].stages;
 }
 
@@ -321,7 +357,7 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int sms, tl_pla
 // descriptor prefetch) while the previous kernel of the stream finishes; the kernel
 // waits for that kernel's completion (griddepcontrol.wait) before it reads or
 // writes global memory.  attr must hold 2 entries.
-template <int BN, int CG, int BK>
+template <int BN, int CG, int BK, int EB>
 void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t smem,
                    cudaStream_t stream) {
   *cfg = cudaLaunchConfig_t{};
@@ -347,15 +383,18 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
 // units (CTAs, or CTA pairs) the device keeps resident at once -- the persistent grid
 // must not exceed it (pairs sit on SM pairs within one GPC).  Returns that count, or
 // -1 if the attribute could not be set.
-template <int BN, int CG, int BK>
+template <int BN, int CG, int BK, int EB = 2>
 int prepare_kernel(DeviceState* st) {
+  // slot of this kernel in the per-device caches: 0-11 the 16-bit tilings, 12-13 the
+  // narrow ones, 16-27 the 8-bit ones
   constexpr int kIdx = BN < 64 ? 12 + (BN == 32)
-                               : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) + 6 * (BK == 128);
+                               : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) +
+                                     6 * (BK * EB == 256) + 16 * (EB == 1);
   constexpr uint32_t bit = 1u << kIdx;
   if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
   std::lock_guard<std::mutex> lock(st->mu);
   if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
-  auto kern = tl::tl_gemm_kernel<BN, CG, BK>;
+  auto kern = tl::tl_gemm_kernel<BN, CG, BK, EB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            st->smem_optin) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -365,7 +404,7 @@ int prepare_kernel(DeviceState* st) {
   if (CG == 2) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    launch_config<BN, CG, BK>(&cfg, attr, static_cast<size_t>(st->smem_optin), nullptr);
+    launch_config<BN, CG, BK, EB>(&cfg, attr, static_cast<size_t>(st->smem_optin), nullptr);
     cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
@@ -379,35 +418,41 @@ int prepare_kernel(DeviceState* st) {
   return units;
 }
 
-template <int BK>
+template <int BK, int EB>
 int resident_units_bk(DeviceState* st, int bm, int bn) {
-  if (bm == 256) return bn == 128 ? prepare_kernel<128, 2, BK>(st) : prepare_kernel<256, 2, BK>(st);
-  if constexpr (BK == 128) {
+  if (bm == 256) {
+    return bn == 128 ? prepare_kernel<128, 2, BK, EB>(st) : prepare_kernel<256, 2, BK, EB>(st);
+  }
+  if constexpr (BK == 128 && EB == 2) {
     if (bn == 16) return prepare_kernel<16, 1, BK>(st);
     if (bn == 32) return prepare_kernel<32, 1, BK>(st);
   }
   switch (bn) {
-    case 64: return prepare_kernel<64, 1, BK>(st);
-    case 128: return prepare_kernel<128, 1, BK>(st);
-    default: return prepare_kernel<256, 1, BK>(st);
+    case 64: return prepare_kernel<64, 1, BK, EB>(st);
+    case 128: return prepare_kernel<128, 1, BK, EB>(st);
+    default: return prepare_kernel<256, 1, BK, EB>(st);
   }
 }
 
-int resident_units(DeviceState* st, const tl_plan& pl) {
-  return pl.bk == 128 ? resident_units_bk<128>(st, pl.bm, pl.bn)
-                      : resident_units_bk<64>(st, pl.bm, pl.bn);
+int resident_units(DeviceState* st, const tl_plan& pl, int eb) {
+  if (eb == 1) {
+    return pl.bk == 256 ? resident_units_bk<256, 1>(st, pl.bm, pl.bn)
+                        : resident_units_bk<128, 1>(st, pl.bm, pl.bn);
+  }
+  return pl.bk == 128 ? resident_units_bk<128, 2>(st, pl.bm, pl.bn)
+                      : resident_units_bk<64, 2>(st, pl.bm, pl.bn);
 }
 
 // Launch with exactly pl.grid CTAs: the work split in `prm` was computed for that grid.
-template <int BN, int CG, int BK>
+template <int BN, int CG, int BK, int EB = 2>
 tl_status launch_bn(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
                     const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
                     cudaStream_t stream) {
-  if (prepare_kernel<BN, CG, BK>(st) < 0) return TL_ERR_LAUNCH;
-  auto kern = tl::tl_gemm_kernel<BN, CG, BK>;
+  if (prepare_kernel<BN, CG, BK, EB>(st) < 0) return TL_ERR_LAUNCH;
+  auto kern = tl::tl_gemm_kernel<BN, CG, BK, EB>;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  launch_config<BN, CG, BK>(&cfg, attr, static_cast<size_t>(pl.smem_bytes), stream);
+  launch_config<BN, CG, BK, EB>(&cfg, attr, static_cast<size_t>(pl.smem_bytes), stream);
   cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -416,23 +461,34 @@ tl_status launch_bn(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
   return TL_OK;
 }
 
-template <int BK>
+template <int BK, int EB>
 tl_status launch_tiling(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
                         const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
                         cudaStream_t stream) {
   if (pl.bm == 256) {
-    return pl.bn == 128 ? launch_bn<128, 2, BK>(st, pl, ta, tb, tc, prm, stream)
-                        : launch_bn<256, 2, BK>(st, pl, ta, tb, tc, prm, stream);
+    return pl.bn == 128 ? launch_bn<128, 2, BK, EB>(st, pl, ta, tb, tc, prm, stream)
+                        : launch_bn<256, 2, BK, EB>(st, pl, ta, tb, tc, prm, stream);
   }
-  if constexpr (BK == 128) {
+  if constexpr (BK == 128 && EB == 2) {
     if (pl.bn == 16) return launch_bn<16, 1, BK>(st, pl, ta, tb, tc, prm, stream);
     if (pl.bn == 32) return launch_bn<32, 1, BK>(st, pl, ta, tb, tc, prm, stream);
   }
   switch (pl.bn) {
-    case 64: return launch_bn<64, 1, BK>(st, pl, ta, tb, tc, prm, stream);
-    case 128: return launch_bn<128, 1, BK>(st, pl, ta, tb, tc, prm, stream);
-    default: return launch_bn<256, 1, BK>(st, pl, ta, tb, tc, prm, stream);
+    case 64: return launch_bn<64, 1, BK, EB>(st, pl, ta, tb, tc, prm, stream);
+    case 128: return launch_bn<128, 1, BK, EB>(st, pl, ta, tb, tc, prm, stream);
+    default: return launch_bn<256, 1, BK, EB>(st, pl, ta, tb, tc, prm, stream);
   }
+}
+
+tl_status launch_plan(DeviceState* st, const tl_plan& pl, int eb, const CUtensorMap& ta,
+                      const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
+                      cudaStream_t stream) {
+  if (eb == 1) {
+    return pl.bk == 256 ? launch_tiling<256, 1>(st, pl, ta, tb, tc, prm, stream)
+                        : launch_tiling<128, 1>(st, pl, ta, tb, tc, prm, stream);
+  }
+  return pl.bk == 128 ? launch_tiling<128, 2>(st, pl, ta, tb, tc, prm, stream)
+                      : launch_tiling<64, 2>(st, pl, ta, tb, tc, prm, stream);
 }
 
 // ---- tensor-map descriptors --------------------------------------------------------
@@ -462,6 +518,12 @@ constexpr size_t kMapCacheMax = 4096;
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash>* g_maps = nullptr;
 
+CUtensorMapDataType map_type(tl_dtype t) {
+  if (t == TL_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (t == TL_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return CU_TENSOR_MAP_DATA_TYPE_UINT8;           // E4M3 / E5M2 codes, moved as bytes
+}
+
 bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* base,
                    const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   MapKey key;
@@ -487,8 +549,7 @@ bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* 
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt =
-      dtype == TL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = map_type(dtype);
   if (enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
@@ -504,22 +565,25 @@ bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* 
 bool encode_2d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inner, uint64_t outer,
                uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {ld_elems * 2};
+  const cuuint64_t strides[1] = {ld_elems * static_cast<uint64_t>(elem_bytes(dtype))};
   const cuuint32_t box[2] = {box_inner, box_outer};
   return encode_cached(map, dtype, 2, base, dims, strides, box);
 }
 
-// A row-major [rows][ld] matrix whose contiguous extent `inner` is a multiple of 64,
-// viewed as the 3-D tensor {64, rows, inner/64} (element (i, r, c) at r*ld + 64c + i)
-// so that one box {64, box_rows, box_chunks} fetches several 64-element chunks of
-// every row.  Exact (no reads past `inner`) because the chunks tile `inner` exactly.
+// A row-major [rows][ld] matrix whose contiguous extent `inner` is a multiple of the
+// 128-byte chunk (c = 64 elements of 2 bytes, 128 of 1 byte), viewed as the 3-D tensor
+// {c, rows, inner/c} (element (i, r, k) at r*ld + c*k + i) so that one box
+// {c, box_rows, box_chunks} fetches several chunks of every row.  Exact (no reads
+// past `inner`) because the chunks tile `inner` exactly.
 bool encode_chunked_3d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inner,
                        uint64_t rows, uint64_t ld_elems, uint32_t box_rows,
                        uint32_t box_chunks) {
-  if (inner % 64 != 0) return false;
-  const cuuint64_t dims[3] = {64, rows, inner / 64};
-  const cuuint64_t strides[2] = {ld_elems * 2, 128};
-  const cuuint32_t box[3] = {64, box_rows, box_chunks};
+  const uint64_t eb = static_cast<uint64_t>(elem_bytes(dtype));
+  const uint64_t chunk = 128 / eb;
+  if (inner % chunk != 0) return false;
+  const cuuint64_t dims[3] = {chunk, rows, inner / chunk};
+  const cuuint64_t strides[2] = {ld_elems * eb, 128};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(chunk), box_rows, box_chunks};
   return encode_cached(map, dtype, 3, base, dims, strides, box);
 }
 
@@ -570,9 +634,11 @@ void* noalloc_scratch(int dev) {
 }
 
 tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-              int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype, int trans_a, int trans_b,
+              int64_t lda, int64_t ldb, int64_t ldc, const Types& ty, int trans_a, int trans_b,
               tl_epilogue epilogue, const tl_plan* forced, cudaStream_t stream,
               bool no_alloc = false) {
+  const tl_dtype dtype = ty.out;
+  const int eb = ty.eb;
   tl_status s = validate_common(M, N, K, dtype, trans_a, trans_b);
   if (s != TL_OK) return s;
   if (epilogue != TL_EPI_NONE && epilogue != TL_EPI_RELU) return TL_ERR_INVALID_ARG;
@@ -585,12 +651,12 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   if (K > 0) {
     if (lda < a_cols || ldb < b_cols) return TL_ERR_INVALID_ARG;
     if (A == nullptr || B == nullptr) return TL_ERR_NULL_PTR;
-    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u)
+    if (eb == 2 && ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u))
       return TL_ERR_ALIGNMENT;
     uintptr_t c0, c1, a0, a1, b0, b1;
     extent(C, M, N, ldc, &c0, &c1);
-    extent(A, a_rows, a_cols, lda, &a0, &a1);
-    extent(B, b_rows, b_cols, ldb, &b0, &b1);
+    extent(A, a_rows, a_cols, lda, &a0, &a1, eb);
+    extent(B, b_rows, b_cols, ldb, &b0, &b1, eb);
     if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return TL_ERR_ALIAS;
   }
   int dev = 0;
@@ -625,30 +691,32 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     pl.stream_k = forced->stream_k;
     pl.swap_ab = forced->swap_ab;
   } else {
-    choose_tiling(M, N, K, trans_a, st->sms, &pl);
+    choose_tiling(M, N, K, trans_a, trans_b, st->sms, &pl, eb);
   }
-  if ((s = complete_plan(M, N, K, trans_a, trans_b, st->sms, &pl)) != TL_OK) return s;
+  if ((s = complete_plan(M, N, K, trans_a, trans_b, st->sms, &pl, eb)) != TL_OK) return s;
   if (pl.smem_bytes > st->smem_optin) return TL_ERR_INVALID_ARG;
   // Re-split over the units this device really keeps resident (CTA pairs: the cluster
   // occupancy can be below SMs / 2).  Callers that cannot allocate get whole tiles only:
   // the split needs a workspace for partial sums.
-  const int resident = resident_units(st, pl);
+  const int resident = resident_units(st, pl, eb);
   if (resident <= 0) return TL_ERR_LAUNCH;
   {
     const int cg = pl.bm / 128;
     const int64_t want_units = forced && forced->grid > 0 ? std::max(1, forced->grid / cg)
                                                            : st->sms / cg;
-    schedule(&pl, std::min<int64_t>(want_units, resident), !no_alloc);
+    schedule(&pl, std::min<int64_t>(want_units, resident), !no_alloc, eb);
   }
   const int64_t ws_split = split_workspace_bytes(pl);
 
-  // Operands the TMA unit cannot address directly go through a padded copy.
-  const bool repack_a = !tma_ok(A, lda);
-  const bool repack_b = !tma_ok(B, ldb);
-  const int64_t lda_w = repack_a ? ceil_div(a_cols, 8) * 8 : lda;
-  const int64_t ldb_w = repack_b ? ceil_div(b_cols, 8) * 8 : ldb;
-  const int64_t ws_a = repack_a ? a_rows * lda_w * 2 : 0;
-  const int64_t ws_b = repack_b ? b_rows * ldb_w * 2 : 0;
+  // Operands the TMA unit cannot address directly go through a padded copy (pitch
+  // rounded up to 16 bytes).
+  const int64_t pad = 16 / eb;
+  const bool repack_a = !tma_ok(A, lda, eb);
+  const bool repack_b = !tma_ok(B, ldb, eb);
+  const int64_t lda_w = repack_a ? ceil_div(a_cols, pad) * pad : lda;
+  const int64_t ldb_w = repack_b ? ceil_div(b_cols, pad) * pad : ldb;
+  const int64_t ws_a = repack_a ? a_rows * lda_w * eb : 0;
+  const int64_t ws_b = repack_b ? b_rows * ldb_w * eb : 0;
   void* ws = nullptr;
   const void* a_use = A;
   const void* b_use = B;
@@ -675,17 +743,23 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
       sk_flags = reinterpret_cast<unsigned long long*>(
           split + static_cast<int64_t>(pl.grid) * 128 * pl.bn * 4);
     }
+    auto repack = [&](const void* src, void* dst, int64_t rows, int64_t cols, int64_t sp,
+                      int64_t dp) {
+      if (eb == 1) {
+        tl::tl_repack_kernel<uint8_t><<<launch_blocks_for(rows * cols), 256, 0, stream>>>(
+            static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), rows, cols, sp, dp);
+      } else {
+        tl::tl_repack_kernel<uint16_t><<<launch_blocks_for(rows * cols), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, sp, dp);
+      }
+    };
     if (repack_a) {
-      tl::tl_repack_kernel<<<launch_blocks_for(a_rows * a_cols), 256, 0, stream>>>(
-          static_cast<const uint16_t*>(A), reinterpret_cast<uint16_t*>(w), a_rows, a_cols, lda,
-          lda_w);
+      repack(A, w, a_rows, a_cols, lda, lda_w);
       a_use = w;
     }
     if (repack_b) {
       uint8_t* wb = w + ws_a_rounded;
-      tl::tl_repack_kernel<<<launch_blocks_for(b_rows * b_cols), 256, 0, stream>>>(
-          static_cast<const uint16_t*>(B), reinterpret_cast<uint16_t*>(wb), b_rows, b_cols, ldb,
-          ldb_w);
+      repack(B, wb, b_rows, b_cols, ldb, ldb_w);
       b_use = wb;
     }
     if (cudaGetLastError() != cudaSuccess) {
@@ -699,11 +773,14 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     const void* ptr;
     int64_t ld;
     int trans;
+    tl_dtype type;
   };
   const bool swap = pl.swap_ab != 0;
   const int64_t kM = swap ? N : M, kN = swap ? M : N;
-  const Operand ka = swap ? Operand{b_use, ldb_w, !trans_b} : Operand{a_use, lda_w, trans_a};
-  const Operand kb = swap ? Operand{a_use, lda_w, !trans_a} : Operand{b_use, ldb_w, trans_b};
+  const Operand ka = swap ? Operand{b_use, ldb_w, !trans_b, ty.b_type}
+                          : Operand{a_use, lda_w, trans_a, ty.a_type};
+  const Operand kb = swap ? Operand{a_use, lda_w, !trans_a, ty.a_type}
+                          : Operand{b_use, ldb_w, trans_b, ty.b_type};
   // C by TMA bulk stores from a swizzled staging buffer, or by plain stores from
   // registers (16-byte vectors when C is aligned).  A forced plan with tma_store = -1
   // asks for plain stores.
@@ -717,22 +794,24 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   std::memset(&tc, 0, sizeof(tc));
   const int cg = pl.bm / 128;
   const uint32_t bn_cta = static_cast<uint32_t>(pl.bn / cg);
-  const uint32_t kchunks = static_cast<uint32_t>(pl.bk / 64);
+  const uint32_t chunk = static_cast<uint32_t>(128 / eb);          // elements per 128 bytes
+  const uint32_t kchunks = static_cast<uint32_t>(pl.bk * eb / 128);
   bool enc_ok = true;
   bool a3d = false, b3d = false;
   if (!ka.trans) {
-    a3d = kchunks > 1 && encode_chunked_3d(&ta, dtype, ka.ptr, K, kM, ka.ld, 128, kchunks);
-    if (!a3d) enc_ok &= encode_2d(&ta, dtype, ka.ptr, K, kM, ka.ld, 64, 128);
+    a3d = kchunks > 1 && encode_chunked_3d(&ta, ka.type, ka.ptr, K, kM, ka.ld, 128, kchunks);
+    if (!a3d) enc_ok &= encode_2d(&ta, ka.type, ka.ptr, K, kM, ka.ld, chunk, 128);
   } else {
-    a3d = encode_chunked_3d(&ta, dtype, ka.ptr, kM, K, ka.ld, pl.bk, 2);
-    if (!a3d) enc_ok &= encode_2d(&ta, dtype, ka.ptr, kM, K, ka.ld, 64, pl.bk);
+    a3d = encode_chunked_3d(&ta, ka.type, ka.ptr, kM, K, ka.ld, pl.bk, 128 / chunk);
+    if (!a3d) enc_ok &= encode_2d(&ta, ka.type, ka.ptr, kM, K, ka.ld, chunk, pl.bk);
   }
   if (kb.trans) {
-    b3d = kchunks > 1 && encode_chunked_3d(&tb, dtype, kb.ptr, K, kN, kb.ld, bn_cta, kchunks);
-    if (!b3d) enc_ok &= encode_2d(&tb, dtype, kb.ptr, K, kN, kb.ld, 64, bn_cta);
+    b3d = kchunks > 1 && encode_chunked_3d(&tb, kb.type, kb.ptr, K, kN, kb.ld, bn_cta, kchunks);
+    if (!b3d) enc_ok &= encode_2d(&tb, kb.type, kb.ptr, K, kN, kb.ld, chunk, bn_cta);
   } else {
-    b3d = bn_cta > 64 && encode_chunked_3d(&tb, dtype, kb.ptr, kN, K, kb.ld, pl.bk, bn_cta / 64);
-    if (!b3d) enc_ok &= encode_2d(&tb, dtype, kb.ptr, kN, K, kb.ld, 64, pl.bk);
+    b3d = bn_cta > chunk &&
+          encode_chunked_3d(&tb, kb.type, kb.ptr, kN, K, kb.ld, pl.bk, bn_cta / chunk);
+    if (!b3d) enc_ok &= encode_2d(&tb, kb.type, kb.ptr, kN, K, kb.ld, chunk, pl.bk);
   }
   if (tma_store) enc_ok &= encode_2d(&tc, dtype, C, N, M, ldc, 64, 32);
   if (!enc_ok) {
@@ -754,6 +833,8 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.trans_a = ka.trans;
   prm.trans_b = kb.trans;
   prm.bf16 = dtype == TL_BF16 ? 1 : 0;
+  prm.scale = ty.scale ? 1 : 0;
+  prm.alpha = ty.alpha;
   prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
   prm.tma_store = tma_store ? 1 : 0;
   prm.c_trans = swap ? 1 : 0;
@@ -767,16 +848,19 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.sk_partials = sk_partials;
   prm.sk_flags = sk_flags;
   prm.sk_token = next_split_token();
-  prm.idesc = tl::mma_idesc_f16(prm.bf16, ka.trans ? 1u : 0u, kb.trans ? 0u : 1u,
-                                static_cast<uint32_t>(pl.bm), static_cast<uint32_t>(pl.bn));
+  prm.idesc = eb == 1
+                  ? tl::mma_idesc_f8(ka.type == TL_E5M2 ? 1u : 0u, kb.type == TL_E5M2 ? 1u : 0u,
+                                     ka.trans ? 1u : 0u, kb.trans ? 0u : 1u,
+                                     static_cast<uint32_t>(pl.bm), static_cast<uint32_t>(pl.bn))
+                  : tl::mma_idesc_f16(prm.bf16, ka.trans ? 1u : 0u, kb.trans ? 0u : 1u,
+                                      static_cast<uint32_t>(pl.bm), static_cast<uint32_t>(pl.bn));
   prm.C = C;
   prm.ldc = ldc;
   prm.status = st->status;
   prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   prm.stall = g_stall.load(std::memory_order_relaxed);
 
-  s = pl.bk == 128 ? launch_tiling<128>(st, pl, ta, tb, tc, prm, stream)
-                   : launch_tiling<64>(st, pl, ta, tb, tc, prm, stream);
+  s = launch_plan(st, pl, eb, ta, tb, tc, prm, stream);
   if (ws) {
     if (cudaFreeAsync(ws, stream) != cudaSuccess) {
       (void)cudaGetLastError();
@@ -793,8 +877,9 @@ extern "C" {
 tl_status tl_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                   int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype, int trans_a,
                   int trans_b, tl_epilogue epilogue, tl_stream_t stream) {
-  return run(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b, epilogue, nullptr,
-             reinterpret_cast<cudaStream_t>(stream));
+  if (dtype != TL_F16 && dtype != TL_BF16) return TL_ERR_INVALID_ARG;
+  return run(A, B, C, M, N, K, lda, ldb, ldc, types_16(dtype), trans_a, trans_b, epilogue,
+             nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tl_status tl_gemm_with_plan(const void* A, const void* B, void* C, int64_t M, int64_t N,
@@ -802,7 +887,20 @@ tl_status tl_gemm_with_plan(const void* A, const void* B, void* C, int64_t M, in
                             int trans_a, int trans_b, tl_epilogue epilogue, const tl_plan* plan,
                             tl_stream_t stream) {
   if (plan == nullptr) return TL_ERR_INVALID_ARG;
-  return run(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b, epilogue, plan,
+  if (dtype != TL_F16 && dtype != TL_BF16) return TL_ERR_INVALID_ARG;
+  return run(A, B, C, M, N, K, lda, ldb, ldc, types_16(dtype), trans_a, trans_b, epilogue, plan,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+tl_status tl_gemm_fp8(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, tl_dtype a_type, tl_dtype b_type,
+                      tl_dtype c_type, int trans_a, int trans_b, float alpha,
+                      tl_epilogue epilogue, const tl_plan* plan, tl_stream_t stream) {
+  if (!is_fp8(a_type) || !is_fp8(b_type)) return TL_ERR_INVALID_ARG;
+  if (c_type != TL_F16 && c_type != TL_BF16) return TL_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return TL_ERR_INVALID_ARG;
+  const Types ty{1, a_type, b_type, c_type, alpha, alpha != 1.0f};
+  return run(A, B, C, M, N, K, lda, ldb, ldc, ty, trans_a, trans_b, epilogue, plan,
              reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -813,8 +911,8 @@ tl_status tl_gemm_plan(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int tran
   if (s != TL_OK) return s;
   std::memset(plan, 0, sizeof(*plan));
   const int sms = num_sms > 0 ? num_sms : kDefaultSms;
-  choose_tiling(M, N, K, trans_a, sms, plan);
-  return complete_plan(M, N, K, trans_a, trans_b, sms, plan);
+  choose_tiling(M, N, K, trans_a, trans_b, sms, plan, elem_bytes(dtype));
+  return complete_plan(M, N, K, trans_a, trans_b, sms, plan, elem_bytes(dtype));
 }
 
 tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
@@ -832,14 +930,15 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
   plan->producers = prod;
   plan->stream_k = sk;
   plan->swap_ab = swap;
-  return complete_plan(M, N, K, trans_a, trans_b, num_sms, plan);
+  return complete_plan(M, N, K, trans_a, trans_b, num_sms, plan, elem_bytes(dtype));
 }
 
 tl_status tl_gemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
                           int64_t K, int64_t lda, int64_t ldb, int64_t ldc, tl_dtype dtype,
                           int trans_a, int trans_b, tl_epilogue epilogue, tl_stream_t stream) {
-  return run(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b, epilogue, nullptr,
-             reinterpret_cast<cudaStream_t>(stream), /*no_alloc=*/true);
+  if (dtype != TL_F16 && dtype != TL_BF16) return TL_ERR_INVALID_ARG;
+  return run(A, B, C, M, N, K, lda, ldb, ldc, types_16(dtype), trans_a, trans_b, epilogue,
+             nullptr, reinterpret_cast<cudaStream_t>(stream), /*no_alloc=*/true);
 }
 
 int64_t tl_gemm_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }

@@ -8,7 +8,8 @@ Recipe (stated once, used everywhere): one CPU ``torch.Generator`` per workload,
 seeded with the workload's seed; A is drawn first, then B, each in fp32 in the
 shape of its *storage* (A is [M, K], or [K, M] when ``trans_a``; B is [K, N], or
 [N, K] when ``trans_b``), then converted to the 16-bit dtype by torch's
-round-to-nearest-even cast.  Distributions follow the workloads the GEMM is
+round-to-nearest-even cast (8-bit E4M3 / E5M2 operands: torch's float8 cast of the
+same fp32 draw).  Distributions follow the workloads the GEMM is
 described with (the pages' quickstart GEMM at 1024^3 with fp16 operands and
 128x128x64 tiles in 3 stages; square bf16 GEMMs with a column-major B; a ragged
 shape that is a multiple of no tile; decode-like skinny products).
@@ -22,8 +23,11 @@ import torch
 
 F16 = 0
 BF16 = 1
-_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
-_NAME = {F16: "f16", BF16: "bf16"}
+E4M3 = 2
+E5M2 = 3
+_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.float8_e4m3fn,
+                E5M2: torch.float8_e5m2}
+_NAME = {F16: "f16", BF16: "bf16", E4M3: "e4m3", E5M2: "e5m2"}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -43,14 +47,43 @@ class Workload:
     seed: int = 0
     plan: tuple | None = None   # (BM, BN, BK, stages) when the workload fixes the tiling
     description: str = ""
+    # 8-bit operands only: B's own format (default: dtype), the output type, the scale
+    b_dtype: int | None = None
+    out_dtype: int = BF16
+    alpha: float = 1.0
+
+    @property
+    def fp8(self) -> bool:
+        return self.dtype in (E4M3, E5M2)
 
     @property
     def torch_dtype(self) -> torch.dtype:
+        """Output (and, for 16-bit workloads, operand) dtype."""
+        return _TORCH_DTYPE[self.out_dtype if self.fp8 else self.dtype]
+
+    @property
+    def c_dtype(self) -> int:
+        return self.out_dtype if self.fp8 else self.dtype
+
+    @property
+    def a_torch_dtype(self) -> torch.dtype:
         return _TORCH_DTYPE[self.dtype]
+
+    @property
+    def b_torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPE[self.b_dtype if self.b_dtype is not None else self.dtype]
+
+    @property
+    def b_fmt(self) -> int:
+        return self.b_dtype if self.b_dtype is not None else self.dtype
 
     @property
     def dtype_name(self) -> str:
         return _NAME[self.dtype]
+
+    @property
+    def elem_bytes(self) -> int:
+        return 1 if self.fp8 else 2
 
     @property
     def flops(self) -> int:
@@ -58,8 +91,8 @@ class Workload:
 
     @property
     def bytes_moved(self) -> int:
-        """Algorithmic HBM bytes: read A and B once, write C once (2-byte elements)."""
-        return 2 * (self.M * self.K + self.K * self.N + self.M * self.N)
+        """Algorithmic HBM bytes: read A and B once, write C (2-byte elements) once."""
+        return self.elem_bytes * (self.M * self.K + self.K * self.N) + 2 * self.M * self.N
 
     def a_shape(self) -> tuple[int, int]:
         return (self.K, self.M) if self.trans_a else (self.M, self.K)
@@ -88,15 +121,15 @@ def make_inputs(w: Workload, seed: int | None = None) -> tuple[torch.Tensor, tor
     """CPU tensors (A, B) in storage layout and the workload's dtype; A drawn first."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
-    a = _draw(w.a_shape(), w.dist_a, w.std_a, w.K, g).to(w.torch_dtype)
-    b = _draw(w.b_shape(), w.dist_b, w.std_b, w.K, g).to(w.torch_dtype)
+    a = _draw(w.a_shape(), w.dist_a, w.std_a, w.K, g).to(w.a_torch_dtype)
+    b = _draw(w.b_shape(), w.dist_b, w.std_b, w.K, g).to(w.b_torch_dtype)
     return a, b
 
 
 def integer_variant(w: Workload, M=None, N=None, K=None, seed=None) -> Workload:
     """Same layout and dtype with small-integer entries, so that every fp32 partial sum
     is exact and GPU and oracle must agree bit for bit."""
-    dist = "int_small" if w.dtype == F16 else "int_unit"
+    dist = "int_small" if w.dtype in (F16, E4M3, E5M2) else "int_unit"
     return dataclasses.replace(
         w, name=w.name + "_int", M=M or w.M, N=N or w.N, K=K or w.K,
         dist_a=dist, dist_b=dist, seed=w.seed if seed is None else seed)
@@ -130,6 +163,13 @@ for _m, _seed in ((16, 5), (64, 6), (128, 7)):
                   "normal", "normal", std_a=1.0, std_b=0.02, seed=_seed,
                   description=f"skinny decode-like GEMM M={_m}, N=K=8192 bf16, activations "
                               "N(0,1), weights N(0,0.02) stored [N,K]"))
+
+# 8-bit operands (one product scale): square products with weights stored [N, K]
+for _n, _seed in ((4096, 8), (8192, 9)):
+    _add(Workload(f"gemm_{_n}_e4m3_tb", _n, _n, _n, E4M3, False, True, False,
+                  "normal", "normal", seed=_seed, out_dtype=BF16, alpha=1.0 / 64,
+                  description=f"FP8 GEMM {_n}^3, E4M3 operands from N(0,1), B column-major, "
+                              "alpha 1/64, bf16 output"))
 
 # The benchmark's headline workload: the quickstart GEMM+ReLU.
 HEADLINE = "gemm_relu_1024_f16_128x128x64s3"
