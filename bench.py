@@ -89,8 +89,17 @@ def whole_job_tflops(flops_per_step: int, steps: int, world: int, max_ms: float)
     return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
 
 
+# Dense 8-bit tensor throughput over 16-bit on this part (nominal 4.5 vs 2.25 PFLOP/s):
+# the 8-bit peak is the measured bf16 peak times this ratio.
+FP8_OVER_BF16 = 2.0
+
+
+def tensor_peak_scale(w: workloads.Workload) -> float:
+    return FP8_OVER_BF16 if w.fp8 else 1.0
+
+
 def is_hbm_bound(w: workloads.Workload, peaks: dict) -> bool:
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ridge = tensor_peak_scale(w) * peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     return w.flops / w.bytes_moved < ridge
 
 
@@ -168,8 +177,13 @@ def oracle_rate(w: workloads.Workload, a_cpu, b_cpu, budget_s: float, threads: i
             sl_a, M_s = a_cpu[:rows].contiguous(), rows
             lda = w.K
         t0 = time.perf_counter()
-        oracle.gemm(sl_a, b_cpu, M_s, w.N, w.K, lda=lda, dtype=w.dtype, trans_a=w.trans_a,
-                    trans_b=w.trans_b, relu=w.relu, threads=threads)
+        if w.fp8:
+            oracle.gemm_fp8(sl_a, b_cpu, M_s, w.N, w.K, lda=lda, a_fmt=w.dtype, b_fmt=w.b_fmt,
+                            out_dtype=w.c_dtype, alpha=w.alpha, trans_a=w.trans_a,
+                            trans_b=w.trans_b, relu=w.relu, threads=threads)
+        else:
+            oracle.gemm(sl_a, b_cpu, M_s, w.N, w.K, lda=lda, dtype=w.dtype,
+                        trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, threads=threads)
         dt = time.perf_counter() - t0
         elapsed += dt
         done_flops += 2 * M_s * w.N * w.K
@@ -204,13 +218,21 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
         plan = tl.plan_for(0, 0, 0, bm, bn, bk, st)
     stream = torch.cuda.Stream(device=dev)
     lda = w.M if w.trans_a else w.K
-    launches_per_step = 1 + int((lda * 2) % 16 != 0) + int(
-        ((w.K if w.trans_b else w.N) * 2) % 16 != 0)
+    eb = w.elem_bytes
+    launches_per_step = 1 + int((lda * eb) % 16 != 0) + int(
+        ((w.K if w.trans_b else w.N) * eb) % 16 != 0)
+
+    def gemm_call(a, b, c):
+        if w.fp8:
+            tl.gemm_fp8(a, b, trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, alpha=w.alpha,
+                        out=c, plan=plan, stream=stream)
+        else:
+            tl.gemm(a, b, trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, out=c, plan=plan,
+                    stream=stream)
 
     def step(i):
         a, b, c = sets[i % rot]
-        tl.gemm(a, b, trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, out=c, plan=plan,
-                stream=stream)
+        gemm_call(a, b, c)
 
     w0 = torch.cuda.Event(enable_timing=True)
     w1 = torch.cuda.Event(enable_timing=True)
@@ -318,8 +340,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
                     uploaded = torch.cuda.Event()
                     uploaded.record(s_in)
                 stream.wait_event(uploaded)
-                tl.gemm(a_d, b_d, trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu, out=c_d,
-                        plan=plan, stream=stream)
+                gemm_call(a_d, b_d, c_d)
                 computed = torch.cuda.Event()
                 computed.record(stream)
                 s_out.wait_event(computed)
@@ -363,7 +384,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
             raise RuntimeError(f"device-side wait gave up in the end-to-end run: {word:#x}")
         e2e = {"value": round(whole_job_tflops(w.flops, e_steps, world, e_ms), 3),
                "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(a_cpu.numel() * 2 + b_cpu.numel() * 2),
+               "h2d_bytes_per_step": int((a_cpu.numel() + b_cpu.numel()) * eb),
                "d2h_bytes_per_step": int(w.M * w.N * 2),
                "steps": e_steps, "ms_per_step": round(e_ms / e_steps, 4),
                "eager_ms_per_step": round(eager_ms / e_graph, 4),
@@ -467,17 +488,19 @@ def main():
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}
     else:
         achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
-        # fp16 and bf16 share the dense tensor rate.  The sustained figure (cuBLAS
-        # looping under the power cap) applies when the timed region ran under the
-        # power cap (sw_power_cap seen in the clock samples); otherwise the burst one.
+        # fp16 and bf16 share the dense tensor rate; 8-bit operands take it times
+        # FP8_OVER_BF16.  The sustained figure (cuBLAS looping under the power cap)
+        # applies when the timed region ran under the power cap (sw_power_cap seen in
+        # the clock samples); otherwise the burst one.
         capped = "sw_power_cap" in ((res.get("clocks") or {}).get("reasons") or [])
-        peak = peaks["bf16_tflops_sustained" if capped else "bf16_tflops"]
+        peak = tensor_peak_scale(w) * peaks["bf16_tflops_sustained" if capped else "bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s"}
     roof["frac"] = round(achieved / peak, 4)
-    roof["peak_source"] = (f"{peaks_src} ({'copy' if hbm else 'sustained, power cap seen' if capped else 'burst'})")
+    roof["peak_source"] = (f"{peaks_src} ({'copy' if hbm else 'sustained, power cap seen' if capped else 'burst'})"
+                           + (" bf16 x 2 for 8-bit operands" if w.fp8 and not hbm else ""))
     if not hbm:
-        roof["frac_of_burst"] = round(achieved / peaks["bf16_tflops"], 4)
+        roof["frac_of_burst"] = round(achieved / (tensor_peak_scale(w) * peaks["bf16_tflops"]), 4)
     roof["traffic"] = load_traffic(w.name)
     roof["kernel_ms"] = round(avg_launch_ms, 6)
     roof["algorithmic"] = {"flops_per_launch": w.flops, "bytes_per_launch": w.bytes_moved}
@@ -495,7 +518,8 @@ def main():
             "roofline": roof, "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["launches_per_step"] * args.steps,
             "clocks": res["clocks"], "plan": res["plan"],
-            "pct_of_nominal_2250": round(100 * value / world / 2250.0, 2)}
+            "pct_of_nominal": round(100 * value / world / (2250.0 * tensor_peak_scale(w)), 2),
+            "nominal_tflops": 2250.0 * tensor_peak_scale(w)}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
