@@ -86,6 +86,11 @@ def _load():
         lib.oracle_gemm_fp8_entries.argtypes = [p, p, i64, i64, i64, i64, i64, ci, ci, ci, ci,
                                                 ci, ctypes.c_double, ci, p, p, i64, p, p, ci]
         lib.oracle_gemm_fp8_entries.restype = ci
+        lib.oracle_attention.argtypes = [p, p, p, p, p, i64, i64, i64, i64, ci, ci, ci]
+        lib.oracle_attention.restype = ci
+        lib.oracle_attention_rows.argtypes = [p, p, p, i64, i64, i64, i64, ci, ci, p, p, p, i64,
+                                              p, ci]
+        lib.oracle_attention_rows.restype = ci
         lib.oracle_decode8_array.argtypes = [p, p, i64, ci]
         lib.oracle_decode8_array.restype = None
         lib.oracle_max_threads.argtypes = []
@@ -251,3 +256,39 @@ def gemm_fp8_entries(A, B, M: int, N: int, K: int, rows, cols, *, a_fmt: int = E
     if rc != 0:
         raise ValueError("oracle_gemm_fp8_entries rejected its arguments")
     return (out, sums) if want_sums else out
+
+
+# ---- attention --------------------------------------------------------------------
+
+def attention(Q, K, V, *, dtype: int = F16, causal: bool = False, threads: int = 0,
+              want_sums: bool = False):
+    """O = softmax(Q K^T / sqrt(D)) V per (batch, head), all four [B, S, H, D]; uint16 bits."""
+    shape = tuple(Q.shape)
+    if len(shape) != 4 or tuple(K.shape) != shape or tuple(V.shape) != shape:
+        raise ValueError("Q, K and V must all be [B, S, H, D]")
+    B, S, H, D = shape
+    q, k, v = (_as_u16(x).reshape(-1) for x in (Q, K, V))
+    o = np.zeros(shape, dtype=np.uint16)
+    sums = np.zeros(shape, dtype=np.float64) if want_sums else None
+    rc = _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                  _ptr(sums) if sums is not None else None, B, S, H, D, dtype,
+                                  int(causal), threads)
+    if rc != 0:
+        raise ValueError("oracle_attention rejected its arguments")
+    return (o, sums) if want_sums else o
+
+
+def attention_rows(Q, K, V, bs, is_, hs, *, dtype: int = F16, causal: bool = False,
+                   threads: int = 0):
+    """Rows O[bs[t], is_[t], hs[t], :] computed one by one (sampled parity); (count, D)."""
+    B, S, H, D = tuple(Q.shape)
+    q, k, v = (_as_u16(x).reshape(-1) for x in (Q, K, V))
+    b_ = np.ascontiguousarray(bs, dtype=np.int64)
+    i_ = np.ascontiguousarray(is_, dtype=np.int64)
+    h_ = np.ascontiguousarray(hs, dtype=np.int64)
+    out = np.zeros((b_.size, D), dtype=np.uint16)
+    rc = _load().oracle_attention_rows(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, dtype, int(causal),
+                                       _ptr(b_), _ptr(i_), _ptr(h_), b_.size, _ptr(out), threads)
+    if rc != 0:
+        raise ValueError("oracle_attention_rows rejected its arguments")
+    return out

@@ -338,6 +338,108 @@ void oracle_decode8_array(const uint8_t* in, double* out, int64_t n, int type) {
   for (int64_t t = 0; t < n; ++t) out[t] = decode8(in[t], type);
 }
 
+/* ---- attention ---------------------------------------------------------------
+ *
+ * The pages' second workload on the same primitives is the FlashAttention forward
+ * pass ("TileLang: a tile language one level below Triton", section "FlashAttention:
+ * online softmax as tile code"): Q, K, V and O are [B, S, H, D] (batch, sequence,
+ * heads, head dim), scores are scaled by 1/sqrt(D), and the causal form lets query
+ * i see keys j <= i.  The oracle writes out the plain definition, not the online
+ * (blockwise, rescaled) form:
+ *
+ *   s_ij = (1/sqrt(D)) * sum_d Q[b,i,h,d] * K[b,j,h,d]        (j < S, and j <= i if causal)
+ *   O[b,i,h,:] = sum_j exp(s_ij - max_j s_ij) V[b,j,h,:] / sum_j exp(s_ij - max_j s_ij)
+ *
+ * in binary64 with libm's exp, rounded once to the 16-bit output format.  The
+ * subtraction of the row maximum changes nothing mathematically (softmax is
+ * shift-invariant); it keeps exp in range.
+ */
+static void attention_row(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                          int64_t S, int64_t H, int64_t D, int dtype, int causal, int64_t b,
+                          int64_t h, int64_t i, double* scores, double* out) {
+  const double scale = 1.0 / sqrt((double)D);
+  const int64_t row = H * D;                      /* elements between sequence positions */
+  const uint16_t* q = Q + (b * S + i) * row + h * D;
+  const int64_t n = causal ? i + 1 : S;
+  double mx = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) {
+    const uint16_t* k = K + (b * S + j) * row + h * D;
+    double acc = 0.0;
+    for (int64_t d = 0; d < D; ++d) acc += decode(q[d], dtype) * decode(k[d], dtype);
+    scores[j] = acc * scale;
+    if (scores[j] > mx) mx = scores[j];
+  }
+  double den = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    scores[j] = exp(scores[j] - mx);
+    den += scores[j];
+  }
+  for (int64_t d = 0; d < D; ++d) out[d] = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    const uint16_t* v = V + (b * S + j) * row + h * D;
+    for (int64_t d = 0; d < D; ++d) out[d] += scores[j] * decode(v[d], dtype);
+  }
+  for (int64_t d = 0; d < D; ++d) out[d] /= den;
+}
+
+static int attention_args_ok(int64_t B, int64_t S, int64_t H, int64_t D, int dtype) {
+  return B >= 0 && S >= 0 && H >= 0 && D > 0 && (dtype == ORACLE_F16 || dtype == ORACLE_BF16);
+}
+
+/* All of O; `sums` (if not NULL) receives the binary64 outputs before rounding. */
+int oracle_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, uint16_t* O,
+                     double* sums, int64_t B, int64_t S, int64_t H, int64_t D, int dtype,
+                     int causal, int nthreads) {
+  if (!attention_args_ok(B, S, H, D, dtype)) return -1;
+  set_threads(nthreads);
+#pragma omp parallel
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double* out = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < B; ++b) {
+      for (int64_t h = 0; h < H; ++h) {
+        for (int64_t i = 0; i < S; ++i) {
+          attention_row(Q, K, V, S, H, D, dtype, causal, b, h, i, scores, out);
+          const int64_t base = ((b * S + i) * H + h) * D;
+          for (int64_t d = 0; d < D; ++d) {
+            if (O) O[base + d] = encode(out[d], dtype);
+            if (sums) sums[base + d] = out[d];
+          }
+        }
+      }
+    }
+    free(scores);
+    free(out);
+  }
+  return 0;
+}
+
+/* Selected rows (b[t], i[t], h[t]) only: out[t*D + d], rounded. */
+int oracle_attention_rows(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t B,
+                          int64_t S, int64_t H, int64_t D, int dtype, int causal,
+                          const int64_t* bs, const int64_t* is, const int64_t* hs, int64_t count,
+                          uint16_t* out, int nthreads) {
+  if (!attention_args_ok(B, S, H, D, dtype)) return -1;
+  for (int64_t t = 0; t < count; ++t) {
+    if (bs[t] < 0 || bs[t] >= B || is[t] < 0 || is[t] >= S || hs[t] < 0 || hs[t] >= H) return -1;
+  }
+  set_threads(nthreads);
+#pragma omp parallel
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double* row = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t t = 0; t < count; ++t) {
+      attention_row(Q, K, V, S, H, D, dtype, causal, bs[t], hs[t], is[t], scores, row);
+      for (int64_t d = 0; d < D; ++d) out[t * D + d] = encode(row[d], dtype);
+    }
+    free(scores);
+    free(row);
+  }
+  return 0;
+}
+
 /* Vector forms of the format conversions, for the pin tests. */
 void oracle_decode_array(const uint16_t* in, double* out, int64_t n, int dtype) {
   for (int64_t t = 0; t < n; ++t) out[t] = decode(in[t], dtype);

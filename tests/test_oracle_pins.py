@@ -410,3 +410,76 @@ def test_fp8_exact_rational_sums_and_entries():
     E = oracle.gemm_fp8_entries(A, B, M, N, K, rows, cols, trans_b=True, alpha=alpha,
                                 out_dtype=oracle.F16)
     assert np.array_equal(E, C[rows, cols])
+
+
+# ---- attention: O = softmax(Q K^T / sqrt(D)) V, [B, S, H, D] -------------------------
+
+def _t16(x, dtype):
+    return torch.as_tensor(np.asarray(x, np.float32)).to(
+        torch.float16 if dtype == oracle.F16 else torch.bfloat16)
+
+
+def _vals(t):
+    return t.to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+def test_attention_equal_scores_give_the_mean_of_v(dtype):
+    """K = 0: every score is 0, softmax is uniform over the visible keys, O = mean of V
+    (over all keys, or over keys 0..i when causal)."""
+    rng = np.random.default_rng(51)
+    B, S, H, D = 2, 9, 3, 16
+    Q = _t16(rng.normal(size=(B, S, H, D)), dtype)
+    K = _t16(np.zeros((B, S, H, D)), dtype)
+    V = _t16(rng.normal(size=(B, S, H, D)), dtype)
+    Vv = _vals(V)
+    O, sums = oracle.attention(Q, K, V, dtype=dtype, want_sums=True)
+    assert np.allclose(sums, np.broadcast_to(Vv.mean(axis=1, keepdims=True), Vv.shape),
+                       rtol=0, atol=1e-12)
+    Oc, sc = oracle.attention(Q, K, V, dtype=dtype, causal=True, want_sums=True)
+    prefix = np.cumsum(Vv, axis=1) / np.arange(1, S + 1)[None, :, None, None]
+    assert np.allclose(sc, prefix, rtol=0, atol=1e-12)
+    assert np.array_equal(Oc[:, 0], V[:, 0].view(torch.int16).numpy().view(np.uint16))
+
+
+def test_attention_one_dominant_key_selects_its_value_row():
+    """Scores differing by more than ~750 leave exp() of the others below 2^-1000: the
+    output is the dominant key's V row, exactly after rounding."""
+    B, S, H, D = 1, 6, 2, 64
+    Q = np.zeros((B, S, H, D)); Q[..., 0] = 64.0
+    K = np.zeros((B, S, H, D)); K[0, 4, :, 0] = 100.0     # s = 64*100/8 = 800 for key 4
+    V = np.arange(B * S * H * D, dtype=np.float64).reshape(B, S, H, D) % 37 - 18
+    Qt, Kt, Vt = (_t16(x, oracle.F16) for x in (Q, K, V))
+    O = oracle.attention(Qt, Kt, Vt, dtype=oracle.F16)
+    want = np.broadcast_to(V[:, 4:5], V.shape)
+    assert np.array_equal(oracle.decode(O, oracle.F16), want)
+
+
+def test_attention_against_numpy_softmax_and_key_permutation():
+    rng = np.random.default_rng(53)
+    B, S, H, D = 2, 13, 2, 32
+    Q, K, V = (_t16(rng.normal(size=(B, S, H, D)), oracle.BF16) for _ in range(3))
+    Qv, Kv, Vv = _vals(Q), _vals(K), _vals(V)
+    for causal in (False, True):
+        _, sums = oracle.attention(Q, K, V, dtype=oracle.BF16, causal=causal, want_sums=True)
+        s = np.einsum("bihd,bjhd->bhij", Qv, Kv) / np.sqrt(D)
+        if causal:
+            s = np.where(np.tril(np.ones((S, S), bool)), s, -np.inf)
+        p = np.exp(s - s.max(axis=-1, keepdims=True))
+        p /= p.sum(axis=-1, keepdims=True)
+        want = np.einsum("bhij,bjhd->bihd", p, Vv)
+        assert np.allclose(sums, want, rtol=1e-12, atol=1e-13)
+    perm = rng.permutation(S)
+    O1 = oracle.attention(Q, K, V, dtype=oracle.BF16)
+    O2 = oracle.attention(Q, K[:, perm], V[:, perm], dtype=oracle.BF16)
+    assert np.array_equal(O1, O2)
+
+
+def test_attention_rows_match_full_output():
+    rng = np.random.default_rng(55)
+    B, S, H, D = 2, 11, 3, 16
+    Q, K, V = (_t16(rng.normal(size=(B, S, H, D)), oracle.F16) for _ in range(3))
+    O = oracle.attention(Q, K, V, dtype=oracle.F16, causal=True)
+    bs, is_, hs = rng.integers(0, B, 20), rng.integers(0, S, 20), rng.integers(0, H, 20)
+    R = oracle.attention_rows(Q, K, V, bs, is_, hs, dtype=oracle.F16, causal=True)
+    assert np.array_equal(R, O[bs, is_, hs])
