@@ -272,6 +272,28 @@ tl_status tl_device_status(int reset, uint32_t* detail);
 void tl_set_wait_timeout_ns(uint64_t ns);
 
 /*
+ * Attention forward pass: O = softmax(Q K^T / sqrt(D)) V for every batch and head,
+ * optionally causal (query i attends to keys j <= i).  This is the pages' second
+ * workload on the same tile primitives ("TileLang: a tile language one level below
+ * Triton", section "FlashAttention: online softmax as tile code"), with their layout
+ * and scale: Q, K, V and O are [B, S, H, D] row-major (batch, sequence, heads, head
+ * dim), scores scaled by 1/sqrt(D).
+ *
+ *   Q, K, V, O  device pointers to dtype elements (TL_F16 or TL_BF16), 16-byte
+ *               aligned (TL_ERR_ALIGNMENT otherwise); O must not overlap Q, K or V.
+ *   D           64 or 128 (TL_ERR_UNSUPPORTED otherwise).
+ *   causal      0 or 1.
+ * B, S or H == 0: returns TL_OK, launches nothing.  Scores and the softmax statistics
+ * are fp32; the probabilities enter the PV product rounded to dtype (as in the
+ * pages' kernel, which casts them to fp16); O accumulates in fp32 and is rounded once.
+ * Asynchronous on `stream`; errors are returned before anything is enqueued, a
+ * device-side timeout is read with tl_device_status().
+ */
+tl_status tl_attention_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                           int64_t S, int64_t H, int64_t D, tl_dtype dtype, int causal,
+                           tl_stream_t stream);
+
+/*
  * Test hook for the failure-detection path; not for production use.  mode 1: every
  * GEMM kernel launched afterwards has its MMA thread wait first on a barrier that
  * nothing arrives on, as if its operands never came.  The wait runs out after the

@@ -93,6 +93,8 @@ def _load() -> ctypes.CDLL:
     lib.tl_device_status.restype = ci
     lib.tl_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.tl_set_wait_timeout_ns.restype = None
+    lib.tl_attention_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, ci, ci, p]
+    lib.tl_attention_fwd.restype = ci
     lib.tl_debug_set_stall.argtypes = [ci]
     lib.tl_debug_set_stall.restype = None
     lib.tl_version.argtypes = []
@@ -178,6 +180,12 @@ def tl_device_status(reset: bool = False) -> tuple[int, int]:
 
 def tl_set_wait_timeout_ns(ns: int) -> None:
     _lib.tl_set_wait_timeout_ns(int(ns))
+
+
+def tl_attention_fwd(Q: int, K: int, V: int, O: int, B: int, S: int, H: int, D: int,
+                     dtype: int, causal: int, stream: int) -> int:
+    """Raw attention call on [B, S, H, D] device buffers; returns tl_status."""
+    return _lib.tl_attention_fwd(Q, K, V, O, B, S, H, D, dtype, causal, stream)
 
 
 def tl_debug_set_stall(mode: int) -> None:
@@ -305,4 +313,30 @@ def gemm_fp8(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool =
                      TL_EPI_RELU if relu else TL_EPI_NONE, plan, s.cuda_stream)
     if st != TL_OK:
         raise TLError(st, "tl_gemm_fp8")
+    return out
+
+
+def attention(q, k, v, *, causal: bool = False, out=None, stream=None):
+    """O = softmax(q k^T / sqrt(D)) v per batch and head; q, k, v (and out) are
+    contiguous [B, S, H, D] fp16/bf16 CUDA tensors of one dtype, D = 64 or 128."""
+    torch = _torch()
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k and v must be CUDA tensors")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must all be [B, S, H, D]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k and v must be contiguous")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must have the same dtype")
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    B, S, H, D = q.shape
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    st = tl_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, H, D,
+                          dt, int(causal), s.cuda_stream)
+    if st != TL_OK:
+        raise TLError(st, "tl_attention_fwd")
     return out

@@ -23,6 +23,7 @@
 #include <random>
 #include <unordered_map>
 
+#include "attn_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "tl_gemm.h"
 
@@ -498,10 +499,11 @@ tl_status launch_plan(DeviceState* st, const tl_plan& pl, int eb, const CUtensor
 // shared by all threads under a mutex.
 struct MapKey {
   uint64_t base;
-  uint64_t dims[3];
-  uint64_t stride0, stride1;
-  uint32_t box[3];
+  uint64_t dims[4];
+  uint64_t strides[3];
+  uint32_t box[4];
   uint32_t dtype_rank;
+  uint32_t pad;
   bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
@@ -532,9 +534,8 @@ bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* 
   for (uint32_t i = 0; i < rank; ++i) {
     key.dims[i] = dims[i];
     key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides[i];
   }
-  key.stride0 = strides[0];
-  key.stride1 = rank > 2 ? strides[1] : 0;
   key.dtype_rank = static_cast<uint32_t>(dtype) * 8u + rank;
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
@@ -548,7 +549,7 @@ bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* 
   }
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt = map_type(dtype);
   if (enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -870,6 +871,108 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   return s;
 }
 
+// ---- attention ---------------------------------------------------------------------
+// Q, K, V, O are [B, S, H, D] row-major; the kernel reads 128-row tiles of one
+// (batch, head) through a 4-D map {D, H, S, B} (box {64, 1, 128, 1}: a 64-element
+// chunk of 128 sequence positions), which zero-fills rows past S.
+bool encode_bshd(CUtensorMap* map, tl_dtype dtype, const void* base, int64_t B, int64_t S,
+                 int64_t H, int64_t D) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(H * D * 2),
+                                 static_cast<cuuint64_t>(S * H * D * 2)};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(tl::kAttnBN), 1};
+  return encode_cached(map, dtype, 4, base, dims, strides, box);
+}
+
+template <int D>
+tl_status launch_attention(DeviceState* st, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const tl::AttnParams& prm, int64_t q_tiles,
+                           cudaStream_t stream) {
+  // at least 120 KB, so that two CTAs never share an SM: each allocates all 512 Tensor
+  // Memory columns, and a second allocation would wait for the first CTA to finish
+  constexpr uint32_t kSmem = tl::attn_smem_bytes<D>() > 122880u ? tl::attn_smem_bytes<D>() : 122880u;
+  constexpr uint32_t bit = 1u << (D == 64 ? 28 : 29);
+  auto kern = tl::tl_attention_kernel<D>;
+  if (static_cast<int64_t>(kSmem) > st->smem_optin) return TL_ERR_UNSUPPORTED;
+  if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
+    std::lock_guard<std::mutex> lock(st->mu);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmem)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TL_ERR_LAUNCH;
+    }
+    st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(q_tiles), static_cast<unsigned>(prm.H),
+                     static_cast<unsigned>(prm.B));
+  cfg.blockDim = dim3(tl::kAttnThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, prm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TL_ERR_LAUNCH;
+  }
+  return TL_OK;
+}
+
+tl_status run_attention(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                        int64_t S, int64_t H, int64_t D, tl_dtype dtype, int causal,
+                        cudaStream_t stream) {
+  if (B < 0 || S < 0 || H < 0 || D <= 0) return TL_ERR_INVALID_ARG;
+  if (dtype != TL_F16 && dtype != TL_BF16) return TL_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return TL_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return TL_ERR_UNSUPPORTED;
+  if (B == 0 || S == 0 || H == 0) return TL_OK;
+  if (S > (int64_t{1} << 31) - 256 || H > 65535 || B > 65535) return TL_ERR_UNSUPPORTED;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return TL_ERR_NULL_PTR;
+  if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+       reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O)) & 15u) {
+    return TL_ERR_ALIGNMENT;
+  }
+  const int64_t elems = B * S * H * D;
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(O), o1 = o0 + static_cast<uintptr_t>(elems * 2);
+  for (const void* x : {Q, K, V}) {
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(x);
+    if (overlaps(o0, o1, x0, x0 + static_cast<uintptr_t>(elems * 2))) return TL_ERR_ALIAS;
+  }
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (st == nullptr) return TL_ERR_DEVICE;
+  if (!st->sm103) return TL_ERR_UNSUPPORTED;
+  tl_status s;
+  for (const void* x : {Q, K, V, static_cast<const void*>(O)}) {
+    if ((s = check_device_pointer(x, dev)) != TL_OK) return s;
+  }
+  CUtensorMap tq, tk, tv;
+  if (!encode_bshd(&tq, dtype, Q, B, S, H, D) || !encode_bshd(&tk, dtype, K, B, S, H, D) ||
+      !encode_bshd(&tv, dtype, V, B, S, H, D)) {
+    return TL_ERR_LAUNCH;
+  }
+  tl::AttnParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.B = static_cast<int32_t>(B);
+  prm.S = static_cast<int32_t>(S);
+  prm.H = static_cast<int32_t>(H);
+  prm.causal = causal;
+  prm.bf16 = dtype == TL_BF16 ? 1 : 0;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  prm.O = O;
+  prm.idesc_s = tl::mma_idesc_f16(prm.bf16, 0u, 0u, 128u, 128u);
+  prm.idesc_o = tl::mma_idesc_f16(prm.bf16, 0u, 1u, 128u, static_cast<uint32_t>(D));
+  prm.status = st->status;
+  prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  const int64_t q_tiles = ceil_div(S, tl::kAttnBM);
+  return D == 64 ? launch_attention<64>(st, tq, tk, tv, prm, q_tiles, stream)
+                 : launch_attention<128>(st, tq, tk, tv, prm, q_tiles, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -974,6 +1077,13 @@ tl_status tl_device_status(int reset, uint32_t* detail) {
 void tl_set_wait_timeout_ns(uint64_t ns) {
   ns = std::max<uint64_t>(100000ull, std::min<uint64_t>(ns, 60000000000ull));
   g_timeout_ns.store(ns, std::memory_order_relaxed);
+}
+
+tl_status tl_attention_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                           int64_t S, int64_t H, int64_t D, tl_dtype dtype, int causal,
+                           tl_stream_t stream) {
+  return run_attention(Q, K, V, O, B, S, H, D, dtype, causal,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 void tl_debug_set_stall(int mode) { g_stall.store(mode == 1 ? 1 : 0, std::memory_order_relaxed); }
