@@ -94,8 +94,8 @@ def whole_job_tflops(flops_per_step: int, steps: int, world: int, max_ms: float)
 FP8_OVER_BF16 = 2.0
 
 
-def tensor_peak_scale(w: workloads.Workload) -> float:
-    return FP8_OVER_BF16 if w.fp8 else 1.0
+def tensor_peak_scale(w) -> float:
+    return FP8_OVER_BF16 if getattr(w, "fp8", False) else 1.0
 
 
 def is_hbm_bound(w: workloads.Workload, peaks: dict) -> bool:
@@ -195,8 +195,172 @@ def oracle_rate(w: workloads.Workload, a_cpu, b_cpu, budget_s: float, threads: i
 
 # ------------------------------------------------------------------ GPU arm ----
 
+def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl):
+    """Warm-up, then exactly args.steps calls of step(i) replayed as CUDA graphs, timed
+    with events on `stream` between barriers; returns (max-over-ranks ms, clocks)."""
+    import torch
+
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            if i == args.warmup - 2:
+                w0.record(stream)
+            step(i)
+        w1.record(stream)
+    torch.cuda.synchronize()
+    status, word = tl.tl_device_status(reset=True)
+    if status != tl.TL_OK:
+        raise RuntimeError(f"device-side wait gave up during warm-up: {word:#x}")
+    if args.steps <= 0:
+        # default: enough steps for a timed region of ~1.5 s, so that the clock samples
+        # taken every 50 ms fall inside it
+        step_ms = max(w0.elapsed_time(w1) / 2.0, 1e-3)
+        args.steps = int(min(200000, max(50, math.ceil(1500.0 / step_ms))))
+        args.steps = int(max_over_ranks(float(args.steps), dist, dev))
+
+    # The timed steps run as CUDA-graph replays of consecutive library calls (one call
+    # per step, inputs rotating as in eager mode), so host-side launch cost does not
+    # hide the device time of small problems.  Exactly args.steps calls are timed.
+    G = rot * max(1, math.ceil(64 / rot))
+    n_full, rem = divmod(args.steps, G)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+
+    g_full = capture(G) if n_full else None
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):
+        for g in (g_full, g_rem):              # one untimed replay of each graph
+            if g is not None:
+                g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(n_full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    status, word = tl.tl_device_status(reset=True)
+    if status != tl.TL_OK:
+        raise RuntimeError(f"device-side wait gave up in the timed region: {word:#x}")
+    return max_over_ranks(total_ms, dist, dev), clk
+
+
+def e2e_pipeline(args, inputs_cpu, out_shape, out_dtype, compute, flops: int, world: int,
+                 stream, dist, dev, tl) -> dict:
+    """The same metric end to end through the public call from pinned host buffers.
+
+    Every step uploads its inputs, runs compute(device inputs, device output) and
+    downloads the output, all inside the timed region.  As a serving loop would, the
+    steps are pipelined: copies in, the computation and the copy out run on three
+    streams over two device buffer sets, so step i's computation overlaps step i+1's
+    upload and step i-1's download; a set is reused only after its download finished.
+    Like the device-resident number, the timed steps replay CUDA graphs of that
+    pipeline (host launch cost excluded); the same steps enqueued eagerly from Python
+    are timed too and reported as eager_ms_per_step.  (Uploads split over two streams
+    were measured no faster: ~210 GB/s either way.)"""
+    import torch
+
+    hosts = [x.pin_memory() for x in inputs_cpu]
+    e_sets = []
+    for _ in range(2):
+        ins = [torch.empty_like(x, device=dev) for x in inputs_cpu]
+        out_d = torch.empty(out_shape, dtype=out_dtype, device=dev)
+        out_h = torch.empty(out_shape, dtype=out_dtype).pin_memory()
+        e_sets.append((ins, out_d, out_h))
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    e_graph = 50                              # pipelined steps per graph
+    e_steps = e_graph * max(1, min(args.steps, 200) // e_graph)
+
+    def run(n):
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        freed = [None, None]           # download of the set's previous step done
+        for i in range(n):
+            k = i % 2
+            ins, out_d, out_h = e_sets[k]
+            if freed[k] is not None:
+                s_in.wait_event(freed[k])
+            with torch.cuda.stream(s_in):
+                for d, h in zip(ins, hosts):
+                    d.copy_(h, non_blocking=True)
+                uploaded = torch.cuda.Event()
+                uploaded.record(s_in)
+            stream.wait_event(uploaded)
+            compute(ins, out_d)
+            computed = torch.cuda.Event()
+            computed.record(stream)
+            s_out.wait_event(computed)
+            with torch.cuda.stream(s_out):
+                out_h.copy_(out_d, non_blocking=True)
+                freed[k] = torch.cuda.Event()
+                freed[k].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    def timed(fn):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):        # graph replays go to the current stream
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    run(4)                                     # warm-up, eager
+    torch.cuda.synchronize()
+    eager_ms = timed(lambda: run(e_graph))
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        run(e_graph)
+    with torch.cuda.stream(stream):
+        g_e2e.replay()                         # one untimed replay
+    torch.cuda.synchronize()
+
+    def replays():
+        for _ in range(e_steps // e_graph):
+            g_e2e.replay()
+
+    e_ms = max_over_ranks(timed(replays), dist, dev)
+    status, word = tl.tl_device_status(reset=True)
+    if status != tl.TL_OK:
+        raise RuntimeError(f"device-side wait gave up in the end-to-end run: {word:#x}")
+    return {"value": round(whole_job_tflops(flops, e_steps, world, e_ms), 3),
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(sum(x.numel() * x.element_size() for x in inputs_cpu)),
+            "d2h_bytes_per_step": int(math.prod(out_shape) *
+                                      torch.empty((), dtype=out_dtype).element_size()),
+            "steps": e_steps, "ms_per_step": round(e_ms / e_steps, 4),
+            "eager_ms_per_step": round(eager_ms / e_graph, 4),
+            "pipelined": "upload, compute and download on three streams, two buffer sets; "
+                         "graphs of 50 steps"}
+
+
 def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
-    import numpy as np  # noqa: F401
     import torch
 
     import tiled_gemm_gb300 as tl
@@ -234,169 +398,72 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
         a, b, c = sets[i % rot]
         gemm_call(a, b, c)
 
-    w0 = torch.cuda.Event(enable_timing=True)
-    w1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            if i == args.warmup - 2:
-                w0.record(stream)
-            step(i)
-        w1.record(stream)
-    torch.cuda.synchronize()
-    status, word = tl.tl_device_status(reset=True)
-    if status != tl.TL_OK:
-        raise RuntimeError(f"device-side wait gave up during warm-up: {word:#x}")
-    if args.steps <= 0:
-        # default: enough steps for a timed region of ~1.5 s, so that the clock samples
-        # taken every 50 ms fall inside it
-        step_ms = max(w0.elapsed_time(w1) / 2.0, 1e-3)
-        args.steps = int(min(200000, max(50, math.ceil(1500.0 / step_ms))))
-        args.steps = int(max_over_ranks(float(args.steps), dist, dev))
-
-    # The timed steps run as CUDA-graph replays of consecutive tl_gemm calls (one call
-    # per step, inputs rotating as in eager mode), so host-side launch cost does not
-    # hide the device time of small problems.  Exactly args.steps calls are timed.
-    G = rot * max(1, math.ceil(64 / rot))
-    n_full, rem = divmod(args.steps, G)
-
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                step(i)
-        return g
-
-    g_full = capture(G) if n_full else None
-    g_rem = capture(rem) if rem else None
-    for g in (g_full, g_rem):              # one untimed replay of each graph
-        if g is not None:
-            g.replay()
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for _ in range(n_full):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        t_end.record(stream)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    per_launch_ms = [total_ms / args.steps]
-    status, word = tl.tl_device_status(reset=True)
-    if status != tl.TL_OK:
-        raise RuntimeError(f"device-side wait gave up in the timed region: {word:#x}")
-
-    max_ms = max_over_ranks(total_ms, dist, dev)
-
-    # ---- end to end through the public API with host buffers --------------------
-    # Every step copies its A and B from pinned host memory, runs tl_gemm and reads C
-    # back into pinned host memory, all inside the timed region.  As a serving loop
-    # would, the steps are pipelined: copies in, the GEMM and the copy out run on three
-    # streams over two device buffer sets, so step i's GEMM overlaps step i+1's upload
-    # and step i-1's download; a set is reused only after its download has finished.
-    # (Uploads split over two streams were measured no faster: ~210 GB/s either way.)
-    # Like the device-resident number, the timed steps replay CUDA graphs of that
-    # pipeline (host launch cost excluded); the same steps enqueued eagerly from Python
-    # are timed too and reported as eager_ms_per_step.
+    max_ms, clk = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
     e2e = None
     if not args.no_e2e:
-        a_h = a_cpu.pin_memory()
-        b_h = b_cpu.pin_memory()
-        e_sets = []
-        for k in range(2):
-            a_d = torch.empty_like(a_cpu, device=dev)
-            b_d = torch.empty_like(b_cpu, device=dev)
-            c_d = torch.empty((w.M, w.N), dtype=w.torch_dtype, device=dev)
-            c_h = torch.empty((w.M, w.N), dtype=w.torch_dtype).pin_memory()
-            e_sets.append((a_d, b_d, c_d, c_h))
-        s_in = torch.cuda.Stream(device=dev)
-        s_out = torch.cuda.Stream(device=dev)
-        e_graph = 50                              # pipelined steps per graph
-        e_steps = e_graph * max(1, min(args.steps, 200) // e_graph)
-
-        def e2e_run(n):
-            s_in.wait_stream(stream)
-            s_out.wait_stream(stream)
-            freed = [None, None]           # download of the set's previous step done
-            for i in range(n):
-                k = i % 2
-                a_d, b_d, c_d, c_h = e_sets[k]
-                if freed[k] is not None:
-                    s_in.wait_event(freed[k])
-                with torch.cuda.stream(s_in):
-                    a_d.copy_(a_h, non_blocking=True)
-                    b_d.copy_(b_h, non_blocking=True)
-                    uploaded = torch.cuda.Event()
-                    uploaded.record(s_in)
-                stream.wait_event(uploaded)
-                gemm_call(a_d, b_d, c_d)
-                computed = torch.cuda.Event()
-                computed.record(stream)
-                s_out.wait_event(computed)
-                with torch.cuda.stream(s_out):
-                    c_h.copy_(c_d, non_blocking=True)
-                    freed[k] = torch.cuda.Event()
-                    freed[k].record(s_out)
-            stream.wait_stream(s_in)
-            stream.wait_stream(s_out)
-
-        def timed(fn):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            if dist is not None:
-                dist.barrier()
-            torch.cuda.synchronize()
-            with torch.cuda.stream(stream):        # graph replays go to the current stream
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-            torch.cuda.synchronize()
-            return e0.elapsed_time(e1)
-
-        e2e_run(4)                                 # warm-up, eager
-        torch.cuda.synchronize()
-        eager_ms = timed(lambda: e2e_run(e_graph))
-        g_e2e = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_e2e, stream=stream):
-            e2e_run(e_graph)
-        with torch.cuda.stream(stream):
-            g_e2e.replay()                         # one untimed replay
-        torch.cuda.synchronize()
-
-        def replays():
-            for _ in range(e_steps // e_graph):
-                g_e2e.replay()
-
-        e_ms = max_over_ranks(timed(replays), dist, dev)
-        status, word = tl.tl_device_status(reset=True)
-        if status != tl.TL_OK:
-            raise RuntimeError(f"device-side wait gave up in the end-to-end run: {word:#x}")
-        e2e = {"value": round(whole_job_tflops(w.flops, e_steps, world, e_ms), 3),
-               "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int((a_cpu.numel() + b_cpu.numel()) * eb),
-               "d2h_bytes_per_step": int(w.M * w.N * 2),
-               "steps": e_steps, "ms_per_step": round(e_ms / e_steps, 4),
-               "eager_ms_per_step": round(eager_ms / e_graph, 4),
-               "pipelined": "upload, tl_gemm and download on three streams, two buffer "
-                            "sets; graphs of 50 steps"}
-
-    return {"total_ms": max_ms, "per_launch_ms": per_launch_ms, "clocks": clk, "e2e": e2e,
+        e2e = e2e_pipeline(args, [a_cpu, b_cpu], (w.M, w.N), w.torch_dtype,
+                           lambda ins, out: gemm_call(ins[0], ins[1], out), w.flops, world,
+                           stream, dist, dev, tl)
+    return {"total_ms": max_ms, "clocks": clk, "e2e": e2e,
             "rotation_sets": rot, "launches_per_step": launches_per_step,
             "plan": tl.tl_gemm_plan(w.M, w.N, w.K, w.dtype, int(w.trans_a), int(w.trans_b),
                                     torch.cuda.get_device_properties(dev).multi_processor_count)
             .as_dict() if plan is None else
             tl.tl_plan_complete(w.M, w.N, w.K, *w.plan, dtype=w.dtype).as_dict()}
+
+
+def run_attn(args, w: workloads.AttnWorkload, rank: int, world: int, dist) -> dict:
+    import torch
+
+    import tiled_gemm_gb300 as tl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q_cpu, k_cpu, v_cpu = workloads.make_attn_inputs(w)
+    rot = 1 if w.bytes_moved >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / w.bytes_moved))
+    q0, k0, v0 = (x.to(dev) for x in (q_cpu, k_cpu, v_cpu))
+    sets = [(q0, k0, v0, torch.empty_like(q0)) if i == 0 else
+            (q0.clone(), k0.clone(), v0.clone(), torch.empty_like(q0)) for i in range(rot)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        q, k, v, o = sets[i % rot]
+        tl.attention(q, k, v, causal=w.causal, out=o, stream=stream)
+
+    max_ms, clk = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_pipeline(args, [q_cpu, k_cpu, v_cpu], tuple(q_cpu.shape), w.torch_dtype,
+                           lambda ins, out: tl.attention(ins[0], ins[1], ins[2], causal=w.causal,
+                                                         out=out, stream=stream),
+                           w.flops, world, stream, dist, dev, tl)
+    return {"total_ms": max_ms, "clocks": clk, "e2e": e2e, "rotation_sets": rot,
+            "launches_per_step": 1, "plan": {"q_tile": 128, "kv_tile": 128, "kv_stages": 2,
+                                             "grid": [math.ceil(w.S / 128), w.H, w.B]}}
+
+
+def oracle_rate_attn(w: workloads.AttnWorkload, q, k, v, budget_s: float, threads: int):
+    """Oracle TFLOP/s on output rows spread over the sequence, repeated for ~budget_s."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(0)
+    n, done_flops, elapsed, reps = 16, 0, 0.0, 0
+    code = oracle.F16 if w.dtype == workloads.F16 else oracle.BF16
+    while elapsed < budget_s:
+        bs = rng.integers(0, w.B, n)
+        is_ = rng.integers(0, w.S, n)
+        hs = rng.integers(0, w.H, n)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, bs, is_, hs, dtype=code, causal=w.causal, threads=threads)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        keys = (is_ + 1) if w.causal else np.full(n, w.S)
+        done_flops += int(4 * w.D * keys.sum())
+        reps += 1
+        if dt < budget_s / 20:
+            n *= 2
+    return done_flops / elapsed / 1e12, elapsed, done_flops, n, reps
 
 
 def main():
@@ -405,7 +472,8 @@ def main():
     ap.add_argument("--steps", type=int, default=0,
                     help="timed steps; 0 (default) sizes the timed region to ~1.5 s")
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=workloads.HEADLINE,
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.ATTN_WORKLOADS))
     ap.add_argument("--impl", default="tl", choices=["tl", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -414,17 +482,34 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    w = workloads.WORKLOADS[args.workload]
+    attn = args.workload in workloads.ATTN_WORKLOADS
+    w = workloads.ATTN_WORKLOADS[args.workload] if attn else workloads.WORKLOADS[args.workload]
+    metric = ("attention forward TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU" if attn
+              else "GEMM+ReLU TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     peaks, peaks_src = load_peaks()
     threads = os.cpu_count() or 1
 
-    config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype_name,
-              "trans_a": w.trans_a, "trans_b": w.trans_b,
-              "epilogue": "relu" if w.relu else "none", "inputs": w.description,
-              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if attn:
+        config = {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D,
+                  "dtype": w.dtype_name, "causal": w.causal, "inputs": w.description,
+                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    else:
+        config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype_name,
+                  "trans_a": w.trans_a, "trans_b": w.trans_b,
+                  "epilogue": "relu" if w.relu else "none", "inputs": w.description,
+                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    def cpu_rate(budget):
+        if attn:
+            q, k, v = workloads.make_attn_inputs(w)
+            r, el, fl, n, reps = oracle_rate_attn(w, q, k, v, budget, threads)
+            return r, el, fl, f"{reps} oracle runs of up to {n} output rows of {w.B * w.S * w.H}"
+        a_cpu, b_cpu = workloads.make_inputs(w)
+        r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, budget, threads)
+        return r, el, fl, f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows)"
 
     if args.impl == "reference":
         # The oracle on the host cores, rank 0 only: each step a bounded row slice.
@@ -432,17 +517,16 @@ def main():
             return
         if args.steps <= 0:
             args.steps = 10
-        a_cpu, b_cpu = workloads.make_inputs(w)
         budget = max(0.5, 150.0 / (args.steps + args.warmup))
         for _ in range(args.warmup):
-            oracle_rate(w, a_cpu, b_cpu, min(budget, 1.0), threads)
+            cpu_rate(min(budget, 1.0))
         rates, times = [], []
         for _ in range(args.steps):
-            r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, budget, threads)
+            r, el, fl, what = cpu_rate(budget)
             rates.append(r)
             times.append(el)
         value = statistics.mean(rates)
-        line = {"metric": "GEMM+ReLU TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU",
+        line = {"metric": metric,
                 "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(1e3 * statistics.mean(times), 3),
@@ -450,8 +534,8 @@ def main():
                 "dtype": "f64", "data": "synthetic", "impl": "reference", "config": config,
                 "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                                  "kind": "oracle",
-                                 "sample": f"row slices of up to {rows} of {w.M} rows per step, "
-                                           f"~{budget:.1f} s of CPU work per step"},
+                                 "sample": f"{what} per step, ~{budget:.1f} s of CPU work "
+                                           "per step"},
                 "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -471,17 +555,15 @@ def main():
     # GPU's clocks (rank 0, N = 1 only).
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        a_cpu, b_cpu = workloads.make_inputs(w)
-        r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, args.cpu_budget_s, threads)
+        r, el, fl, what = cpu_rate(args.cpu_budget_s)
         cpu = {"value": round(r, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows), "
-                         f"{fl / 1e9:.2f} GFLOP in {el:.1f} s"}
+               "sample": f"{what}, {fl / 1e9:.2f} GFLOP in {el:.1f} s"}
 
-    res = run_tl(args, w, rank, world, dist)
+    res = (run_attn if attn else run_tl)(args, w, rank, world, dist)
     total_ms = res["total_ms"]
     value = whole_job_tflops(w.flops, args.steps, world, total_ms)
     avg_launch_ms = total_ms / args.steps        # back-to-back launches in the graph
-    hbm = is_hbm_bound(w, peaks)
+    hbm = False if attn else is_hbm_bound(w, peaks)
     if hbm:
         achieved = w.bytes_moved / (avg_launch_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -498,7 +580,8 @@ def main():
                 "unit": "TFLOP/s"}
     roof["frac"] = round(achieved / peak, 4)
     roof["peak_source"] = (f"{peaks_src} ({'copy' if hbm else 'sustained, power cap seen' if capped else 'burst'})"
-                           + (" bf16 x 2 for 8-bit operands" if w.fp8 and not hbm else ""))
+                           + (" bf16 x 2 for 8-bit operands" if tensor_peak_scale(w) > 1 and not hbm
+                              else ""))
     if not hbm:
         roof["frac_of_burst"] = round(achieved / (tensor_peak_scale(w) * peaks["bf16_tflops"]), 4)
     roof["traffic"] = load_traffic(w.name)
@@ -506,7 +589,7 @@ def main():
     roof["algorithmic"] = {"flops_per_launch": w.flops, "bytes_per_launch": w.bytes_moved}
     if rank != 0:
         return
-    line = {"metric": "GEMM+ReLU TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU",
+    line = {"metric": metric,
             "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -75,6 +75,20 @@ __host__ __device__ constexpr uint32_t attn_smem_bytes() {
   return 1024u + attn_tile_bytes<D>() * 5u + 128u * 128u * 2u + attn_barrier_bytes();
 }
 
+// 2^x by the special-function unit's approximation (relative error ~2^-22, enough
+// for probabilities that are rounded to 16 bits); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The running maximum is only moved (and O rescaled) when a row's new maximum exceeds
+// it by more than this many doublings: probabilities computed against a stale
+// maximum then stay below 2^8, exact enough in fp32 and well inside the 16-bit range
+// of P, and the final division by the row sum cancels the common factor.
+constexpr float kRescaleThreshold = 8.0f;
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi, int bf16) {
   if (bf16) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -274,27 +288,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // scale into the log2 domain and mask keys past the end (and, causal, past qi)
       const int kv0 = i * kAttnBN;
       const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
-      float mx = m;
+      float mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 128; ++j) {
-        const float x = j < lim ? __uint_as_float(sv[j]) * p.scale_log2 : -INFINITY;
+        const float x = j < lim ? __uint_as_float(sv[j]) : -INFINITY;
         sv[j] = __float_as_uint(x);
         mx = fmaxf(mx, x);
       }
-      // a row that sees no key yet (mx = -inf) keeps m = -inf and writes P = 0
-      const float corr = (mx == -INFINITY) ? 1.0f : exp2f(m - mx);
+      mx *= p.scale_log2;
+      // keep the stale maximum unless the row's maximum grew by more than the threshold
+      // (a row that has seen no key yet, m = -inf, takes the new one)
+      const float m_use = (mx > m + kRescaleThreshold) ? mx : m;
+      const float corr = (m_use == m) ? 1.0f : fast_exp2(m - m_use);
       float rs = 0.0f;
       uint32_t pk[64];
+      if (m_use == -INFINITY) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
-        const float p0 = (mx == -INFINITY) ? 0.0f : exp2f(x0 - mx);
-        const float p1 = (mx == -INFINITY) ? 0.0f : exp2f(x1 - mx);
-        rs += p0 + p1;
-        pk[j] = pack_half2(p0, p1, p.bf16);
+        for (int j = 0; j < 64; ++j) pk[j] = 0u;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * j]), p.scale_log2, -m_use));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * j + 1]), p.scale_log2, -m_use));
+          rs += p0 + p1;
+          pk[j] = pack_half2(p0, p1, p.bf16);
+        }
       }
       l = l * corr + rs;
-      m = mx;
+      m = m_use;
       if (i > 0) {
         // PV_{i-1} has landed in O and released the P buffer
         if (!(ok = wait_warp(pv_done, static_cast<uint32_t>(i - 1) & 1u, kSiteAttnPvDone))) break;

@@ -171,5 +171,57 @@ for _n, _seed in ((4096, 8), (8192, 9)):
                   description=f"FP8 GEMM {_n}^3, E4M3 operands from N(0,1), B column-major, "
                               "alpha 1/64, bf16 output"))
 
+# ---- attention forward: O = softmax(Q K^T / sqrt(D)) V over [B, S, H, D] ------------
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    B: int
+    S: int
+    H: int
+    D: int
+    dtype: int
+    causal: bool
+    seed: int = 0
+    description: str = ""
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPE[self.dtype]
+
+    @property
+    def dtype_name(self) -> str:
+        return _NAME[self.dtype]
+
+    @property
+    def flops(self) -> int:
+        """Two products of 2*S*S*D per (batch, head); half of that when causal."""
+        full = 4 * self.B * self.H * self.S * self.S * self.D
+        return full // 2 if self.causal else full
+
+    @property
+    def bytes_moved(self) -> int:
+        return 4 * 2 * self.B * self.S * self.H * self.D          # Q, K, V read, O written
+
+
+def make_attn_inputs(w: AttnWorkload, seed: int | None = None):
+    """CPU tensors (Q, K, V), each [B, S, H, D] drawn N(0,1) in fp32 in that order."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    shape = (w.B, w.S, w.H, w.D)
+    return tuple(torch.randn(shape, generator=g, dtype=torch.float32).to(w.torch_dtype)
+                 for _ in range(3))
+
+
+ATTN_WORKLOADS: dict[str, AttnWorkload] = {}
+for _w in (AttnWorkload("attn_fwd_b1_h8_s1024_d64_causal_f16", 1, 1024, 8, 64, F16, True, 20,
+                        "the pages' FlashAttention example size: batch 1, 8 heads, seq 1024, "
+                        "dim 64, causal, fp16, N(0,1)"),
+           AttnWorkload("attn_fwd_b4_h32_s4096_d128_bf16", 4, 4096, 32, 128, BF16, False, 21,
+                        "attention 4x32 heads, seq 4096, dim 128, bf16, N(0,1)"),
+           AttnWorkload("attn_fwd_b4_h32_s4096_d128_causal_bf16", 4, 4096, 32, 128, BF16, True,
+                        22, "causal attention 4x32 heads, seq 4096, dim 128, bf16, N(0,1)")):
+    ATTN_WORKLOADS[_w.name] = _w
+
 # The benchmark's headline workload: the quickstart GEMM+ReLU.
 HEADLINE = "gemm_relu_1024_f16_128x128x64s3"
