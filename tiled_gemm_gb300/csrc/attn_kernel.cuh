@@ -11,9 +11,12 @@
 // tiles wholly above the diagonal and masks the diagonal tile.
 //
 // One CTA per 128-query tile of one (batch, head), 256 threads:
-//   warp 0 (one thread)  TMA producer: the Q tile once, then K and V tiles (128 keys)
-//                        through a 2-stage ring.  A 4-D tensor map over [B, S, H, D]
-//                        zero-fills keys and queries past the sequence end.
+//   warps 0, 2 (one thread each)  TMA producers: warp 0 loads the Q tile once and then
+//                        K tiles (128 keys) through a 2-stage ring, warp 2 the V tiles
+//                        through their own 2-stage ring.  K_i is released as soon as
+//                        S_i has read it, V_i only after PV_i, so the K loads run well
+//                        ahead.  A 4-D tensor map over [B, S, H, D] zero-fills keys and
+//                        queries past the sequence end.
 //   warp 1 (one thread)  MMA issuer: S_i = Q K_i^T into Tensor Memory (two S buffers,
 //                        so S_{i+1} is computed while the softmax works on S_i), then
 //                        O += P_i V_i into the Tensor Memory accumulator O.  Warp 1
@@ -25,7 +28,7 @@
 //                        values into a swizzled shared buffer (the A operand of the PV
 //                        MMA) and hands it to the MMA thread.  At the end it divides
 //                        O by l and stores the row.
-//   warps 2-3            idle.
+//   warp 3               idle.
 //
 // Every wait is bounded as in the GEMM kernel; on a timeout the status word records
 // the site and every role unwinds.
@@ -67,7 +70,7 @@ __host__ __device__ constexpr uint32_t attn_tile_bytes() {      // 128 rows x D,
   return 128u * D * 2u;
 }
 
-__host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 14u + 16u; }
+__host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 18u + 32u; }
 
 template <int D>
 __host__ __device__ constexpr uint32_t attn_smem_bytes() {
@@ -115,23 +118,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const uint32_t sQ = base;
-  const uint32_t sK = sQ + kTile;                 // K of stage s at sK + s * 2 * kTile
+  const uint32_t sK = sQ + kTile;                 // K of stage s at sK + s * kTile
+  const uint32_t sV = sK + 2 * kTile;             // V of stage s at sV + s * kTile
   const uint32_t sP = sQ + 5 * kTile;
   const uint32_t sBar = sP + 128u * 128u * 2u;
-  auto kv_full = [&](int s) { return sBar + 8u * s; };
-  auto kv_empty = [&](int s) { return sBar + 8u * (2 + s); };
+  auto k_full = [&](int s) { return sBar + 8u * s; };
+  auto k_empty = [&](int s) { return sBar + 8u * (2 + s); };
+  auto v_full = [&](int s) { return sBar + 8u * (14 + s); };
+  auto v_empty = [&](int s) { return sBar + 8u * (16 + s); };
   auto s_full = [&](int s) { return sBar + 8u * (4 + s); };
   auto s_empty = [&](int s) { return sBar + 8u * (6 + s); };
   const uint32_t q_full = sBar + 8u * 8;
   const uint32_t p_full = sBar + 8u * 9;
   const uint32_t pv_done = sBar + 8u * 10;
   const uint32_t done_bar = sBar + 8u * 11;
-  const uint32_t slot = sBar + 8u * 12;
+  const uint32_t slot = sBar + 8u * 18;
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
-  volatile int32_t* const lap_armed = reinterpret_cast<volatile int32_t*>(tmem_slot_ptr + 2);  // [2]
-  volatile int32_t* const q_armed = lap_armed + 2;
+  volatile int32_t* const lap_k = reinterpret_cast<volatile int32_t*>(tmem_slot_ptr + 2);  // [2]
+  volatile int32_t* const lap_v = lap_k + 2;                                                 // [2]
+  volatile int32_t* const q_armed = lap_v + 2;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -145,8 +152,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
       mbar_init(s_empty(s), 4);          // the four softmax warps
     }
@@ -155,7 +164,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(pv_done, 1);
     mbar_init(done_bar, 1);
     *abort_flag = 0u;
-    lap_armed[0] = lap_armed[1] = -1;
+    lap_k[0] = lap_k[1] = lap_v[0] = lap_v[1] = -1;
     *q_armed = 0;
     fence_barrier_init();
   }
@@ -173,28 +182,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer --
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ producers --
     if (lane == 0) {
       grid_dependency_wait();
-      mbar_arrive_expect_tx(q_full, kTile);
-      for (int c = 0; c < kChunks; ++c) tma_load_4d(sQ + c * kChunkBytes, &tmap_q, q_full, 64 * c, h, q0, b);
-      *q_armed = 1;
+      const bool is_k = warp == 0;
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, kTile);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_4d(sQ + c * kChunkBytes, &tmap_q, q_full, 64 * c, h, q0, b);
+        *q_armed = 1;
+      }
       for (int i = 0; i < n_kv; ++i) {
         const int st = i & 1;
         const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
-        if (!wait_bounded<false>(kv_empty(st), ph ^ 1u, abort_flag, p.timeout_ns)) {
+        const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
+        const uint32_t full = is_k ? k_full(st) : v_full(st);
+        if (!wait_bounded<false>(empty, ph ^ 1u, abort_flag, p.timeout_ns)) {
           record_timeout(p.status, abort_flag, kSiteAttnKvEmpty);
           break;
         }
-        mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
-        const uint32_t k_dst = sK + st * 2 * kTile;
-        const uint32_t v_dst = k_dst + kTile;
-        for (int c = 0; c < kChunks; ++c) {
-          tma_load_4d(k_dst + c * kChunkBytes, &tmap_k, kv_full(st), 64 * c, h, i * kAttnBN, b);
-          tma_load_4d(v_dst + c * kChunkBytes, &tmap_v, kv_full(st), 64 * c, h, i * kAttnBN, b);
-        }
-        lap_armed[st] = i >> 1;
+        mbar_arrive_expect_tx(full, kTile);
+        const uint32_t dst = (is_k ? sK : sV) + st * kTile;
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_4d(dst + c * kChunkBytes, is_k ? &tmap_k : &tmap_v, full, 64 * c, h,
+                      i * kAttnBN, b);
+        (is_k ? lap_k : lap_v)[st] = i >> 1;
       }
     }
   } else if (warp == 1) {
@@ -213,7 +226,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (i < n_kv) {
           const int st = i & 1;
           const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
-          if (!wait_bounded<false>(kv_full(st), ph, abort_flag, p.timeout_ns)) {
+          if (!wait_bounded<false>(k_full(st), ph, abort_flag, p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteAttnKvFull);
             break;
           }
@@ -222,13 +235,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint64_t k_desc = smem_desc_sw128(sK + st * 2 * kTile, 16u, 1024u);
+          const uint64_t k_desc = smem_desc_sw128(sK + st * kTile, 16u, 1024u);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             mma_f16_ss(tmem_base + st * 128u, q_desc + kmaj(k), k_desc + kmaj(k), p.idesc_s,
                        k > 0 ? 1u : 0u);
           }
           mma_commit(s_full(st));
+          mma_commit(k_empty(st));        // K_i is read once S_i has completed
         }
         if (i >= 1) {
           const int j = i - 1;
@@ -238,17 +252,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             record_timeout(p.status, abort_flag, kSiteAttnPFull);
             break;
           }
+          if (!wait_bounded<false>(v_full(st), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                                   p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteAttnKvFull);
+            break;
+          }
           tc_fence_after_sync();
           // V is the N-major B operand: 64-column chunks of 128 key rows (LBO = chunk
           // stride), K step = 16 key rows of 128 B
-          const uint64_t v_desc = smem_desc_sw128(sK + st * 2 * kTile + kTile, kChunkBytes, 1024u);
+          const uint64_t v_desc = smem_desc_sw128(sV + st * kTile, kChunkBytes, 1024u);
 #pragma unroll
           for (int k = 0; k < kAttnBN / 16; ++k) {
             mma_f16_ss(tmem_base + 256u, p_desc + kmaj(k),
                        v_desc + ((static_cast<uint64_t>(k) * 16u * 128u) >> 4), p.idesc_o,
                        (j > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(kv_empty(st));
+          mma_commit(v_empty(st));
           mma_commit(pv_done);
         }
       }
@@ -385,9 +404,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (*q_armed && !wait_bounded<false>(q_full, 0, nullptr, p.timeout_ns))
       record_timeout(p.status, abort_flag, kSiteAttnDrain);
     for (int st = 0; st < 2; ++st) {
-      const int lap = lap_armed[st];
-      if (lap >= 0 && !wait_bounded<false>(kv_full(st), static_cast<uint32_t>(lap) & 1u, nullptr,
-                                           p.timeout_ns)) {
+      const int lk = lap_k[st], lv = lap_v[st];
+      if (lk >= 0 && !wait_bounded<false>(k_full(st), static_cast<uint32_t>(lk) & 1u, nullptr,
+                                          p.timeout_ns)) {
+        record_timeout(p.status, abort_flag, kSiteAttnDrain);
+      }
+      if (lv >= 0 && !wait_bounded<false>(v_full(st), static_cast<uint32_t>(lv) & 1u, nullptr,
+                                          p.timeout_ns)) {
         record_timeout(p.status, abort_flag, kSiteAttnDrain);
       }
     }
