@@ -307,19 +307,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // scale into the log2 domain and mask keys past the end (and, causal, past qi)
       const int kv0 = i * kAttnBN;
       const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
-      float mx = -INFINITY;
+      // Row maximum with eight independent partial maxima (a single running maximum
+      // would be a 128-long dependency chain); masking only on the tiles that need it.
+      float mxp[8];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        const float x = j < lim ? __uint_as_float(sv[j]) : -INFINITY;
-        sv[j] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+      for (int t = 0; t < 8; ++t) mxp[t] = -INFINITY;
+      if (lim < 128) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          const float x = j < lim ? __uint_as_float(sv[j]) : -INFINITY;
+          sv[j] = __float_as_uint(x);
+          mxp[j & 7] = fmaxf(mxp[j & 7], x);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) mxp[j & 7] = fmaxf(mxp[j & 7], __uint_as_float(sv[j]));
       }
+      float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                       fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       mx *= p.scale_log2;
       // keep the stale maximum unless the row's maximum grew by more than the threshold
       // (a row that has seen no key yet, m = -inf, takes the new one)
       const float m_use = (mx > m + kRescaleThreshold) ? mx : m;
       const float corr = (m_use == m) ? 1.0f : fast_exp2(m - m_use);
-      float rs = 0.0f;
+      float rsp[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) rsp[t] = 0.0f;
       uint32_t pk[64];
       if (m_use == -INFINITY) {
 #pragma unroll
@@ -329,10 +342,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int j = 0; j < 64; ++j) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * j]), p.scale_log2, -m_use));
           const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * j + 1]), p.scale_log2, -m_use));
-          rs += p0 + p1;
+          rsp[j & 7] += p0 + p1;
           pk[j] = pack_half2(p0, p1, p.bf16);
         }
       }
+      const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
       l = l * corr + rs;
       m = m_use;
       if (i > 0) {
