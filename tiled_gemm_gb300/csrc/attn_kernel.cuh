@@ -25,9 +25,10 @@
 //                        It loads S_i's row, masks, updates the running max m and sum
 //                        l, rescales its row of O in Tensor Memory when m grew (after
 //                        PV_{i-1} has landed), writes P_i = exp2(S_i - m) as 16-bit
-//                        values into a swizzled shared buffer (the A operand of the PV
-//                        MMA) and hands it to the MMA thread.  At the end it divides
-//                        O by l and stores the row.
+//                        values into one of two swizzled shared buffers (the A operand
+//                        of the PV MMA; two, so that P_i is written while PV_{i-1} runs)
+//                        and hands it to the MMA thread.  At the end it divides O by l
+//                        and stores the row.
 //   warp 3               idle.
 //
 // Every wait is bounded as in the GEMM kernel; on a timeout the status word records
@@ -70,12 +71,12 @@ __host__ __device__ constexpr uint32_t attn_tile_bytes() {      // 128 rows x D,
   return 128u * D * 2u;
 }
 
-__host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 18u + 32u; }
+__host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 20u + 32u; }
 
 template <int D>
 __host__ __device__ constexpr uint32_t attn_smem_bytes() {
-  // +1024 alignment slack; Q; 2 stages of K and V; P (128 x 128 16-bit); barriers
-  return 1024u + attn_tile_bytes<D>() * 5u + 128u * 128u * 2u + attn_barrier_bytes();
+  // +1024 alignment slack; Q; 2 stages of K and of V; P (2 x 128 x 128 16-bit); barriers
+  return 1024u + attn_tile_bytes<D>() * 5u + 2u * 128u * 128u * 2u + attn_barrier_bytes();
 }
 
 // 2^x by the special-function unit's approximation (relative error ~2^-22, enough
@@ -120,8 +121,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t sQ = base;
   const uint32_t sK = sQ + kTile;                 // K of stage s at sK + s * kTile
   const uint32_t sV = sK + 2 * kTile;             // V of stage s at sV + s * kTile
-  const uint32_t sP = sQ + 5 * kTile;
-  const uint32_t sBar = sP + 128u * 128u * 2u;
+  constexpr uint32_t kPBytes = 128u * 128u * 2u;
+  const uint32_t sP = sQ + 5 * kTile;             // P buffer t at sP + t * kPBytes
+  const uint32_t sBar = sP + 2 * kPBytes;
   auto k_full = [&](int s) { return sBar + 8u * s; };
   auto k_empty = [&](int s) { return sBar + 8u * (2 + s); };
   auto v_full = [&](int s) { return sBar + 8u * (14 + s); };
@@ -129,10 +131,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto s_full = [&](int s) { return sBar + 8u * (4 + s); };
   auto s_empty = [&](int s) { return sBar + 8u * (6 + s); };
   const uint32_t q_full = sBar + 8u * 8;
-  const uint32_t p_full = sBar + 8u * 9;
-  const uint32_t pv_done = sBar + 8u * 10;
   const uint32_t done_bar = sBar + 8u * 11;
-  const uint32_t slot = sBar + 8u * 18;
+  auto p_full = [&](int t) { return sBar + 8u * (12 + t); };    // P buffer t written
+  auto pv_done = [&](int t) { return sBar + 8u * (18 + t); };   // PV on P buffer t done
+  const uint32_t slot = sBar + 8u * 20;
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
@@ -160,8 +162,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(s_empty(s), 4);          // the four softmax warps
     }
     mbar_init(q_full, 1);
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(p_full(t), 4);
+      mbar_init(pv_done(t), 1);
+    }
     mbar_init(done_bar, 1);
     *abort_flag = 0u;
     lap_k[0] = lap_k[1] = lap_v[0] = lap_v[1] = -1;
@@ -215,7 +219,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     grid_dependency_wait();
     if (lane == 0) {
       const uint64_t q_desc = smem_desc_sw128(sQ, 16u, 1024u);
-      const uint64_t p_desc = smem_desc_sw128(sP, 16u, 1024u);
       // K-major step k (16 elements): chunk k/4, then 32 B along the swizzled row
       auto kmaj = [](int k) -> uint64_t {
         return (static_cast<uint64_t>(k / 4) * kChunkBytes + (k % 4) * 32u) >> 4;
@@ -246,8 +249,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (i >= 1) {
           const int j = i - 1;
-          const int st = j & 1;
-          if (!wait_bounded<false>(p_full, static_cast<uint32_t>(j) & 1u, abort_flag,
+          const int st = j & 1;                       // V stage and P buffer of tile j
+          if (!wait_bounded<false>(p_full(st), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
                                    p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteAttnPFull);
             break;
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // V is the N-major B operand: 64-column chunks of 128 key rows (LBO = chunk
           // stride), K step = 16 key rows of 128 B
           const uint64_t v_desc = smem_desc_sw128(sV + st * kTile, kChunkBytes, 1024u);
+          const uint64_t p_desc = smem_desc_sw128(sP + st * kPBytes, 16u, 1024u);
 #pragma unroll
           for (int k = 0; k < kAttnBN / 16; ++k) {
             mma_f16_ss(tmem_base + 256u, p_desc + kmaj(k),
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                        (j > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(v_empty(st));
-          mma_commit(pv_done);
+          mma_commit(pv_done(st));
         }
       }
       mma_commit(done_bar);
@@ -346,46 +350,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           pk[j] = pack_half2(p0, p1, p.bf16);
         }
       }
+      // P buffer i % 2 is free once PV_{i-2} has read it (long done by now); in the
+      // swizzled A operand, chunk c holds keys 64c..64c+63 and 16-byte unit u of row r
+      // lands at unit u ^ (r % 8)
+      if (i >= 2 && !(ok = wait_warp(pv_done(st), static_cast<uint32_t>((i - 2) >> 1) & 1u,
+                                     kSiteAttnPvDone))) {
+        break;
+      }
+      const uint32_t p_row = sP + st * kPBytes + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+      for (int g = 0; g < 16; ++g) {
+        const uint32_t dst = p_row + (g >> 3) * kChunkBytes + (((g & 7) ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[4 * g]),
+                     "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
+                     : "memory");
+      }
       const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
       l = l * corr + rs;
       m = m_use;
-      if (i > 0) {
-        // PV_{i-1} has landed in O and released the P buffer
-        if (!(ok = wait_warp(pv_done, static_cast<uint32_t>(i - 1) & 1u, kSiteAttnPvDone))) break;
+      if (i > 0 && __any_sync(0xFFFFFFFFu, corr != 1.0f)) {
+        // rescaling O needs PV_{i-1} to have landed in it (PV_i, which reads this P,
+        // waits for the p_full arrival below)
+        const int jp = i - 1;
+        if (!(ok = wait_warp(pv_done(jp & 1), static_cast<uint32_t>(jp >> 1) & 1u,
+                             kSiteAttnPvDone))) {
+          break;
+        }
         tc_fence_after_sync();
-        if (__any_sync(0xFFFFFFFFu, corr != 1.0f)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_load_32cols(lane_base + 256u + 32u * c, ov);
-            tmem_load_wait();
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_load_32cols(lane_base + 256u + 32u * c, ov);
+          tmem_load_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * corr);
-            tmem_store_32cols(lane_base + 256u + 32u * c, ov);
-          }
-          tmem_store_wait();
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * corr);
+          tmem_store_32cols(lane_base + 256u + 32u * c, ov);
         }
-      }
-      // P row into the swizzled A operand: chunk c holds keys 64c..64c+63; 16-byte
-      // unit u of row r lands at unit u ^ (r % 8)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t row_addr = sP + c * kChunkBytes + static_cast<uint32_t>(row) * 128u;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t dst = row_addr + ((u ^ (row & 7)) << 4);
-          const int k = c * 32 + u * 4;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[k]),
-                       "r"(pk[k + 1]), "r"(pk[k + 2]), "r"(pk[k + 3])
-                       : "memory");
-        }
+        tmem_store_wait();
       }
       fence_proxy_async_shared();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(st));
     }
-    if (ok && n_kv > 0 && wait_warp(pv_done, static_cast<uint32_t>(n_kv - 1) & 1u, kSiteAttnPvDone)) {
+    if (ok && n_kv > 0 &&
+        wait_warp(pv_done((n_kv - 1) & 1), static_cast<uint32_t>((n_kv - 1) >> 1) & 1u,
+                  kSiteAttnPvDone)) {
       tc_fence_after_sync();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.O) +
