@@ -40,7 +40,7 @@ import workloads  # noqa: E402
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["tiled_gemm_gb300/csrc/gemm_kernel.cuh", "tiled_gemm_gb300/csrc/sm103_ptx.cuh",
-                  "tiled_gemm_gb300/csrc/tl_gemm.cu"]
+                  "tiled_gemm_gb300/csrc/attn_kernel.cuh", "tiled_gemm_gb300/csrc/tl_gemm.cu"]
 
 
 def kernel_source_hash() -> str:
