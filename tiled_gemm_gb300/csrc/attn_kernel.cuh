@@ -25,10 +25,9 @@
 //                        It loads S_i's row, masks, updates the running max m and sum
 //                        l, rescales its row of O in Tensor Memory when m grew (after
 //                        PV_{i-1} has landed), writes P_i = exp2(S_i - m) as 16-bit
-//                        values into one of two swizzled shared buffers (the A operand
-//                        of the PV MMA; two, so that P_i is written while PV_{i-1} runs)
-//                        and hands it to the MMA thread.  At the end it divides O by l
-//                        and stores the row.
+//                        pairs back over its row of S_i in Tensor Memory, where the PV
+//                        MMA takes it as its A operand, and hands it to the MMA thread.
+//                        At the end it divides O by l and stores the row.
 //   warp 3               idle.
 //
 // Every wait is bounded as in the GEMM kernel; on a timeout the status word records
@@ -75,8 +74,8 @@ __host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 20u + 
 
 template <int D>
 __host__ __device__ constexpr uint32_t attn_smem_bytes() {
-  // +1024 alignment slack; Q; 2 stages of K and of V; P (2 x 128 x 128 16-bit); barriers
-  return 1024u + attn_tile_bytes<D>() * 5u + 2u * 128u * 128u * 2u + attn_barrier_bytes();
+  // +1024 alignment slack; Q; 2 stages of K and of V; barriers
+  return 1024u + attn_tile_bytes<D>() * 5u + attn_barrier_bytes();
 }
 
 // 2^x by the special-function unit's approximation (relative error ~2^-22, enough
@@ -121,19 +120,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t sQ = base;
   const uint32_t sK = sQ + kTile;                 // K of stage s at sK + s * kTile
   const uint32_t sV = sK + 2 * kTile;             // V of stage s at sV + s * kTile
-  constexpr uint32_t kPBytes = 128u * 128u * 2u;
-  const uint32_t sP = sQ + 5 * kTile;             // P buffer t at sP + t * kPBytes
-  const uint32_t sBar = sP + 2 * kPBytes;
+  const uint32_t sBar = sQ + 5 * kTile;
   auto k_full = [&](int s) { return sBar + 8u * s; };
   auto k_empty = [&](int s) { return sBar + 8u * (2 + s); };
   auto v_full = [&](int s) { return sBar + 8u * (14 + s); };
   auto v_empty = [&](int s) { return sBar + 8u * (16 + s); };
   auto s_full = [&](int s) { return sBar + 8u * (4 + s); };
-  auto s_empty = [&](int s) { return sBar + 8u * (6 + s); };
   const uint32_t q_full = sBar + 8u * 8;
   const uint32_t done_bar = sBar + 8u * 11;
-  auto p_full = [&](int t) { return sBar + 8u * (12 + t); };    // P buffer t written
-  auto pv_done = [&](int t) { return sBar + 8u * (18 + t); };   // PV on P buffer t done
+  auto p_full = [&](int t) { return sBar + 8u * (12 + t); };    // P written in S buffer t
+  auto pv_done = [&](int t) { return sBar + 8u * (18 + t); };   // PV from S buffer t done
   const uint32_t slot = sBar + 8u * 20;
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
@@ -159,7 +155,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 4);          // the four softmax warps
     }
     mbar_init(q_full, 1);
     for (int t = 0; t < 2; ++t) {
@@ -233,10 +228,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             record_timeout(p.status, abort_flag, kSiteAttnKvFull);
             break;
           }
-          if (!wait_bounded<false>(s_empty(st), ph ^ 1u, abort_flag, p.timeout_ns)) {
-            record_timeout(p.status, abort_flag, kSiteAttnSEmpty);
-            break;
-          }
+          // S buffer st last held P_{i-2}; PV_{i-2}, issued before this point by this
+          // thread, reads it before these MMAs overwrite it (tcgen05 operations of one
+          // thread execute in order), so no wait is needed
           tc_fence_after_sync();
           const uint64_t k_desc = smem_desc_sw128(sK + st * kTile, 16u, 1024u);
 #pragma unroll
@@ -264,10 +258,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // V is the N-major B operand: 64-column chunks of 128 key rows (LBO = chunk
           // stride), K step = 16 key rows of 128 B
           const uint64_t v_desc = smem_desc_sw128(sV + st * kTile, kChunkBytes, 1024u);
-          const uint64_t p_desc = smem_desc_sw128(sP + st * kPBytes, 16u, 1024u);
+          // P_j is the A operand in Tensor Memory, over S_j: 16 keys = 8 columns per step
 #pragma unroll
           for (int k = 0; k < kAttnBN / 16; ++k) {
-            mma_f16_ss(tmem_base + 256u, p_desc + kmaj(k),
+            mma_f16_ts(tmem_base + 256u, tmem_base + st * 128u + 8u * k,
                        v_desc + ((static_cast<uint64_t>(k) * 16u * 128u) >> 4), p.idesc_o,
                        (j > 0 || k > 0) ? 1u : 0u);
           }
@@ -305,9 +299,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int c = 0; c < 4; ++c)
         tmem_load_32cols(lane_base + st * 128u + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
       tmem_load_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty(st));
       // scale into the log2 domain and mask keys past the end (and, causal, past qi)
       const int kv0 = i * kAttnBN;
       const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
@@ -350,21 +341,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           pk[j] = pack_half2(p0, p1, p.bf16);
         }
       }
-      // P buffer i % 2 is free once PV_{i-2} has read it (long done by now); in the
-      // swizzled A operand, chunk c holds keys 64c..64c+63 and 16-byte unit u of row r
-      // lands at unit u ^ (r % 8)
-      if (i >= 2 && !(ok = wait_warp(pv_done(st), static_cast<uint32_t>((i - 2) >> 1) & 1u,
-                                     kSiteAttnPvDone))) {
-        break;
-      }
-      const uint32_t p_row = sP + st * kPBytes + static_cast<uint32_t>(row) * 128u;
-#pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        const uint32_t dst = p_row + (g >> 3) * kChunkBytes + (((g & 7) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[4 * g]),
-                     "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
-                     : "memory");
-      }
+      // P_i (16-bit pairs, keys 2c and 2c+1 in column c) over this row's S_i in Tensor
+      // Memory, where the PV MMA reads it as its A operand
+      tmem_store_32cols(lane_base + st * 128u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_store_32cols(lane_base + st * 128u + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
       l = l * corr + rs;
       m = m_use;
@@ -388,7 +368,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         tmem_store_wait();
       }
-      fence_proxy_async_shared();
+      tmem_store_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(st));
