@@ -66,7 +66,7 @@ typedef enum {
   TL_ERR_INVALID_ARG = 1,  /* negative size, ld too small, bad enum, bad plan      */
   TL_ERR_NULL_PTR = 2,     /* NULL matrix pointer with a non-empty extent          */
   TL_ERR_ALIGNMENT = 3,    /* a matrix pointer not aligned to its 2-byte element   */
-  TL_ERR_UNSUPPORTED = 4,  /* valid request this build cannot run (no sm_103 GPU,  */
+  TL_ERR_UNSUPPORTED = 4,  /* valid request the library cannot run (no sm_103 GPU,*/
                            /* size beyond the library's limits)                    */
   TL_ERR_ALIAS = 5,        /* C overlaps A or B                                    */
   TL_ERR_DEVICE = 6,       /* pointer not on the current device, CUDA query failed */
