@@ -109,7 +109,7 @@ struct GemmParams {
   // holds the tile's first k-block adds the partials in order and writes C.
   int32_t dp_tiles;
   int64_t sk_iters;
-  float* sk_partials;                 // [unit][cta][4 warps][BN cols][32 lanes]
+  float* sk_partials;                 // [unit][cta][4 warps][BN/4 col groups][32 lanes][4]
   unsigned long long* sk_flags;       // [unit][cta][4 warps]
   unsigned long long sk_token;        // unique to this launch, never 0
   uint32_t idesc;
@@ -587,9 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (v_end < n_clusters && sk_begin(p, v_end, n_clusters) < tile_end) ++v_end;
       }
       const int slot_q = (static_cast<int>(rank) * 4 + q);     // this warp's slot in a unit
-      auto partial_at = [&](int unit, int col) -> float* {
-        return p.sk_partials +
-               ((static_cast<int64_t>(unit) * CG * 4 + slot_q) * BN + col) * 32 + lane;
+      // lane-major groups of four columns: one 16-byte access per lane per group, and
+      // the warp's 32 lanes cover 512 contiguous bytes
+      auto partial4_at = [&](int unit, int col4) -> float4* {
+        return reinterpret_cast<float4*>(p.sk_partials) +
+               ((static_cast<int64_t>(unit) * CG * 4 + slot_q) * (BN / 4) + col4) * 32 + lane;
       };
       auto flag_at = [&](int unit) -> unsigned long long* {
         return p.sk_flags + static_cast<int64_t>(unit) * CG * 4 + slot_q;
@@ -651,18 +653,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (store_partial) {
-          // fp32 partial sum: for each column the warp's 32 lanes write 128 B
+          // fp32 partial sum, four columns per 16-byte store
 #pragma unroll
-          for (int j = 0; j < kEC; ++j)
-            __stcg(partial_at(cluster_id, c * kEC + j), __uint_as_float(v[j]));
+          for (int j = 0; j < kEC / 4; ++j)
+            __stcg(partial4_at(cluster_id, c * (kEC / 4) + j),
+                   make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
           continue;
         }
         // finisher: add the later k-blocks' partials, in unit order
         for (int u2 = cluster_id + 1; u2 < v_end; ++u2) {
           if (!contributes(u2)) continue;
 #pragma unroll
-          for (int j = 0; j < kEC; ++j)
-            v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(partial_at(u2, c * kEC + j)));
+          for (int j = 0; j < kEC / 4; ++j) {
+            const float4 t = __ldcg(partial4_at(u2, c * (kEC / 4) + j));
+            v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + t.x);
+            v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + t.y);
+            v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + t.z);
+            v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + t.w);
+          }
         }
         if (p.scale) {
 #pragma unroll
@@ -729,9 +738,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (store_partial) {
-        __threadfence();                  // this lane's partial is visible before the flag
+        // the warp's partial stores happen before lane 0's fence (warp barrier); the
+        // GPU-scope fence and release store make all of them visible before the flag
         __syncwarp();
-        if (lane == 0) st_release_gpu_u64(flag_at(cluster_id), p.sk_token);
+        if (lane == 0) {
+          __threadfence();
+          st_release_gpu_u64(flag_at(cluster_id), p.sk_token);
+        }
       } else if (v_end > cluster_id + 1) {
         __syncwarp();                     // all lanes have read the partials: reset flags
         if (lane == 0)
