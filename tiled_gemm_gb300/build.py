@@ -19,7 +19,6 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libtl_gemm.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 SOURCES = ["tl_gemm.cu"]
-DEPS = ["tl_gemm.cu", "gemm_kernel.cuh", "sm103_ptx.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,7 +33,7 @@ def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
-    deps = [os.path.join(CSRC, d) for d in DEPS] + [os.path.join(ROOT, "include", "tl_gemm.h"),
+    deps = [os.path.join(CSRC, d) for d in os.listdir(CSRC) if d.endswith((".cu", ".cuh"))] + [os.path.join(ROOT, "include", "tl_gemm.h"),
                                                      os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -56,7 +56,6 @@ enum AttnWaitSite : uint32_t {
 struct AttnParams {
   int32_t B, S, H;
   int32_t causal;
-  int32_t bf16;
   float scale_log2;             // log2(e) / sqrt(D)
   void* O;
   uint32_t idesc_s;             // S = Q K^T: M 128, N 128, both K-major
@@ -92,16 +91,47 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // of P, and the final division by the row sum cancels the common factor.
 constexpr float kRescaleThreshold = 8.0f;
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi, int bf16) {
-  if (bf16) {
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  if constexpr (kBf16) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
   }
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int D>
+// The softmax is bound by instruction issue (one warp per scheduler), so its
+// arithmetic uses packed fp32 pairs (one f32x2 instruction does two scores' worth)
+// and a three-input maximum (two new scores per step).
+__device__ __forceinline__ uint64_t pair_bits(float2 a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 pair_of(uint64_t r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pair_bits(a)), "l"(pair_bits(b)), "l"(pair_bits(c)));
+  return pair_of(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pair_bits(a)), "l"(pair_bits(b)));
+  return pair_of(d);
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+template <int D, bool kBf16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     tl_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
@@ -299,53 +329,54 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int c = 0; c < 4; ++c)
         tmem_load_32cols(lane_base + st * 128u + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
       tmem_load_wait();
-      // scale into the log2 domain and mask keys past the end (and, causal, past qi)
+      // keys past the end (and, causal, past qi) are masked
       const int kv0 = i * kAttnBN;
       const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
-      // Row maximum with eight independent partial maxima (a single running maximum
-      // would be a 128-long dependency chain); masking only on the tiles that need it.
-      float mxp[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mxp[t] = -INFINITY;
+      // Row maximum with four independent partial maxima, two new scores per step (a
+      // single running maximum would be a long dependency chain); masking only on the
+      // tiles that need it.
       if (lim < 128) {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const float x = j < lim ? __uint_as_float(sv[j]) : -INFINITY;
-          sv[j] = __float_as_uint(x);
-          mxp[j & 7] = fmaxf(mxp[j & 7], x);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 128; ++j) mxp[j & 7] = fmaxf(mxp[j & 7], __uint_as_float(sv[j]));
+        for (int j = 0; j < 128; ++j)
+          if (j >= lim) sv[j] = __float_as_uint(-INFINITY);
       }
-      float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                       fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+      float mxp[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) mxp[t] = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        mxp[j & 3] = max3(mxp[j & 3], __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
+      float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
       mx *= p.scale_log2;
       // keep the stale maximum unless the row's maximum grew by more than the threshold
       // (a row that has seen no key yet, m = -inf, takes the new one)
       const float m_use = (mx > m + kRescaleThreshold) ? mx : m;
       const float corr = (m_use == m) ? 1.0f : fast_exp2(m - m_use);
-      float rsp[8];
+      float2 rsp[4];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) rsp[t] = 0.0f;
+      for (int t = 0; t < 4; ++t) rsp[t] = make_float2(0.0f, 0.0f);
       uint32_t pk[64];
       if (m_use == -INFINITY) {
 #pragma unroll
         for (int j = 0; j < 64; ++j) pk[j] = 0u;
       } else {
+        const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm = make_float2(-m_use, -m_use);
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * j]), p.scale_log2, -m_use));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * j + 1]), p.scale_log2, -m_use));
-          rsp[j & 7] += p0 + p1;
-          pk[j] = pack_half2(p0, p1, p.bf16);
+          const float2 y = fma2(make_float2(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
+                                sc, nm);
+          const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+          rsp[j & 3] = add2(rsp[j & 3], e);
+          pk[j] = pack_half2<kBf16>(e.x, e.y);
         }
       }
       // P_i (16-bit pairs, keys 2c and 2c+1 in column c) over this row's S_i in Tensor
       // Memory, where the PV MMA reads it as its A operand
       tmem_store_32cols(lane_base + st * 128u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_store_32cols(lane_base + st * 128u + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
+      const float2 rs2 = add2(add2(rsp[0], rsp[1]), add2(rsp[2], rsp[3]));
+      const float rs = rs2.x + rs2.y;
       l = l * corr + rs;
       m = m_use;
       if (i > 0 && __any_sync(0xFFFFFFFFu, corr != 1.0f)) {
@@ -389,8 +420,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint32_t o2[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            o2[j] = pack_half2(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv,
-                               p.bf16);
+            o2[j] = pack_half2<kBf16>(__uint_as_float(ov[2 * j]) * inv,
+                                      __uint_as_float(ov[2 * j + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);

@@ -885,15 +885,15 @@ bool encode_bshd(CUtensorMap* map, tl_dtype dtype, const void* base, int64_t B, 
   return encode_cached(map, dtype, 4, base, dims, strides, box);
 }
 
-template <int D>
+template <int D, bool kBf16>
 tl_status launch_attention(DeviceState* st, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const tl::AttnParams& prm, int64_t q_tiles,
                            cudaStream_t stream) {
   // at least 120 KB, so that two CTAs never share an SM: each allocates all 512 Tensor
   // Memory columns, and a second allocation would wait for the first CTA to finish
   constexpr uint32_t kSmem = tl::attn_smem_bytes<D>() > 122880u ? tl::attn_smem_bytes<D>() : 122880u;
-  constexpr uint32_t bit = 1u << (D == 64 ? 28 : 29);
-  auto kern = tl::tl_attention_kernel<D>;
+  constexpr uint32_t bit = 1u << (28 + (D == 128) + 2 * kBf16);
+  auto kern = tl::tl_attention_kernel<D, kBf16>;
   if (static_cast<int64_t>(kSmem) > st->smem_optin) return TL_ERR_UNSUPPORTED;
   if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
     std::lock_guard<std::mutex> lock(st->mu);
@@ -961,16 +961,19 @@ tl_status run_attention(const void* Q, const void* K, const void* V, void* O, in
   prm.S = static_cast<int32_t>(S);
   prm.H = static_cast<int32_t>(H);
   prm.causal = causal;
-  prm.bf16 = dtype == TL_BF16 ? 1 : 0;
+  const uint32_t bf16 = dtype == TL_BF16 ? 1u : 0u;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   prm.O = O;
-  prm.idesc_s = tl::mma_idesc_f16(prm.bf16, 0u, 0u, 128u, 128u);
-  prm.idesc_o = tl::mma_idesc_f16(prm.bf16, 0u, 1u, 128u, static_cast<uint32_t>(D));
+  prm.idesc_s = tl::mma_idesc_f16(bf16, 0u, 0u, 128u, 128u);
+  prm.idesc_o = tl::mma_idesc_f16(bf16, 0u, 1u, 128u, static_cast<uint32_t>(D));
   prm.status = st->status;
   prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   const int64_t q_tiles = ceil_div(S, tl::kAttnBM);
-  return D == 64 ? launch_attention<64>(st, tq, tk, tv, prm, q_tiles, stream)
-                 : launch_attention<128>(st, tq, tk, tv, prm, q_tiles, stream);
+  if (dtype == TL_BF16)
+    return D == 64 ? launch_attention<64, true>(st, tq, tk, tv, prm, q_tiles, stream)
+                   : launch_attention<128, true>(st, tq, tk, tv, prm, q_tiles, stream);
+  return D == 64 ? launch_attention<64, false>(st, tq, tk, tv, prm, q_tiles, stream)
+                 : launch_attention<128, false>(st, tq, tk, tv, prm, q_tiles, stream);
 }
 
 }  // namespace
