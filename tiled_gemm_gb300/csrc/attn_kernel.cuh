@@ -10,24 +10,36 @@
 // by log2(e), and divides by the row sum once at the end; the causal form skips key
 // tiles wholly above the diagonal and masks the diagonal tile.
 //
-// One CTA per 128-query tile of one (batch, head), 256 threads:
-//   warps 0, 2 (one thread each)  TMA producers: warp 0 loads the Q tile once and then
-//                        K tiles (128 keys) through a 2-stage ring, warp 2 the V tiles
-//                        through their own 2-stage ring.  K_i is released as soon as
-//                        S_i has read it, V_i only after PV_i, so the K loads run well
-//                        ahead.  A 4-D tensor map over [B, S, H, D] zero-fills keys and
-//                        queries past the sequence end.
+// Work unit: one 128-query tile of one (batch, head).  The grid is persistent (at most
+// one CTA per SM, 256 threads), and every CTA walks its own fixed list of units, so the
+// loads and first products of a unit overlap the end of the one before:
+//   * CTA c takes work items c, c + G, c + 2G, ... (G CTAs).  An item is one unit, the
+//     query tiles of a head in turn (consecutive items share K and V, which the CTAs
+//     running side by side then read from L2), longest causal tile first;
+//   * causal with more units than SMs: an item is the pair of query tiles (n-1-k, k)
+//     of one head, n + 1 key tiles in all for every item, so the static split is even.
+// Roles:
+//   warps 0, 2 (one thread each)  TMA producers: warp 0 loads each unit's Q tile (two
+//                        Q buffers, so the next unit's is in flight early) and the K
+//                        tiles (128 keys) through a 2-stage ring, warp 2 the V tiles
+//                        through their own 2-stage ring; the rings run on across units.
+//                        K_i is released as soon as S_i has read it, V_i only after
+//                        PV_i, so the K loads run well ahead.  A 4-D tensor map over
+//                        [B, S, H, D] zero-fills keys and queries past the sequence end.
 //   warp 1 (one thread)  MMA issuer: S_i = Q K_i^T into Tensor Memory (two S buffers,
 //                        so S_{i+1} is computed while the softmax works on S_i), then
-//                        O += P_i V_i into the Tensor Memory accumulator O.  Warp 1
-//                        also owns the Tensor Memory allocation.
+//                        O += P_i V_i into the Tensor Memory accumulator O.  The next
+//                        unit's S_0 goes in before the last PV of the current one.  Warp
+//                        1 also owns the Tensor Memory allocation.
 //   warps 4-7            softmax: thread r owns query row r (its Tensor Memory lane).
 //                        It loads S_i's row, masks, updates the running max m and sum
 //                        l, rescales its row of O in Tensor Memory when m grew (after
 //                        PV_{i-1} has landed), writes P_i = exp2(S_i - m) as 16-bit
 //                        pairs back over its row of S_i in Tensor Memory, where the PV
 //                        MMA takes it as its A operand, and hands it to the MMA thread.
-//                        At the end it divides O by l and stores the row.
+//                        At the end of a unit it divides O by l and stores the row; the
+//                        next unit's first PV, which overwrites O, waits for its P_0,
+//                        which these warps write only after that.
 //   warp 3               idle.
 //
 // Every wait is bounded as in the GEMM kernel; on a timeout the status word records
@@ -46,7 +58,7 @@ enum AttnWaitSite : uint32_t {
   kSiteAttnKvEmpty = 21,
   kSiteAttnQFull = 22,
   kSiteAttnKvFull = 23,
-  kSiteAttnSEmpty = 24,
+  kSiteAttnQEmpty = 24,
   kSiteAttnPFull = 25,
   kSiteAttnSFull = 26,
   kSiteAttnPvDone = 27,
@@ -56,6 +68,10 @@ enum AttnWaitSite : uint32_t {
 struct AttnParams {
   int32_t B, S, H;
   int32_t causal;
+  int32_t n_q_tiles;            // ceil(S / 128)
+  int32_t items_per_head;       // n_q_tiles, or ceil(n_q_tiles / 2) with pairing
+  int32_t n_items;              // B * H * items_per_head
+  int32_t pair;                 // an item is the query tiles (n-1-k, k) of a head
   float scale_log2;             // log2(e) / sqrt(D)
   void* O;
   uint32_t idesc_s;             // S = Q K^T: M 128, N 128, both K-major
@@ -69,12 +85,15 @@ __host__ __device__ constexpr uint32_t attn_tile_bytes() {      // 128 rows x D,
   return 128u * D * 2u;
 }
 
-__host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 20u + 32u; }
+// Barriers: K full and V full per stage, and 2 each of s_full, q_full, q_empty,
+// p_full, pv_done; done.  Then the Tensor Memory slot, the abort flag and the laps of the
+// last load into each K, V and Q buffer.
+__host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 15u + 4u * 8u; }
 
 template <int D>
 __host__ __device__ constexpr uint32_t attn_smem_bytes() {
-  // +1024 alignment slack; Q; 2 stages of K and of V; barriers
-  return 1024u + attn_tile_bytes<D>() * 5u + attn_barrier_bytes();
+  // +1024 alignment slack; 2 Q buffers; 2 stages of K and of V; barriers
+  return 1024u + attn_tile_bytes<D>() * 6u + attn_barrier_bytes();
 }
 
 // 2^x by the special-function unit's approximation (relative error ~2^-22, enough
@@ -147,54 +166,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const uint32_t sQ = base;
-  const uint32_t sK = sQ + kTile;                 // K of stage s at sK + s * kTile
+  const uint32_t sQ = base;                       // Q buffer t at sQ + t * kTile
+  const uint32_t sK = sQ + 2 * kTile;             // K of stage s at sK + s * kTile
   const uint32_t sV = sK + 2 * kTile;             // V of stage s at sV + s * kTile
-  const uint32_t sBar = sQ + 5 * kTile;
+  const uint32_t sBar = sV + 2 * kTile;
+  // Key tile g uses K and V stage g & 1 and S buffer g & 1.  The stages are released by
+  // the barriers that mark the products reading them: K_g by s_full (S_g done), V_g by
+  // pv_done (PV_g done).  A producer reusing stage g & 1 waits for the completion of tile
+  // g - 2 there; the next completion on that barrier is tile g's own, which needs the
+  // load it has not issued yet, so its parity wait cannot see a later phase.
   auto k_full = [&](int s) { return sBar + 8u * s; };
-  auto k_empty = [&](int s) { return sBar + 8u * (2 + s); };
-  auto v_full = [&](int s) { return sBar + 8u * (14 + s); };
-  auto v_empty = [&](int s) { return sBar + 8u * (16 + s); };
+  auto v_full = [&](int s) { return sBar + 8u * (2 + s); };
   auto s_full = [&](int s) { return sBar + 8u * (4 + s); };
-  const uint32_t q_full = sBar + 8u * 8;
-  const uint32_t done_bar = sBar + 8u * 11;
-  auto p_full = [&](int t) { return sBar + 8u * (12 + t); };    // P written in S buffer t
-  auto pv_done = [&](int t) { return sBar + 8u * (18 + t); };   // PV from S buffer t done
-  const uint32_t slot = sBar + 8u * 20;
+  auto q_full = [&](int t) { return sBar + 8u * (6 + t); };
+  auto q_empty = [&](int t) { return sBar + 8u * (8 + t); };
+  auto p_full = [&](int t) { return sBar + 8u * (10 + t); };    // P written in S buffer t
+  auto pv_done = [&](int t) { return sBar + 8u * (12 + t); };   // PV from S buffer t done
+  const uint32_t done_bar = sBar + 8u * 14;
+  const uint32_t slot = sBar + 8u * 15;
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
+  // laps of the last load issued into each K, V and Q buffer (-1: none), for the drain
   volatile int32_t* const lap_k = reinterpret_cast<volatile int32_t*>(tmem_slot_ptr + 2);  // [2]
   volatile int32_t* const lap_v = lap_k + 2;                                                 // [2]
-  volatile int32_t* const q_armed = lap_v + 2;
+  volatile int32_t* const lap_q = lap_v + 2;                                                 // [2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_q_tiles = static_cast<int>(gridDim.x);
-  const int qt = n_q_tiles - 1 - static_cast<int>(blockIdx.x);   // longest causal tiles first
-  const int h = static_cast<int>(blockIdx.y);
-  const int b = static_cast<int>(blockIdx.z);
-  const int q0 = qt * kAttnBM;
-  const int kv_end = p.causal ? min(p.S, q0 + kAttnBM) : p.S;
-  const int n_kv = (kv_end + kAttnBN - 1) / kAttnBN;
+
+  // This CTA's units in order: f(q-tile, head, batch) returns false to stop early.
+  auto for_each_unit = [&](auto&& f) {
+    for (int w = static_cast<int>(blockIdx.x); w < p.n_items; w += static_cast<int>(gridDim.x)) {
+      const int hb = w / p.items_per_head;
+      const int k = w - hb * p.items_per_head;
+      const int h = hb % p.H, b = hb / p.H;
+      const int hi = p.n_q_tiles - 1 - k;
+      if (!f(hi, h, b)) return;
+      if (p.pair && k != hi && !f(k, h, b)) return;
+    }
+  };
+  auto kv_tiles = [&](int qt) {
+    const int kv_end = p.causal ? min(p.S, (qt + 1) * kAttnBM) : p.S;
+    return (kv_end + kAttnBN - 1) / kAttnBN;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
       mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+      lap_k[s] = lap_v[s] = -1;
       mbar_init(s_full(s), 1);
-    }
-    mbar_init(q_full, 1);
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(p_full(t), 4);
-      mbar_init(pv_done(t), 1);
+      mbar_init(q_full(s), 1);
+      mbar_init(q_empty(s), 1);
+      mbar_init(p_full(s), 4);
+      mbar_init(pv_done(s), 1);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0u;
-    lap_k[0] = lap_k[1] = lap_v[0] = lap_v[1] = -1;
-    *q_armed = 0;
+    lap_q[0] = lap_q[1] = -1;
     fence_barrier_init();
   }
   if (threadIdx.x == 64) {
@@ -216,89 +246,121 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       grid_dependency_wait();
       const bool is_k = warp == 0;
-      if (is_k) {
-        mbar_arrive_expect_tx(q_full, kTile);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(sQ + c * kChunkBytes, &tmap_q, q_full, 64 * c, h, q0, b);
-        *q_armed = 1;
-      }
-      for (int i = 0; i < n_kv; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
-        const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
-        const uint32_t full = is_k ? k_full(st) : v_full(st);
-        if (!wait_bounded<false>(empty, ph ^ 1u, abort_flag, p.timeout_ns)) {
-          record_timeout(p.status, abort_flag, kSiteAttnKvEmpty);
-          break;
+      int g = 0;                                  // key tiles loaded so far (all units)
+      int u = 0;                                  // units so far
+      for_each_unit([&](int qt, int h, int b) -> bool {
+        if (is_k) {
+          const int qb = u & 1;
+          if (!wait_bounded<false>(q_empty(qb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u,
+                                   abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteAttnQEmpty);
+            return false;
+          }
+          mbar_arrive_expect_tx(q_full(qb), kTile);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(sQ + qb * kTile + c * kChunkBytes, &tmap_q, q_full(qb), 64 * c, h,
+                        qt * kAttnBM, b);
+          lap_q[qb] = u >> 1;
         }
-        mbar_arrive_expect_tx(full, kTile);
-        const uint32_t dst = (is_k ? sK : sV) + st * kTile;
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(dst + c * kChunkBytes, is_k ? &tmap_k : &tmap_v, full, 64 * c, h,
-                      i * kAttnBN, b);
-        (is_k ? lap_k : lap_v)[st] = i >> 1;
-      }
+        ++u;
+        const int n_kv = kv_tiles(qt);
+        for (int i = 0; i < n_kv; ++i, ++g) {
+          const int st = g & 1;
+          const int lap = g >> 1;
+          const uint32_t ph = static_cast<uint32_t>(lap) & 1u;
+          const uint32_t empty = is_k ? s_full(st) : pv_done(st);
+          const uint32_t full = is_k ? k_full(st) : v_full(st);
+          if (!wait_bounded<false>(empty, ph ^ 1u, abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteAttnKvEmpty);
+            return false;
+          }
+          mbar_arrive_expect_tx(full, kTile);
+          const uint32_t dst = (is_k ? sK : sV) + st * kTile;
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(dst + c * kChunkBytes, is_k ? &tmap_k : &tmap_v, full, 64 * c, h,
+                        i * kAttnBN, b);
+          (is_k ? lap_k : lap_v)[st] = lap;
+        }
+        return true;
+      });
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer --
     grid_dependency_wait();
     if (lane == 0) {
-      const uint64_t q_desc = smem_desc_sw128(sQ, 16u, 1024u);
       // K-major step k (16 elements): chunk k/4, then 32 B along the swizzled row
       auto kmaj = [](int k) -> uint64_t {
         return (static_cast<uint64_t>(k / 4) * kChunkBytes + (k % 4) * 32u) >> 4;
       };
-      bool ok = wait_bounded<false>(q_full, 0, abort_flag, p.timeout_ns);
-      if (!ok) record_timeout(p.status, abort_flag, kSiteAttnQFull);
-      for (int i = 0; ok && i <= n_kv; ++i) {
-        if (i < n_kv) {
-          const int st = i & 1;
-          const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
-          if (!wait_bounded<false>(k_full(st), ph, abort_flag, p.timeout_ns)) {
-            record_timeout(p.status, abort_flag, kSiteAttnKvFull);
-            break;
-          }
-          // S buffer st last held P_{i-2}; PV_{i-2}, issued before this point by this
+      // Descriptors of buffer 0; buffer t is kTile further on (the start address field
+      // holds address / 16 in 14 bits, and every buffer lies below 256 KB, so adding
+      // t * kTile / 16 cannot carry out of it).  V is the N-major B operand: 64-column
+      // chunks of 128 key rows (LBO = chunk stride), K step = 16 key rows of 128 B.
+      const uint64_t q_desc0 = smem_desc_sw128(sQ, 16u, 1024u);
+      const uint64_t k_desc0 = smem_desc_sw128(sK, 16u, 1024u);
+      const uint64_t v_desc0 = smem_desc_sw128(sV, kChunkBytes, 1024u);
+      // This thread's waits sit between batches of MMAs, where every cycle it spends
+      // leaves the tensor pipe idle: one non-blocking test first, the bounded wait only
+      // when the phase is still open.
+      auto wait_fast = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (wait_bounded<false>(bar, parity, abort_flag, p.timeout_ns)) return true;
+        record_timeout(p.status, abort_flag, site);
+        return false;
+      };
+      // O += P_j V_j for key tile j (all units' tiles counted together); `first`: the
+      // unit's first tile, whose product overwrites O
+      auto pv = [&](int j, bool first) -> bool {
+        const int st = j & 1;                       // P buffer and V stage of tile j
+        const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+        if (!wait_fast(p_full(st), ph, kSiteAttnPFull)) return false;
+        if (!wait_fast(v_full(st), ph, kSiteAttnKvFull)) return false;
+        tc_fence_after_sync();
+        const uint64_t v_desc = v_desc0 + static_cast<uint64_t>(st) * (kTile >> 4);
+        // P_j is the A operand in Tensor Memory, over S_j: 16 keys = 8 columns per step
+#pragma unroll
+        for (int k = 0; k < kAttnBN / 16; ++k) {
+          mma_f16_ts(tmem_base + 256u, tmem_base + st * 128u + 8u * k,
+                     v_desc + ((static_cast<uint64_t>(k) * 16u * 128u) >> 4), p.idesc_o,
+                     (!first || k > 0) ? 1u : 0u);
+        }
+        mma_commit(pv_done(st));          // also releases V stage st
+        return true;
+      };
+      int g = 0, u = 0;
+      int pend = -1;                               // key tile whose PV is still to issue
+      bool pend_first = false;
+      bool ok = true;
+      for_each_unit([&](int qt, int, int) -> bool {
+        const int qb = u & 1;
+        if (!wait_fast(q_full(qb), static_cast<uint32_t>(u >> 1) & 1u, kSiteAttnQFull))
+          return ok = false;
+        const uint64_t q_desc = q_desc0 + static_cast<uint64_t>(qb) * (kTile >> 4);
+        const int n_kv = kv_tiles(qt);
+        for (int i = 0; i < n_kv; ++i, ++g) {
+          const int st = g & 1;                     // S buffer and K stage
+          if (!wait_fast(k_full(st), static_cast<uint32_t>(g >> 1) & 1u, kSiteAttnKvFull))
+            return ok = false;
+          // S buffer st last held P_{g-2}; PV_{g-2}, issued before this point by this
           // thread, reads it before these MMAs overwrite it (tcgen05 operations of one
           // thread execute in order), so no wait is needed
           tc_fence_after_sync();
-          const uint64_t k_desc = smem_desc_sw128(sK + st * kTile, 16u, 1024u);
+          const uint64_t k_desc = k_desc0 + static_cast<uint64_t>(st) * (kTile >> 4);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             mma_f16_ss(tmem_base + st * 128u, q_desc + kmaj(k), k_desc + kmaj(k), p.idesc_s,
                        k > 0 ? 1u : 0u);
           }
-          mma_commit(s_full(st));
-          mma_commit(k_empty(st));        // K_i is read once S_i has completed
+          mma_commit(s_full(st));           // also releases K stage st
+          if (i == n_kv - 1) mma_commit(q_empty(qb));
+          if (pend >= 0 && !pv(pend, pend_first)) return ok = false;
+          pend = g;
+          pend_first = i == 0;
         }
-        if (i >= 1) {
-          const int j = i - 1;
-          const int st = j & 1;                       // V stage and P buffer of tile j
-          if (!wait_bounded<false>(p_full(st), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                                   p.timeout_ns)) {
-            record_timeout(p.status, abort_flag, kSiteAttnPFull);
-            break;
-          }
-          if (!wait_bounded<false>(v_full(st), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                                   p.timeout_ns)) {
-            record_timeout(p.status, abort_flag, kSiteAttnKvFull);
-            break;
-          }
-          tc_fence_after_sync();
-          // V is the N-major B operand: 64-column chunks of 128 key rows (LBO = chunk
-          // stride), K step = 16 key rows of 128 B
-          const uint64_t v_desc = smem_desc_sw128(sV + st * kTile, kChunkBytes, 1024u);
-          // P_j is the A operand in Tensor Memory, over S_j: 16 keys = 8 columns per step
-#pragma unroll
-          for (int k = 0; k < kAttnBN / 16; ++k) {
-            mma_f16_ts(tmem_base + 256u, tmem_base + st * 128u + 8u * k,
-                       v_desc + ((static_cast<uint64_t>(k) * 16u * 128u) >> 4), p.idesc_o,
-                       (j > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(v_empty(st));
-          mma_commit(pv_done(st));
-        }
-      }
+        ++u;
+        return true;
+      });
+      if (ok && pend >= 0) (void)pv(pend, pend_first);
       mma_commit(done_bar);
       if (!wait_bounded<false>(done_bar, 0, nullptr, p.timeout_ns))
         record_timeout(p.status, abort_flag, kSiteAttnDrain);
@@ -308,10 +370,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     grid_dependency_wait();
     const int qd = warp & 3;                        // Tensor Memory lane quadrant
     const int row = qd * 32 + lane;                 // this thread's query row in the tile
-    const int qi = q0 + row;                        // its position in the sequence
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
-    float m = -INFINITY, l = 0.0f;
-    bool ok = true;
     auto wait_warp = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
       bool r = true;
       if (lane == 0) r = wait_bounded<false>(bar, parity, abort_flag, p.timeout_ns);
@@ -320,93 +379,97 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!r && lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, site);
       return r;
     };
-    for (int i = 0; ok && i < n_kv; ++i) {
-      const int st = i & 1;
-      if (!(ok = wait_warp(s_full(st), static_cast<uint32_t>(i >> 1) & 1u, kSiteAttnSFull))) break;
-      tc_fence_after_sync();
-      uint32_t sv[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_load_32cols(lane_base + st * 128u + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
-      tmem_load_wait();
-      // keys past the end (and, causal, past qi) are masked
-      const int kv0 = i * kAttnBN;
-      const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
-      // Row maximum with four independent partial maxima, two new scores per step (a
-      // single running maximum would be a long dependency chain); masking only on the
-      // tiles that need it.
-      if (lim < 128) {
-#pragma unroll
-        for (int j = 0; j < 128; ++j)
-          if (j >= lim) sv[j] = __float_as_uint(-INFINITY);
-      }
-      float mxp[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) mxp[t] = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 64; ++j)
-        mxp[j & 3] = max3(mxp[j & 3], __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
-      float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-      mx *= p.scale_log2;
-      // keep the stale maximum unless the row's maximum grew by more than the threshold
-      // (a row that has seen no key yet, m = -inf, takes the new one)
-      const float m_use = (mx > m + kRescaleThreshold) ? mx : m;
-      const float corr = (m_use == m) ? 1.0f : fast_exp2(m - m_use);
-      float2 rsp[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) rsp[t] = make_float2(0.0f, 0.0f);
-      uint32_t pk[64];
-      if (m_use == -INFINITY) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) pk[j] = 0u;
-      } else {
-        const float2 sc = make_float2(p.scale_log2, p.scale_log2);
-        const float2 nm = make_float2(-m_use, -m_use);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float2 y = fma2(make_float2(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
-                                sc, nm);
-          const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-          rsp[j & 3] = add2(rsp[j & 3], e);
-          pk[j] = pack_half2<kBf16>(e.x, e.y);
-        }
-      }
-      // P_i (16-bit pairs, keys 2c and 2c+1 in column c) over this row's S_i in Tensor
-      // Memory, where the PV MMA reads it as its A operand
-      tmem_store_32cols(lane_base + st * 128u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_store_32cols(lane_base + st * 128u + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      const float2 rs2 = add2(add2(rsp[0], rsp[1]), add2(rsp[2], rsp[3]));
-      const float rs = rs2.x + rs2.y;
-      l = l * corr + rs;
-      m = m_use;
-      if (i > 0 && __any_sync(0xFFFFFFFFu, corr != 1.0f)) {
-        // rescaling O needs PV_{i-1} to have landed in it (PV_i, which reads this P,
-        // waits for the p_full arrival below)
-        const int jp = i - 1;
-        if (!(ok = wait_warp(pv_done(jp & 1), static_cast<uint32_t>(jp >> 1) & 1u,
-                             kSiteAttnPvDone))) {
-          break;
-        }
+    int g = 0;                                      // key tiles so far (all units)
+    for_each_unit([&](int qt, int h, int b) -> bool {
+      const int qi = qt * kAttnBM + row;            // this thread's query in the sequence
+      const int n_kv = kv_tiles(qt);
+      float m = -INFINITY, l = 0.0f;
+      for (int i = 0; i < n_kv; ++i, ++g) {
+        const int st = g & 1;
+        if (!wait_warp(s_full(st), static_cast<uint32_t>(g >> 1) & 1u, kSiteAttnSFull))
+          return false;
         tc_fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_load_32cols(lane_base + 256u + 32u * c, ov);
-          tmem_load_wait();
+        uint32_t sv[128];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * corr);
-          tmem_store_32cols(lane_base + 256u + 32u * c, ov);
+        for (int c = 0; c < 4; ++c)
+          tmem_load_32cols(lane_base + st * 128u + 32u * c,
+                           *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+        tmem_load_wait();
+        // keys past the end (and, causal, past qi) are masked
+        const int kv0 = i * kAttnBN;
+        const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
+        // Row maximum with four independent partial maxima, two new scores per step (a
+        // single running maximum would be a long dependency chain); masking only on
+        // the tiles that need it.
+        if (lim < 128) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j)
+            if (j >= lim) sv[j] = __float_as_uint(-INFINITY);
+        }
+        float mxp[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) mxp[t] = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          mxp[j & 3] = max3(mxp[j & 3], __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
+        float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+        mx *= p.scale_log2;
+        // keep the stale maximum unless the row's maximum grew by more than the
+        // threshold (a row that has seen no key yet, m = -inf, takes the new one)
+        const float m_use = (mx > m + kRescaleThreshold) ? mx : m;
+        const float corr = (m_use == m) ? 1.0f : fast_exp2(m - m_use);
+        float2 rsp[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) rsp[t] = make_float2(0.0f, 0.0f);
+        uint32_t pk[64];
+        if (m_use == -INFINITY) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) pk[j] = 0u;
+        } else {
+          const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+          const float2 nm = make_float2(-m_use, -m_use);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const float2 y = fma2(make_float2(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
+                                  sc, nm);
+            const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+            rsp[j & 3] = add2(rsp[j & 3], e);
+            pk[j] = pack_half2<kBf16>(e.x, e.y);
+          }
+        }
+        // P (16-bit pairs, keys 2c and 2c+1 in column c) over this row's S in Tensor
+        // Memory, where the PV MMA reads it as its A operand
+        tmem_store_32cols(lane_base + st * 128u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_store_32cols(lane_base + st * 128u + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        const float2 rs2 = add2(add2(rsp[0], rsp[1]), add2(rsp[2], rsp[3]));
+        l = l * corr + (rs2.x + rs2.y);
+        m = m_use;
+        if (i > 0 && __any_sync(0xFFFFFFFFu, corr != 1.0f)) {
+          // rescaling O needs the previous tile's PV to have landed in it (this tile's
+          // PV, which reads this P, waits for the p_full arrival below)
+          const int jp = g - 1;
+          if (!wait_warp(pv_done(jp & 1), static_cast<uint32_t>(jp >> 1) & 1u, kSiteAttnPvDone))
+            return false;
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_load_32cols(lane_base + 256u + 32u * c, ov);
+            tmem_load_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * corr);
+            tmem_store_32cols(lane_base + 256u + 32u * c, ov);
+          }
         }
         tmem_store_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(st));
       }
-      tmem_store_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(st));
-    }
-    if (ok && n_kv > 0 &&
-        wait_warp(pv_done((n_kv - 1) & 1), static_cast<uint32_t>((n_kv - 1) >> 1) & 1u,
-                  kSiteAttnPvDone)) {
+      // the unit's last PV has landed: O / l to the output rows
+      const int jl = g - 1;
+      if (!wait_warp(pv_done(jl & 1), static_cast<uint32_t>(jl >> 1) & 1u, kSiteAttnPvDone))
+        return false;
       tc_fence_after_sync();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.O) +
@@ -424,10 +487,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                       __uint_as_float(ov[2 * j + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
         }
       }
-    }
+      // the reads of O are complete (wait::ld) before this warp's next p_full arrival,
+      // which the next unit's first PV (overwriting O) waits for
+      return true;
+    });
   }
 
   // ------------------------------------------------------------------ teardown --
@@ -436,18 +503,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0) {
     // every load issued must have landed before the CTA exits
-    if (*q_armed && !wait_bounded<false>(q_full, 0, nullptr, p.timeout_ns))
-      record_timeout(p.status, abort_flag, kSiteAttnDrain);
+    auto drain = [&](uint32_t bar, int lap) {
+      if (lap >= 0 && !wait_bounded<false>(bar, static_cast<uint32_t>(lap) & 1u, nullptr,
+                                           p.timeout_ns)) {
+        record_timeout(p.status, abort_flag, kSiteAttnDrain);
+      }
+    };
     for (int st = 0; st < 2; ++st) {
-      const int lk = lap_k[st], lv = lap_v[st];
-      if (lk >= 0 && !wait_bounded<false>(k_full(st), static_cast<uint32_t>(lk) & 1u, nullptr,
-                                          p.timeout_ns)) {
-        record_timeout(p.status, abort_flag, kSiteAttnDrain);
-      }
-      if (lv >= 0 && !wait_bounded<false>(v_full(st), static_cast<uint32_t>(lv) & 1u, nullptr,
-                                          p.timeout_ns)) {
-        record_timeout(p.status, abort_flag, kSiteAttnDrain);
-      }
+      drain(k_full(st), lap_k[st]);
+      drain(v_full(st), lap_v[st]);
+      drain(q_full(st), lap_q[st]);
     }
   }
   __syncthreads();

@@ -887,10 +887,11 @@ bool encode_bshd(CUtensorMap* map, tl_dtype dtype, const void* base, int64_t B, 
 
 template <int D, bool kBf16>
 tl_status launch_attention(DeviceState* st, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const tl::AttnParams& prm, int64_t q_tiles,
+                           const CUtensorMap& tv, const tl::AttnParams& prm, int64_t grid,
                            cudaStream_t stream) {
   // at least 120 KB, so that two CTAs never share an SM: each allocates all 512 Tensor
-  // Memory columns, and a second allocation would wait for the first CTA to finish
+  // Memory columns, and a second allocation would wait for the first CTA to finish (the
+  // grid has at most one CTA per SM, but another kernel's CTA could still be resident)
   constexpr uint32_t kSmem = tl::attn_smem_bytes<D>() > 122880u ? tl::attn_smem_bytes<D>() : 122880u;
   constexpr uint32_t bit = 1u << (28 + (D == 128) + 2 * kBf16);
   auto kern = tl::tl_attention_kernel<D, kBf16>;
@@ -908,8 +909,7 @@ tl_status launch_attention(DeviceState* st, const CUtensorMap& tq, const CUtenso
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(q_tiles), static_cast<unsigned>(prm.H),
-                     static_cast<unsigned>(prm.B));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(tl::kAttnThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
@@ -968,12 +968,23 @@ tl_status run_attention(const void* Q, const void* K, const void* V, void* O, in
   prm.idesc_o = tl::mma_idesc_f16(bf16, 0u, 1u, 128u, static_cast<uint32_t>(D));
   prm.status = st->status;
   prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  // Work items for the persistent grid: single query tiles, or (causal, more tiles than
+  // SMs) pairs of tiles (n-1-k, k) of one head, n + 1 key tiles per pair.
   const int64_t q_tiles = ceil_div(S, tl::kAttnBM);
+  const bool pair = causal && B * H * q_tiles > st->sms;
+  const int64_t per_head = pair ? ceil_div(q_tiles, 2) : q_tiles;
+  const int64_t items = B * H * per_head;
+  if (items > INT32_MAX) return TL_ERR_UNSUPPORTED;
+  prm.n_q_tiles = static_cast<int32_t>(q_tiles);
+  prm.items_per_head = static_cast<int32_t>(per_head);
+  prm.n_items = static_cast<int32_t>(items);
+  prm.pair = pair ? 1 : 0;
+  const int64_t grid = std::min<int64_t>(items, st->sms);
   if (dtype == TL_BF16)
-    return D == 64 ? launch_attention<64, true>(st, tq, tk, tv, prm, q_tiles, stream)
-                   : launch_attention<128, true>(st, tq, tk, tv, prm, q_tiles, stream);
-  return D == 64 ? launch_attention<64, false>(st, tq, tk, tv, prm, q_tiles, stream)
-                 : launch_attention<128, false>(st, tq, tk, tv, prm, q_tiles, stream);
+    return D == 64 ? launch_attention<64, true>(st, tq, tk, tv, prm, grid, stream)
+                   : launch_attention<128, true>(st, tq, tk, tv, prm, grid, stream);
+  return D == 64 ? launch_attention<64, false>(st, tq, tk, tv, prm, grid, stream)
+                 : launch_attention<128, false>(st, tq, tk, tv, prm, grid, stream);
 }
 
 }  // namespace
