@@ -85,15 +85,23 @@ __host__ __device__ constexpr uint32_t attn_tile_bytes() {      // 128 rows x D,
   return 128u * D * 2u;
 }
 
-// Barriers: K full and V full per stage, and 2 each of s_full, q_full, q_empty,
-// p_full, pv_done; done.  Then the Tensor Memory slot, the abort flag and the laps of the
-// last load into each K, V and Q buffer.
-__host__ __device__ constexpr uint32_t attn_barrier_bytes() { return 8u * 15u + 4u * 8u; }
+// Tensor Memory: three S buffers of 128 columns (the MMA thread issues S_g before PV_{g-2},
+// so S_g must not land on P_{g-2}), then the O accumulator at column 384.
+constexpr int kAttnSBufs = 3;
+constexpr uint32_t kAttnOCol = 128u * kAttnSBufs;
+
+// Barriers: K full and V full per stage (2), q_full and q_empty per Q buffer (2),
+// s_full, p_full and pv_done per S buffer (3), done.  Then the Tensor Memory slot, the
+// abort flag and the laps of the last load into each K, V and Q buffer.
+__host__ __device__ constexpr uint32_t attn_barrier_bytes() {
+  return 8u * (4u + 4u + 3u * kAttnSBufs + 1u) + 4u * 8u;
+}
 
 template <int D>
 __host__ __device__ constexpr uint32_t attn_smem_bytes() {
-  // +1024 alignment slack; 2 Q buffers; 2 stages of K and of V; barriers
-  return 1024u + attn_tile_bytes<D>() * 6u + attn_barrier_bytes();
+  // +1024 alignment slack; 2 Q buffers; 2 stages of K and of V; the O staging tile;
+  // barriers
+  return 1024u + attn_tile_bytes<D>() * 7u + attn_barrier_bytes();
 }
 
 // 2^x by the special-function unit's approximation (relative error ~2^-22, enough
@@ -154,12 +162,14 @@ template <int D, bool kBf16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     tl_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+                        const __grid_constant__ CUtensorMap tmap_v,
+                        const __grid_constant__ CUtensorMap tmap_o, const AttnParams p) {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   constexpr int kChunks = D / 64;                 // 128-byte chunks of a row
   constexpr uint32_t kTile = attn_tile_bytes<D>();
   constexpr uint32_t kChunkBytes = 128u * 128u;   // one 64-element chunk of 128 rows
-  constexpr uint32_t kTmemCols = 512;             // S[2] at 0, 128; O at 256
+  constexpr uint32_t kTmemCols = 512;             // S[3] at 0, 128, 256; O at 384
+  static_assert(kAttnOCol + D <= kTmemCols, "S buffers and O fit in Tensor Memory");
 
   grid_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -169,21 +179,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t sQ = base;                       // Q buffer t at sQ + t * kTile
   const uint32_t sK = sQ + 2 * kTile;             // K of stage s at sK + s * kTile
   const uint32_t sV = sK + 2 * kTile;             // V of stage s at sV + s * kTile
-  const uint32_t sBar = sV + 2 * kTile;
-  // Key tile g uses K and V stage g & 1 and S buffer g & 1.  The stages are released by
-  // the barriers that mark the products reading them: K_g by s_full (S_g done), V_g by
-  // pv_done (PV_g done).  A producer reusing stage g & 1 waits for the completion of tile
-  // g - 2 there; the next completion on that barrier is tile g's own, which needs the
-  // load it has not issued yet, so its parity wait cannot see a later phase.
+  const uint32_t sStage = sV + 2 * kTile;         // O of 128 rows on its way out
+  const uint32_t sBar = sStage + kTile;
+  // Key tile g (counted over all of this CTA's units) uses K and V stage g & 1 and S
+  // buffer g % 3.  The stages are released by the barriers that mark the products
+  // reading them: K_g by s_full (S_g done), V_g by pv_done (PV_g done).  A producer
+  // reusing a stage for tile g waits for tile g - 2's completion there; the next
+  // completion on that S buffer's barrier is tile g + 1's, which needs a load the
+  // producer has not issued yet, so its parity wait cannot see a later phase.
   auto k_full = [&](int s) { return sBar + 8u * s; };
   auto v_full = [&](int s) { return sBar + 8u * (2 + s); };
-  auto s_full = [&](int s) { return sBar + 8u * (4 + s); };
-  auto q_full = [&](int t) { return sBar + 8u * (6 + t); };
-  auto q_empty = [&](int t) { return sBar + 8u * (8 + t); };
-  auto p_full = [&](int t) { return sBar + 8u * (10 + t); };    // P written in S buffer t
-  auto pv_done = [&](int t) { return sBar + 8u * (12 + t); };   // PV from S buffer t done
-  const uint32_t done_bar = sBar + 8u * 14;
-  const uint32_t slot = sBar + 8u * 15;
+  auto q_full = [&](int t) { return sBar + 8u * (4 + t); };
+  auto q_empty = [&](int t) { return sBar + 8u * (6 + t); };
+  auto s_full = [&](int b) { return sBar + 8u * (8 + b); };                   // S_g computed
+  auto p_full = [&](int b) { return sBar + 8u * (8 + kAttnSBufs + b); };      // P_g over S_g
+  auto pv_done = [&](int b) { return sBar + 8u * (8 + 2 * kAttnSBufs + b); }; // PV_g done
+  const uint32_t done_bar = sBar + 8u * (8 + 3 * kAttnSBufs);
+  const uint32_t slot = done_bar + 8u;
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
@@ -216,11 +228,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(k_full(s), 1);
       mbar_init(v_full(s), 1);
       lap_k[s] = lap_v[s] = -1;
-      mbar_init(s_full(s), 1);
       mbar_init(q_full(s), 1);
       mbar_init(q_empty(s), 1);
-      mbar_init(p_full(s), 4);
-      mbar_init(pv_done(s), 1);
+    }
+    for (int b = 0; b < kAttnSBufs; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(p_full(b), 4);
+      mbar_init(pv_done(b), 1);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0u;
@@ -231,6 +245,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tma_prefetch_map(&tmap_q);
     tma_prefetch_map(&tmap_k);
     tma_prefetch_map(&tmap_v);
+    tma_prefetch_map(&tmap_o);
   }
   if (warp == 1) {
     tmem_alloc(slot, kTmemCols);
@@ -267,13 +282,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int i = 0; i < n_kv; ++i, ++g) {
           const int st = g & 1;
           const int lap = g >> 1;
-          const uint32_t ph = static_cast<uint32_t>(lap) & 1u;
-          const uint32_t empty = is_k ? s_full(st) : pv_done(st);
-          const uint32_t full = is_k ? k_full(st) : v_full(st);
-          if (!wait_bounded<false>(empty, ph ^ 1u, abort_flag, p.timeout_ns)) {
-            record_timeout(p.status, abort_flag, kSiteAttnKvEmpty);
-            return false;
+          if (g >= 2) {
+            // stage st last held tile g - 2: wait for the product that read it
+            const int b = (g - 2) % kAttnSBufs;
+            const uint32_t ph = static_cast<uint32_t>((g - 2) / kAttnSBufs) & 1u;
+            if (!wait_bounded<false>(is_k ? s_full(b) : pv_done(b), ph, abort_flag,
+                                     p.timeout_ns)) {
+              record_timeout(p.status, abort_flag, kSiteAttnKvEmpty);
+              return false;
+            }
           }
+          const uint32_t full = is_k ? k_full(st) : v_full(st);
           mbar_arrive_expect_tx(full, kTile);
           const uint32_t dst = (is_k ? sK : sV) + st * kTile;
           for (int c = 0; c < kChunks; ++c)
@@ -308,28 +327,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         record_timeout(p.status, abort_flag, site);
         return false;
       };
-      // O += P_j V_j for key tile j (all units' tiles counted together); `first`: the
-      // unit's first tile, whose product overwrites O
-      auto pv = [&](int j, bool first) -> bool {
-        const int st = j & 1;                       // P buffer and V stage of tile j
-        const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-        if (!wait_fast(p_full(st), ph, kSiteAttnPFull)) return false;
-        if (!wait_fast(v_full(st), ph, kSiteAttnKvFull)) return false;
+      // O += P_j V_j for a key tile j (all units' tiles counted together) in S buffer b
+      // (phase ph there); `first`: the unit's first tile, whose product overwrites O
+      struct Pending {
+        int j, b;
+        uint32_t ph;
+        bool first;
+      };
+      auto pv = [&](const Pending& t) -> bool {
+        const int vs = t.j & 1;                     // V stage of tile j
+        if (!wait_fast(p_full(t.b), t.ph, kSiteAttnPFull)) return false;
+        if (!wait_fast(v_full(vs), static_cast<uint32_t>(t.j >> 1) & 1u, kSiteAttnKvFull))
+          return false;
         tc_fence_after_sync();
-        const uint64_t v_desc = v_desc0 + static_cast<uint64_t>(st) * (kTile >> 4);
+        const uint64_t v_desc = v_desc0 + static_cast<uint64_t>(vs) * (kTile >> 4);
         // P_j is the A operand in Tensor Memory, over S_j: 16 keys = 8 columns per step
 #pragma unroll
         for (int k = 0; k < kAttnBN / 16; ++k) {
-          mma_f16_ts(tmem_base + 256u, tmem_base + st * 128u + 8u * k,
+          mma_f16_ts(tmem_base + kAttnOCol, tmem_base + t.b * 128u + 8u * k,
                      v_desc + ((static_cast<uint64_t>(k) * 16u * 128u) >> 4), p.idesc_o,
-                     (!first || k > 0) ? 1u : 0u);
+                     (!t.first || k > 0) ? 1u : 0u);
         }
-        mma_commit(pv_done(st));          // also releases V stage st
+        mma_commit(pv_done(t.b));         // also releases V stage vs
         return true;
       };
+      // S_g goes in before PV_{g-2}: while this thread waits for P_{g-2}, the pipe still
+      // holds S_g's products, and the softmax finds S_{g-1} ready when it is done
       int g = 0, u = 0;
-      int pend = -1;                               // key tile whose PV is still to issue
-      bool pend_first = false;
+      int sb = 0;                                  // S buffer of tile g
+      uint32_t sph = 0;                            // its phase
+      Pending pend0{}, pend1{};                    // PVs still to issue, oldest first
+      int n_pend = 0;
       bool ok = true;
       for_each_unit([&](int qt, int, int) -> bool {
         const int qb = u & 1;
@@ -338,29 +366,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint64_t q_desc = q_desc0 + static_cast<uint64_t>(qb) * (kTile >> 4);
         const int n_kv = kv_tiles(qt);
         for (int i = 0; i < n_kv; ++i, ++g) {
-          const int st = g & 1;                     // S buffer and K stage
+          const int st = g & 1;                     // K stage
           if (!wait_fast(k_full(st), static_cast<uint32_t>(g >> 1) & 1u, kSiteAttnKvFull))
             return ok = false;
-          // S buffer st last held P_{g-2}; PV_{g-2}, issued before this point by this
+          // S buffer sb last held P_{g-3}; PV_{g-3}, issued before this point by this
           // thread, reads it before these MMAs overwrite it (tcgen05 operations of one
           // thread execute in order), so no wait is needed
           tc_fence_after_sync();
           const uint64_t k_desc = k_desc0 + static_cast<uint64_t>(st) * (kTile >> 4);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            mma_f16_ss(tmem_base + st * 128u, q_desc + kmaj(k), k_desc + kmaj(k), p.idesc_s,
+            mma_f16_ss(tmem_base + sb * 128u, q_desc + kmaj(k), k_desc + kmaj(k), p.idesc_s,
                        k > 0 ? 1u : 0u);
           }
-          mma_commit(s_full(st));           // also releases K stage st
+          mma_commit(s_full(sb));           // also releases K stage st
           if (i == n_kv - 1) mma_commit(q_empty(qb));
-          if (pend >= 0 && !pv(pend, pend_first)) return ok = false;
-          pend = g;
-          pend_first = i == 0;
+          const Pending cur{g, sb, sph, i == 0};
+          if (n_pend == 2) {
+            if (!pv(pend0)) return ok = false;
+            pend0 = pend1;
+            pend1 = cur;
+          } else if (n_pend == 1) {
+            pend1 = cur;
+            n_pend = 2;
+          } else {
+            pend0 = cur;
+            n_pend = 1;
+          }
+          if (++sb == kAttnSBufs) {
+            sb = 0;
+            sph ^= 1u;
+          }
         }
         ++u;
         return true;
       });
-      if (ok && pend >= 0) (void)pv(pend, pend_first);
+      if (ok && n_pend >= 1) ok = pv(pend0);
+      if (ok && n_pend == 2) ok = pv(pend1);
       mma_commit(done_bar);
       if (!wait_bounded<false>(done_bar, 0, nullptr, p.timeout_ns))
         record_timeout(p.status, abort_flag, kSiteAttnDrain);
@@ -371,6 +413,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int qd = warp & 3;                        // Tensor Memory lane quadrant
     const int row = qd * 32 + lane;                 // this thread's query row in the tile
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
+    // This warp's 32 rows of the O staging tile: 64-column chunks of 32 rows x 128 B, the
+    // 16-byte units of a row XOR-swizzled by the row (the TMA store's 128-byte swizzle;
+    // the tile is 1024-byte aligned)
+    const uint32_t stage_w = sStage + static_cast<uint32_t>(qd) * (kTile / 4u);
     auto wait_warp = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
       bool r = true;
       if (lane == 0) r = wait_bounded<false>(bar, parity, abort_flag, p.timeout_ns);
@@ -379,122 +425,167 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!r && lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, site);
       return r;
     };
-    int g = 0;                                      // key tiles so far (all units)
-    for_each_unit([&](int qt, int h, int b) -> bool {
-      const int qi = qt * kAttnBM + row;            // this thread's query in the sequence
-      const int n_kv = kv_tiles(qt);
-      float m = -INFINITY, l = 0.0f;
-      for (int i = 0; i < n_kv; ++i, ++g) {
-        const int st = g & 1;
-        if (!wait_warp(s_full(st), static_cast<uint32_t>(g >> 1) & 1u, kSiteAttnSFull))
-          return false;
-        tc_fence_after_sync();
-        uint32_t sv[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_load_32cols(lane_base + st * 128u + 32u * c,
-                           *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
-        tmem_load_wait();
-        // keys past the end (and, causal, past qi) are masked
-        const int kv0 = i * kAttnBN;
-        const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
-        // Row maximum with four independent partial maxima, two new scores per step (a
-        // single running maximum would be a long dependency chain); masking only on
-        // the tiles that need it.
-        if (lim < 128) {
-#pragma unroll
-          for (int j = 0; j < 128; ++j)
-            if (j >= lim) sv[j] = __float_as_uint(-INFINITY);
-        }
-        float mxp[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) mxp[t] = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j)
-          mxp[j & 3] = max3(mxp[j & 3], __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
-        float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-        mx *= p.scale_log2;
-        // keep the stale maximum unless the row's maximum grew by more than the
-        // threshold (a row that has seen no key yet, m = -inf, takes the new one)
-        const float m_use = (mx > m + kRescaleThreshold) ? mx : m;
-        const float corr = (m_use == m) ? 1.0f : fast_exp2(m - m_use);
-        float2 rsp[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) rsp[t] = make_float2(0.0f, 0.0f);
-        uint32_t pk[64];
-        if (m_use == -INFINITY) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j) pk[j] = 0u;
-        } else {
-          const float2 sc = make_float2(p.scale_log2, p.scale_log2);
-          const float2 nm = make_float2(-m_use, -m_use);
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float2 y = fma2(make_float2(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
-                                  sc, nm);
-            const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-            rsp[j & 3] = add2(rsp[j & 3], e);
-            pk[j] = pack_half2<kBf16>(e.x, e.y);
-          }
-        }
-        // P (16-bit pairs, keys 2c and 2c+1 in column c) over this row's S in Tensor
-        // Memory, where the PV MMA reads it as its A operand
-        tmem_store_32cols(lane_base + st * 128u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_store_32cols(lane_base + st * 128u + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        const float2 rs2 = add2(add2(rsp[0], rsp[1]), add2(rsp[2], rsp[3]));
-        l = l * corr + (rs2.x + rs2.y);
-        m = m_use;
-        if (i > 0 && __any_sync(0xFFFFFFFFu, corr != 1.0f)) {
-          // rescaling O needs the previous tile's PV to have landed in it (this tile's
-          // PV, which reads this P, waits for the p_full arrival below)
-          const int jp = g - 1;
-          if (!wait_warp(pv_done(jp & 1), static_cast<uint32_t>(jp >> 1) & 1u, kSiteAttnPvDone))
-            return false;
-          tc_fence_after_sync();
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_load_32cols(lane_base + 256u + 32u * c, ov);
-            tmem_load_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * corr);
-            tmem_store_32cols(lane_base + 256u + 32u * c, ov);
-          }
-        }
-        tmem_store_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(st));
-      }
-      // the unit's last PV has landed: O / l to the output rows
-      const int jl = g - 1;
-      if (!wait_warp(pv_done(jl & 1), static_cast<uint32_t>(jl >> 1) & 1u, kSiteAttnPvDone))
-        return false;
+    bool in_flight = false;                         // a TMA store may still read the staging
+    // O / l of a finished unit, whose last PV is the one from S buffer ob (phase oph),
+    // into this warp's staging rows
+    auto stage_o = [&](int ob, uint32_t oph, float lsum) -> bool {
+      if (!wait_warp(pv_done(ob), oph, kSiteAttnPvDone)) return false;
       tc_fence_after_sync();
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.O) +
-                       ((static_cast<int64_t>(b) * p.S + qi) * p.H + h) * D;
+      if (in_flight) {
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+      }
+      const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
-        tmem_load_32cols(lane_base + 256u + 32u * c, ov);
+        tmem_load_32cols(lane_base + kAttnOCol + 32u * c, ov);
         tmem_load_wait();
-        if (qi < p.S) {
-          uint32_t o2[16];
+        uint32_t o2[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            o2[j] = pack_half2<kBf16>(__uint_as_float(ov[2 * j]) * inv,
-                                      __uint_as_float(ov[2 * j + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+        for (int j = 0; j < 16; ++j)
+          o2[j] = pack_half2<kBf16>(__uint_as_float(ov[2 * j]) * inv,
+                                    __uint_as_float(ov[2 * j + 1]) * inv);
+        const uint32_t chunk = stage_w + static_cast<uint32_t>(c >> 1) * 4096u + lane * 128u;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t unit = static_cast<uint32_t>((c & 1) * 4 + j) ^ (lane & 7u);
+          st_shared_v4(chunk + unit * 16u, o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
         }
       }
-      // the reads of O are complete (wait::ld) before this warp's next p_full arrival,
-      // which the next unit's first PV (overwriting O) waits for
       return true;
-    });
+    };
+    // the staged rows to O: rows past the sequence end are clipped by the tensor map
+    auto store_o = [&](int qt, int h, int b) {
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        for (int c = 0; c < kChunks; ++c)
+          tma_store_4d(&tmap_o, stage_w + static_cast<uint32_t>(c) * 4096u, 64 * c, h,
+                       qt * kAttnBM + qd * 32, b);
+        bulk_commit_group();
+      }
+      in_flight = true;
+    };
+    int sb = 0;                                     // S buffer of the current key tile
+    uint32_t sph = 0;                               // its phase
+    int pb = 0;                                     // S buffer of the previous key tile
+    uint32_t pph = 0;                               // its phase
+    // the previous unit, whose O goes out once this unit's first P is ready (its first
+    // PV overwrites O, so that P is handed over only after O has been read)
+    bool have_prev = false;
+    float l_prev = 0.0f;
+    int qt_prev = 0, h_prev = 0, b_prev = 0;
+    const bool all_ok = [&] {
+      bool done = true;
+      for_each_unit([&](int qt, int h, int b) -> bool {
+        const int qi = qt * kAttnBM + row;          // this thread's query in the sequence
+        const int n_kv = kv_tiles(qt);
+        float m = -INFINITY, l = 0.0f;
+        for (int i = 0; i < n_kv; ++i) {
+          const int st = sb;
+          if (!wait_warp(s_full(st), sph, kSiteAttnSFull)) return done = false;
+          tc_fence_after_sync();
+          uint32_t sv[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_load_32cols(lane_base + st * 128u + 32u * c,
+                             *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+          tmem_load_wait();
+          // keys past the end (and, causal, past qi) are masked
+          const int kv0 = i * kAttnBN;
+          const int lim = p.causal ? min(p.S - kv0, qi - kv0 + 1) : p.S - kv0;
+          // Row maximum with four independent partial maxima, two new scores per step (a
+          // single running maximum would be a long dependency chain); masking only on
+          // the tiles that need it.
+          if (lim < 128) {
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+              if (j >= lim) sv[j] = __float_as_uint(-INFINITY);
+          }
+          float mxp[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) mxp[t] = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            mxp[j & 3] = max3(mxp[j & 3], __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
+          float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+          mx *= p.scale_log2;
+          // keep the stale maximum unless the row's maximum grew by more than the
+          // threshold (a row that has seen no key yet, m = -inf, takes the new one)
+          const float m_use = (mx > m + kRescaleThreshold) ? mx : m;
+          const float corr = (m_use == m) ? 1.0f : fast_exp2(m - m_use);
+          float2 rsp[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) rsp[t] = make_float2(0.0f, 0.0f);
+          uint32_t pk[64];
+          if (m_use == -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) pk[j] = 0u;
+          } else {
+            const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm = make_float2(-m_use, -m_use);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const float2 y = fma2(make_float2(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1])),
+                                    sc, nm);
+              const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+              rsp[j & 3] = add2(rsp[j & 3], e);
+              pk[j] = pack_half2<kBf16>(e.x, e.y);
+            }
+          }
+          // P (16-bit pairs, keys 2c and 2c+1 in column c) over this row's S in Tensor
+          // Memory, where the PV MMA reads it as its A operand
+          tmem_store_32cols(lane_base + st * 128u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_store_32cols(lane_base + st * 128u + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+          const float2 rs2 = add2(add2(rsp[0], rsp[1]), add2(rsp[2], rsp[3]));
+          l = l * corr + (rs2.x + rs2.y);
+          m = m_use;
+          if (i > 0 && __any_sync(0xFFFFFFFFu, corr != 1.0f)) {
+            // rescaling O needs the previous tile's PV to have landed in it (this tile's
+            // PV, which reads this P, waits for the p_full arrival below)
+            if (!wait_warp(pv_done(pb), pph, kSiteAttnPvDone)) return done = false;
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_load_32cols(lane_base + kAttnOCol + 32u * c, ov);
+              tmem_load_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * corr);
+              tmem_store_32cols(lane_base + kAttnOCol + 32u * c, ov);
+            }
+          }
+          tmem_store_wait();
+          // the previous unit's O is read out of Tensor Memory before this P is handed
+          // over (pb is still that unit's last tile)
+          const bool flush = i == 0 && have_prev;
+          if (flush && !stage_o(pb, pph, l_prev)) return done = false;
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full(st));
+          if (flush) store_o(qt_prev, h_prev, b_prev);
+          pb = sb;
+          pph = sph;
+          if (++sb == kAttnSBufs) {
+            sb = 0;
+            sph ^= 1u;
+          }
+        }
+        have_prev = true;
+        l_prev = l;
+        qt_prev = qt;
+        h_prev = h;
+        b_prev = b;
+        return true;
+      });
+      return done;
+    }();
+    // the last unit's O
+    if (all_ok && have_prev && stage_o(pb, pph, l_prev)) store_o(qt_prev, h_prev, b_prev);
+    // the staging must stay valid until the bulk stores have read it; their global
+    // writes complete before the grid is reported finished
+    if (in_flight && lane == 0) bulk_wait_group_read<0>();
   }
 
   // ------------------------------------------------------------------ teardown --

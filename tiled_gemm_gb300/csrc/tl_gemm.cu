@@ -876,18 +876,19 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
 // (batch, head) through a 4-D map {D, H, S, B} (box {64, 1, 128, 1}: a 64-element
 // chunk of 128 sequence positions), which zero-fills rows past S.
 bool encode_bshd(CUtensorMap* map, tl_dtype dtype, const void* base, int64_t B, int64_t S,
-                 int64_t H, int64_t D) {
+                 int64_t H, int64_t D, uint32_t box_rows) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(H * D * 2),
                                  static_cast<cuuint64_t>(S * H * D * 2)};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(tl::kAttnBN), 1};
+  const cuuint32_t box[4] = {64, 1, box_rows, 1};
   return encode_cached(map, dtype, 4, base, dims, strides, box);
 }
 
 template <int D, bool kBf16>
 tl_status launch_attention(DeviceState* st, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const tl::AttnParams& prm, int64_t grid,
+                           const CUtensorMap& tv, const CUtensorMap& to,
+                           const tl::AttnParams& prm, int64_t grid,
                            cudaStream_t stream) {
   // at least 120 KB, so that two CTAs never share an SM: each allocates all 512 Tensor
   // Memory columns, and a second allocation would wait for the first CTA to finish (the
@@ -915,7 +916,7 @@ tl_status launch_attention(DeviceState* st, const CUtensorMap& tq, const CUtenso
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, prm) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, prm) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_LAUNCH;
   }
@@ -950,9 +951,12 @@ tl_status run_attention(const void* Q, const void* K, const void* V, void* O, in
   for (const void* x : {Q, K, V, static_cast<const void*>(O)}) {
     if ((s = check_device_pointer(x, dev)) != TL_OK) return s;
   }
-  CUtensorMap tq, tk, tv;
-  if (!encode_bshd(&tq, dtype, Q, B, S, H, D) || !encode_bshd(&tk, dtype, K, B, S, H, D) ||
-      !encode_bshd(&tv, dtype, V, B, S, H, D)) {
+  // Q, K, V in boxes of 128 rows; O is stored by each softmax warp in boxes of 32 rows
+  CUtensorMap tq, tk, tv, to;
+  if (!encode_bshd(&tq, dtype, Q, B, S, H, D, tl::kAttnBM) ||
+      !encode_bshd(&tk, dtype, K, B, S, H, D, tl::kAttnBN) ||
+      !encode_bshd(&tv, dtype, V, B, S, H, D, tl::kAttnBN) ||
+      !encode_bshd(&to, dtype, O, B, S, H, D, 32)) {
     return TL_ERR_LAUNCH;
   }
   tl::AttnParams prm;
@@ -981,10 +985,10 @@ tl_status run_attention(const void* Q, const void* K, const void* V, void* O, in
   prm.pair = pair ? 1 : 0;
   const int64_t grid = std::min<int64_t>(items, st->sms);
   if (dtype == TL_BF16)
-    return D == 64 ? launch_attention<64, true>(st, tq, tk, tv, prm, grid, stream)
-                   : launch_attention<128, true>(st, tq, tk, tv, prm, grid, stream);
-  return D == 64 ? launch_attention<64, false>(st, tq, tk, tv, prm, grid, stream)
-                 : launch_attention<128, false>(st, tq, tk, tv, prm, grid, stream);
+    return D == 64 ? launch_attention<64, true>(st, tq, tk, tv, to, prm, grid, stream)
+                   : launch_attention<128, true>(st, tq, tk, tv, to, prm, grid, stream);
+  return D == 64 ? launch_attention<64, false>(st, tq, tk, tv, to, prm, grid, stream)
+                 : launch_attention<128, false>(st, tq, tk, tv, to, prm, grid, stream);
 }
 
 }  // namespace
