@@ -334,12 +334,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t ph;
         bool first;
       };
-      auto pv = [&](const Pending& t) -> bool {
+      auto pv_wait = [&](const Pending& t) -> bool {
+        return wait_fast(p_full(t.b), t.ph, kSiteAttnPFull) &&
+               wait_fast(v_full(t.j & 1), static_cast<uint32_t>(t.j >> 1) & 1u, kSiteAttnKvFull);
+      };
+      auto pv_issue = [&](const Pending& t) {
         const int vs = t.j & 1;                     // V stage of tile j
-        if (!wait_fast(p_full(t.b), t.ph, kSiteAttnPFull)) return false;
-        if (!wait_fast(v_full(vs), static_cast<uint32_t>(t.j >> 1) & 1u, kSiteAttnKvFull))
-          return false;
-        tc_fence_after_sync();
         const uint64_t v_desc = v_desc0 + static_cast<uint64_t>(vs) * (kTile >> 4);
         // P_j is the A operand in Tensor Memory, over S_j: 16 keys = 8 columns per step
 #pragma unroll
@@ -349,10 +349,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      (!t.first || k > 0) ? 1u : 0u);
         }
         mma_commit(pv_done(t.b));         // also releases V stage vs
-        return true;
       };
-      // S_g goes in before PV_{g-2}: while this thread waits for P_{g-2}, the pipe still
-      // holds S_g's products, and the softmax finds S_{g-1} ready when it is done
+      // One batch per key tile: S_g, then PV_{g-2}.  With PV two tiles behind, P_{g-2} is
+      // normally ready by the time K_g is, and the softmax, busy with tile g - 1, needs
+      // S_g only a softmax later.  The batch's barriers are tested together and waited
+      // on only if one is still open: every cycle this thread spends between batches
+      // leaves the tensor pipe idle.
       int g = 0, u = 0;
       int sb = 0;                                  // S buffer of tile g
       uint32_t sph = 0;                            // its phase
@@ -367,8 +369,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int n_kv = kv_tiles(qt);
         for (int i = 0; i < n_kv; ++i, ++g) {
           const int st = g & 1;                     // K stage
-          if (!wait_fast(k_full(st), static_cast<uint32_t>(g >> 1) & 1u, kSiteAttnKvFull))
-            return ok = false;
+          const uint32_t kph = static_cast<uint32_t>(g >> 1) & 1u;
+          const bool with_pv = n_pend == 2;
+          bool ready = mbar_test_wait(k_full(st), kph);
+          if (with_pv)
+            ready = mbar_test_wait(p_full(pend0.b), pend0.ph) &&
+                    mbar_test_wait(v_full(pend0.j & 1), static_cast<uint32_t>(pend0.j >> 1) & 1u) &&
+                    ready;
+          if (!ready) {
+            if (!wait_fast(k_full(st), kph, kSiteAttnKvFull)) return ok = false;
+            if (with_pv && !pv_wait(pend0)) return ok = false;
+          }
           // S buffer sb last held P_{g-3}; PV_{g-3}, issued before this point by this
           // thread, reads it before these MMAs overwrite it (tcgen05 operations of one
           // thread execute in order), so no wait is needed
@@ -382,8 +393,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mma_commit(s_full(sb));           // also releases K stage st
           if (i == n_kv - 1) mma_commit(q_empty(qb));
           const Pending cur{g, sb, sph, i == 0};
-          if (n_pend == 2) {
-            if (!pv(pend0)) return ok = false;
+          if (with_pv) {
+            pv_issue(pend0);
             pend0 = pend1;
             pend1 = cur;
           } else if (n_pend == 1) {
@@ -401,8 +412,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ++u;
         return true;
       });
-      if (ok && n_pend >= 1) ok = pv(pend0);
-      if (ok && n_pend == 2) ok = pv(pend1);
+      if (ok && n_pend >= 1 && (ok = pv_wait(pend0))) {
+        tc_fence_after_sync();
+        pv_issue(pend0);
+      }
+      if (ok && n_pend == 2 && (ok = pv_wait(pend1))) {
+        tc_fence_after_sync();
+        pv_issue(pend1);
+      }
       mma_commit(done_bar);
       if (!wait_bounded<false>(done_bar, 0, nullptr, p.timeout_ns))
         record_timeout(p.status, abort_flag, kSiteAttnDrain);
