@@ -500,8 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       if (p.stall) {
         // Nothing arrives on "done" before the MMA thread itself commits to it below, so
-        // this wait can only run out: the timeout and unwind path under test.
-        if (!wait_bounded<kPair>(done_bar, 0, abort_flag, p.timeout_ns))
+        // this wait can only run out: the timeout and unwind path under test.  It gets
+        // half the limit, so that it runs out before the waits of the other roles, which
+        // start at about the same time and wait for this thread's products.
+        if (!wait_bounded<kPair>(done_bar, 0, abort_flag, p.timeout_ns / 2))
           record_timeout(p.status, abort_flag, kSiteInjected);
         ok = false;
       }
