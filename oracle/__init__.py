@@ -91,6 +91,12 @@ def _load():
         lib.oracle_attention_rows.argtypes = [p, p, p, i64, i64, i64, i64, ci, ci, p, p, p, i64,
                                               p, ci]
         lib.oracle_attention_rows.restype = ci
+        lib.oracle_gemm_mx.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, i64,
+                                       ci, ci, ci, ci, ci]
+        lib.oracle_gemm_mx.restype = ci
+        lib.oracle_gemm_mx_entries.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i64,
+                                               ci, ci, ci, ci, p, p, i64, p, p, ci]
+        lib.oracle_gemm_mx_entries.restype = ci
         lib.oracle_decode8_array.argtypes = [p, p, i64, ci]
         lib.oracle_decode8_array.restype = None
         lib.oracle_max_threads.argtypes = []
@@ -233,6 +239,54 @@ def gemm_fp8(A, B, M: int, N: int, K: int, *, a_fmt: int = E4M3, b_fmt: int = E4
         raise ValueError("oracle_gemm_fp8 rejected its arguments")
     c = c[:, :N]
     return (c, sums) if want_sums else c
+
+
+def gemm_mx(A, B, SA, SB, M: int, N: int, K: int, *, a_fmt: int = E4M3, b_fmt: int = E4M3,
+            out_dtype: int = BF16, lda: int | None = None, ldb: int | None = None,
+            ldc: int | None = None, sfa_ld: int | None = None, sfb_ld: int | None = None,
+            relu: bool = False, threads: int = 0, want_sums: bool = False):
+    """Block-scaled 8-bit product: A [M,K] and B [N,K] K-major codes, SA [M, sfa_ld] and
+    SB [N, sfb_ld] E8M0 codes, one per 32 K elements; uint16 bits (M, N)."""
+    a, b = _as_u8(A).reshape(-1), _as_u8(B).reshape(-1)
+    sa, sb = _as_u8(SA).reshape(-1), _as_u8(SB).reshape(-1)
+    lda = lda if lda is not None else K
+    ldb = ldb if ldb is not None else K
+    ldc = ldc if ldc is not None else N
+    sfa_ld = sfa_ld if sfa_ld is not None else K // 32
+    sfb_ld = sfb_ld if sfb_ld is not None else K // 32
+    c = np.zeros((M, ldc), dtype=np.uint16)
+    sums = np.zeros((M, N), dtype=np.float64) if want_sums else None
+    rc = _load().oracle_gemm_mx(_ptr(a), _ptr(b), _ptr(sa), _ptr(sb), _ptr(c),
+                                _ptr(sums) if sums is not None else None, M, N, K, lda, ldb,
+                                ldc, sfa_ld, sfb_ld, a_fmt, b_fmt, out_dtype, int(relu), threads)
+    if rc != 0:
+        raise ValueError("oracle_gemm_mx rejected its arguments")
+    c = c[:, :N]
+    return (c, sums) if want_sums else c
+
+
+def gemm_mx_entries(A, B, SA, SB, M: int, N: int, K: int, rows, cols, *, a_fmt: int = E4M3,
+                    b_fmt: int = E4M3, out_dtype: int = BF16, lda: int | None = None,
+                    ldb: int | None = None, sfa_ld: int | None = None, sfb_ld: int | None = None,
+                    relu: bool = False, threads: int = 0, want_sums: bool = False):
+    """Selected entries of the block-scaled product, computed one by one."""
+    a, b = _as_u8(A).reshape(-1), _as_u8(B).reshape(-1)
+    sa, sb = _as_u8(SA).reshape(-1), _as_u8(SB).reshape(-1)
+    lda = lda if lda is not None else K
+    ldb = ldb if ldb is not None else K
+    sfa_ld = sfa_ld if sfa_ld is not None else K // 32
+    sfb_ld = sfb_ld if sfb_ld is not None else K // 32
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    cidx = np.ascontiguousarray(cols, dtype=np.int64)
+    out = np.zeros(r.shape, dtype=np.uint16)
+    sums = np.zeros(r.shape, dtype=np.float64) if want_sums else None
+    rc = _load().oracle_gemm_mx_entries(_ptr(a), _ptr(b), _ptr(sa), _ptr(sb), M, N, K, lda, ldb,
+                                        sfa_ld, sfb_ld, a_fmt, b_fmt, out_dtype, int(relu),
+                                        _ptr(r), _ptr(cidx), r.size, _ptr(out),
+                                        _ptr(sums) if sums is not None else None, threads)
+    if rc != 0:
+        raise ValueError("oracle_gemm_mx_entries rejected its arguments")
+    return (out, sums) if want_sums else out
 
 
 def gemm_fp8_entries(A, B, M: int, N: int, K: int, rows, cols, *, a_fmt: int = E4M3,

@@ -338,6 +338,86 @@ void oracle_decode8_array(const uint8_t* in, double* out, int64_t n, int type) {
   for (int64_t t = 0; t < n; ++t) out[t] = decode8(in[t], type);
 }
 
+/* ---- the block-scaled (MX) FP8 GEMM ------------------------------------------
+ *
+ * The pages' block-scaled form: 8-bit operands in which every 32 consecutive K
+ * elements of a row share one power-of-two scale, E8M0 codes SFA (per row of A)
+ * and SFB (per column of the product, i.e. per row of the K-major B) ("NVIDIA
+ * backend codegen" page, section 4.6.3; "TileLang: a tile language one level
+ * below Triton", block-scaled MMA).  Written out:
+ *
+ *   C[i,j] = round_out( epi( sum_{k<K} x_a(A[i,k]) 2^(SFA[i][k/32] - 127)
+ *                                      * x_b(B[j,k]) 2^(SFB[j][k/32] - 127) ) )
+ *
+ * A is [M,K] and B is [N,K], both K-major (the layout of the MX formats, whose
+ * blocks run along K); SFA is [M][sfa_ld] and SFB is [N][sfb_ld] bytes, block b of
+ * row r at r*ld + b.  An E8M0 code e is the value 2^(e - 127) for e < 255; e = 255 is
+ * NaN.  K must be a multiple of the block size 32.  The sum runs over k in order in
+ * binary64 (every scaled product is exact there).
+ */
+static double e8m0(uint8_t e) { return e == 255 ? NAN : ldexp(1.0, (int)e - 127); }
+
+static double dot_mx(const uint8_t* A, const uint8_t* B, const uint8_t* SA, const uint8_t* SB,
+                     int64_t K, int64_t lda, int64_t ldb, int64_t sfa_ld, int64_t sfb_ld,
+                     int a_type, int b_type, int64_t i, int64_t j) {
+  double s = 0.0;
+  for (int64_t k = 0; k < K; ++k) {
+    const double a = decode8(A[i * lda + k], a_type) * e8m0(SA[i * sfa_ld + k / 32]);
+    const double b = decode8(B[j * ldb + k], b_type) * e8m0(SB[j * sfb_ld + k / 32]);
+    s += a * b;
+  }
+  return s;
+}
+
+static int mx_args_ok(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                      int64_t sfa_ld, int64_t sfb_ld, int a_type, int b_type, int out_dtype) {
+  if (M < 0 || N < 0 || K < 0 || K % 32 != 0) return 0;
+  if (!fp8_args_ok(a_type, b_type, out_dtype)) return 0;
+  if (K > 0 && (lda < K || ldb < K || sfa_ld < K / 32 || sfb_ld < K / 32)) return 0;
+  return 1;
+}
+
+int oracle_gemm_mx(const uint8_t* A, const uint8_t* B, const uint8_t* SA, const uint8_t* SB,
+                   uint16_t* C, double* sums, int64_t M, int64_t N, int64_t K, int64_t lda,
+                   int64_t ldb, int64_t ldc, int64_t sfa_ld, int64_t sfb_ld, int a_type,
+                   int b_type, int out_dtype, int relu, int nthreads) {
+  if (!mx_args_ok(M, N, K, lda, ldb, sfa_ld, sfb_ld, a_type, b_type, out_dtype)) return -1;
+  if (M == 0 || N == 0) return 0;
+  if (ldc < N) return -1;
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      const double s =
+          epilogue(dot_mx(A, B, SA, SB, K, lda, ldb, sfa_ld, sfb_ld, a_type, b_type, i, j), relu);
+      if (C) C[i * ldc + j] = encode(s, out_dtype);
+      if (sums) sums[i * N + j] = s;
+    }
+  }
+  return 0;
+}
+
+int oracle_gemm_mx_entries(const uint8_t* A, const uint8_t* B, const uint8_t* SA,
+                           const uint8_t* SB, int64_t M, int64_t N, int64_t K, int64_t lda,
+                           int64_t ldb, int64_t sfa_ld, int64_t sfb_ld, int a_type, int b_type,
+                           int out_dtype, int relu, const int64_t* rows, const int64_t* cols,
+                           int64_t count, uint16_t* out, double* sums, int nthreads) {
+  if (!mx_args_ok(M, N, K, lda, ldb, sfa_ld, sfb_ld, a_type, b_type, out_dtype)) return -1;
+  for (int64_t t = 0; t < count; ++t) {
+    if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+  }
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t t = 0; t < count; ++t) {
+    const double s = epilogue(dot_mx(A, B, SA, SB, K, lda, ldb, sfa_ld, sfb_ld, a_type, b_type,
+                                     rows[t], cols[t]),
+                              relu);
+    if (out) out[t] = encode(s, out_dtype);
+    if (sums) sums[t] = s;
+  }
+  return 0;
+}
+
 /* ---- attention ---------------------------------------------------------------
  *
  * The pages' second workload on the same primitives is the FlashAttention forward

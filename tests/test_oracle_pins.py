@@ -414,6 +414,101 @@ def test_fp8_exact_rational_sums_and_entries():
 
 # ---- attention: O = softmax(Q K^T / sqrt(D)) V, [B, S, H, D] -------------------------
 
+# ---- the block-scaled (MX) FP8 product ---------------------------------------------
+# Pinned against: the plain FP8 oracle (all scales 2^0), a closed form over blocks of
+# ones, a numpy product of torch-decoded operands scaled block by block, an exact
+# scale-shift invariance, and NaN codes.
+
+
+def _mx_codes(rng, shape, fmt):
+    """Random finite 8-bit codes (torch's conversion of normal samples)."""
+    v = torch.from_numpy(rng.normal(0.0, 2.0, shape).astype(np.float32))
+    return v.to(FP8_TORCH[fmt]).view(torch.uint8).numpy()
+
+
+def test_mx_unit_scales_reduce_to_the_fp8_product():
+    rng = np.random.default_rng(41)
+    M, N, K = 9, 11, 96
+    for fa, fb in ((oracle.E4M3, oracle.E4M3), (oracle.E5M2, oracle.E4M3)):
+        A, B = _mx_codes(rng, (M, K), fa), _mx_codes(rng, (N, K), fb)
+        SA = np.full((M, K // 32), 127, np.uint8)
+        SB = np.full((N, K // 32), 127, np.uint8)
+        c, s = oracle.gemm_mx(A, B, SA, SB, M, N, K, a_fmt=fa, b_fmt=fb, want_sums=True)
+        c8, s8 = oracle.gemm_fp8(A, B, M, N, K, a_fmt=fa, b_fmt=fb, trans_b=True,
+                                 want_sums=True)
+        assert np.array_equal(c, c8) and np.array_equal(s, s8)
+
+
+def test_mx_blocks_of_ones_closed_form():
+    # A = B = 1.0: C[i,j] = sum over blocks b of 32 * 2^(SA[i,b]-127) * 2^(SB[j,b]-127)
+    rng = np.random.default_rng(42)
+    M, N, K = 5, 6, 128
+    one = int(_codes8(np.array([1.0]), oracle.E4M3)[0])
+    A = np.full((M, K), one, np.uint8)
+    B = np.full((N, K), one, np.uint8)
+    SA = rng.integers(110, 140, (M, K // 32)).astype(np.uint8)
+    SB = rng.integers(110, 140, (N, K // 32)).astype(np.uint8)
+    _, s = oracle.gemm_mx(A, B, SA, SB, M, N, K, want_sums=True)
+    for i in range(M):
+        for j in range(N):
+            want = sum(Fraction(32) * Fraction(2) ** (int(SA[i, b]) + int(SB[j, b]) - 254)
+                       for b in range(K // 32))
+            assert Fraction(s[i, j]) == want
+
+
+def test_mx_against_numpy_blockwise_scaling():
+    rng = np.random.default_rng(43)
+    M, N, K = 7, 10, 160
+    A, B = _mx_codes(rng, (M, K), oracle.E4M3), _mx_codes(rng, (N, K), oracle.E5M2)
+    SA = rng.integers(115, 135, (M, K // 32)).astype(np.uint8)
+    SB = rng.integers(115, 135, (N, K // 32)).astype(np.uint8)
+    a = torch.from_numpy(A).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    b = torch.from_numpy(B).view(torch.float8_e5m2).to(torch.float64).numpy()
+    a = a * np.repeat(np.exp2(SA.astype(np.float64) - 127), 32, axis=1)
+    b = b * np.repeat(np.exp2(SB.astype(np.float64) - 127), 32, axis=1)
+    _, s = oracle.gemm_mx(A, B, SA, SB, M, N, K, b_fmt=oracle.E5M2, want_sums=True)
+    np.testing.assert_allclose(s, a @ b.T, rtol=1e-13, atol=1e-300)
+    # entries computed one by one agree bit for bit with the full product
+    rows, cols = np.array([0, 3, 6]), np.array([9, 0, 4])
+    c = oracle.gemm_mx(A, B, SA, SB, M, N, K, b_fmt=oracle.E5M2)
+    e = oracle.gemm_mx_entries(A, B, SA, SB, M, N, K, rows, cols, b_fmt=oracle.E5M2)
+    assert np.array_equal(e, c[rows, cols])
+
+
+def test_mx_scale_shift_invariance_and_nan_code():
+    rng = np.random.default_rng(44)
+    M, N, K = 4, 5, 64
+    A, B = _mx_codes(rng, (M, K), oracle.E4M3), _mx_codes(rng, (N, K), oracle.E4M3)
+    SA = rng.integers(120, 130, (M, 2)).astype(np.uint8)
+    SB = rng.integers(120, 130, (N, 2)).astype(np.uint8)
+    _, s0 = oracle.gemm_mx(A, B, SA, SB, M, N, K, want_sums=True)
+    # 2^d on every A scale of block 1 and 2^-d on every B scale of block 1: same sums
+    SA2, SB2 = SA.copy(), SB.copy()
+    SA2[:, 1] += 3
+    SB2[:, 1] -= 3
+    _, s1 = oracle.gemm_mx(A, B, SA2, SB2, M, N, K, want_sums=True)
+    assert np.array_equal(s0, s1)
+    # doubling a row's scales doubles its row of sums exactly
+    SA3 = SA.copy()
+    SA3[2] += 1
+    _, s3 = oracle.gemm_mx(A, B, SA3, SB, M, N, K, want_sums=True)
+    assert np.array_equal(s3[2], 2 * s0[2]) and np.array_equal(np.delete(s3, 2, 0), np.delete(s0, 2, 0))
+    # E8M0 255 is NaN: only the rows it scales become NaN
+    SA4 = SA.copy()
+    SA4[1, 0] = 255
+    _, s4 = oracle.gemm_mx(A, B, SA4, SB, M, N, K, want_sums=True)
+    assert np.all(np.isnan(s4[1])) and np.all(np.isfinite(np.delete(s4, 1, 0)))
+
+
+def test_mx_rejects_bad_arguments():
+    A = np.zeros((4, 48), np.uint8)
+    S = np.zeros((4, 2), np.uint8)
+    with pytest.raises(ValueError):
+        oracle.gemm_mx(A, A, S, S, 4, 4, 48)                 # K not a multiple of 32
+    with pytest.raises(ValueError):
+        oracle.gemm_mx(A, A, S, S, 4, 4, 32, sfa_ld=0)       # scale rows too short
+
+
 def _t16(x, dtype):
     return torch.as_tensor(np.asarray(x, np.float32)).to(
         torch.float16 if dtype == oracle.F16 else torch.bfloat16)
