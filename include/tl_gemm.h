@@ -272,6 +272,35 @@ tl_status tl_device_status(int reset, uint32_t* detail);
 void tl_set_wait_timeout_ns(uint64_t ns);
 
 /*
+ * Block-scaled 8-bit GEMM (the MX formats): 8-bit operands in which every 32
+ * consecutive K elements of a row share one power-of-two scale ("NVIDIA backend
+ * codegen" page, section 4.6.3: the block-scaled MMA, tcgen05 kind::mxf8f6f4 with
+ * the scale factors in Tensor Memory):
+ *
+ *   C[i*ldc+j] = epi( sum_k x(A[i*lda+k]) 2^(SFA[i*sfa_ld+k/32] - 127)
+ *                           * x(B[j*ldb+k]) 2^(SFB[j*sfb_ld+k/32] - 127) )
+ *
+ *   A        device pointer, M x K codes of a_type (TL_E4M3 or TL_E5M2), K-major.
+ *   B        device pointer, N x K codes of b_type, K-major (the MX layout: C = A B^T).
+ *   SFA/SFB  device pointers to E8M0 scale codes (the value 2^(e-127); 255 is NaN),
+ *            one byte per 32-element block of each row of A / B.  Their row pitches
+ *            sfa_ld / sfb_ld are in bytes, multiples of 4 and at least 4*ceil(K/128)
+ *            (whole groups of four blocks; codes of blocks past K/32 are ignored).
+ *   C        device pointer, M x N of c_type (TL_F16 or TL_BF16), rounded once from
+ *            the fp32 accumulator; epilogue TL_EPI_NONE or TL_EPI_RELU.
+ * K must be a multiple of 32 (TL_ERR_INVALID_ARG).  A and B must be 16-byte aligned
+ * with lda, ldb multiples of 16; SFA, SFB 4-byte aligned; C 2-byte aligned
+ * (TL_ERR_ALIGNMENT otherwise).  C must not overlap an input (TL_ERR_ALIAS).
+ * M or N == 0: TL_OK, nothing launched; K == 0: C = 0.  Asynchronous on `stream`;
+ * the caller owns every buffer; errors are returned before anything is enqueued, a
+ * device-side timeout is read with tl_device_status().
+ */
+tl_status tl_gemm_mx(const void* A, const void* B, const void* SFA, const void* SFB, void* C,
+                     int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                     int64_t sfa_ld, int64_t sfb_ld, tl_dtype a_type, tl_dtype b_type,
+                     tl_dtype c_type, tl_epilogue epilogue, tl_stream_t stream);
+
+/*
  * Attention forward pass: O = softmax(Q K^T / sqrt(D)) V for every batch and head,
  * optionally causal (query i attends to keys j <= i).  This is the pages' second
  * workload on the same tile primitives ("TileLang: a tile language one level below

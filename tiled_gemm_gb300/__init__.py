@@ -83,6 +83,9 @@ def _load() -> ctypes.CDLL:
     lib.tl_gemm_fp8.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, ci,
                                 ctypes.c_float, ci, ctypes.POINTER(Plan), p]
     lib.tl_gemm_fp8.restype = ci
+    lib.tl_gemm_mx.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, i64, ci, ci, ci,
+                               ci, p]
+    lib.tl_gemm_mx.restype = ci
     lib.tl_gemm_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, p]
     lib.tl_gemm_noalloc.restype = ci
     lib.tl_gemm_noalloc_scratch_bytes.argtypes = []
@@ -120,6 +123,14 @@ def tl_gemm_with_plan(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, 
                       plan: Plan, stream: int) -> int:
     return _lib.tl_gemm_with_plan(A, B, C, M, N, K, lda, ldb, ldc, dtype, trans_a, trans_b,
                                   epilogue, ctypes.byref(plan), stream)
+
+
+def tl_gemm_mx(A: int, B: int, SFA: int, SFB: int, C: int, M: int, N: int, K: int, lda: int,
+               ldb: int, ldc: int, sfa_ld: int, sfb_ld: int, a_type: int, b_type: int,
+               c_type: int, epilogue: int, stream: int) -> int:
+    """Raw block-scaled 8-bit call (K-major codes, E8M0 scales per 32 K); returns tl_status."""
+    return _lib.tl_gemm_mx(A, B, SFA, SFB, C, M, N, K, lda, ldb, ldc, sfa_ld, sfb_ld, a_type,
+                           b_type, c_type, epilogue, stream)
 
 
 def tl_gemm_fp8(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
@@ -313,6 +324,40 @@ def gemm_fp8(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool =
                      TL_EPI_RELU if relu else TL_EPI_NONE, plan, s.cuda_stream)
     if st != TL_OK:
         raise TLError(st, "tl_gemm_fp8")
+    return out
+
+
+def gemm_mx(a, b, sfa, sfb, *, relu: bool = False, out_dtype=None, out=None, stream=None):
+    """C = epi(A B^T) in a block-scaled 8-bit format, on the current device.
+
+    ``a`` [M, K] and ``b`` [N, K] are K-major torch.float8_e4m3fn / torch.float8_e5m2
+    tensors; ``sfa`` [M, >= 4*ceil(K/128)] and ``sfb`` [N, ...] are uint8 E8M0 scale
+    codes, one per 32 elements of K.  The output is ``out_dtype`` (torch.bfloat16 by
+    default, or torch.float16), or ``out``'s dtype when ``out`` is given.
+    """
+    torch = _torch()
+    if not all(t.is_cuda for t in (a, b, sfa, sfb)):
+        raise ValueError("a, b, sfa and sfb must be CUDA tensors")
+    if sfa.dtype != torch.uint8 or sfb.dtype != torch.uint8:
+        raise ValueError("the scales must be uint8 E8M0 codes")
+    at, bt = _fp8_code(a), _fp8_code(b)
+    M, K = a.size(0), a.size(1)
+    N = b.size(0)
+    if b.size(1) != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {b.size(1)}")
+    if out is None:
+        odt = out_dtype if out_dtype is not None else torch.bfloat16
+        out = torch.empty((M, N), dtype=odt, device=a.device)
+    elif tuple(out.shape) != (M, N):
+        raise ValueError("out has the wrong shape")
+    ct = _dtype_code(out)
+    s = stream if stream is not None else torch.cuda.current_stream(a.device)
+    st = tl_gemm_mx(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), out.data_ptr(),
+                    M, N, K, _ld(a, "a"), _ld(b, "b"), _ld(out, "out"), _ld(sfa, "sfa"),
+                    _ld(sfb, "sfb"), at, bt, ct, TL_EPI_RELU if relu else TL_EPI_NONE,
+                    s.cuda_stream)
+    if st != TL_OK:
+        raise TLError(st, "tl_gemm_mx")
     return out
 
 

@@ -1,0 +1,327 @@
+// mx_kernel.cuh -- block-scaled 8-bit GEMM (the MX formats) on tcgen05.
+//
+// C = epi( sum_k x_a(A[i,k]) 2^(SFA[i][k/32] - 127) * x_b(B[j,k]) 2^(SFB[j][k/32] - 127) )
+// with A [M,K] and B [N,K] K-major E4M3/E5M2 codes and one E8M0 scale per 32 K elements
+// of every row ("NVIDIA backend codegen" page, section 4.6.3: the Blackwell form of the
+// block-scaled MMA, tcgen05 kind::mxf8f6f4.block_scale with the scale factors already
+// in Tensor Memory).  fp32 accumulation in Tensor Memory; fp16 or bf16 out.
+//
+// One CTA per 128 x 128 tile of C, 256 threads:
+//   warp 0 (one thread)  TMA producer: a stage is 128 K bytes of A (128 rows) and of B
+//                        (128 rows), 128-byte swizzle, S stages in a ring.
+//   warp 1 (one thread)  MMA issuer (and the Tensor Memory allocation): per stage four
+//                        128 x 128 x 32 block-scaled MMAs, one per 32-element block, the
+//                        scale byte of block k selected by the descriptor's scale ids.
+//   warps 4-7            scale loaders, then the epilogue.  Only the warp of a lane
+//                        quadrant can write its Tensor Memory lanes, so these four warps
+//                        put each stage's scales there (tcgen05.st) ahead of the MMA;
+//                        after the last stage they read the accumulator, apply ReLU,
+//                        cast and store the tile.
+//
+// Scale layout in Tensor Memory for M = N = 128 and one scale per 32 elements (found
+// with an exact probe: operands of ones, distinct power-of-two scales), four columns
+// per operand per stage, each 32-bit word holding the scales of the stage's four
+// blocks in its four bytes (byte k = the scale id of MMA k):
+//   A: row i reads lane i, column sfa + i/32;
+//   B: column j of the product, for rows in lane quadrant q, reads lane 32q + j%32,
+//      column sfb + j/32 -- so B's words are written into every quadrant.
+// Both scale addresses stay on 4-column boundaries (an unaligned one is a misaligned
+// address fault).
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace tl {
+
+constexpr int kMxBM = 128;
+constexpr int kMxBN = 128;
+constexpr int kMxBK = 128;          // K bytes (= elements) per stage: four 32-element blocks
+constexpr int kMxStages = 4;
+constexpr int kMxThreads = 256;
+constexpr uint32_t kMxStageBytes = 2u * kMxBM * kMxBK;   // A + B
+constexpr uint32_t kMxTmemCols = 256;                     // accumulator 0-127, scales 128-
+constexpr uint32_t kMxSfCol = 128;                        // stage s: A at +8s, B at +8s+4
+
+enum MxWaitSite : uint32_t {
+  kSiteMxEmpty = 31,
+  kSiteMxFull = 32,
+  kSiteMxScales = 33,
+  kSiteMxAcc = 34,
+  kSiteMxDrain = 35,
+};
+
+struct MxParams {
+  int32_t M, N, K;
+  int32_t k_blocks;           // ceil(K / 128)
+  const uint8_t* SA;          // [M][sfa_ld] E8M0, 4-byte aligned, sfa_ld % 4 == 0
+  const uint8_t* SB;          // [N][sfb_ld]
+  int64_t sfa_ld, sfb_ld;     // >= 4 * k_blocks
+  void* C;
+  int64_t ldc;
+  int32_t relu;
+  int32_t c_vec;              // C and ldc allow 16-byte stores
+  uint32_t idesc;             // formats, K-major both, N 128, M 128, E8M0 scales
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+__host__ __device__ constexpr uint32_t mx_smem_bytes() {
+  return 1024u + kMxStages * kMxStageBytes + 8u * (3 * kMxStages + 1) + 16u + 4u * kMxStages;
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scales: B scale id (bits 4-5),
+// A and B formats (7-9, 10-12: E4M3 = 0, E5M2 = 1), both K-major (15, 16 = 0), N >> 3
+// (17-22), scale format E8M0 (bit 23), M >> 4 (24-28), A scale id (29-30).
+__host__ __device__ constexpr uint32_t mma_idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t m,
+                                                    uint32_t n) {
+  return (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t mx_scale_ids(uint32_t idesc, uint32_t k) {
+  return idesc | (k << 4) | (k << 29);
+}
+
+__device__ __forceinline__ void mma_mx_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_store_1col(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_store_4cols(uint32_t taddr, uint32_t a, uint32_t b,
+                                                 uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// The four scale bytes of stage kb of one row: an aligned 32-bit word; rows past the
+// matrix and blocks past K read as 2^0 (their operands are zero, and a NaN code there
+// must not reach the sum).
+__device__ __forceinline__ uint32_t mx_scale_word(const uint8_t* S, int64_t ld, int row,
+                                                  int rows, int kb, int n_blk) {
+  if (row >= rows) return 0x7F7F7F7Fu;
+  uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(S + static_cast<int64_t>(row) * ld + 4 * kb));
+  const int valid = n_blk - 4 * kb;
+  if (valid < 4) {
+    const uint32_t keep = (1u << (8 * valid)) - 1u;
+    w = (w & keep) | (0x7F7F7F7Fu & ~keep);
+  }
+  return w;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    tl_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b, const MxParams p) {
+  constexpr int S = kMxStages;
+  constexpr uint32_t kA = kMxBM * kMxBK;           // bytes of A per stage
+  grid_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const uint32_t sBar = base + S * kMxStageBytes;
+  auto full = [&](int s) { return sBar + 8u * s; };
+  auto empty = [&](int s) { return sBar + 8u * (S + s); };
+  auto sf_full = [&](int s) { return sBar + 8u * (2 * S + s); };
+  const uint32_t acc_full = sBar + 8u * (3 * S);
+  const uint32_t slot = acc_full + 8u;
+  volatile uint32_t* const tmem_slot_ptr =
+      reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
+  volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
+  volatile int32_t* const lap_armed = reinterpret_cast<volatile int32_t*>(tmem_slot_ptr + 4);  // [S]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m0 = static_cast<int>(blockIdx.y) * kMxBM;
+  const int n0 = static_cast<int>(blockIdx.x) * kMxBN;
+  const int n_blk = p.K / 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+      mbar_init(sf_full(s), 4);
+      lap_armed[s] = -1;
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 64) {
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, kMxTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot_ptr;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer --
+    if (lane == 0) {
+      grid_dependency_wait();
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int s = kb % S;
+        const int lap = kb / S;
+        if (!wait_bounded<false>(empty(s), (static_cast<uint32_t>(lap) & 1u) ^ 1u, abort_flag,
+                                 p.timeout_ns)) {
+          record_timeout(p.status, abort_flag, kSiteMxEmpty);
+          break;
+        }
+        mbar_arrive_expect_tx(full(s), kMxStageBytes);
+        const uint32_t dst = base + s * kMxStageBytes;
+        tma_load_2d(dst, &tmap_a, full(s), kb * kMxBK, m0);
+        tma_load_2d(dst + kA, &tmap_b, full(s), kb * kMxBK, n0);
+        lap_armed[s] = lap;
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer --
+    grid_dependency_wait();
+    if (lane == 0) {
+      const uint64_t a_desc0 = smem_desc_sw128(base, 16u, 1024u);
+      const uint64_t b_desc0 = smem_desc_sw128(base + kA, 16u, 1024u);
+      bool ok = true;
+      for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = static_cast<uint32_t>(kb / S) & 1u;
+        if (!wait_bounded<false>(full(s), ph, abort_flag, p.timeout_ns)) {
+          record_timeout(p.status, abort_flag, kSiteMxFull);
+          ok = false;
+          break;
+        }
+        if (!wait_bounded<false>(sf_full(s), ph, abort_flag, p.timeout_ns)) {
+          record_timeout(p.status, abort_flag, kSiteMxScales);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t stage = (static_cast<uint64_t>(s) * kMxStageBytes) >> 4;
+        const uint32_t sfa = tmem_base + kMxSfCol + 8u * s;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          // 32 K bytes per MMA: 32 B along the 128-byte swizzled row
+          mma_mx_ss(tmem_base, a_desc0 + stage + 2u * k, b_desc0 + stage + 2u * k,
+                    mx_scale_ids(p.idesc, static_cast<uint32_t>(k)), sfa, sfa + 4u,
+                    (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(empty(s));             // frees the stage's operands and scales
+      }
+      if (ok) mma_commit(acc_full);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------- scales, then epilogue --
+    grid_dependency_wait();
+    const int q = warp & 3;                         // Tensor Memory lane quadrant
+    const int row = q * 32 + lane;                  // this thread's row of the tile
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    auto wait_warp = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
+      bool r = true;
+      if (lane == 0) r = wait_bounded<false>(bar, parity, abort_flag, p.timeout_ns);
+      __syncwarp();
+      r = __shfl_sync(0xFFFFFFFFu, r ? 1 : 0, 0) != 0;
+      if (!r && lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, site);
+      return r;
+    };
+    bool ok = true;
+    // this thread's words of stage kb: A for row m0 + row, B for columns n0 + 32c + lane
+    auto load_words = [&](int kb, uint32_t& wa, uint32_t (&wb)[4]) {
+      wa = mx_scale_word(p.SA, p.sfa_ld, m0 + row, p.M, kb, n_blk);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) wb[c] = mx_scale_word(p.SB, p.sfb_ld, n0 + 32 * c + lane, p.N, kb, n_blk);
+    };
+    uint32_t wa = 0, wb[4] = {0, 0, 0, 0};
+    if (p.k_blocks > 0) load_words(0, wa, wb);
+    for (int kb = 0; kb < p.k_blocks; ++kb) {
+      const int s = kb % S;
+      // the next stage's words are loaded before this stage's wait, so their latency
+      // runs under it
+      uint32_t na = 0, nb[4] = {0, 0, 0, 0};
+      if (kb + 1 < p.k_blocks) load_words(kb + 1, na, nb);
+      if (!(ok = wait_warp(empty(s), (static_cast<uint32_t>(kb / S) & 1u) ^ 1u, kSiteMxEmpty)))
+        break;
+      tc_fence_after_sync();
+      const uint32_t col = kMxSfCol + 8u * s;
+      tmem_store_1col(lane_base + col + static_cast<uint32_t>(q), wa);
+      tmem_store_4cols(lane_base + col + 4u, wb[0], wb[1], wb[2], wb[3]);
+      tmem_store_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sf_full(s));
+      wa = na;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) wb[c] = nb[c];
+    }
+    if (ok && wait_warp(acc_full, 0, kSiteMxAcc)) {
+      tc_fence_after_sync();
+      const int gi = m0 + row;
+      uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(gi) * p.ldc;
+#pragma unroll 1
+      for (int c = 0; c < kMxBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_load_32cols(lane_base + 32u * c, v);
+        tmem_load_wait();
+        if (gi >= p.M) continue;
+        uint32_t o2[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float x0 = __uint_as_float(v[2 * j]), x1 = __uint_as_float(v[2 * j + 1]);
+          if (p.relu) {
+            x0 = x0 > 0.0f ? x0 : 0.0f;
+            x1 = x1 > 0.0f ? x1 : 0.0f;
+          }
+          o2[j] = pack2<kBf16, false>(x0, x1);
+        }
+        const int gj = n0 + 32 * c;
+        if (p.c_vec && gj + 32 <= p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(crow + gj);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (gj + j < p.N) crow[gj + j] = static_cast<uint16_t>(o2[j >> 1] >> (16 * (j & 1)));
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown --
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // every load issued must have landed before the CTA exits
+    for (int s = 0; s < S; ++s) {
+      const int lap = lap_armed[s];
+      if (lap >= 0 && !wait_bounded<false>(full(s), static_cast<uint32_t>(lap) & 1u, nullptr,
+                                           p.timeout_ns)) {
+        record_timeout(p.status, abort_flag, kSiteMxDrain);
+      }
+    }
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kMxTmemCols);
+  }
+}
+
+}  // namespace tl

@@ -25,6 +25,7 @@
 
 #include "attn_kernel.cuh"
 #include "gemm_kernel.cuh"
+#include "mx_kernel.cuh"
 #include "tl_gemm.h"
 
 namespace {
@@ -387,7 +388,7 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
 template <int BN, int CG, int BK, int EB = 2>
 int prepare_kernel(DeviceState* st) {
   // slot of this kernel in the per-device caches: 0-11 the 16-bit tilings, 12-13 the
-  // narrow ones, 16-27 the 8-bit ones
+  // narrow ones, 16-27 the 8-bit ones (14-15: the block-scaled kernel, 28-31: attention)
   constexpr int kIdx = BN < 64 ? 12 + (BN == 32)
                                : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) +
                                      6 * (BK * EB == 256) + 16 * (EB == 1);
@@ -991,6 +992,111 @@ tl_status run_attention(const void* Q, const void* K, const void* V, void* O, in
                  : launch_attention<128, false>(st, tq, tk, tv, to, prm, grid, stream);
 }
 
+// ---- the block-scaled (MX) 8-bit GEMM ---------------------------------------------
+tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, void* C,
+                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                 int64_t sfa_ld, int64_t sfb_ld, tl_dtype a_type, tl_dtype b_type,
+                 tl_dtype c_type, tl_epilogue epilogue, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || K % 32 != 0) return TL_ERR_INVALID_ARG;
+  if (!is_fp8(a_type) || !is_fp8(b_type)) return TL_ERR_INVALID_ARG;
+  if (c_type != TL_F16 && c_type != TL_BF16) return TL_ERR_INVALID_ARG;
+  if (epilogue != TL_EPI_NONE && epilogue != TL_EPI_RELU) return TL_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return TL_OK;
+  if (M > INT32_MAX - tl::kMxBM || N > INT32_MAX - tl::kMxBN || K > INT32_MAX - tl::kMxBK)
+    return TL_ERR_UNSUPPORTED;
+  if (ldc < N) return TL_ERR_INVALID_ARG;
+  if (C == nullptr) return TL_ERR_NULL_PTR;
+  if (reinterpret_cast<uintptr_t>(C) & 1u) return TL_ERR_ALIGNMENT;
+  const int64_t k_blocks = ceil_div(K, tl::kMxBK);
+  if (K > 0) {
+    if (lda < K || ldb < K || sfa_ld < 4 * k_blocks || sfb_ld < 4 * k_blocks)
+      return TL_ERR_INVALID_ARG;
+    if (A == nullptr || B == nullptr || SA == nullptr || SB == nullptr) return TL_ERR_NULL_PTR;
+    // operands straight to the TMA unit; the scales as aligned 32-bit words
+    if (!tma_ok(A, lda, 1) || !tma_ok(B, ldb, 1)) return TL_ERR_ALIGNMENT;
+    if (((reinterpret_cast<uintptr_t>(SA) | reinterpret_cast<uintptr_t>(SB)) & 3u) ||
+        (sfa_ld & 3) || (sfb_ld & 3))
+      return TL_ERR_ALIGNMENT;
+    uintptr_t c0, c1, x0, x1;
+    extent(C, M, N, ldc, &c0, &c1);
+    const struct { const void* p; int64_t rows, cols, ld; } ins[4] = {
+        {A, M, K, lda}, {B, N, K, ldb}, {SA, M, 4 * k_blocks, sfa_ld}, {SB, N, 4 * k_blocks, sfb_ld}};
+    for (const auto& in : ins) {
+      extent(in.p, in.rows, in.cols, in.ld, &x0, &x1, 1);
+      if (overlaps(c0, c1, x0, x1)) return TL_ERR_ALIAS;
+    }
+  }
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (st == nullptr) return TL_ERR_DEVICE;
+  if (!st->sm103) return TL_ERR_UNSUPPORTED;
+  tl_status s;
+  if ((s = check_device_pointer(C, dev)) != TL_OK) return s;
+  if (K == 0) {
+    tl::tl_fill_zero_kernel<<<launch_blocks_for(M * N), 256, 0, stream>>>(static_cast<uint16_t*>(C),
+                                                                         M, N, ldc);
+    return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_LAUNCH;
+  }
+  for (const void* x : {A, B, SA, SB}) {
+    if ((s = check_device_pointer(x, dev)) != TL_OK) return s;
+  }
+  CUtensorMap ta, tb;
+  if (!encode_2d(&ta, a_type, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(lda), tl::kMxBK, tl::kMxBM) ||
+      !encode_2d(&tb, b_type, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(ldb), tl::kMxBK, tl::kMxBN)) {
+    return TL_ERR_LAUNCH;
+  }
+  tl::MxParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.M = static_cast<int32_t>(M);
+  prm.N = static_cast<int32_t>(N);
+  prm.K = static_cast<int32_t>(K);
+  prm.k_blocks = static_cast<int32_t>(k_blocks);
+  prm.SA = static_cast<const uint8_t*>(SA);
+  prm.SB = static_cast<const uint8_t*>(SB);
+  prm.sfa_ld = sfa_ld;
+  prm.sfb_ld = sfb_ld;
+  prm.C = C;
+  prm.ldc = ldc;
+  prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
+  prm.c_vec = tma_ok(C, ldc) ? 1 : 0;
+  prm.idesc = tl::mma_idesc_mx(a_type == TL_E5M2 ? 1u : 0u, b_type == TL_E5M2 ? 1u : 0u,
+                               tl::kMxBM, tl::kMxBN);
+  prm.status = st->status;
+  prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  constexpr uint32_t kSmem = tl::mx_smem_bytes();
+  if (static_cast<int64_t>(kSmem) > st->smem_optin) return TL_ERR_UNSUPPORTED;
+  const bool bf16 = c_type == TL_BF16;
+  auto kern = bf16 ? tl::tl_gemm_mx_kernel<true> : tl::tl_gemm_mx_kernel<false>;
+  const uint32_t bit = 1u << (14 + (bf16 ? 1 : 0));      // attribute slots 14, 15
+  if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
+    std::lock_guard<std::mutex> lock(st->mu);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmem)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TL_ERR_LAUNCH;
+    }
+    st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(N, tl::kMxBN)),
+                     static_cast<unsigned>(ceil_div(M, tl::kMxBM)));
+  cfg.blockDim = dim3(tl::kMxThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, prm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TL_ERR_LAUNCH;
+  }
+  return TL_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1011,6 +1117,14 @@ tl_status tl_gemm_with_plan(const void* A, const void* B, void* C, int64_t M, in
   if (dtype != TL_F16 && dtype != TL_BF16) return TL_ERR_INVALID_ARG;
   return run(A, B, C, M, N, K, lda, ldb, ldc, types_16(dtype), trans_a, trans_b, epilogue, plan,
              reinterpret_cast<cudaStream_t>(stream));
+}
+
+tl_status tl_gemm_mx(const void* A, const void* B, const void* SFA, const void* SFB, void* C,
+                     int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                     int64_t sfa_ld, int64_t sfb_ld, tl_dtype a_type, tl_dtype b_type,
+                     tl_dtype c_type, tl_epilogue epilogue, tl_stream_t stream) {
+  return run_mx(A, B, SFA, SFB, C, M, N, K, lda, ldb, ldc, sfa_ld, sfb_ld, a_type, b_type, c_type,
+                epilogue, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tl_status tl_gemm_fp8(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,

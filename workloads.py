@@ -171,6 +171,95 @@ for _n, _seed in ((4096, 8), (8192, 9)):
                   description=f"FP8 GEMM {_n}^3, E4M3 operands from N(0,1), B column-major, "
                               "alpha 1/64, bf16 output"))
 
+# ---- block-scaled (MX) 8-bit products: A [M,K], B [N,K], one E8M0 scale per 32 K ----
+
+@dataclasses.dataclass(frozen=True)
+class MxWorkload:
+    name: str
+    M: int
+    N: int
+    K: int
+    a_fmt: int = E4M3
+    b_fmt: int = E4M3
+    out_dtype: int = BF16
+    relu: bool = False
+    dist: str = "mx"        # "mx": N(0, std) values quantised block by block (below);
+                            # otherwise codes converted from draws of _draw and scale
+                            # codes drawn uniformly in [sf_lo, sf_hi]
+    std: float = 1.0
+    sf_lo: int = 120
+    sf_hi: int = 134
+    sf_pad: int = 0         # extra scale bytes per row beyond 4*ceil(K/128)
+    seed: int = 0
+    description: str = ""
+
+    @property
+    def sf_ld(self) -> int:
+        return 4 * ((self.K + 127) // 128) + self.sf_pad
+
+    @property
+    def c_torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPE[self.out_dtype]
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def bytes_moved(self) -> int:
+        return (self.M + self.N) * (self.K + self.sf_ld) + 2 * self.M * self.N
+
+
+# largest normal exponent and value of each 8-bit element format
+_FP8_EMAX = {E4M3: (8, 448.0), E5M2: (15, 57344.0)}
+
+
+def _mx_quantise(x: torch.Tensor, fmt: int, sf_ld: int):
+    """The usual MX encoding of fp32 rows x [rows, K]: per block of 32, the shared
+    exponent is floor(log2(max |x|)) minus the element format's largest exponent (as an
+    E8M0 code, clamped to [0, 254]), and the elements are x / 2^exponent converted to
+    the 8-bit format, clamped to its largest normal value.  Scale bytes past K/32 are
+    the code of 2^0."""
+    rows, K = x.shape
+    blk = x.reshape(rows, K // 32, 32)
+    amax = blk.abs().amax(dim=-1).clamp_min(2.0 ** -120)
+    emax, vmax = _FP8_EMAX[fmt]
+    e = (torch.floor(torch.log2(amax)) - emax).clamp(-127, 127)
+    q = (blk / torch.exp2(e).unsqueeze(-1)).clamp(-vmax, vmax)
+    codes = q.reshape(rows, K).to(_TORCH_DTYPE[fmt])
+    sf = torch.full((rows, sf_ld), 127, dtype=torch.uint8)
+    sf[:, :K // 32] = (e + 127).to(torch.uint8)
+    return codes, sf
+
+
+def make_mx_inputs(w: MxWorkload, seed: int | None = None):
+    """CPU tensors (A, B, SA, SB): 8-bit A [M,K] and B [N,K] and uint8 scale codes
+    SA [M, sf_ld] and SB [N, sf_ld].  dist "mx": A's then B's N(0, std) values, each
+    quantised by _mx_quantise; otherwise A's and B's codes from _draw, then SA and SB
+    uniform in [sf_lo, sf_hi]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    if w.dist == "mx":
+        xa = torch.randn((w.M, w.K), generator=g, dtype=torch.float32) * w.std
+        xb = torch.randn((w.N, w.K), generator=g, dtype=torch.float32) * w.std
+        a, sa = _mx_quantise(xa, w.a_fmt, w.sf_ld)
+        b, sb = _mx_quantise(xb, w.b_fmt, w.sf_ld)
+        return a, b, sa, sb
+    a = _draw((w.M, w.K), w.dist, w.std, w.K, g).to(_TORCH_DTYPE[w.a_fmt])
+    b = _draw((w.N, w.K), w.dist, w.std, w.K, g).to(_TORCH_DTYPE[w.b_fmt])
+    sa = torch.randint(w.sf_lo, w.sf_hi + 1, (w.M, w.sf_ld), generator=g).to(torch.uint8)
+    sb = torch.randint(w.sf_lo, w.sf_hi + 1, (w.N, w.sf_ld), generator=g).to(torch.uint8)
+    return a, b, sa, sb
+
+
+MX_WORKLOADS: dict[str, MxWorkload] = {}
+for _n, _seed in ((4096, 30), (8192, 31)):
+    _w = MxWorkload(f"gemm_mx_{_n}_e4m3", _n, _n, _n, seed=_seed,
+                    description=f"block-scaled 8-bit GEMM {_n}^3: N(0,1) operands in the MX "
+                                "encoding (E4M3 elements, one E8M0 scale per 32 K), bf16 "
+                                "output")
+    MX_WORKLOADS[_w.name] = _w
+
 # ---- attention forward: O = softmax(Q K^T / sqrt(D)) V over [B, S, H, D] ------------
 
 @dataclasses.dataclass(frozen=True)
