@@ -40,7 +40,8 @@ import workloads  # noqa: E402
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["tiled_gemm_gb300/csrc/gemm_kernel.cuh", "tiled_gemm_gb300/csrc/sm103_ptx.cuh",
-                  "tiled_gemm_gb300/csrc/attn_kernel.cuh", "tiled_gemm_gb300/csrc/tl_gemm.cu"]
+                  "tiled_gemm_gb300/csrc/attn_kernel.cuh", "tiled_gemm_gb300/csrc/mx_kernel.cuh",
+                  "tiled_gemm_gb300/csrc/tl_gemm.cu"]
 
 
 def kernel_source_hash() -> str:
@@ -187,6 +188,27 @@ def oracle_rate(w: workloads.Workload, a_cpu, b_cpu, budget_s: float, threads: i
         dt = time.perf_counter() - t0
         elapsed += dt
         done_flops += 2 * M_s * w.N * w.K
+        reps += 1
+        if dt < budget_s / 20 and rows < w.M:
+            rows = min(w.M, rows * 2)
+    return done_flops / elapsed / 1e12, elapsed, done_flops, rows, reps
+
+
+def oracle_rate_mx(w: workloads.MxWorkload, a_cpu, b_cpu, sa_cpu, budget_s: float, sb_cpu,
+                   threads: int):
+    """Oracle TFLOP/s of the block-scaled product on whole-row slices, for ~budget_s."""
+    import oracle
+    oracle.build()
+    rows = max(1, min(w.M, 8))
+    done_flops, elapsed, reps = 0, 0.0, 0
+    while elapsed < budget_s:
+        t0 = time.perf_counter()
+        oracle.gemm_mx(a_cpu[:rows].contiguous(), b_cpu, sa_cpu[:rows].contiguous(), sb_cpu,
+                       rows, w.N, w.K, a_fmt=w.a_fmt, b_fmt=w.b_fmt, out_dtype=w.out_dtype,
+                       sfa_ld=w.sf_ld, sfb_ld=w.sf_ld, relu=w.relu, threads=threads)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done_flops += 2 * rows * w.N * w.K
         reps += 1
         if dt < budget_s / 20 and rows < w.M:
             rows = min(w.M, rows * 2)
@@ -412,6 +434,37 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
             tl.tl_plan_complete(w.M, w.N, w.K, *w.plan, dtype=w.dtype).as_dict()}
 
 
+def run_mx(args, w: workloads.MxWorkload, rank: int, world: int, dist) -> dict:
+    import torch
+
+    import tiled_gemm_gb300 as tl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ins_cpu = workloads.make_mx_inputs(w)
+    rot = 1 if w.bytes_moved >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / w.bytes_moved))
+    first = [x.to(dev) for x in ins_cpu]
+    sets = [(first if i == 0 else [x.clone() for x in first]) +
+            [torch.empty((w.M, w.N), dtype=w.c_torch_dtype, device=dev)] for i in range(rot)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(ins, out):
+        tl.gemm_mx(ins[0], ins[1], ins[2], ins[3], relu=w.relu, out=out, stream=stream)
+
+    def step(i):
+        st = sets[i % rot]
+        call(st[:4], st[4])
+
+    max_ms, clk = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_pipeline(args, list(ins_cpu), (w.M, w.N), w.c_torch_dtype, call, w.flops,
+                           world, stream, dist, dev, tl)
+    return {"total_ms": max_ms, "clocks": clk, "e2e": e2e, "rotation_sets": rot,
+            "launches_per_step": 1,
+            "plan": {"tile": [128, 128, 128], "stages": 4, "cta_group": 1,
+                     "grid": [math.ceil(w.N / 128), math.ceil(w.M / 128)]}}
+
+
 def run_attn(args, w: workloads.AttnWorkload, rank: int, world: int, dist) -> dict:
     import torch
 
@@ -473,7 +526,8 @@ def main():
                     help="timed steps; 0 (default) sizes the timed region to ~1.5 s")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=workloads.HEADLINE,
-                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.ATTN_WORKLOADS))
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.ATTN_WORKLOADS)
+                    + sorted(workloads.MX_WORKLOADS))
     ap.add_argument("--impl", default="tl", choices=["tl", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -483,8 +537,11 @@ def main():
         ap.error("--warmup must be >= 3")
 
     attn = args.workload in workloads.ATTN_WORKLOADS
-    w = workloads.ATTN_WORKLOADS[args.workload] if attn else workloads.WORKLOADS[args.workload]
+    mx = args.workload in workloads.MX_WORKLOADS
+    w = (workloads.ATTN_WORKLOADS[args.workload] if attn else
+         workloads.MX_WORKLOADS[args.workload] if mx else workloads.WORKLOADS[args.workload])
     metric = ("attention forward TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU" if attn
+              else "block-scaled 8-bit GEMM TFLOP/s and % of GB300 dense fp8 peak, 1 GPU" if mx
               else "GEMM+ReLU TFLOP/s and % of GB300 dense fp16/bf16 peak, 1 GPU")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -495,6 +552,12 @@ def main():
     if attn:
         config = {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D,
                   "dtype": w.dtype_name, "causal": w.causal, "inputs": w.description,
+                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    elif mx:
+        config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype_name,
+                  "layout": "A [M,K], B [N,K], both K-major", "scales": "E8M0 per 32 K",
+                  "out": "bf16" if w.out_dtype == workloads.BF16 else "f16",
+                  "epilogue": "relu" if w.relu else "none", "inputs": w.description,
                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     else:
         config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype_name,
@@ -507,6 +570,11 @@ def main():
             q, k, v = workloads.make_attn_inputs(w)
             r, el, fl, n, reps = oracle_rate_attn(w, q, k, v, budget, threads)
             return r, el, fl, f"{reps} oracle runs of up to {n} output rows of {w.B * w.S * w.H}"
+        if mx:
+            a_cpu, b_cpu, sa_cpu, sb_cpu = workloads.make_mx_inputs(w)
+            r, el, fl, rows, reps = oracle_rate_mx(w, a_cpu, b_cpu, sa_cpu, budget, sb_cpu,
+                                                   threads)
+            return r, el, fl, f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows)"
         a_cpu, b_cpu = workloads.make_inputs(w)
         r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, budget, threads)
         return r, el, fl, f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows)"
@@ -559,7 +627,7 @@ def main():
         cpu = {"value": round(r, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{what}, {fl / 1e9:.2f} GFLOP in {el:.1f} s"}
 
-    res = (run_attn if attn else run_tl)(args, w, rank, world, dist)
+    res = (run_attn if attn else run_mx if mx else run_tl)(args, w, rank, world, dist)
     total_ms = res["total_ms"]
     value = whole_job_tflops(w.flops, args.steps, world, total_ms)
     avg_launch_ms = total_ms / args.steps        # back-to-back launches in the graph

@@ -284,13 +284,13 @@ void tl_set_wait_timeout_ns(uint64_t ns);
  *   B        device pointer, N x K codes of b_type, K-major (the MX layout: C = A B^T).
  *   SFA/SFB  device pointers to E8M0 scale codes (the value 2^(e-127); 255 is NaN),
  *            one byte per 32-element block of each row of A / B.  Their row pitches
- *            sfa_ld / sfb_ld are in bytes, multiples of 4 and at least 4*ceil(K/128)
- *            (whole groups of four blocks; codes of blocks past K/32 are ignored).
+ *            sfa_ld / sfb_ld are in bytes, at least 4*ceil(K/128) (whole groups of four
+ *            blocks); codes of blocks past K/32 and of the padding are ignored.
  *   C        device pointer, M x N of c_type (TL_F16 or TL_BF16), rounded once from
  *            the fp32 accumulator; epilogue TL_EPI_NONE or TL_EPI_RELU.
- * K must be a multiple of 32 (TL_ERR_INVALID_ARG).  A and B must be 16-byte aligned
- * with lda, ldb multiples of 16; SFA, SFB 4-byte aligned; C 2-byte aligned
- * (TL_ERR_ALIGNMENT otherwise).  C must not overlap an input (TL_ERR_ALIAS).
+ * K must be a multiple of 32 (TL_ERR_INVALID_ARG).  A, B, SFA and SFB must be 16-byte
+ * aligned with lda, ldb, sfa_ld and sfb_ld multiples of 16 (all four are read by the
+ * TMA unit); C 2-byte aligned (TL_ERR_ALIGNMENT otherwise).  C must not overlap an input (TL_ERR_ALIAS).
  * M or N == 0: TL_OK, nothing launched; K == 0: C = 0.  Asynchronous on `stream`;
  * the caller owns every buffer; errors are returned before anything is enqueued, a
  * device-side timeout is read with tl_device_status().

@@ -91,7 +91,7 @@ def test_random_within_tolerance(M, N, K, a_fmt, b_fmt):
 def test_scale_bytes_past_k_are_ignored_and_pitches_padded():
     # K = 1056 is 33 blocks: the last group of four holds one real block.  Every byte
     # past block 32, and the padding of the pitch, is the NaN code: none may reach C.
-    w = _w(300, 200, 1056, 55, exact=True, sf_pad=12)
+    w = _w(300, 200, 1056, 55, exact=True, sf_pad=16)
     a, b, sa, sb = workloads.make_mx_inputs(w)
     sa[:, 33:] = 255
     sb[:, 33:] = 255
@@ -123,26 +123,27 @@ def test_k_zero_and_bad_arguments():
     c = GuardedC(64, 64, 64, torch.bfloat16)
     x = torch.zeros(64 * 256, dtype=torch.uint8, device="cuda")
     p = x.data_ptr()
-    st = tl.tl_gemm_mx(p, p, p, p, c.ptr, 64, 64, 0, 16, 16, 64, 4, 4, E4M3, E4M3, BF16, 0, s)
+    st = tl.tl_gemm_mx(p, p, p, p, c.ptr, 64, 64, 0, 16, 16, 64, 16, 16, E4M3, E4M3, BF16, 0,
+                       s)
     assert st == tl.TL_OK
     torch.cuda.synchronize()
     assert np.all(c.result() == 0)
     c.check_guards()
     args = (p, p, p, p, c.ptr, 64, 64, 128, 128, 128, 64)
-    ok = args + (4, 4, E4M3, E4M3, BF16, 0, s)
+    ok = args + (16, 16, E4M3, E4M3, BF16, 0, s)
     assert tl.tl_gemm_mx(*ok) == tl.TL_OK
     torch.cuda.synchronize()
-    assert tl.tl_gemm_mx(p, p, p, p, c.ptr, 64, 64, 96 + 8, 128, 128, 64, 4, 4, E4M3, E4M3,
+    assert tl.tl_gemm_mx(p, p, p, p, c.ptr, 64, 64, 96 + 8, 128, 128, 64, 16, 16, E4M3, E4M3,
                          BF16, 0, s) == tl.TL_ERR_INVALID_ARG           # K % 32 != 0
-    assert tl.tl_gemm_mx(*args, 4, 4, BF16, E4M3, BF16, 0, s) == tl.TL_ERR_INVALID_ARG
-    assert tl.tl_gemm_mx(*args, 4, 4, E4M3, E4M3, E4M3, 0, s) == tl.TL_ERR_INVALID_ARG
-    assert tl.tl_gemm_mx(*args, 2, 4, E4M3, E4M3, BF16, 0, s) == tl.TL_ERR_INVALID_ARG  # short
-    assert tl.tl_gemm_mx(*args, 6, 4, E4M3, E4M3, BF16, 0, s) == tl.TL_ERR_ALIGNMENT    # pitch
-    assert tl.tl_gemm_mx(p, p, p + 2, p, c.ptr, 64, 64, 128, 128, 128, 64, 4, 4, E4M3, E4M3,
+    assert tl.tl_gemm_mx(*args, 16, 16, BF16, E4M3, BF16, 0, s) == tl.TL_ERR_INVALID_ARG
+    assert tl.tl_gemm_mx(*args, 16, 16, E4M3, E4M3, E4M3, 0, s) == tl.TL_ERR_INVALID_ARG
+    assert tl.tl_gemm_mx(*args, 2, 16, E4M3, E4M3, BF16, 0, s) == tl.TL_ERR_INVALID_ARG  # short
+    assert tl.tl_gemm_mx(*args, 20, 16, E4M3, E4M3, BF16, 0, s) == tl.TL_ERR_ALIGNMENT   # pitch
+    assert tl.tl_gemm_mx(p, p, p + 4, p, c.ptr, 64, 64, 128, 128, 128, 64, 16, 16, E4M3, E4M3,
                          BF16, 0, s) == tl.TL_ERR_ALIGNMENT
-    assert tl.tl_gemm_mx(p + 8, p, p, p, c.ptr, 64, 64, 128, 128, 128, 64, 4, 4, E4M3, E4M3,
+    assert tl.tl_gemm_mx(p + 8, p, p, p, c.ptr, 64, 64, 128, 128, 128, 64, 16, 16, E4M3, E4M3,
                          BF16, 0, s) == tl.TL_ERR_ALIGNMENT
-    assert tl.tl_gemm_mx(p, p, p, p, p, 64, 64, 128, 128, 128, 64, 4, 4, E4M3, E4M3, BF16, 0,
+    assert tl.tl_gemm_mx(p, p, p, p, p, 64, 64, 128, 128, 128, 64, 16, 16, E4M3, E4M3, BF16, 0,
                          s) == tl.TL_ERR_ALIAS
     assert tl.tl_device_status(reset=True)[0] == tl.TL_OK
 

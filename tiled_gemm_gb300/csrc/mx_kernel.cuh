@@ -8,13 +8,16 @@
 //
 // One CTA per 128 x 128 tile of C, 256 threads:
 //   warp 0 (one thread)  TMA producer: a stage is 128 K bytes of A (128 rows) and of B
-//                        (128 rows), 128-byte swizzle, S stages in a ring.
+//                        (128 rows), 128-byte swizzle, S stages in a ring; every
+//                        kMxGroup stages also the tile's scale bytes for those stages
+//                        (128 rows x 32 bytes of SFA and of SFB, unswizzled, two buffers).
 //   warp 1 (one thread)  MMA issuer (and the Tensor Memory allocation): per stage four
 //                        128 x 128 x 32 block-scaled MMAs, one per 32-element block, the
 //                        scale byte of block k selected by the descriptor's scale ids.
 //   warps 4-7            scale loaders, then the epilogue.  Only the warp of a lane
 //                        quadrant can write its Tensor Memory lanes, so these four warps
-//                        put each stage's scales there (tcgen05.st) ahead of the MMA;
+//                        copy each stage's scales there from shared memory (tcgen05.st)
+//                        ahead of the MMA;
 //                        after the last stage they read the accumulator, apply ReLU,
 //                        cast and store the tile.
 //
@@ -37,10 +40,12 @@ constexpr int kMxBM = 128;
 constexpr int kMxBN = 128;
 constexpr int kMxBK = 128;          // K bytes (= elements) per stage: four 32-element blocks
 constexpr int kMxStages = 4;
+constexpr int kMxGroup = 8;         // stages per TMA load of scale bytes (32 bytes a row)
 constexpr int kMxThreads = 256;
 constexpr uint32_t kMxStageBytes = 2u * kMxBM * kMxBK;   // A + B
 constexpr uint32_t kMxTmemCols = 256;                     // accumulator 0-127, scales 128-
 constexpr uint32_t kMxSfCol = 128;                        // stage s: A at +8s, B at +8s+4
+constexpr uint32_t kMxScaleBytes = 4u * kMxGroup * (kMxBM + kMxBN);   // one scale buffer
 
 enum MxWaitSite : uint32_t {
   kSiteMxEmpty = 31,
@@ -53,9 +58,6 @@ enum MxWaitSite : uint32_t {
 struct MxParams {
   int32_t M, N, K;
   int32_t k_blocks;           // ceil(K / 128)
-  const uint8_t* SA;          // [M][sfa_ld] E8M0, 4-byte aligned, sfa_ld % 4 == 0
-  const uint8_t* SB;          // [N][sfb_ld]
-  int64_t sfa_ld, sfb_ld;     // >= 4 * k_blocks
   void* C;
   int64_t ldc;
   int32_t relu;
@@ -66,7 +68,11 @@ struct MxParams {
 };
 
 __host__ __device__ constexpr uint32_t mx_smem_bytes() {
-  return 1024u + kMxStages * kMxStageBytes + 8u * (3 * kMxStages + 1) + 16u + 4u * kMxStages;
+  // +1024 alignment slack; operand stages; two scale buffers; barriers (full, empty,
+  // sf_full per stage, sg_full and sg_empty per scale buffer, acc_full); Tensor Memory
+  // slot, abort flag and the laps of the last loads (stages, then scale buffers)
+  return 1024u + kMxStages * kMxStageBytes + 2u * kMxScaleBytes +
+         8u * (3 * kMxStages + 5) + 16u + 4u * (kMxStages + 2);
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scales: B scale id (bits 4-5),
@@ -103,13 +109,13 @@ __device__ __forceinline__ void tmem_store_4cols(uint32_t taddr, uint32_t a, uin
                : "memory");
 }
 
-// The four scale bytes of stage kb of one row: an aligned 32-bit word; rows past the
-// matrix and blocks past K read as 2^0 (their operands are zero, and a NaN code there
-// must not reach the sum).
-__device__ __forceinline__ uint32_t mx_scale_word(const uint8_t* S, int64_t ld, int row,
-                                                  int rows, int kb, int n_blk) {
+// The four scale bytes of stage kb of one row, from the row's 32 bytes of the current
+// group in shared memory; rows past the matrix and blocks past K read as 2^0 (their
+// operands are zero, and a NaN code there must not reach the sum).
+__device__ __forceinline__ uint32_t mx_scale_word(const uint8_t* group_row, int row, int rows,
+                                                  int kb, int n_blk) {
   if (row >= rows) return 0x7F7F7F7Fu;
-  uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(S + static_cast<int64_t>(row) * ld + 4 * kb));
+  uint32_t w = *reinterpret_cast<const uint32_t*>(group_row + 4 * (kb % kMxGroup));
   const int valid = n_blk - 4 * kb;
   if (valid < 4) {
     const uint32_t keep = (1u << (8 * valid)) - 1u;
@@ -121,7 +127,9 @@ __device__ __forceinline__ uint32_t mx_scale_word(const uint8_t* S, int64_t ld, 
 template <bool kBf16>
 __global__ void __launch_bounds__(kMxThreads, 1)
     tl_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                      const __grid_constant__ CUtensorMap tmap_b, const MxParams p) {
+                      const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_sa,
+                      const __grid_constant__ CUtensorMap tmap_sb, const MxParams p) {
   constexpr int S = kMxStages;
   constexpr uint32_t kA = kMxBM * kMxBK;           // bytes of A per stage
   grid_launch_dependents();
@@ -129,16 +137,20 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const uint32_t sBar = base + S * kMxStageBytes;
+  const uint32_t sScale = base + S * kMxStageBytes;     // scale buffer t at + t * kMxScaleBytes
+  const uint32_t sBar = sScale + 2u * kMxScaleBytes;
   auto full = [&](int s) { return sBar + 8u * s; };
   auto empty = [&](int s) { return sBar + 8u * (S + s); };
   auto sf_full = [&](int s) { return sBar + 8u * (2 * S + s); };
-  const uint32_t acc_full = sBar + 8u * (3 * S);
+  auto sg_full = [&](int t) { return sBar + 8u * (3 * S + t); };      // scale buffer loaded
+  auto sg_empty = [&](int t) { return sBar + 8u * (3 * S + 2 + t); }; // scale buffer read
+  const uint32_t acc_full = sBar + 8u * (3 * S + 4);
   const uint32_t slot = acc_full + 8u;
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
   volatile int32_t* const lap_armed = reinterpret_cast<volatile int32_t*>(tmem_slot_ptr + 4);  // [S]
+  volatile int32_t* const lap_sg = lap_armed + S;                                                // [2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -153,6 +165,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(sf_full(s), 4);
       lap_armed[s] = -1;
     }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(sg_full(t), 1);
+      mbar_init(sg_empty(t), 4);
+      lap_sg[t] = -1;
+    }
     mbar_init(acc_full, 1);
     *abort_flag = 0u;
     fence_barrier_init();
@@ -160,6 +177,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   if (threadIdx.x == 64) {
     tma_prefetch_map(&tmap_a);
     tma_prefetch_map(&tmap_b);
+    tma_prefetch_map(&tmap_sa);
+    tma_prefetch_map(&tmap_sb);
   }
   if (warp == 1) {
     tmem_alloc(slot, kMxTmemCols);
@@ -175,6 +194,21 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (lane == 0) {
       grid_dependency_wait();
       for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (kb % kMxGroup == 0) {
+          // the scale bytes of stages kb .. kb + kMxGroup - 1
+          const int g = kb / kMxGroup;
+          const int t = g & 1;
+          if (!wait_bounded<false>(sg_empty(t), (static_cast<uint32_t>(g >> 1) & 1u) ^ 1u,
+                                   abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteMxEmpty);
+            break;
+          }
+          mbar_arrive_expect_tx(sg_full(t), kMxScaleBytes);
+          const uint32_t dst = sScale + t * kMxScaleBytes;
+          tma_load_2d(dst, &tmap_sa, sg_full(t), 4 * kMxGroup * g, m0);
+          tma_load_2d(dst + 4u * kMxGroup * kMxBM, &tmap_sb, sg_full(t), 4 * kMxGroup * g, n0);
+          lap_sg[t] = g >> 1;
+        }
         const int s = kb % S;
         const int lap = kb / S;
         if (!wait_bounded<false>(empty(s), (static_cast<uint32_t>(lap) & 1u) ^ 1u, abort_flag,
@@ -238,20 +272,26 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       return r;
     };
     bool ok = true;
-    // this thread's words of stage kb: A for row m0 + row, B for columns n0 + 32c + lane
-    auto load_words = [&](int kb, uint32_t& wa, uint32_t (&wb)[4]) {
-      wa = mx_scale_word(p.SA, p.sfa_ld, m0 + row, p.M, kb, n_blk);
+    for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
+      const int g = kb / kMxGroup;
+      const int t = g & 1;
+      if (kb % kMxGroup == 0 &&
+          !(ok = wait_warp(sg_full(t), static_cast<uint32_t>(g >> 1) & 1u, kSiteMxScales)))
+        break;
+      // this thread's words: A for row m0 + row, B for columns n0 + 32c + lane (every
+      // quadrant writes all of B's, which each quadrant reads from its own lanes)
+      const uint8_t* grp = base_ptr + (sScale - base) + t * kMxScaleBytes;
+      const uint32_t wa = mx_scale_word(grp + row * 4 * kMxGroup, m0 + row, p.M, kb, n_blk);
+      uint32_t wb[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) wb[c] = mx_scale_word(p.SB, p.sfb_ld, n0 + 32 * c + lane, p.N, kb, n_blk);
-    };
-    uint32_t wa = 0, wb[4] = {0, 0, 0, 0};
-    if (p.k_blocks > 0) load_words(0, wa, wb);
-    for (int kb = 0; kb < p.k_blocks; ++kb) {
+      for (int c = 0; c < 4; ++c)
+        wb[c] = mx_scale_word(grp + 4 * kMxGroup * (kMxBM + 32 * c + lane), n0 + 32 * c + lane,
+                              p.N, kb, n_blk);
+      if (kb % kMxGroup == kMxGroup - 1 || kb == p.k_blocks - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sg_empty(t));       // this warp is done with the buffer
+      }
       const int s = kb % S;
-      // the next stage's words are loaded before this stage's wait, so their latency
-      // runs under it
-      uint32_t na = 0, nb[4] = {0, 0, 0, 0};
-      if (kb + 1 < p.k_blocks) load_words(kb + 1, na, nb);
       if (!(ok = wait_warp(empty(s), (static_cast<uint32_t>(kb / S) & 1u) ^ 1u, kSiteMxEmpty)))
         break;
       tc_fence_after_sync();
@@ -262,9 +302,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(sf_full(s));
-      wa = na;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) wb[c] = nb[c];
     }
     if (ok && wait_warp(acc_full, 0, kSiteMxAcc)) {
       tc_fence_after_sync();
@@ -311,6 +348,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     for (int s = 0; s < S; ++s) {
       const int lap = lap_armed[s];
       if (lap >= 0 && !wait_bounded<false>(full(s), static_cast<uint32_t>(lap) & 1u, nullptr,
+                                           p.timeout_ns)) {
+        record_timeout(p.status, abort_flag, kSiteMxDrain);
+      }
+    }
+    for (int t = 0; t < 2; ++t) {
+      const int lap = lap_sg[t];
+      if (lap >= 0 && !wait_bounded<false>(sg_full(t), static_cast<uint32_t>(lap) & 1u, nullptr,
                                            p.timeout_ns)) {
         record_timeout(p.status, abort_flag, kSiteMxDrain);
       }

@@ -504,7 +504,7 @@ struct MapKey {
   uint64_t strides[3];
   uint32_t box[4];
   uint32_t dtype_rank;
-  uint32_t pad;
+  uint32_t swizzle;                          // 1: 128-byte swizzle, 0: none
   bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
@@ -528,7 +528,8 @@ CUtensorMapDataType map_type(tl_dtype t) {
 }
 
 bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* base,
-                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                   bool swizzle = true) {
   MapKey key;
   std::memset(&key, 0, sizeof(key));                        // padding bytes take part
   key.base = reinterpret_cast<uint64_t>(base);
@@ -538,6 +539,7 @@ bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* 
     if (i + 1 < rank) key.strides[i] = strides[i];
   }
   key.dtype_rank = static_cast<uint32_t>(dtype) * 8u + rank;
+  key.swizzle = swizzle ? 1u : 0u;
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     if (g_maps != nullptr) {
@@ -553,7 +555,8 @@ bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* 
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt = map_type(dtype);
   if (enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
     return false;
   }
@@ -565,11 +568,11 @@ bool encode_cached(CUtensorMap* map, tl_dtype dtype, uint32_t rank, const void* 
 }
 
 bool encode_2d(CUtensorMap* map, tl_dtype dtype, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, bool swizzle = true) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {ld_elems * static_cast<uint64_t>(elem_bytes(dtype))};
   const cuuint32_t box[2] = {box_inner, box_outer};
-  return encode_cached(map, dtype, 2, base, dims, strides, box);
+  return encode_cached(map, dtype, 2, base, dims, strides, box, swizzle);
 }
 
 // A row-major [rows][ld] matrix whose contiguous extent `inner` is a multiple of the
@@ -1014,9 +1017,7 @@ tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, v
     if (A == nullptr || B == nullptr || SA == nullptr || SB == nullptr) return TL_ERR_NULL_PTR;
     // operands straight to the TMA unit; the scales as aligned 32-bit words
     if (!tma_ok(A, lda, 1) || !tma_ok(B, ldb, 1)) return TL_ERR_ALIGNMENT;
-    if (((reinterpret_cast<uintptr_t>(SA) | reinterpret_cast<uintptr_t>(SB)) & 3u) ||
-        (sfa_ld & 3) || (sfb_ld & 3))
-      return TL_ERR_ALIGNMENT;
+    if (!tma_ok(SA, sfa_ld, 1) || !tma_ok(SB, sfb_ld, 1)) return TL_ERR_ALIGNMENT;
     uintptr_t c0, c1, x0, x1;
     extent(C, M, N, ldc, &c0, &c1);
     const struct { const void* p; int64_t rows, cols, ld; } ins[4] = {
@@ -1040,11 +1041,17 @@ tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, v
   for (const void* x : {A, B, SA, SB}) {
     if ((s = check_device_pointer(x, dev)) != TL_OK) return s;
   }
-  CUtensorMap ta, tb;
+  // operands in 128-byte swizzled boxes; the scales in plain boxes of one group of
+  // stages (kMxGroup stages x 4 bytes) of 128 rows
+  CUtensorMap ta, tb, tsa, tsb;
   if (!encode_2d(&ta, a_type, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                  static_cast<uint64_t>(lda), tl::kMxBK, tl::kMxBM) ||
       !encode_2d(&tb, b_type, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                 static_cast<uint64_t>(ldb), tl::kMxBK, tl::kMxBN)) {
+                 static_cast<uint64_t>(ldb), tl::kMxBK, tl::kMxBN) ||
+      !encode_2d(&tsa, TL_E4M3, SA, static_cast<uint64_t>(sfa_ld), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(sfa_ld), 4u * tl::kMxGroup, tl::kMxBM, false) ||
+      !encode_2d(&tsb, TL_E4M3, SB, static_cast<uint64_t>(sfb_ld), static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(sfb_ld), 4u * tl::kMxGroup, tl::kMxBN, false)) {
     return TL_ERR_LAUNCH;
   }
   tl::MxParams prm;
@@ -1053,10 +1060,6 @@ tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, v
   prm.N = static_cast<int32_t>(N);
   prm.K = static_cast<int32_t>(K);
   prm.k_blocks = static_cast<int32_t>(k_blocks);
-  prm.SA = static_cast<const uint8_t*>(SA);
-  prm.SB = static_cast<const uint8_t*>(SB);
-  prm.sfa_ld = sfa_ld;
-  prm.sfb_ld = sfb_ld;
   prm.C = C;
   prm.ldc = ldc;
   prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
@@ -1090,7 +1093,7 @@ tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, v
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, prm) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, prm) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_LAUNCH;
   }

@@ -189,13 +189,22 @@ class MxWorkload:
     std: float = 1.0
     sf_lo: int = 120
     sf_hi: int = 134
-    sf_pad: int = 0         # extra scale bytes per row beyond 4*ceil(K/128)
+    sf_pad: int = 0         # extra scale bytes per row (a multiple of 16)
     seed: int = 0
     description: str = ""
 
     @property
     def sf_ld(self) -> int:
-        return 4 * ((self.K + 127) // 128) + self.sf_pad
+        """Scale pitch in bytes: 4*ceil(K/128) rounded up to 16, plus sf_pad."""
+        return 16 * ((4 * ((self.K + 127) // 128) + 15) // 16) + self.sf_pad
+
+    @property
+    def fp8(self) -> bool:
+        return True
+
+    @property
+    def dtype_name(self) -> str:
+        return f"{_NAME[self.a_fmt]}x{_NAME[self.b_fmt]}-mx"
 
     @property
     def c_torch_dtype(self) -> torch.dtype:
