@@ -6,13 +6,13 @@
 // block-scaled MMA, tcgen05 kind::mxf8f6f4.block_scale with the scale factors already
 // in Tensor Memory).  fp32 accumulation in Tensor Memory; fp16 or bf16 out.
 //
-// One CTA per 128 x 128 tile of C, 256 threads:
+// One CTA per 128 x BN tile of C (BN = 128 or 256), 256 threads:
 //   warp 0 (one thread)  TMA producer: a stage is 128 K bytes of A (128 rows) and of B
 //                        (128 rows), 128-byte swizzle, S stages in a ring; every
 //                        kMxGroup stages also the tile's scale bytes for those stages
 //                        (128 rows x 32 bytes of SFA and of SFB, unswizzled, two buffers).
 //   warp 1 (one thread)  MMA issuer (and the Tensor Memory allocation): per stage four
-//                        128 x 128 x 32 block-scaled MMAs, one per 32-element block, the
+//                        128 x BN x 32 block-scaled MMAs, one per 32-element block, the
 //                        scale byte of block k selected by the descriptor's scale ids.
 //   warps 4-7            scale loaders, then the epilogue.  Only the warp of a lane
 //                        quadrant can write its Tensor Memory lanes, so these four warps
@@ -21,15 +21,15 @@
 //                        after the last stage they read the accumulator, apply ReLU,
 //                        cast and store the tile.
 //
-// Scale layout in Tensor Memory for M = N = 128 and one scale per 32 elements (found
-// with an exact probe: operands of ones, distinct power-of-two scales), four columns
-// per operand per stage, each 32-bit word holding the scales of the stage's four
-// blocks in its four bytes (byte k = the scale id of MMA k):
-//   A: row i reads lane i, column sfa + i/32;
+// Scale layout in Tensor Memory for M = 128, N = 128 or 256 and one scale per 32
+// elements (found with an exact probe: operands of ones, distinct power-of-two
+// scales), each 32-bit word holding the scales of the stage's four blocks in its four
+// bytes (byte k = the scale id of MMA k):
+//   A: row i reads lane i, column sfa + i/32 (four columns);
 //   B: column j of the product, for rows in lane quadrant q, reads lane 32q + j%32,
-//      column sfb + j/32 -- so B's words are written into every quadrant.
-// Both scale addresses stay on 4-column boundaries (an unaligned one is a misaligned
-// address fault).
+//      column sfb + j/32 (N/32 columns) -- so B's words go into every quadrant.
+// The scale addresses stay on the boundaries the probe used (4 columns at N = 128,
+// 16 at N = 256): an unaligned one is a misaligned address fault.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -37,15 +37,23 @@
 namespace tl {
 
 constexpr int kMxBM = 128;
-constexpr int kMxBN = 128;
 constexpr int kMxBK = 128;          // K bytes (= elements) per stage: four 32-element blocks
 constexpr int kMxStages = 4;
 constexpr int kMxGroup = 8;         // stages per TMA load of scale bytes (32 bytes a row)
 constexpr int kMxThreads = 256;
-constexpr uint32_t kMxStageBytes = 2u * kMxBM * kMxBK;   // A + B
-constexpr uint32_t kMxTmemCols = 256;                     // accumulator 0-127, scales 128-
-constexpr uint32_t kMxSfCol = 128;                        // stage s: A at +8s, B at +8s+4
-constexpr uint32_t kMxScaleBytes = 4u * kMxGroup * (kMxBM + kMxBN);   // one scale buffer
+
+// The sizes of the 128 x BN tile.
+template <int BN>
+struct MxTile {
+  static_assert(BN == 128 || BN == 256, "tile width 128 or 256");
+  static constexpr uint32_t kStageBytes = (kMxBM + BN) * kMxBK;        // A + B of a stage
+  static constexpr uint32_t kTmemCols = BN == 128 ? 256u : 512u;
+  static constexpr uint32_t kSfCol = BN;                 // scales after the accumulator
+  static constexpr uint32_t kSfStride = BN == 128 ? 8u : 32u;     // columns per stage
+  static constexpr uint32_t kSfB = BN == 128 ? 4u : 16u;          // B's offset in a stage
+  static constexpr uint32_t kScaleBytes = 4u * kMxGroup * (kMxBM + BN);   // one buffer
+  static_assert(kSfCol + kMxStages * kSfStride <= kTmemCols, "scales fit in Tensor Memory");
+};
 
 enum MxWaitSite : uint32_t {
   kSiteMxEmpty = 31,
@@ -62,16 +70,17 @@ struct MxParams {
   int64_t ldc;
   int32_t relu;
   int32_t c_vec;              // C and ldc allow 16-byte stores
-  uint32_t idesc;             // formats, K-major both, N 128, M 128, E8M0 scales
+  uint32_t idesc;             // formats, K-major both, N, M 128, E8M0 scales
   uint32_t* status;
   uint64_t timeout_ns;
 };
 
+template <int BN>
 __host__ __device__ constexpr uint32_t mx_smem_bytes() {
   // +1024 alignment slack; operand stages; two scale buffers; barriers (full, empty,
   // sf_full per stage, sg_full and sg_empty per scale buffer, acc_full); Tensor Memory
   // slot, abort flag and the laps of the last loads (stages, then scale buffers)
-  return 1024u + kMxStages * kMxStageBytes + 2u * kMxScaleBytes +
+  return 1024u + kMxStages * MxTile<BN>::kStageBytes + 2u * MxTile<BN>::kScaleBytes +
          8u * (3 * kMxStages + 5) + 16u + 4u * (kMxStages + 2);
 }
 
@@ -124,12 +133,13 @@ __device__ __forceinline__ uint32_t mx_scale_word(const uint8_t* group_row, int 
   return w;
 }
 
-template <bool kBf16>
+template <bool kBf16, int BN>
 __global__ void __launch_bounds__(kMxThreads, 1)
     tl_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_sa,
                       const __grid_constant__ CUtensorMap tmap_sb, const MxParams p) {
+  using T = MxTile<BN>;
   constexpr int S = kMxStages;
   constexpr uint32_t kA = kMxBM * kMxBK;           // bytes of A per stage
   grid_launch_dependents();
@@ -137,8 +147,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const uint32_t sScale = base + S * kMxStageBytes;     // scale buffer t at + t * kMxScaleBytes
-  const uint32_t sBar = sScale + 2u * kMxScaleBytes;
+  const uint32_t sScale = base + S * T::kStageBytes;     // scale buffer t at + t * T::kScaleBytes
+  const uint32_t sBar = sScale + 2u * T::kScaleBytes;
   auto full = [&](int s) { return sBar + 8u * s; };
   auto empty = [&](int s) { return sBar + 8u * (S + s); };
   auto sf_full = [&](int s) { return sBar + 8u * (2 * S + s); };
@@ -155,7 +165,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m0 = static_cast<int>(blockIdx.y) * kMxBM;
-  const int n0 = static_cast<int>(blockIdx.x) * kMxBN;
+  const int n0 = static_cast<int>(blockIdx.x) * BN;
   const int n_blk = p.K / 32;
 
   if (threadIdx.x == 0) {
@@ -181,7 +191,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     tma_prefetch_map(&tmap_sb);
   }
   if (warp == 1) {
-    tmem_alloc(slot, kMxTmemCols);
+    tmem_alloc(slot, T::kTmemCols);
     tmem_relinquish_alloc_permit();
   }
   tc_fence_before_sync();
@@ -203,8 +213,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             record_timeout(p.status, abort_flag, kSiteMxEmpty);
             break;
           }
-          mbar_arrive_expect_tx(sg_full(t), kMxScaleBytes);
-          const uint32_t dst = sScale + t * kMxScaleBytes;
+          mbar_arrive_expect_tx(sg_full(t), T::kScaleBytes);
+          const uint32_t dst = sScale + t * T::kScaleBytes;
           tma_load_2d(dst, &tmap_sa, sg_full(t), 4 * kMxGroup * g, m0);
           tma_load_2d(dst + 4u * kMxGroup * kMxBM, &tmap_sb, sg_full(t), 4 * kMxGroup * g, n0);
           lap_sg[t] = g >> 1;
@@ -216,8 +226,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           record_timeout(p.status, abort_flag, kSiteMxEmpty);
           break;
         }
-        mbar_arrive_expect_tx(full(s), kMxStageBytes);
-        const uint32_t dst = base + s * kMxStageBytes;
+        mbar_arrive_expect_tx(full(s), T::kStageBytes);
+        const uint32_t dst = base + s * T::kStageBytes;
         tma_load_2d(dst, &tmap_a, full(s), kb * kMxBK, m0);
         tma_load_2d(dst + kA, &tmap_b, full(s), kb * kMxBK, n0);
         lap_armed[s] = lap;
@@ -244,13 +254,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint64_t stage = (static_cast<uint64_t>(s) * kMxStageBytes) >> 4;
-        const uint32_t sfa = tmem_base + kMxSfCol + 8u * s;
+        const uint64_t stage = (static_cast<uint64_t>(s) * T::kStageBytes) >> 4;
+        const uint32_t sfa = tmem_base + T::kSfCol + T::kSfStride * s;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           // 32 K bytes per MMA: 32 B along the 128-byte swizzled row
           mma_mx_ss(tmem_base, a_desc0 + stage + 2u * k, b_desc0 + stage + 2u * k,
-                    mx_scale_ids(p.idesc, static_cast<uint32_t>(k)), sfa, sfa + 4u,
+                    mx_scale_ids(p.idesc, static_cast<uint32_t>(k)), sfa, sfa + T::kSfB,
                     (kb > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(empty(s));             // frees the stage's operands and scales
@@ -280,11 +290,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         break;
       // this thread's words: A for row m0 + row, B for columns n0 + 32c + lane (every
       // quadrant writes all of B's, which each quadrant reads from its own lanes)
-      const uint8_t* grp = base_ptr + (sScale - base) + t * kMxScaleBytes;
+      const uint8_t* grp = base_ptr + (sScale - base) + t * T::kScaleBytes;
       const uint32_t wa = mx_scale_word(grp + row * 4 * kMxGroup, m0 + row, p.M, kb, n_blk);
-      uint32_t wb[4];
+      uint32_t wb[BN / 32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < BN / 32; ++c)
         wb[c] = mx_scale_word(grp + 4 * kMxGroup * (kMxBM + 32 * c + lane), n0 + 32 * c + lane,
                               p.N, kb, n_blk);
       if (kb % kMxGroup == kMxGroup - 1 || kb == p.k_blocks - 1) {
@@ -295,9 +305,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       if (!(ok = wait_warp(empty(s), (static_cast<uint32_t>(kb / S) & 1u) ^ 1u, kSiteMxEmpty)))
         break;
       tc_fence_after_sync();
-      const uint32_t col = kMxSfCol + 8u * s;
+      const uint32_t col = T::kSfCol + T::kSfStride * s;
       tmem_store_1col(lane_base + col + static_cast<uint32_t>(q), wa);
-      tmem_store_4cols(lane_base + col + 4u, wb[0], wb[1], wb[2], wb[3]);
+#pragma unroll
+      for (int c = 0; c < BN / 32; c += 4)
+        tmem_store_4cols(lane_base + col + T::kSfB + c, wb[c], wb[c + 1], wb[c + 2], wb[c + 3]);
       tmem_store_wait();
       tc_fence_before_sync();
       __syncwarp();
@@ -308,7 +320,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const int gi = m0 + row;
       uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(gi) * p.ldc;
 #pragma unroll 1
-      for (int c = 0; c < kMxBN / 32; ++c) {
+      for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         tmem_load_32cols(lane_base + 32u * c, v);
         tmem_load_wait();
@@ -364,7 +376,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   tc_fence_after_sync();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kMxTmemCols);
+    tmem_dealloc(tmem_base, T::kTmemCols);
   }
 }
 

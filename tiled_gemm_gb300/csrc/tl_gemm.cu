@@ -51,7 +51,7 @@ struct DeviceState {
   int sms = 0;
   int smem_optin = 0;                        // max dynamic shared memory per CTA
   uint32_t* status = nullptr;
-  std::atomic<uint32_t> attr_done{0};        // bit i: smem attribute set for kernel i
+  std::atomic<uint64_t> attr_done{0};        // bit i: smem attribute set for kernel i
   int max_units[32] = {};                    // resident CTAs (pairs) per kernel
   std::mutex mu;
 };
@@ -388,7 +388,7 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
 template <int BN, int CG, int BK, int EB = 2>
 int prepare_kernel(DeviceState* st) {
   // slot of this kernel in the per-device caches: 0-11 the 16-bit tilings, 12-13 the
-  // narrow ones, 16-27 the 8-bit ones (14-15: the block-scaled kernel, 28-31: attention)
+  // narrow ones, 16-27 the 8-bit ones (28-31: attention, 32-35: the block-scaled kernel)
   constexpr int kIdx = BN < 64 ? 12 + (BN == 32)
                                : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) +
                                      6 * (BK * EB == 256) + 16 * (EB == 1);
@@ -996,6 +996,70 @@ tl_status run_attention(const void* Q, const void* K, const void* V, void* O, in
 }
 
 // ---- the block-scaled (MX) 8-bit GEMM ---------------------------------------------
+template <int BN, bool kBf16>
+tl_status launch_mx(const void* A, const void* B, const void* SA, const void* SB, void* C,
+                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                    int64_t sfa_ld, int64_t sfb_ld, tl_dtype a_type, tl_dtype b_type,
+                    tl_epilogue epilogue, DeviceState* st, cudaStream_t stream) {
+  const int64_t k_blocks = ceil_div(K, tl::kMxBK);
+  // operands in 128-byte swizzled boxes; the scales in plain boxes of one group of
+  // stages (kMxGroup stages x 4 bytes) of 128 rows
+  CUtensorMap ta, tb, tsa, tsb;
+  if (!encode_2d(&ta, a_type, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(lda), tl::kMxBK, tl::kMxBM) ||
+      !encode_2d(&tb, b_type, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(ldb), tl::kMxBK, BN) ||
+      !encode_2d(&tsa, TL_E4M3, SA, static_cast<uint64_t>(sfa_ld), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(sfa_ld), 4u * tl::kMxGroup, tl::kMxBM, false) ||
+      !encode_2d(&tsb, TL_E4M3, SB, static_cast<uint64_t>(sfb_ld), static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(sfb_ld), 4u * tl::kMxGroup, BN, false)) {
+    return TL_ERR_LAUNCH;
+  }
+  tl::MxParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.M = static_cast<int32_t>(M);
+  prm.N = static_cast<int32_t>(N);
+  prm.K = static_cast<int32_t>(K);
+  prm.k_blocks = static_cast<int32_t>(k_blocks);
+  prm.C = C;
+  prm.ldc = ldc;
+  prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
+  prm.c_vec = tma_ok(C, ldc) ? 1 : 0;
+  prm.idesc = tl::mma_idesc_mx(a_type == TL_E5M2 ? 1u : 0u, b_type == TL_E5M2 ? 1u : 0u,
+                               tl::kMxBM, BN);
+  prm.status = st->status;
+  prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  constexpr uint32_t kSmem = tl::mx_smem_bytes<BN>();
+  if (static_cast<int64_t>(kSmem) > st->smem_optin) return TL_ERR_UNSUPPORTED;
+  auto kern = tl::tl_gemm_mx_kernel<kBf16, BN>;
+  constexpr uint64_t bit = 1ull << (32 + 2 * (BN == 256) + (kBf16 ? 1 : 0));   // slots 32-35
+  if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
+    std::lock_guard<std::mutex> lock(st->mu);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmem)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TL_ERR_LAUNCH;
+    }
+    st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(N, BN)),
+                     static_cast<unsigned>(ceil_div(M, tl::kMxBM)));
+  cfg.blockDim = dim3(tl::kMxThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, prm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TL_ERR_LAUNCH;
+  }
+  return TL_OK;
+}
+
 tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, void* C,
                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                  int64_t sfa_ld, int64_t sfb_ld, tl_dtype a_type, tl_dtype b_type,
@@ -1005,7 +1069,7 @@ tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, v
   if (c_type != TL_F16 && c_type != TL_BF16) return TL_ERR_INVALID_ARG;
   if (epilogue != TL_EPI_NONE && epilogue != TL_EPI_RELU) return TL_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TL_OK;
-  if (M > INT32_MAX - tl::kMxBM || N > INT32_MAX - tl::kMxBN || K > INT32_MAX - tl::kMxBK)
+  if (M > INT32_MAX - tl::kMxBM || N > INT32_MAX - 256 || K > INT32_MAX - tl::kMxBK)
     return TL_ERR_UNSUPPORTED;
   if (ldc < N) return TL_ERR_INVALID_ARG;
   if (C == nullptr) return TL_ERR_NULL_PTR;
@@ -1041,63 +1105,20 @@ tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, v
   for (const void* x : {A, B, SA, SB}) {
     if ((s = check_device_pointer(x, dev)) != TL_OK) return s;
   }
-  // operands in 128-byte swizzled boxes; the scales in plain boxes of one group of
-  // stages (kMxGroup stages x 4 bytes) of 128 rows
-  CUtensorMap ta, tb, tsa, tsb;
-  if (!encode_2d(&ta, a_type, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                 static_cast<uint64_t>(lda), tl::kMxBK, tl::kMxBM) ||
-      !encode_2d(&tb, b_type, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                 static_cast<uint64_t>(ldb), tl::kMxBK, tl::kMxBN) ||
-      !encode_2d(&tsa, TL_E4M3, SA, static_cast<uint64_t>(sfa_ld), static_cast<uint64_t>(M),
-                 static_cast<uint64_t>(sfa_ld), 4u * tl::kMxGroup, tl::kMxBM, false) ||
-      !encode_2d(&tsb, TL_E4M3, SB, static_cast<uint64_t>(sfb_ld), static_cast<uint64_t>(N),
-                 static_cast<uint64_t>(sfb_ld), 4u * tl::kMxGroup, tl::kMxBN, false)) {
-    return TL_ERR_LAUNCH;
-  }
-  tl::MxParams prm;
-  std::memset(&prm, 0, sizeof(prm));
-  prm.M = static_cast<int32_t>(M);
-  prm.N = static_cast<int32_t>(N);
-  prm.K = static_cast<int32_t>(K);
-  prm.k_blocks = static_cast<int32_t>(k_blocks);
-  prm.C = C;
-  prm.ldc = ldc;
-  prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
-  prm.c_vec = tma_ok(C, ldc) ? 1 : 0;
-  prm.idesc = tl::mma_idesc_mx(a_type == TL_E5M2 ? 1u : 0u, b_type == TL_E5M2 ? 1u : 0u,
-                               tl::kMxBM, tl::kMxBN);
-  prm.status = st->status;
-  prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
-  constexpr uint32_t kSmem = tl::mx_smem_bytes();
-  if (static_cast<int64_t>(kSmem) > st->smem_optin) return TL_ERR_UNSUPPORTED;
-  const bool bf16 = c_type == TL_BF16;
-  auto kern = bf16 ? tl::tl_gemm_mx_kernel<true> : tl::tl_gemm_mx_kernel<false>;
-  const uint32_t bit = 1u << (14 + (bf16 ? 1 : 0));      // attribute slots 14, 15
-  if (!(st->attr_done.load(std::memory_order_acquire) & bit)) {
-    std::lock_guard<std::mutex> lock(st->mu);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmem)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TL_ERR_LAUNCH;
-    }
-    st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(N, tl::kMxBN)),
-                     static_cast<unsigned>(ceil_div(M, tl::kMxBM)));
-  cfg.blockDim = dim3(tl::kMxThreads);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, prm) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return TL_ERR_LAUNCH;
-  }
-  return TL_OK;
+  // 128 x 256 tiles (half the tiles and a quarter less operand traffic per flop) unless
+  // N fits one 128-wide tile
+  if (N > 128)
+    return c_type == TL_BF16 ? launch_mx<256, true>(A, B, SA, SB, C, M, N, K, lda, ldb, ldc,
+                                                   sfa_ld, sfb_ld, a_type, b_type, epilogue, st,
+                                                   stream)
+                             : launch_mx<256, false>(A, B, SA, SB, C, M, N, K, lda, ldb, ldc,
+                                                    sfa_ld, sfb_ld, a_type, b_type, epilogue, st,
+                                                    stream);
+  return c_type == TL_BF16 ? launch_mx<128, true>(A, B, SA, SB, C, M, N, K, lda, ldb, ldc, sfa_ld,
+                                                 sfb_ld, a_type, b_type, epilogue, st, stream)
+                           : launch_mx<128, false>(A, B, SA, SB, C, M, N, K, lda, ldb, ldc,
+                                                  sfa_ld, sfb_ld, a_type, b_type, epilogue, st,
+                                                  stream);
 }
 
 }  // namespace
