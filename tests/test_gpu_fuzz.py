@@ -6,9 +6,9 @@ depth, any stage count that fits, stream-K forced on or off, a persistent grid b
 the tile count, the operand swap, 16/32-column tiles, plain stores), or the planner's
 own choice.  Operands are small integers, so every fp32 partial sum is exact and the
 result must match the oracle bit for bit; the canary guard band around C checks that
-every element is written once and nothing outside C is touched.  The 8-bit path and
-the attention pass get their own random cases.  The seeds are fixed: a failure is
-reproducible from the case's printed parameters.
+every element is written once and nothing outside C is touched.  The 8-bit path, the
+block-scaled 8-bit product and the attention pass get their own random cases.  The
+seeds are fixed: a failure is reproducible from the case's printed parameters.
 """
 import numpy as np
 import pytest
@@ -101,3 +101,19 @@ def test_random_attention_cases(seed):
     code = oracle.F16 if dtype == torch.float16 else oracle.BF16
     ref = oracle.attention(q, k, v, dtype=code, causal=causal)
     assert_within_tolerance(got.reshape(-1, D), ref.reshape(-1, D), code)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_block_scaled_cases_bit_exact(seed):
+    from test_gpu_mx import _oracle, run_mx
+    rng = np.random.default_rng(5000 + seed)
+    M, N = (int(x) for x in rng.integers(1, 700, 2))
+    K = 32 * int(rng.integers(1, 48))
+    w = workloads.MxWorkload("fuzzmx", M, N, K,
+                             a_fmt=workloads.E4M3 if rng.integers(2) else workloads.E5M2,
+                             b_fmt=workloads.E4M3 if rng.integers(2) else workloads.E5M2,
+                             out_dtype=workloads.F16 if rng.integers(2) else workloads.BF16,
+                             relu=bool(rng.integers(2)), dist="int_small", sf_lo=126,
+                             sf_hi=128, sf_pad=16 * int(rng.integers(0, 3)), seed=seed)
+    a, b, sa, sb = workloads.make_mx_inputs(w)
+    assert_bit_exact(run_mx(w, a, b, sa, sb), _oracle(w, a, b, sa, sb))
