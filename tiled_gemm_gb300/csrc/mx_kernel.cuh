@@ -41,6 +41,7 @@ constexpr int kMxBK = 128;          // K bytes (= elements) per stage: four 32-e
 constexpr int kMxStages = 4;
 constexpr int kMxGroup = 8;         // stages per TMA load of scale bytes (32 bytes a row)
 constexpr int kMxThreads = 256;
+constexpr uint32_t kMxEpiBytes = 4u * 32u * 64u;   // one 32 x 32 bf16/fp16 staging tile per epilogue warp
 
 // The sizes of the 128 x BN tile.
 template <int BN>
@@ -81,7 +82,7 @@ __host__ __device__ constexpr uint32_t mx_smem_bytes() {
   // sf_full per stage, sg_full and sg_empty per scale buffer, acc_full); Tensor Memory
   // slot, abort flag and the laps of the last loads (stages, then scale buffers)
   return 1024u + kMxStages * MxTile<BN>::kStageBytes + 2u * MxTile<BN>::kScaleBytes +
-         8u * (3 * kMxStages + 5) + 16u + 4u * (kMxStages + 2);
+         kMxEpiBytes + 8u * (3 * kMxStages + 5) + 16u + 4u * (kMxStages + 2);
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scales: B scale id (bits 4-5),
@@ -148,7 +149,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const uint32_t sScale = base + S * T::kStageBytes;     // scale buffer t at + t * T::kScaleBytes
-  const uint32_t sBar = sScale + 2u * T::kScaleBytes;
+  const uint32_t sEpi = sScale + 2u * T::kScaleBytes;     // epilogue warp q at + 2048 q
+  const uint32_t sBar = sEpi + kMxEpiBytes;
   auto full = [&](int s) { return sBar + 8u * s; };
   auto empty = [&](int s) { return sBar + 8u * (S + s); };
   auto sf_full = [&](int s) { return sBar + 8u * (2 * S + s); };
@@ -318,13 +320,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (ok && wait_warp(acc_full, 0, kSiteMxAcc)) {
       tc_fence_after_sync();
       const int gi = m0 + row;
-      uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(gi) * p.ldc;
+      uint16_t* const c16 = reinterpret_cast<uint16_t*>(p.C);
+      uint16_t* crow = c16 + static_cast<int64_t>(gi) * p.ldc;
+      // This warp's 32 x 32 staging tile: row r's 64 bytes at 64 r, its four 16-byte units
+      // XOR-swizzled by (r/2) % 4.  Each thread writes its row of the chunk there, then
+      // every store instruction writes 8 rows x 64 contiguous bytes instead of 32 rows x
+      // 16 (the rows of C are ldc apart).
+      uint8_t* const stg = base_ptr + (sEpi - base) + static_cast<uint32_t>(q) * 2048u;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         tmem_load_32cols(lane_base + 32u * c, v);
         tmem_load_wait();
-        if (gi >= p.M) continue;
         uint32_t o2[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -337,11 +344,25 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         const int gj = n0 + 32 * c;
         if (p.c_vec && gj + 32 <= p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(crow + gj);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
-        } else {
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t u = static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+            *reinterpret_cast<uint4*>(stg + lane * 64 + u * 16) =
+                make_uint4(o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = (lane >> 2) + 8 * i;        // row of this warp's 32
+            const int j = lane & 3;                   // its 16-byte unit (8 columns)
+            const uint32_t u = static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(r) >> 1) & 3u);
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 64 + u * 16);
+            const int grow = m0 + 32 * q + r;
+            if (grow < p.M)
+              *reinterpret_cast<uint4*>(c16 + static_cast<int64_t>(grow) * p.ldc + gj + 8 * j) = val;
+          }
+          __syncwarp();                               // the tile is read before it is reused
+        } else if (gi < p.M) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (gj + j < p.N) crow[gj + j] = static_cast<uint16_t>(o2[j >> 1] >> (16 * (j & 1)));
