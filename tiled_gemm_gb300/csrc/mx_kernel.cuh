@@ -6,7 +6,8 @@
 // block-scaled MMA, tcgen05 kind::mxf8f6f4.block_scale with the scale factors already
 // in Tensor Memory).  fp32 accumulation in Tensor Memory; fp16 or bf16 out.
 //
-// One CTA per 128 x BN tile of C (BN = 128 or 256), 256 threads:
+// Tiles of 128 x BN of C (BN = 128 or 256); a persistent grid of at most one CTA per SM,
+// each CTA walking tiles blockIdx.x, + gridDim.x, ...; 256 threads:
 //   warp 0 (one thread)  TMA producer: a stage is 128 K bytes of A (128 rows) and of B
 //                        (128 rows), 128-byte swizzle, S stages in a ring; every
 //                        kMxGroup stages also the tile's scale bytes for those stages
@@ -18,8 +19,9 @@
 //                        quadrant can write its Tensor Memory lanes, so these four warps
 //                        copy each stage's scales there from shared memory (tcgen05.st)
 //                        ahead of the MMA;
-//                        after the last stage they read the accumulator, apply ReLU,
-//                        cast and store the tile.
+//                        after a tile's last stage they read the accumulator (freeing
+//                        it for the next tile, whose loads are already in flight), apply
+//                        ReLU, cast and store the tile.
 //
 // Scale layout in Tensor Memory for M = 128, N = 128 or 256 and one scale per 32
 // elements (found with an exact probe: operands of ones, distinct power-of-two
@@ -67,6 +69,8 @@ enum MxWaitSite : uint32_t {
 struct MxParams {
   int32_t M, N, K;
   int32_t k_blocks;           // ceil(K / 128)
+  int32_t tiles_n;            // ceil(N / BN)
+  int32_t num_tiles;          // ceil(M / 128) * tiles_n
   void* C;
   int64_t ldc;
   int32_t relu;
@@ -79,10 +83,10 @@ struct MxParams {
 template <int BN>
 __host__ __device__ constexpr uint32_t mx_smem_bytes() {
   // +1024 alignment slack; operand stages; two scale buffers; barriers (full, empty,
-  // sf_full per stage, sg_full and sg_empty per scale buffer, acc_full); Tensor Memory
+  // sf_full per stage, sg_full and sg_empty per scale buffer, acc_full, acc_empty); Tensor Memory
   // slot, abort flag and the laps of the last loads (stages, then scale buffers)
   return 1024u + kMxStages * MxTile<BN>::kStageBytes + 2u * MxTile<BN>::kScaleBytes +
-         kMxEpiBytes + 8u * (3 * kMxStages + 5) + 16u + 4u * (kMxStages + 2);
+         kMxEpiBytes + 8u * (3 * kMxStages + 6) + 16u + 4u * (kMxStages + 2);
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scales: B scale id (bits 4-5),
@@ -157,7 +161,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   auto sg_full = [&](int t) { return sBar + 8u * (3 * S + t); };      // scale buffer loaded
   auto sg_empty = [&](int t) { return sBar + 8u * (3 * S + 2 + t); }; // scale buffer read
   const uint32_t acc_full = sBar + 8u * (3 * S + 4);
-  const uint32_t slot = acc_full + 8u;
+  const uint32_t acc_empty = sBar + 8u * (3 * S + 5);  // the epilogue has read the accumulator
+  const uint32_t slot = acc_empty + 8u;
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
@@ -166,8 +171,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m0 = static_cast<int>(blockIdx.y) * kMxBM;
-  const int n0 = static_cast<int>(blockIdx.x) * BN;
   const int n_blk = p.K / 32;
 
   if (threadIdx.x == 0) {
@@ -183,6 +186,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       lap_sg[t] = -1;
     }
     mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -201,38 +205,52 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
+  // The CTA's tiles: t = blockIdx.x, + gridDim.x, ...; tile t is rows 128 (t / tiles_n)
+  // and columns BN (t % tiles_n).  Every role walks the same list; the stage ring and the
+  // scale buffers run on across tiles (gs counts stages, gg groups of kMxGroup stages).
+  const int first = static_cast<int>(blockIdx.x);
+  const int step = static_cast<int>(gridDim.x);
+
   if (warp == 0) {
     // -------------------------------------------------------------- producer --
     if (lane == 0) {
       grid_dependency_wait();
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        if (kb % kMxGroup == 0) {
-          // the scale bytes of stages kb .. kb + kMxGroup - 1
-          const int g = kb / kMxGroup;
-          const int t = g & 1;
-          if (!wait_bounded<false>(sg_empty(t), (static_cast<uint32_t>(g >> 1) & 1u) ^ 1u,
-                                   abort_flag, p.timeout_ns)) {
+      int gs = 0, gg = 0;
+      bool ok = true;
+      for (int tile = first; ok && tile < p.num_tiles; tile += step) {
+        const int m0 = (tile / p.tiles_n) * kMxBM;
+        const int n0 = (tile % p.tiles_n) * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++gs) {
+          if (kb % kMxGroup == 0) {
+            // the scale bytes of stages kb .. kb + kMxGroup - 1
+            const int t = gg & 1;
+            if (!wait_bounded<false>(sg_empty(t), (static_cast<uint32_t>(gg >> 1) & 1u) ^ 1u,
+                                     abort_flag, p.timeout_ns)) {
+              record_timeout(p.status, abort_flag, kSiteMxEmpty);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(sg_full(t), T::kScaleBytes);
+            const uint32_t dst = sScale + t * T::kScaleBytes;
+            tma_load_2d(dst, &tmap_sa, sg_full(t), 4 * kb, m0);
+            tma_load_2d(dst + 4u * kMxGroup * kMxBM, &tmap_sb, sg_full(t), 4 * kb, n0);
+            lap_sg[t] = gg >> 1;
+            ++gg;
+          }
+          const int s = gs % S;
+          const int lap = gs / S;
+          if (!wait_bounded<false>(empty(s), (static_cast<uint32_t>(lap) & 1u) ^ 1u, abort_flag,
+                                   p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteMxEmpty);
+            ok = false;
             break;
           }
-          mbar_arrive_expect_tx(sg_full(t), T::kScaleBytes);
-          const uint32_t dst = sScale + t * T::kScaleBytes;
-          tma_load_2d(dst, &tmap_sa, sg_full(t), 4 * kMxGroup * g, m0);
-          tma_load_2d(dst + 4u * kMxGroup * kMxBM, &tmap_sb, sg_full(t), 4 * kMxGroup * g, n0);
-          lap_sg[t] = g >> 1;
+          mbar_arrive_expect_tx(full(s), T::kStageBytes);
+          const uint32_t dst = base + s * T::kStageBytes;
+          tma_load_2d(dst, &tmap_a, full(s), kb * kMxBK, m0);
+          tma_load_2d(dst + kA, &tmap_b, full(s), kb * kMxBK, n0);
+          lap_armed[s] = lap;
         }
-        const int s = kb % S;
-        const int lap = kb / S;
-        if (!wait_bounded<false>(empty(s), (static_cast<uint32_t>(lap) & 1u) ^ 1u, abort_flag,
-                                 p.timeout_ns)) {
-          record_timeout(p.status, abort_flag, kSiteMxEmpty);
-          break;
-        }
-        mbar_arrive_expect_tx(full(s), T::kStageBytes);
-        const uint32_t dst = base + s * T::kStageBytes;
-        tma_load_2d(dst, &tmap_a, full(s), kb * kMxBK, m0);
-        tma_load_2d(dst + kA, &tmap_b, full(s), kb * kMxBK, n0);
-        lap_armed[s] = lap;
       }
     }
   } else if (warp == 1) {
@@ -242,32 +260,42 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const uint64_t a_desc0 = smem_desc_sw128(base, 16u, 1024u);
       const uint64_t b_desc0 = smem_desc_sw128(base + kA, 16u, 1024u);
       bool ok = true;
-      for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = static_cast<uint32_t>(kb / S) & 1u;
-        if (!wait_bounded<false>(full(s), ph, abort_flag, p.timeout_ns)) {
-          record_timeout(p.status, abort_flag, kSiteMxFull);
+      int gs = 0, ti = 0;
+      for (int tile = first; ok && tile < p.num_tiles; tile += step, ++ti) {
+        // the accumulator is free once the epilogue has read the previous tile's
+        if (!wait_bounded<false>(acc_empty, (static_cast<uint32_t>(ti) & 1u) ^ 1u, abort_flag,
+                                 p.timeout_ns)) {
+          record_timeout(p.status, abort_flag, kSiteMxAcc);
           ok = false;
           break;
         }
-        if (!wait_bounded<false>(sf_full(s), ph, abort_flag, p.timeout_ns)) {
-          record_timeout(p.status, abort_flag, kSiteMxScales);
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t stage = (static_cast<uint64_t>(s) * T::kStageBytes) >> 4;
-        const uint32_t sfa = tmem_base + T::kSfCol + T::kSfStride * s;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++gs) {
+          const int s = gs % S;
+          const uint32_t ph = static_cast<uint32_t>(gs / S) & 1u;
+          if (!wait_bounded<false>(full(s), ph, abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteMxFull);
+            ok = false;
+            break;
+          }
+          if (!wait_bounded<false>(sf_full(s), ph, abort_flag, p.timeout_ns)) {
+            record_timeout(p.status, abort_flag, kSiteMxScales);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t stage = (static_cast<uint64_t>(s) * T::kStageBytes) >> 4;
+          const uint32_t sfa = tmem_base + T::kSfCol + T::kSfStride * s;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          // 32 K bytes per MMA: 32 B along the 128-byte swizzled row
-          mma_mx_ss(tmem_base, a_desc0 + stage + 2u * k, b_desc0 + stage + 2u * k,
-                    mx_scale_ids(p.idesc, static_cast<uint32_t>(k)), sfa, sfa + T::kSfB,
-                    (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {
+            // 32 K bytes per MMA: 32 B along the 128-byte swizzled row
+            mma_mx_ss(tmem_base, a_desc0 + stage + 2u * k, b_desc0 + stage + 2u * k,
+                      mx_scale_ids(p.idesc, static_cast<uint32_t>(k)), sfa, sfa + T::kSfB,
+                      (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(empty(s));           // frees the stage's operands and scales
         }
-        mma_commit(empty(s));             // frees the stage's operands and scales
+        if (ok) mma_commit(acc_full);
       }
-      if (ok) mma_commit(acc_full);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------- scales, then epilogue --
@@ -283,55 +311,67 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       if (!r && lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, site);
       return r;
     };
+    // This warp's 32 x 32 staging tile: row r's 64 bytes at 64 r, its four 16-byte units
+    // XOR-swizzled by (r/2) % 4.  Each thread writes its row of a chunk there, then every
+    // store instruction writes 8 rows x 64 contiguous bytes instead of 32 rows x 16 (the
+    // rows of C are ldc apart).
+    uint8_t* const stg = base_ptr + (sEpi - base) + static_cast<uint32_t>(q) * 2048u;
+    uint16_t* const c16 = reinterpret_cast<uint16_t*>(p.C);
     bool ok = true;
-    for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
-      const int g = kb / kMxGroup;
-      const int t = g & 1;
-      if (kb % kMxGroup == 0 &&
-          !(ok = wait_warp(sg_full(t), static_cast<uint32_t>(g >> 1) & 1u, kSiteMxScales)))
-        break;
-      // this thread's words: A for row m0 + row, B for columns n0 + 32c + lane (every
-      // quadrant writes all of B's, which each quadrant reads from its own lanes)
-      const uint8_t* grp = base_ptr + (sScale - base) + t * T::kScaleBytes;
-      const uint32_t wa = mx_scale_word(grp + row * 4 * kMxGroup, m0 + row, p.M, kb, n_blk);
-      uint32_t wb[BN / 32];
+    int gs = 0, gg = 0, ti = 0;
+    for (int tile = first; ok && tile < p.num_tiles; tile += step, ++ti) {
+      const int m0 = (tile / p.tiles_n) * kMxBM;
+      const int n0 = (tile % p.tiles_n) * BN;
+      int t = 0;                                    // scale buffer of the current group
+      for (int kb = 0; ok && kb < p.k_blocks; ++kb, ++gs) {
+        if (kb % kMxGroup == 0) {
+          t = gg & 1;
+          if (!(ok = wait_warp(sg_full(t), static_cast<uint32_t>(gg >> 1) & 1u, kSiteMxScales)))
+            break;
+        }
+        // this thread's words: A for row m0 + row, B for columns n0 + 32c + lane (every
+        // quadrant writes all of B's, which each quadrant reads from its own lanes)
+        const uint8_t* grp = base_ptr + (sScale - base) + t * T::kScaleBytes;
+        const uint32_t wa = mx_scale_word(grp + row * 4 * kMxGroup, m0 + row, p.M, kb, n_blk);
+        uint32_t wb[BN / 32];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        wb[c] = mx_scale_word(grp + 4 * kMxGroup * (kMxBM + 32 * c + lane), n0 + 32 * c + lane,
-                              p.N, kb, n_blk);
-      if (kb % kMxGroup == kMxGroup - 1 || kb == p.k_blocks - 1) {
+        for (int c = 0; c < BN / 32; ++c)
+          wb[c] = mx_scale_word(grp + 4 * kMxGroup * (kMxBM + 32 * c + lane), n0 + 32 * c + lane,
+                                p.N, kb, n_blk);
+        if (kb % kMxGroup == kMxGroup - 1 || kb == p.k_blocks - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sg_empty(t));     // this warp is done with the buffer
+          ++gg;
+        }
+        const int s = gs % S;
+        if (!(ok = wait_warp(empty(s), (static_cast<uint32_t>(gs / S) & 1u) ^ 1u, kSiteMxEmpty)))
+          break;
+        tc_fence_after_sync();
+        const uint32_t col = T::kSfCol + T::kSfStride * s;
+        tmem_store_1col(lane_base + col + static_cast<uint32_t>(q), wa);
+#pragma unroll
+        for (int c = 0; c < BN / 32; c += 4)
+          tmem_store_4cols(lane_base + col + T::kSfB + c, wb[c], wb[c + 1], wb[c + 2], wb[c + 3]);
+        tmem_store_wait();
+        tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sg_empty(t));       // this warp is done with the buffer
+        if (lane == 0) mbar_arrive(sf_full(s));
       }
-      const int s = kb % S;
-      if (!(ok = wait_warp(empty(s), (static_cast<uint32_t>(kb / S) & 1u) ^ 1u, kSiteMxEmpty)))
-        break;
-      tc_fence_after_sync();
-      const uint32_t col = T::kSfCol + T::kSfStride * s;
-      tmem_store_1col(lane_base + col + static_cast<uint32_t>(q), wa);
-#pragma unroll
-      for (int c = 0; c < BN / 32; c += 4)
-        tmem_store_4cols(lane_base + col + T::kSfB + c, wb[c], wb[c + 1], wb[c + 2], wb[c + 3]);
-      tmem_store_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sf_full(s));
-    }
-    if (ok && wait_warp(acc_full, 0, kSiteMxAcc)) {
+      if (!ok || !(ok = wait_warp(acc_full, static_cast<uint32_t>(ti) & 1u, kSiteMxAcc))) break;
       tc_fence_after_sync();
       const int gi = m0 + row;
-      uint16_t* const c16 = reinterpret_cast<uint16_t*>(p.C);
       uint16_t* crow = c16 + static_cast<int64_t>(gi) * p.ldc;
-      // This warp's 32 x 32 staging tile: row r's 64 bytes at 64 r, its four 16-byte units
-      // XOR-swizzled by (r/2) % 4.  Each thread writes its row of the chunk there, then
-      // every store instruction writes 8 rows x 64 contiguous bytes instead of 32 rows x
-      // 16 (the rows of C are ldc apart).
-      uint8_t* const stg = base_ptr + (sEpi - base) + static_cast<uint32_t>(q) * 2048u;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         tmem_load_32cols(lane_base + 32u * c, v);
         tmem_load_wait();
+        if (c == BN / 32 - 1) {
+          // the whole accumulator is in registers or stored: the next tile may overwrite it
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+        }
         uint32_t o2[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {

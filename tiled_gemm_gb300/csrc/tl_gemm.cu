@@ -1021,6 +1021,8 @@ tl_status launch_mx(const void* A, const void* B, const void* SA, const void* SB
   prm.N = static_cast<int32_t>(N);
   prm.K = static_cast<int32_t>(K);
   prm.k_blocks = static_cast<int32_t>(k_blocks);
+  prm.tiles_n = static_cast<int32_t>(ceil_div(N, BN));
+  prm.num_tiles = static_cast<int32_t>(ceil_div(M, tl::kMxBM) * prm.tiles_n);
   prm.C = C;
   prm.ldc = ldc;
   prm.relu = epilogue == TL_EPI_RELU ? 1 : 0;
@@ -1046,8 +1048,8 @@ tl_status launch_mx(const void* A, const void* B, const void* SA, const void* SB
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(N, BN)),
-                     static_cast<unsigned>(ceil_div(M, tl::kMxBM)));
+  // persistent: at most one CTA per SM (the shared memory allows no more)
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(prm.num_tiles, st->sms)));
   cfg.blockDim = dim3(tl::kMxThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
@@ -1069,7 +1071,8 @@ tl_status run_mx(const void* A, const void* B, const void* SA, const void* SB, v
   if (c_type != TL_F16 && c_type != TL_BF16) return TL_ERR_INVALID_ARG;
   if (epilogue != TL_EPI_NONE && epilogue != TL_EPI_RELU) return TL_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TL_OK;
-  if (M > INT32_MAX - tl::kMxBM || N > INT32_MAX - 256 || K > INT32_MAX - tl::kMxBK)
+  if (M > INT32_MAX - tl::kMxBM || N > INT32_MAX - 256 || K > INT32_MAX - tl::kMxBK ||
+      ceil_div(M, tl::kMxBM) * ceil_div(N, 128) > INT32_MAX)
     return TL_ERR_UNSUPPORTED;
   if (ldc < N) return TL_ERR_INVALID_ARG;
   if (C == nullptr) return TL_ERR_NULL_PTR;
