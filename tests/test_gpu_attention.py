@@ -13,6 +13,7 @@ import torch
 
 import oracle
 import tiled_gemm_gb300 as tl
+import workloads
 from gpu_helpers import assert_bit_exact, assert_within_tolerance
 
 pytestmark = pytest.mark.gpu
@@ -67,6 +68,50 @@ def test_attention_against_oracle(B, S, H, D, causal, dtype):
     got = _run(q, k, v, causal)
     ref = oracle.attention(q, k, v, dtype=code, causal=causal)
     assert_within_tolerance(got.reshape(-1, D), ref.reshape(-1, D), code)
+
+
+def _sampled_rows(B, S, H, rng, n):
+    """Row indices spread over every batch, head and position, with the first and last
+    query of every 128-tile among them."""
+    bs = rng.integers(0, B, n)
+    hs = rng.integers(0, H, n)
+    is_ = rng.integers(0, S, n)
+    edges = np.unique(np.clip(np.concatenate([np.arange(0, S, 128), np.arange(127, S, 128),
+                                              [S - 1]]), 0, S - 1))
+    m = min(edges.size, n // 2)
+    is_[:m] = edges[:m]
+    return bs, is_, hs
+
+
+# More units (128-query tiles of a batch and head) than SMs: every CTA walks several, and
+# causal work goes in pairs of tiles (n-1-k, k) -- S = 1920 has an odd tile count, so one
+# pair is a single middle tile.
+WALK_CASES = [(2, 2048, 40, 64, True), (2, 2048, 40, 64, False), (2, 1920, 24, 128, True),
+              (1, 4000, 20, 128, False)]
+
+
+@pytest.mark.parametrize("B,S,H,D,causal", WALK_CASES)
+def test_attention_many_units_per_cta_sampled(B, S, H, D, causal):
+    dtype = torch.bfloat16
+    q, k, v = _inputs(B, S, H, D, dtype, 7000 + S + H + int(causal))
+    got = _run(q, k, v, causal).reshape(B, S, H, D)
+    rng = np.random.default_rng(S + H)
+    bs, is_, hs = _sampled_rows(B, S, H, rng, 600)
+    ref = oracle.attention_rows(q, k, v, bs, is_, hs, dtype=oracle.BF16, causal=causal)
+    assert_within_tolerance(got[bs, is_, hs], ref, oracle.BF16)
+
+
+@pytest.mark.parametrize("name", ["attn_fwd_b4_h32_s4096_d128_causal_bf16",
+                                  "attn_fwd_b4_h32_s4096_d128_bf16"])
+def test_attention_workloads_sampled(name):
+    w = workloads.ATTN_WORKLOADS[name]
+    q, k, v = workloads.make_attn_inputs(w)
+    got = _run(q, k, v, w.causal).reshape(w.B, w.S, w.H, w.D)
+    rng = np.random.default_rng(13)
+    bs, is_, hs = _sampled_rows(w.B, w.S, w.H, rng, 400)
+    code = oracle.F16 if w.dtype == workloads.F16 else oracle.BF16
+    ref = oracle.attention_rows(q, k, v, bs, is_, hs, dtype=code, causal=w.causal)
+    assert_within_tolerance(got[bs, is_, hs], ref, code)
 
 
 @pytest.mark.parametrize("causal", [False, True])
