@@ -356,3 +356,68 @@ def test_alias_is_rejected_on_device_buffers():
 def test_device_status_clean_after_all_calls():
     st, word = tl.tl_device_status(reset=False)
     assert st == tl.TL_OK, f"bounded wait gave up: {word:#x}"
+
+
+def test_concurrent_streams_and_host_threads():
+    # Two host threads, each with its own stream, enqueue split GEMMs (stream-K forced,
+    # so each call has its own partial-sum workspace and flags), block-scaled products
+    # and attention back to back with no synchronisation between them.  Every result
+    # must still be the oracle's.
+    import threading
+
+    from test_gpu_mx import _oracle as mx_oracle
+    plan = tl.plan_for(0, 0, 0, 128, 128, 64, 3, raster_group=3, stream_k=1)
+    jobs = []
+    for t in range(2):
+        w = _w(700, 900, 2100, F16, False, True, True, "int_small", 80 + t)
+        a, b = workloads.make_inputs(w)
+        wm = workloads.MxWorkload("c", 300, 500, 1024, dist="int_small", sf_lo=126, sf_hi=128,
+                                  seed=90 + t)
+        am, bm, sam, sbm = workloads.make_mx_inputs(wm)
+        g = torch.Generator().manual_seed(95 + t)
+        qkv = [torch.randn((2, 600, 4, 64), generator=g).to(torch.bfloat16) for _ in range(3)]
+        jobs.append({
+            "w": w, "a": a, "b": b, "wm": wm, "mx": (am, bm, sam, sbm), "qkv": qkv,
+            "dev": [x.cuda() for x in (a, b)], "dev_mx": [x.cuda() for x in (am, bm, sam, sbm)],
+            "dev_qkv": [x.cuda() for x in qkv],
+            "out_g": [torch.empty((w.M, w.N), dtype=torch.float16, device="cuda") for _ in range(3)],
+            "out_m": [torch.empty((wm.M, wm.N), dtype=torch.bfloat16, device="cuda") for _ in range(3)],
+            "out_a": [torch.empty((2, 600, 4, 64), dtype=torch.bfloat16, device="cuda")
+                      for _ in range(3)]})
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(job):
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            for rep in range(3):
+                tl.gemm(job["dev"][0], job["dev"][1], trans_b=True, relu=True,
+                        out=job["out_g"][rep], plan=plan, stream=s)
+                tl.gemm_mx(*job["dev_mx"], out=job["out_m"][rep], stream=s)
+                tl.attention(*job["dev_qkv"], causal=True, out=job["out_a"][rep], stream=s)
+            s.synchronize()
+        except Exception as e:          # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(j,)) for j in jobs]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    st, word = tl.tl_device_status(reset=True)
+    assert st == tl.TL_OK, hex(word)
+    for job in jobs:
+        w, wm = job["w"], job["wm"]
+        ref_g = oracle_full(job["a"], job["b"], w.M, w.N, w.K, w.dtype, False, True, True)
+        ref_m = mx_oracle(wm, *job["mx"])
+        ref_a = oracle.attention(*job["qkv"], dtype=oracle.BF16, causal=True)
+        for rep in range(3):
+            assert_bit_exact(job["out_g"][rep].cpu().view(torch.int16).numpy().view(np.uint16),
+                             ref_g)
+            assert_bit_exact(job["out_m"][rep].cpu().view(torch.int16).numpy().view(np.uint16),
+                             ref_m)
+            got_a = job["out_a"][rep].cpu().view(torch.int16).numpy().view(np.uint16)
+            assert_within_tolerance(got_a.reshape(-1, 64), ref_a.reshape(-1, 64), oracle.BF16)
