@@ -4,6 +4,10 @@
  *   C = epi(op(A) . op(B)),  epi in {identity, ReLU},  fp16/bf16 in and out,
  *   fp32 accumulation in Tensor Memory, round-to-nearest-even on the output.
  *
+ * The same pipeline also serves 8-bit operands (tl_gemm_fp8: one product scale;
+ * tl_gemm_mx: one E8M0 scale per 32 K elements) and the attention forward pass
+ * (tl_attention_fwd); each declaration below states its own semantics and sources.
+ *
  * Sources of the semantics (the pages the operation is described on):
  *   - The tiled GEMM itself: the quickstart kernel copies A and B tiles global ->
  *     shared, multiplies them into an fp32 accumulator under a multi-stage
