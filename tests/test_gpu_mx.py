@@ -174,3 +174,16 @@ def test_workloads_sampled(name):
     ref = oracle.gemm_mx_entries(a, b, sa, sb, w.M, w.N, w.K, rows, cols, sfa_ld=wi.sf_ld,
                                  sfb_ld=wi.sf_ld)
     assert_bit_exact(got[rows, cols], ref)
+
+
+def test_narrow_tiles_many_per_cta_sampled():
+    # N <= 128 takes the 128-wide tile; 157 tiles over at most one CTA per SM, so CTAs
+    # walk several, with K not a multiple of 128 (a partial last stage and scale group)
+    w = _w(20000, 100, 1312, 58, exact=True)
+    a, b, sa, sb = workloads.make_mx_inputs(w)
+    got = run_mx(w, a, b, sa, sb)
+    rng = np.random.default_rng(14)
+    rows, cols = sample_indices(w.M, w.N, 3000, rng, bm=128, bn=128)
+    ref = oracle.gemm_mx_entries(a, b, sa, sb, w.M, w.N, w.K, rows, cols, sfa_ld=w.sf_ld,
+                                 sfb_ld=w.sf_ld)
+    assert_bit_exact(got[rows, cols], ref)
