@@ -127,6 +127,24 @@ def test_stream_k_split_choices():
         tl.tl_plan_complete(64, 64, 64, 128, 64, 64, 3, stream_k=2)
 
 
+def test_one_wave_of_narrow_tiles():
+    # every 128 x 64 tile of C has an SM of its own and K is moderate: whole 128 x 64 x 128
+    # tiles, one per CTA, in every layout
+    for M, N, K, ta, tb in ((1024, 1024, 1024, 0, 0), (768, 768, 2048, 1, 0),
+                            (512, 2048, 4096, 0, 1), (1024, 1024, 6144, 1, 1),
+                            (8 * 128, 19 * 64, 1024, 0, 0)):
+        p = tl.tl_gemm_plan(M, N, K, trans_a=ta, trans_b=tb, num_sms=152)
+        assert (p.bm, p.bn, p.bk, p.stages, p.swap_ab) == (128, 64, 128, 4, 0)
+        assert p.sk_iters == 0 and p.grid == p.tiles <= 152
+    # one tile more than SMs, long or short K, 8-bit operands, skinny M: the other rules
+    assert tl.tl_gemm_plan(8 * 128, 19 * 64 + 1, 1024, num_sms=152).bn != 64
+    assert tl.tl_gemm_plan(1024, 1024, 1024, num_sms=100).bm == 256
+    assert tl.tl_gemm_plan(1024, 1024, 16384, num_sms=152).bm == 256
+    assert tl.tl_gemm_plan(1024, 1024, 512, num_sms=152).bk != 128
+    assert tl.tl_gemm_plan(1024, 1024, 2048, dtype=tl.TL_E4M3, trans_b=1, num_sms=152).bk == 256
+    assert tl.tl_gemm_plan(16, 2048, 1024, num_sms=152).swap_ab == 1
+
+
 def test_skinny_products_swap_operands():
     # M <= 32 against long N and K: the kernel runs on C^T with M as the MMA's N,
     # the 64 tiles of 128 rows of C^T split by k-block over all SMs

@@ -146,6 +146,20 @@ def test_narrow_tiles_without_swap(bn, stages):
     _check_full(_w(300, bn - 3, 1300, F16, True, True, False, "uniform", 72 + bn), plan=plan)
 
 
+@pytest.mark.parametrize("ta,tb", list(itertools.product([False, True], repeat=2)))
+def test_one_wave_of_narrow_tiles_auto_plan(ta, tb):
+    # the planner's own pick when every 128 x 64 tile has an SM: ragged M, N and K, the
+    # last k-block partial
+    M, N, K = 700, 650, 1100
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = tl.tl_gemm_plan(M, N, K, F16, int(ta), int(tb), sms)
+    assert (p.bm, p.bn, p.bk, p.sk_iters) == (128, 64, 128, 0)
+    if ta == tb:
+        _check_full(_w(M, N, K, F16, ta, tb, True, "int_small", 81 + ta), exact=True)
+    else:
+        _check_full(_w(M, N, K, BF16, ta, tb, False, "uniform", 85 + ta))
+
+
 @pytest.mark.parametrize("bm,bn,bk,stages", [(128, 64, 64, 4), (128, 256, 128, 2),
                                              (256, 128, 64, 3), (256, 256, 128, 3)])
 def test_plain_stores_instead_of_tma_stores(bm, bn, bk, stages):

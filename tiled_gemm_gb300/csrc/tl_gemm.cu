@@ -317,6 +317,26 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, in
     pl->swap_ab = 1;
     return;
   }
+  // One wave of narrow tiles.  When every 128 x 64 tile of C gets an SM of its own, the
+  // call lasts one tile's k-loop plus its fill and epilogue.  Each k-block is paced by
+  // the bytes the SM loads (A's 128 rows plus B's share; about 64 B per clock from L2),
+  // which is the same 48 KB for a 128 x 64 tile as for one CTA of a 256 x 128 pair.  So
+  // the narrow tile, which puts the most SMs to work and has the shortest epilogue,
+  // finishes first.  Measured on GB300 (fp16, ReLU) it beats the pair tiles that the cost
+  // model below would pick:
+  //   1024^3              8.25 us vs  9.72 us
+  //   768 x 768 x 2048   11.5 us  vs 13.0 us
+  //   512 x 2048 x 4096  18.9 us  vs 25.4 us
+  // Past about K = 6144, pair tiles split by k-block over all SMs catch up, and they
+  // win by 1024 x 1024 x 16384 (44.5 us vs 60.9 us).
+  if (eb == 2 && K >= 1024 && K <= 6144 &&
+      ceil_div(M, 128) * ceil_div(N, 64) <= static_cast<int64_t>(sms)) {
+    pl->bm = 128;
+    pl->bn = 64;
+    pl->bk = 128;
+    pl->stages = 4;
+    return;
+  }
   // Relative time of one tile per unit of K.  Shared memory (~128 B/clk per SM)
   // carries both the TMA writes and the MMA operand reads, so a 1-CTA 128 x N tile
   // needs 128 (128 + N) / N bytes per MMA cycle: 192 for N = 256, 256 for N = 128;
