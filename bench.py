@@ -104,6 +104,33 @@ def is_hbm_bound(w: workloads.Workload, peaks: dict) -> bool:
     return w.flops / w.bytes_moved < ridge
 
 
+def roofline(w, avg_launch_ms: float, peaks: dict, peaks_src: str, clocks, attn: bool) -> dict:
+    """The dominant kernel against its roofline: algorithmic flops (or bytes, for a
+    product under the ridge point) per launch over the average launch time, and the
+    fraction of the measured peak.  fp16 and bf16 share the dense tensor rate; 8-bit
+    operands take it times FP8_OVER_BF16.  The sustained figure (cuBLAS looping under
+    the power cap) applies when the timed region ran under the power cap (sw_power_cap
+    seen in the clock samples); otherwise the burst one."""
+    hbm = False if attn else is_hbm_bound(w, peaks)
+    capped = "sw_power_cap" in ((clocks or {}).get("reasons") or [])
+    if hbm:
+        achieved = w.bytes_moved / (avg_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}
+    else:
+        achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
+        peak = tensor_peak_scale(w) * peaks["bf16_tflops_sustained" if capped else "bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s"}
+    roof["frac"] = round(achieved / peak, 4)
+    roof["peak_source"] = (f"{peaks_src} ({'copy' if hbm else 'sustained, power cap seen' if capped else 'burst'})"
+                           + (" bf16 x 2 for 8-bit operands" if tensor_peak_scale(w) > 1 and not hbm
+                              else ""))
+    if not hbm:
+        roof["frac_of_burst"] = round(achieved / (tensor_peak_scale(w) * peaks["bf16_tflops"]), 4)
+    return roof
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 50 ms while the timed region runs."""
 
@@ -137,28 +164,36 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                    power.append(float(parts[3]))
-                except ValueError:
-                    continue
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(name)
+            lines = f.readlines()
         os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
-                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+        return summarise_clocks(lines)
+
+
+def summarise_clocks(lines) -> dict:
+    """Median SM clock over the busy samples (above half the highest), the highest clock
+    limit and power seen, and every throttle reason that was active in any sample.  Each
+    line is one `nvidia-smi --format=csv,noheader,nounits` row of ClockSampler.QUERY."""
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+            power.append(float(parts[3]))
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+    return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+            "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ CPU oracle ----
@@ -683,27 +718,7 @@ def main():
     total_ms = res["total_ms"]
     value = whole_job_tflops(w.flops, args.steps, world, total_ms)
     avg_launch_ms = total_ms / args.steps        # back-to-back launches in the graph
-    hbm = False if attn else is_hbm_bound(w, peaks)
-    if hbm:
-        achieved = w.bytes_moved / (avg_launch_ms * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}
-    else:
-        achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
-        # fp16 and bf16 share the dense tensor rate; 8-bit operands take it times
-        # FP8_OVER_BF16.  The sustained figure (cuBLAS looping under the power cap)
-        # applies when the timed region ran under the power cap (sw_power_cap seen in
-        # the clock samples); otherwise the burst one.
-        capped = "sw_power_cap" in ((res.get("clocks") or {}).get("reasons") or [])
-        peak = tensor_peak_scale(w) * peaks["bf16_tflops_sustained" if capped else "bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s"}
-    roof["frac"] = round(achieved / peak, 4)
-    roof["peak_source"] = (f"{peaks_src} ({'copy' if hbm else 'sustained, power cap seen' if capped else 'burst'})"
-                           + (" bf16 x 2 for 8-bit operands" if tensor_peak_scale(w) > 1 and not hbm
-                              else ""))
-    if not hbm:
-        roof["frac_of_burst"] = round(achieved / (tensor_peak_scale(w) * peaks["bf16_tflops"]), 4)
+    roof = roofline(w, avg_launch_ms, peaks, peaks_src, res.get("clocks"), attn)
     roof["traffic"] = load_traffic(w.name)
     roof["kernel_ms"] = round(avg_launch_ms, 6)
     roof["algorithmic"] = {"flops_per_launch": w.flops, "bytes_per_launch": w.bytes_moved}

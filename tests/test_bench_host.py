@@ -1,0 +1,152 @@
+"""The benchmark's host-side bookkeeping on CPU: the roofline figures, the clock and
+throttle summary, the gate that reports DRAM traffic only for the kernel sources it was
+captured on, and the JSON line of both arms.  No GPU and no nvidia-smi: the clock
+samples are written here, and the GPU leg of the library arm is replaced by its result
+record."""
+import json
+import os
+
+import pytest
+
+import bench
+import workloads
+
+PEAKS = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+
+
+def test_tensor_bound_roofline_takes_burst_or_sustained_peak():
+    w = workloads.WORKLOADS["gemm_relu_1024_f16_128x128x64s3"]
+    assert w.flops == 2 * 1024 ** 3
+    r = bench.roofline(w, 0.01, PEAKS, "measured", {"reasons": []}, attn=False)
+    achieved = 2 * 1024 ** 3 / 1e-5 / 1e12
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(achieved, abs=0.05)
+    assert r["peak"] == 2000.0 and r["frac"] == pytest.approx(achieved / 2000.0, abs=1e-4)
+    assert "burst" in r["peak_source"]
+    capped = bench.roofline(w, 0.01, PEAKS, "measured", {"reasons": ["sw_power_cap"]}, False)
+    assert capped["peak"] == 1600.0
+    assert capped["frac"] == pytest.approx(achieved / 1600.0, abs=1e-4)
+    assert capped["frac_of_burst"] == pytest.approx(achieved / 2000.0, abs=1e-4)
+    assert "power cap" in capped["peak_source"]
+    # no clock record at all: the burst peak
+    assert bench.roofline(w, 0.01, PEAKS, "fallback", None, False)["peak"] == 2000.0
+
+
+def test_eight_bit_operands_double_the_tensor_peak():
+    w = workloads.WORKLOADS["gemm_8192_e4m3_tb"]
+    r = bench.roofline(w, 1.0, PEAKS, "measured", {"reasons": []}, attn=False)
+    assert r["peak"] == 2 * 2000.0 and "8-bit" in r["peak_source"]
+    assert r["frac"] == pytest.approx(w.flops / 1e-3 / 1e12 / 4000.0, abs=1e-4)
+
+
+def test_skinny_product_is_measured_against_memory_bandwidth():
+    w = workloads.WORKLOADS["gemm_m16_n8192_k8192_bf16"]
+    # 16 x 8192 x 8192: about 16 flops per byte, far under the ridge point (~333 here)
+    assert w.flops / w.bytes_moved < PEAKS["bf16_tflops"] * 1e12 / (PEAKS["hbm_gbs"] * 1e9)
+    assert bench.is_hbm_bound(w, PEAKS)
+    assert not bench.is_hbm_bound(workloads.WORKLOADS["gemm_8192_bf16_tb"], PEAKS)
+    r = bench.roofline(w, 0.025, PEAKS, "measured", {"reasons": ["sw_power_cap"]}, False)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6000.0
+    assert r["achieved"] == pytest.approx(w.bytes_moved / 2.5e-5 / 1e9, abs=0.05)
+    assert "frac_of_burst" not in r
+
+
+def test_attention_is_always_a_contraction():
+    w = workloads.ATTN_WORKLOADS["attn_fwd_b4_h32_s4096_d128_bf16"]
+    r = bench.roofline(w, 1.0, PEAKS, "measured", {"reasons": []}, attn=True)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0
+
+
+def _row(sm, power, reasons=()):
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    flags = ["Active" if n in reasons else "Not Active" for n in names]
+    return ", ".join(["0", str(sm), "2070", str(power), "0x0"] + flags) + "\n"
+
+
+def test_clock_summary_takes_the_median_of_busy_samples_and_every_reason_seen():
+    lines = [_row(345, 110.0), _row(2070, 800.0), _row(1890, 1390.5, ["sw_power_cap"]),
+             _row(1950, 1200.0), "garbage line\n", "0, [N/A], 2070, 5, 0x0, a, b, c, d\n",
+             _row(2070, 900.0)]
+    c = bench.summarise_clocks(lines)
+    # the idle 345 MHz sample is under half the highest and is left out of the median
+    assert c["sm_mhz"] == pytest.approx(2010.0)
+    assert c["sm_max_mhz"] == 2070.0 and c["power_w_max"] == 1390.5
+    assert c["samples"] == 5 and c["reasons"] == ["sw_power_cap"]
+    hot = bench.summarise_clocks([_row(1200, 700.0, ["hw_thermal_slowdown", "hw_slowdown"])])
+    assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.summarise_clocks([])["reasons"] == ["no samples"]
+
+
+def test_traffic_is_reported_only_for_the_sources_it_was_captured_on(monkeypatch):
+    with open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")) as f:
+        table = json.load(f)
+    name = "gemm_relu_1024_f16_128x128x64s3"
+    entry = table[name]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: entry["kernel_source_hash"])
+    assert bench.load_traffic(name) == entry["dram_bytes_per_launch"]
+    assert bench.load_traffic("no_such_workload") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.load_traffic(name) is None
+
+
+def test_source_hash_covers_every_kernel_source():
+    for rel in bench.KERNEL_SOURCES:
+        assert os.path.exists(os.path.join(bench.ROOT, rel)), rel
+    csrc = os.path.join(bench.ROOT, "tiled_gemm_gb300", "csrc")
+    kernels = {f"tiled_gemm_gb300/csrc/{f}" for f in os.listdir(csrc)
+               if f.endswith((".cu", ".cuh"))}
+    assert kernels <= set(bench.KERNEL_SOURCES)
+
+
+CONTRACT_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                 "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"}
+
+
+def _main_line(monkeypatch, capsys, argv):
+    monkeypatch.setattr("sys.argv", ["bench.py"] + argv)
+    bench.main()
+    out = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(out) == 1
+    return json.loads(out[0])
+
+
+def test_json_line_of_the_library_arm(monkeypatch, capsys):
+    # the GPU leg replaced by its result record: 10 steps of 0.01 ms each
+    import torch
+    monkeypatch.setattr(torch.cuda, "set_device", lambda *_: None)
+    clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    fake = {"total_ms": 0.1, "rotation_sets": 42, "launches_per_step": 1, "clocks": clocks,
+            "plan": {"bm": 128}, "e2e": {"value": 50.0, "unit": "TFLOP/s",
+                                         "h2d_bytes_per_step": 4 << 20,
+                                         "d2h_bytes_per_step": 2 << 20}}
+    monkeypatch.setattr(bench, "run_tl", lambda *a: fake)
+    d = _main_line(monkeypatch, capsys, ["--steps", "10", "--warmup", "3", "--no-cpu-baseline"])
+    assert CONTRACT_KEYS <= set(d)
+    w = workloads.WORKLOADS[workloads.HEADLINE]
+    assert d["config"]["workload"] == workloads.HEADLINE and d["n_gpus"] == 1
+    assert d["value"] == pytest.approx(w.flops * 10 / 1e-4 / 1e12, rel=1e-4)
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None and d["dtype"] == "f16"
+    assert d["gpu_launches"] == 10 and d["clocks"] == clocks
+    assert d["roofline"]["bound"] == "tensor" and d["roofline"]["kernel_ms"] == 0.01
+    assert d["roofline"]["algorithmic"]["flops_per_launch"] == w.flops
+    assert "42 sets" in d["config"]["l2"]
+
+
+def test_json_line_of_the_reference_arm(monkeypatch, capsys):
+    # the oracle's timing replaced by a fixed rate: the line carries the arm's own keys
+    monkeypatch.setattr(bench, "oracle_rate",
+                        lambda w, a, b, budget, threads: (0.004, 0.5, 2e9, 64, 3))
+    d = _main_line(monkeypatch, capsys, ["--impl", "reference", "--steps", "2",
+                                         "--warmup", "3"])
+    assert d["impl"] == "reference" and d["value"] == 0.004 and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == 0.004
+    assert d["e2e"] == {"value": 0.004, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == workloads.HEADLINE
+
+
+def test_warmup_below_three_is_refused(monkeypatch):
+    monkeypatch.setattr("sys.argv", ["bench.py", "--warmup", "2"])
+    with pytest.raises(SystemExit):
+        bench.main()

@@ -37,7 +37,7 @@ def _rank_main(rank: int, world: int, port: int, times, out):
 def test_two_gloo_ranks_agree_on_the_slowest_time_and_step_count():
     world, port = 2, _free_port()
     times = [12.5, 17.25]
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()    # no fork of a threaded test process
     out = manager.dict()
     mp.spawn(_rank_main, args=(world, port, times, out), nprocs=world, join=True)
     assert out[0] == out[1] == (17.25, 101)
