@@ -104,8 +104,15 @@ def assert_within_tolerance(got_bits, ref_bits, dtype_code, rtol=1e-2, atol=1e-2
     assert np.all(np.isfinite(got)), "non-finite output"
     err = np.abs(got - ref)
     bad = err > atol + rtol * np.abs(ref)
+    ref_max = float(np.abs(ref).max(initial=0.0))
+    ref_rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
     stats = {"max_abs": float(err.max(initial=0.0)),
              "max_rel": float((err / np.maximum(np.abs(ref), 1e-30)).max(initial=0.0)),
+             # scale-free figures: the largest error over the largest output, and the
+             # RMS error over the RMS output (0 where the reference is all zero)
+             "norm_max": float(err.max(initial=0.0)) / ref_max if ref_max > 0 else 0.0,
+             "rel_rms": (float(np.sqrt(np.mean(err * err))) / ref_rms
+                         if ref_rms > 0 else 0.0),
              "mismatch": float(bad.mean()) if bad.size else 0.0}
     assert not bad.any(), f"{int(bad.sum())} of {bad.size} outside tolerance; {stats}"
     return stats

@@ -7,6 +7,7 @@ Bars:
 * full-size workloads: every element on the tile edges plus random entries against
   the oracle computed one by one, and the canary guard band for coverage.
 """
+import dataclasses
 import itertools
 
 import numpy as np
@@ -300,6 +301,26 @@ def test_large_workloads_sampled(name):
     refv = oracle.decode(ref, w.dtype)
     scale = np.abs(refv).max()
     assert stats["max_abs"] <= scale * 2.0 ** -6, (stats, scale)
+
+
+def test_unit_variance_variant_of_the_square_workload_sampled():
+    # "N(0,1)/sqrt(K) entries" read for both operands gives C a standard deviation of
+    # 1/sqrt(K) = 1/64, where the absolute 1e-2 term of the tolerance is loose.  With
+    # A ~ N(0,1) and only B scaled, C ~ N(0,1) and the relative term decides.
+    w = dataclasses.replace(workloads.WORKLOADS["gemm_4096_bf16_tb"], name="unit_variance",
+                            dist_a="normal", seed=12)
+    a, b = workloads.make_inputs(w)
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu)
+    c.check_guards()
+    rng = np.random.default_rng(8)
+    rows, cols = sample_indices(w.M, w.N, 6000, rng)
+    ref = oracle.gemm_entries(a, b, w.M, w.N, w.K, rows, cols, dtype=w.dtype,
+                              trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu)
+    stats = assert_within_tolerance(got[rows, cols], ref, w.dtype)
+    assert 0.8 < np.std(oracle.decode(ref, w.dtype)) < 1.25
+    # the fp32 sum and the binary64 sum round to the same bf16 value except near ties,
+    # where they differ by one unit in the last place (2^-7 relative at most)
+    assert stats["norm_max"] <= 2.0 ** -6 and stats["rel_rms"] <= 2.0 ** -7, stats
 
 
 @pytest.mark.parametrize("name", ["gemm_8192_bf16_tb", "gemm_relu_3000x5000x4100_f16",
