@@ -25,14 +25,15 @@ GOLDEN = os.path.join(ROOT, "tests", "golden", "pages_resource_numbers.json")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tl_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(tl_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for required in ("tl_gemm", "tl_gemm_plan", "tl_gemm_with_plan", "tl_plan_complete",
-                     "tl_status_string", "tl_device_status", "tl_set_wait_timeout_ns",
-                     "tl_version"):
+                     "tl_gemm_fp8", "tl_gemm_mx", "tl_attention_fwd", "tl_gemm_noalloc",
+                     "tl_gemm_noalloc_scratch_bytes", "tl_status_string", "tl_device_status",
+                     "tl_set_wait_timeout_ns", "tl_version"):
         assert required in names
 
 
