@@ -1,7 +1,8 @@
 """Host-side checks of the C ABI that need no GPU.
 
 * The shared library loads and exports every function that include/tl_gemm.h
-  declares.
+  declares, and the Python binding passes every argument with the width and kind
+  (pointer, 4- or 8-byte integer, float) that the header declares.
 * The host planner reproduces the pages' printed resource numbers for the
   quickstart tiling (tests/golden/pages_resource_numbers.json): 16 KB per operand
   tile, 64/96/128 KB of operand ring for 2/3/4 stages, B ring at offset 48 KB,
@@ -239,3 +240,55 @@ def test_fp8_plans():
     for bm, bn in ((128, 64), (256, 128)):
         with pytest.raises(tl.TLError):
             tl.tl_plan_complete(1024, 1024, 1024, bm, bn, 128, 4, dtype=tl.TL_E4M3, trans_b=0)
+
+
+def _prototypes():
+    """{name: (return type, [parameter types])} from the header's declarations."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w \t\*]*?)\s*\b(tl_[a-z0-9_]+)\s*\(([^)]*)\)\s*;",
+                                        text):
+        params = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
+        # drop the parameter name: the type is everything before the last identifier
+        types = [re.sub(r"\s*\b\w+$", "", p) if re.search(r"[\w\*]\s+\w+$|\*\w+$", p) else p
+                 for p in params]
+        protos[name] = (ret.strip(), types)
+    return protos
+
+
+def _c_kind(t: str) -> str:
+    t = t.replace("const", "").strip()
+    if "*" in t or t == "tl_stream_t":
+        return "ptr"
+    if t in ("int64_t", "uint64_t"):
+        return "8"
+    if t in ("int", "int32_t", "uint32_t", "tl_dtype", "tl_epilogue", "tl_status"):
+        return "4"
+    if t in ("float", "double"):
+        return "f4" if t == "float" else "f8"
+    if t == "void":
+        return "void"
+    raise AssertionError(f"unexpected C type {t!r}")
+
+
+def _ctypes_kind(t) -> str:
+    if t is None:
+        return "void"
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "ptr"
+    if t in (ctypes.c_float, ctypes.c_double):
+        return "f4" if t is ctypes.c_float else "f8"
+    return str(ctypes.sizeof(t))
+
+
+def test_binding_signatures_match_the_header():
+    # every argument of every call crosses the ABI with the header's width: a 4-byte int
+    # passed where the library reads an int64_t (or the reverse) would go unnoticed
+    protos = _prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, (ret, params) in protos.items():
+        fn = getattr(tl.LIBRARY, name)
+        want = [_c_kind(p) for p in params]
+        got = [_ctypes_kind(a) for a in (fn.argtypes or [])]
+        assert got == want, (name, got, want)
+        assert _ctypes_kind(fn.restype) == _c_kind(ret), (name, fn.restype, ret)
