@@ -652,18 +652,18 @@ def main():
                   "epilogue": "relu" if w.relu else "none", "inputs": w.description,
                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
-    def cpu_rate(budget):
+    def cpu_rate(budget, nthreads=threads):
         if attn:
             q, k, v = workloads.make_attn_inputs(w)
-            r, el, fl, n, reps = oracle_rate_attn(w, q, k, v, budget, threads)
+            r, el, fl, n, reps = oracle_rate_attn(w, q, k, v, budget, nthreads)
             return r, el, fl, f"{reps} oracle runs of up to {n} output rows of {w.B * w.S * w.H}"
         if mx:
             a_cpu, b_cpu, sa_cpu, sb_cpu = workloads.make_mx_inputs(w)
             r, el, fl, rows, reps = oracle_rate_mx(w, a_cpu, b_cpu, sa_cpu, budget, sb_cpu,
-                                                   threads)
+                                                   nthreads)
             return r, el, fl, f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows)"
         a_cpu, b_cpu = workloads.make_inputs(w)
-        r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, budget, threads)
+        r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, budget, nthreads)
         return r, el, fl, f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows)"
 
     if args.impl == "reference":
@@ -711,8 +711,14 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, el, fl, what = cpu_rate(args.cpu_budget_s)
+        # one thread for a short sample: the per-core rate, and the single-core time that
+        # the whole workload would take
+        r1, el1, fl1, what1 = cpu_rate(min(args.cpu_budget_s, 2.0), 1)
         cpu = {"value": round(r, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{what}, {fl / 1e9:.2f} GFLOP in {el:.1f} s"}
+               "sample": f"{what}, {fl / 1e9:.2f} GFLOP in {el:.1f} s",
+               "single_core": {"value": round(r1, 6), "unit": "TFLOP/s",
+                               "sample": f"{what1}, {fl1 / 1e9:.3f} GFLOP in {el1:.1f} s",
+                               "workload_s": round(w.flops / (r1 * 1e12), 1)}}
 
     res = (run_attn if attn else run_mx if mx else run_tl)(args, w, rank, world, dist)
     total_ms = res["total_ms"]

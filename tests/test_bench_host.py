@@ -133,6 +133,25 @@ def test_json_line_of_the_library_arm(monkeypatch, capsys):
     assert "42 sets" in d["config"]["l2"]
 
 
+def test_cpu_baseline_runs_the_oracle_on_all_cores_and_on_one(monkeypatch, capsys):
+    # the real oracle on the host cores for a tiny budget, the GPU leg stubbed as above
+    import torch
+    monkeypatch.setattr(torch.cuda, "set_device", lambda *_: None)
+    fake = {"total_ms": 0.1, "rotation_sets": 42, "launches_per_step": 1,
+            "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
+            "plan": {}, "e2e": None}
+    monkeypatch.setattr(bench, "run_tl", lambda *a: fake)
+    d = _main_line(monkeypatch, capsys, ["--steps", "10", "--warmup", "3",
+                                         "--cpu-budget-s", "0.2"])
+    cpu = d["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] == (os.cpu_count() or 1)
+    assert cpu["value"] > 0 and "GFLOP" in cpu["sample"]
+    one = cpu["single_core"]
+    assert one["value"] > 0 and one["unit"] == "TFLOP/s"
+    w = workloads.WORKLOADS[workloads.HEADLINE]
+    assert one["workload_s"] == pytest.approx(w.flops / (one["value"] * 1e12), rel=0.01, abs=0.1)
+
+
 def test_json_line_of_the_reference_arm(monkeypatch, capsys):
     # the oracle's timing replaced by a fixed rate: the line carries the arm's own keys
     monkeypatch.setattr(bench, "oracle_rate",
