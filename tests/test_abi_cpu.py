@@ -292,3 +292,21 @@ def test_binding_signatures_match_the_header():
         got = [_ctypes_kind(a) for a in (fn.argtypes or [])]
         assert got == want, (name, got, want)
         assert _ctypes_kind(fn.restype) == _c_kind(ret), (name, fn.restype, ret)
+
+
+def test_tensor_helpers_refuse_host_tensors_instead_of_falling_back():
+    # every tensor-level call runs only through the CUDA library: host tensors are an
+    # error before anything is enqueued, never a CPU computation
+    import torch
+    a = torch.zeros((8, 16), dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA"):
+        tl.gemm(a, a.t().contiguous())
+    f8 = torch.zeros((8, 32), dtype=torch.float8_e4m3fn)
+    with pytest.raises(ValueError, match="CUDA"):
+        tl.gemm_fp8(f8, f8, trans_b=True)
+    sf = torch.full((8, 16), 127, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        tl.gemm_mx(f8, f8, sf, sf)
+    q = torch.zeros((1, 4, 1, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        tl.attention(q, q, q)
