@@ -310,3 +310,19 @@ def test_tensor_helpers_refuse_host_tensors_instead_of_falling_back():
     q = torch.zeros((1, 4, 1, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         tl.attention(q, q, q)
+
+
+def test_import_fails_loudly_without_the_built_library(tmp_path):
+    # a copy of the package with no built library: importing it raises, naming the build
+    # step; nothing else stands in for the CUDA library
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "tiled_gemm_gb300")
+    shutil.copytree(src, tmp_path / "tiled_gemm_gb300",
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    r = subprocess.run([sys.executable, "-c", "import tiled_gemm_gb300"], cwd=tmp_path,
+                       env=dict(os.environ, PYTHONPATH=str(tmp_path)), capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "not built" in r.stderr
