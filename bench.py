@@ -85,6 +85,12 @@ def max_over_ranks(x: float, dist, device) -> float:
     return float(t.item())
 
 
+def sig4(x: float) -> float:
+    """x to 4 significant figures (the oracle's rates are far below 1 TFLOP/s, where a
+    fixed number of decimals would keep too few digits)."""
+    return float(f"{x:.4g}")
+
+
 def whole_job_tflops(flops_per_step: int, steps: int, world: int, max_ms: float) -> float:
     """Throughput of the whole job: every rank ran `steps` steps; the slowest rank's time."""
     return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
@@ -682,16 +688,16 @@ def main():
             times.append(el)
         value = statistics.mean(rates)
         line = {"metric": metric,
-                "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "value": sig4(value), "unit": "TFLOP/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(1e3 * statistics.mean(times), 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic", "impl": "reference", "config": config,
-                "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                "cpu_baseline": {"value": sig4(value), "unit": "TFLOP/s", "cores": threads,
                                  "kind": "oracle",
                                  "sample": f"{what} per step, ~{budget:.1f} s of CPU work "
                                            "per step"},
-                "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "e2e": {"value": sig4(value), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -714,9 +720,9 @@ def main():
         # one thread for a short sample: the per-core rate, and the single-core time that
         # the whole workload would take
         r1, el1, fl1, what1 = cpu_rate(min(args.cpu_budget_s, 2.0), 1)
-        cpu = {"value": round(r, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": sig4(r), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{what}, {fl / 1e9:.2f} GFLOP in {el:.1f} s",
-               "single_core": {"value": round(r1, 6), "unit": "TFLOP/s",
+               "single_core": {"value": sig4(r1), "unit": "TFLOP/s",
                                "sample": f"{what1}, {fl1 / 1e9:.3f} GFLOP in {el1:.1f} s",
                                "workload_s": round(w.flops / (r1 * 1e12), 1)}}
 

@@ -149,7 +149,9 @@ def test_cpu_baseline_runs_the_oracle_on_all_cores_and_on_one(monkeypatch, capsy
     one = cpu["single_core"]
     assert one["value"] > 0 and one["unit"] == "TFLOP/s"
     w = workloads.WORKLOADS[workloads.HEADLINE]
-    assert one["workload_s"] == pytest.approx(w.flops / (one["value"] * 1e12), rel=0.01, abs=0.1)
+    # the rate keeps 4 significant figures, the time one decimal
+    assert one["workload_s"] == pytest.approx(w.flops / (one["value"] * 1e12), rel=1e-3, abs=0.1)
+    assert bench.sig4(4.6449e-05) == 4.645e-05 and bench.sig4(1234.56) == 1235.0
 
 
 def test_json_line_of_the_reference_arm(monkeypatch, capsys):
