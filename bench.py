@@ -75,6 +75,19 @@ def load_traffic(workload: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def rotation_sets(bytes_per_set: int) -> int:
+    """Input sets the timed steps rotate over, so that the working set exceeds twice the
+    L2 cache (1 when one set alone does)."""
+    return 1 if bytes_per_set >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / bytes_per_set))
+
+
+def l2_note(bytes_per_set: int) -> str:
+    rot = rotation_sets(bytes_per_set)
+    if rot == 1:
+        return "operands larger than 2x L2"
+    return f"inputs rotate over {rot} sets ({rot * bytes_per_set / 2**20:.0f} MiB > 2x L2)"
+
+
 def max_over_ranks(x: float, dist, device) -> float:
     """The largest value of x over all ranks (x itself without a process group)."""
     if dist is None:
@@ -138,14 +151,15 @@ def roofline(w, avg_launch_ms: float, peaks: dict, peaks_src: str, clocks, attn:
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 50 ms while the timed region runs."""
+    """nvidia-smi clock/throttle samples every 50 ms while the timed region runs (the
+    fallback when NVML cannot be loaded in-process)."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu_index = gpu_index
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
         self.proc = None
         self.path = None
 
@@ -154,12 +168,15 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
+
+    def mark(self, which: str) -> None:
+        """Start or end of the timed region (the nvidia-smi record keeps every sample)."""
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -173,33 +190,147 @@ class ClockSampler:
         with open(self.path) as f:
             lines = f.readlines()
         os.unlink(self.path)
-        return summarise_clocks(lines)
+        return dict(summarise_clocks(lines), source="nvidia-smi every 50 ms")
+
+
+# NVML clock-event reason bits (nvmlClocksEventReason*) that the record names
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def nvml_reason_names(mask: int) -> set:
+    return {name for bit, name in NVML_REASONS.items() if mask & bit}
+
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read in-process through NVML every
+    `period_s` (read-only queries: nothing on the GPU is changed).  Samples are kept
+    between mark("start") and mark("end"), so that even a timed region of a few
+    milliseconds has a record of its own."""
+
+    def __init__(self, uuid: str | None, pci_bus_id: str | None, index: int,
+                 period_s: float = 0.002):
+        import ctypes
+        import threading
+        self._ct = ctypes
+        self._threading = threading
+        self.period_s = period_s
+        self.samples = []            # (host time, sm MHz, power W, reason mask)
+        self.window = [None, None]
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        found = False
+        for key in ([f"GPU-{uuid}", uuid] if uuid else []):
+            if key and self.lib.nvmlDeviceGetHandleByUUID(
+                    ctypes.c_char_p(key.encode()), ctypes.byref(self.handle)) == 0:
+                found = True
+                break
+        if not found and pci_bus_id:
+            found = self.lib.nvmlDeviceGetHandleByPciBusId_v2(
+                ctypes.c_char_p(pci_bus_id.encode()), ctypes.byref(self.handle)) == 0
+        if not found:
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index),
+                                                      ctypes.byref(self.handle)) != 0:
+                raise OSError("no NVML handle for the device")
+        self.matched = "uuid" if found and uuid else ("pci" if found else "index")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = (float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.handle, ctypes.c_int(1), ctypes.byref(mx)) == 0 else None)
+        self._stop = threading.Event()
+        self._thread = None
+
+    def _read(self):
+        ct = self._ct
+        clk, mw, reasons = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok = self.lib.nvmlDeviceGetClockInfo(self.handle, ct.c_int(1), ct.byref(clk)) == 0
+        pw = self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw)) == 0
+        rs = self._reasons(self.handle, ct.byref(reasons)) == 0
+        if ok:
+            self.samples.append((time.perf_counter(), float(clk.value),
+                                 mw.value / 1000.0 if pw else None,
+                                 int(reasons.value) if rs else 0))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._read()
+            time.sleep(self.period_s)
+
+    def start(self):
+        self._thread = self._threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def mark(self, which: str) -> None:
+        self.window[0 if which == "start" else 1] = time.perf_counter()
+
+    def stop(self) -> dict:
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+        t0, t1 = self.window
+        inside = [s for s in self.samples
+                  if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
+        rec = summarise_samples([(s[1], self.max_mhz, s[2], nvml_reason_names(s[3]))
+                                 for s in inside])
+        rec["source"] = f"NVML every {self.period_s * 1e3:.0f} ms ({self.matched})"
+        return rec
+
+
+def clock_sampler(dev_index: int):
+    """An NVML sampler for the CUDA device, or the nvidia-smi one if NVML is missing."""
+    uuid = pci = None
+    try:
+        import torch
+        props = torch.cuda.get_device_properties(dev_index)
+        u = getattr(props, "uuid", None)
+        uuid = str(u) if u is not None else None
+        if hasattr(props, "pci_bus_id"):
+            pci = (f"{getattr(props, 'pci_domain_id', 0):08x}:{props.pci_bus_id:02x}:"
+                   f"{getattr(props, 'pci_device_id', 0):02x}.0")
+    except Exception:
+        pass
+    try:
+        return NvmlClockSampler(uuid, pci, dev_index)
+    except (OSError, AttributeError):
+        return ClockSampler(f"GPU-{uuid}" if uuid else str(dev_index))
+
+
+def summarise_samples(samples) -> dict:
+    """Median SM clock over the busy samples (above half the highest), the highest clock
+    limit and power seen, and every throttle reason active in any sample.  Each sample
+    is (SM MHz, max SM MHz or None, power W or None, set of reason names)."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    sm = [s[0] for s in samples]
+    smax = [s[1] for s in samples if s[1] is not None]
+    power = [s[2] for s in samples if s[2] is not None]
+    reasons = set().union(*[s[3] for s in samples])
+    busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+    return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None, "samples": len(sm),
+            "reasons": sorted(reasons)}
 
 
 def summarise_clocks(lines) -> dict:
-    """Median SM clock over the busy samples (above half the highest), the highest clock
-    limit and power seen, and every throttle reason that was active in any sample.  Each
-    line is one `nvidia-smi --format=csv,noheader,nounits` row of ClockSampler.QUERY."""
-    sm, smax, power, reasons = [], [], [], set()
+    """summarise_samples over `nvidia-smi --format=csv,noheader,nounits` rows of
+    ClockSampler.QUERY (unparsable rows are skipped)."""
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    samples = []
     for line in lines:
         parts = [p.strip() for p in line.split(",")]
         if len(parts) < 9:
             continue
         try:
-            sm.append(float(parts[1]))
-            smax.append(float(parts[2]))
-            power.append(float(parts[3]))
+            sm, smax, power = float(parts[1]), float(parts[2]), float(parts[3])
         except ValueError:
             continue
-        for name, val in zip(names, parts[5:9]):
-            if val.lower() == "active":
-                reasons.add(name)
-    if not sm:
-        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-    busy = [s for s in sm if s > 0.5 * max(sm)] or sm
-    return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
-            "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+        samples.append((sm, smax, power,
+                        {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
+    return summarise_samples(samples)
 
 
 # ------------------------------------------------------------------ CPU oracle ----
@@ -208,7 +339,7 @@ def oracle_rate(w: workloads.Workload, a_cpu, b_cpu, budget_s: float, threads: i
     """Oracle TFLOP/s on whole-row slices of the workload, repeated for ~budget_s."""
     import oracle
     oracle.build()
-    rows = max(1, min(w.M, 8))
+    rows = max(1, min(w.M, threads))            # one output row per thread to start
     done_flops, elapsed, reps = 0, 0.0, 0
     a_rows = a_cpu if w.trans_a else None
     while elapsed < budget_s:
@@ -240,7 +371,7 @@ def oracle_rate_mx(w: workloads.MxWorkload, a_cpu, b_cpu, sa_cpu, budget_s: floa
     """Oracle TFLOP/s of the block-scaled product on whole-row slices, for ~budget_s."""
     import oracle
     oracle.build()
-    rows = max(1, min(w.M, 8))
+    rows = max(1, min(w.M, threads))
     done_flops, elapsed, reps = 0, 0.0, 0
     while elapsed < budget_s:
         t0 = time.perf_counter()
@@ -258,9 +389,69 @@ def oracle_rate_mx(w: workloads.MxWorkload, a_cpu, b_cpu, sa_cpu, budget_s: floa
 
 # ------------------------------------------------------------------ GPU arm ----
 
-def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl):
+def graph_chunks(steps: int, rot: int, max_calls: int = 64, min_chunks: int = 5):
+    """Split `steps` consecutive calls into the CUDA graphs of the timed region.
+
+    Returns [(first step, calls, reuse)]: chunks of calls replayed back to back, at
+    least `min_chunks` of them when steps allow, so that the per-chunk times give a
+    spread.  Many steps: one graph of G calls (G a multiple of the rotation, so every
+    replay walks the same input sets in order) replayed steps // G times, then the
+    remainder (reuse = True marks replays of that first graph).  Few steps: near-equal
+    consecutive chunks, each captured with its own step indices."""
+    if steps <= 0:
+        return []
+    G = rot * max(1, math.ceil(max_calls / rot))
+    if steps >= min_chunks * G:
+        n_full, rem = divmod(steps, G)
+        chunks = [(i * G, G, i > 0) for i in range(n_full)]
+        if rem:
+            chunks.append((n_full * G, rem, False))
+        return chunks
+    n = min(steps, min_chunks)
+    bounds = [steps * j // n for j in range(n + 1)]
+    return [(bounds[j], bounds[j + 1] - bounds[j], False) for j in range(n)]
+
+
+def percentile(xs, q: float) -> float:
+    """Linear-interpolation percentile (q in [0, 100]) of a non-empty list."""
+    s = sorted(xs)
+    pos = (len(s) - 1) * q / 100.0
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(s) - 1)
+    return s[lo] + (s[hi] - s[lo]) * (pos - lo)
+
+
+def spread_of(chunk_ms, chunks) -> dict:
+    """Per-call time of each chunk (its events' interval over its calls): min, p10, p50,
+    p90 and max over the chunks of the largest size (a shorter remainder chunk is left
+    out, so that every figure averages the same number of calls)."""
+    size = max(c[1] for c in chunks)
+    per_call = [ms / c[1] for ms, c in zip(chunk_ms, chunks) if c[1] == size]
+    return {"chunks": len(per_call), "calls_per_chunk": size,
+            "ms_per_call": {"min": round(min(per_call), 6),
+                            "p10": round(percentile(per_call, 10), 6),
+                            "p50": round(percentile(per_call, 50), 6),
+                            "p90": round(percentile(per_call, 90), 6),
+                            "max": round(max(per_call), 6)}}
+
+
+def spread_line(spread, flops: int):
+    """The spread record with the throughput at each per-call time (TFLOP/s; the
+    slowest chunk gives the lowest rate)."""
+    if not spread:
+        return None
+    ms = spread["ms_per_call"]
+    return dict(spread, tflops={k: round(flops / (v * 1e-3) / 1e12, 1) for k, v in ms.items()})
+
+
+def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl, preheat_s: float = 2.0):
     """Warm-up, then exactly args.steps calls of step(i) replayed as CUDA graphs, timed
-    with events on `stream` between barriers; returns (max-over-ranks ms, clocks)."""
+    with events on `stream` between barriers; returns (max-over-ranks ms, clocks,
+    spread).
+
+    Before the timed region the graphs are replayed, untimed, for about preheat_s, so
+    that the timed steps run at the clock the GPU settles at under this load (for the
+    large products, the power cap) rather than at the first milliseconds' boost."""
     import torch
 
     w0 = torch.cuda.Event(enable_timing=True)
@@ -275,57 +466,70 @@ def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl):
     status, word = tl.tl_device_status(reset=True)
     if status != tl.TL_OK:
         raise RuntimeError(f"device-side wait gave up during warm-up: {word:#x}")
+    step_ms = max(w0.elapsed_time(w1) / 2.0, 1e-3)
     if args.steps <= 0:
-        # default: enough steps for a timed region of ~1.5 s, so that the clock samples
-        # taken every 50 ms fall inside it
-        step_ms = max(w0.elapsed_time(w1) / 2.0, 1e-3)
+        # default: a timed region of ~1.5 s
         args.steps = int(min(200000, max(50, math.ceil(1500.0 / step_ms))))
         args.steps = int(max_over_ranks(float(args.steps), dist, dev))
 
     # The timed steps run as CUDA-graph replays of consecutive library calls (one call
     # per step, inputs rotating as in eager mode), so host-side launch cost does not
     # hide the device time of small problems.  Exactly args.steps calls are timed.
-    G = rot * max(1, math.ceil(64 / rot))
-    n_full, rem = divmod(args.steps, G)
+    chunks = graph_chunks(args.steps, rot)
 
-    def capture(n):
+    def capture(first, n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
+            for i in range(first, first + n):
                 step(i)
         return g
 
-    g_full = capture(G) if n_full else None
-    g_rem = capture(rem) if rem else None
+    graphs = []
+    for first, n, reuse in chunks:
+        graphs.append(graphs[0] if reuse else capture(first, n))
+    # The pre-heat graph walks every input set once, in order, so that the first timed
+    # call finds its set as cold as every later one.
+    G = rot * max(1, math.ceil(64 / rot))
+    pre = graphs[0] if chunks[0][1] == G else capture(0, G)
+    distinct = list({id(g): g for g in graphs + [pre]}.values())
     with torch.cuda.stream(stream):
-        for g in (g_full, g_rem):              # one untimed replay of each graph
-            if g is not None:
-                g.replay()
+        for g in distinct:                     # one untimed replay of each graph
+            g.replay()
     torch.cuda.synchronize()
+    # pre-heat: untimed replays, back to back with the timed ones
+    reps = int(min(100000, max(1, math.ceil(preheat_s * 1e3 / (step_ms * G)))))
 
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = clock_sampler(torch.cuda.current_device())
     clocks.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(len(chunks) + 1)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for _ in range(n_full):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        t_end.record(stream)
+        for _ in range(reps):
+            pre.replay()
+        events[0].record(stream)
+        for j, g in enumerate(graphs):
+            g.replay()
+            events[j + 1].record(stream)
+    # the clock record covers the device's timed region: from when the first event
+    # completes (polled) to the end of the last replay
+    while not events[0].query():
+        time.sleep(0.0002)
+    clocks.mark("start")
     torch.cuda.synchronize()
+    clocks.mark("end")
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = events[0].elapsed_time(events[-1])
+    chunk_ms = [events[j].elapsed_time(events[j + 1]) for j in range(len(chunks))]
     status, word = tl.tl_device_status(reset=True)
     if status != tl.TL_OK:
         raise RuntimeError(f"device-side wait gave up in the timed region: {word:#x}")
-    return max_over_ranks(total_ms, dist, dev), clk
+    spread = spread_of(chunk_ms, chunks)
+    spread["preheat_ms"] = round(reps * step_ms * G, 1)
+    return max_over_ranks(total_ms, dist, dev), clk, spread
 
 
 def library_context(name: str, step, rot: int, stream, steps: int, flops: int) -> dict:
@@ -465,7 +669,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
     dev = torch.device("cuda", torch.cuda.current_device())
     a_cpu, b_cpu = workloads.make_inputs(w)
     per_set = w.bytes_moved
-    rot = 1 if per_set >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / per_set))
+    rot = rotation_sets(per_set)
     sets = []
     a0, b0 = a_cpu.to(dev), b_cpu.to(dev)
     for i in range(rot):
@@ -495,7 +699,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
         a, b, c = sets[i % rot]
         gemm_call(a, b, c)
 
-    max_ms, clk = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
     e2e = None
     if not args.no_e2e:
         e2e = e2e_pipeline(args, [a_cpu, b_cpu], (w.M, w.N), w.torch_dtype,
@@ -510,7 +714,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
                 c.relu_()
         context = library_context("torch.matmul (cuBLAS)" + (" + relu_" if w.relu else ""),
                                   lib_step, rot, stream, args.steps, w.flops)
-    return {"total_ms": max_ms, "clocks": clk, "e2e": e2e, "context": context,
+    return {"total_ms": max_ms, "clocks": clk, "spread": spread, "e2e": e2e, "context": context,
             "rotation_sets": rot, "launches_per_step": launches_per_step,
             "plan": tl.tl_gemm_plan(w.M, w.N, w.K, w.dtype, int(w.trans_a), int(w.trans_b),
                                     torch.cuda.get_device_properties(dev).multi_processor_count)
@@ -525,7 +729,7 @@ def run_mx(args, w: workloads.MxWorkload, rank: int, world: int, dist) -> dict:
 
     dev = torch.device("cuda", torch.cuda.current_device())
     ins_cpu = workloads.make_mx_inputs(w)
-    rot = 1 if w.bytes_moved >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / w.bytes_moved))
+    rot = rotation_sets(w.bytes_moved)
     first = [x.to(dev) for x in ins_cpu]
     sets = [(first if i == 0 else [x.clone() for x in first]) +
             [torch.empty((w.M, w.N), dtype=w.c_torch_dtype, device=dev)] for i in range(rot)]
@@ -538,13 +742,13 @@ def run_mx(args, w: workloads.MxWorkload, rank: int, world: int, dist) -> dict:
         st = sets[i % rot]
         call(st[:4], st[4])
 
-    max_ms, clk = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
     e2e = None
     if not args.no_e2e:
         e2e = e2e_pipeline(args, list(ins_cpu), (w.M, w.N), w.c_torch_dtype, call, w.flops,
                            world, stream, dist, dev, tl)
-    return {"total_ms": max_ms, "clocks": clk, "e2e": e2e, "rotation_sets": rot,
-            "launches_per_step": 1,
+    return {"total_ms": max_ms, "clocks": clk, "spread": spread, "e2e": e2e,
+            "rotation_sets": rot, "launches_per_step": 1,
             "plan": {"tile": [128, 128, 128], "stages": 4, "cta_group": 1,
                      "grid": [math.ceil(w.N / 128), math.ceil(w.M / 128)]}}
 
@@ -556,7 +760,7 @@ def run_attn(args, w: workloads.AttnWorkload, rank: int, world: int, dist) -> di
 
     dev = torch.device("cuda", torch.cuda.current_device())
     q_cpu, k_cpu, v_cpu = workloads.make_attn_inputs(w)
-    rot = 1 if w.bytes_moved >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / w.bytes_moved))
+    rot = rotation_sets(w.bytes_moved)
     q0, k0, v0 = (x.to(dev) for x in (q_cpu, k_cpu, v_cpu))
     sets = [(q0, k0, v0, torch.empty_like(q0)) if i == 0 else
             (q0.clone(), k0.clone(), v0.clone(), torch.empty_like(q0)) for i in range(rot)]
@@ -566,7 +770,7 @@ def run_attn(args, w: workloads.AttnWorkload, rank: int, world: int, dist) -> di
         q, k, v, o = sets[i % rot]
         tl.attention(q, k, v, causal=w.causal, out=o, stream=stream)
 
-    max_ms, clk = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
 
     def lib_step(i):
         q, k, v, _ = sets[i % rot]
@@ -581,8 +785,8 @@ def run_attn(args, w: workloads.AttnWorkload, rank: int, world: int, dist) -> di
                            lambda ins, out: tl.attention(ins[0], ins[1], ins[2], causal=w.causal,
                                                          out=out, stream=stream),
                            w.flops, world, stream, dist, dev, tl)
-    return {"total_ms": max_ms, "clocks": clk, "e2e": e2e, "context": context,
-            "rotation_sets": rot, "launches_per_step": 1,
+    return {"total_ms": max_ms, "clocks": clk, "spread": spread, "e2e": e2e,
+            "context": context, "rotation_sets": rot, "launches_per_step": 1,
             "plan": {"q_tile": 128, "kv_tile": 128, "kv_stages": 2, "s_buffers": 3,
                      "grid": "persistent, at most one CTA per SM"}}
 
@@ -645,30 +849,38 @@ def main():
     if attn:
         config = {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D,
                   "dtype": w.dtype_name, "causal": w.causal, "inputs": w.description,
-                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                  "l2": l2_note(w.bytes_moved)}
     elif mx:
         config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype_name,
                   "layout": "A [M,K], B [N,K], both K-major", "scales": "E8M0 per 32 K",
                   "out": "bf16" if w.out_dtype == workloads.BF16 else "f16",
                   "epilogue": "relu" if w.relu else "none", "inputs": w.description,
-                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                  "l2": l2_note(w.bytes_moved)}
     else:
         config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype_name,
                   "trans_a": w.trans_a, "trans_b": w.trans_b,
                   "epilogue": "relu" if w.relu else "none", "inputs": w.description,
-                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                  "l2": l2_note(w.bytes_moved)}
+
+    cpu_inputs = []              # drawn once, on first use
 
     def cpu_rate(budget, nthreads=threads):
+        if not cpu_inputs:
+            cpu_inputs.extend(workloads.make_attn_inputs(w) if attn else
+                              workloads.make_mx_inputs(w) if mx else workloads.make_inputs(w))
         if attn:
-            q, k, v = workloads.make_attn_inputs(w)
+            q, k, v = cpu_inputs
             r, el, fl, n, reps = oracle_rate_attn(w, q, k, v, budget, nthreads)
             return r, el, fl, f"{reps} oracle runs of up to {n} output rows of {w.B * w.S * w.H}"
         if mx:
-            a_cpu, b_cpu, sa_cpu, sb_cpu = workloads.make_mx_inputs(w)
+            a_cpu, b_cpu, sa_cpu, sb_cpu = cpu_inputs
             r, el, fl, rows, reps = oracle_rate_mx(w, a_cpu, b_cpu, sa_cpu, budget, sb_cpu,
                                                    nthreads)
             return r, el, fl, f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows)"
-        a_cpu, b_cpu = workloads.make_inputs(w)
+        a_cpu, b_cpu = cpu_inputs
         r, el, fl, rows, reps = oracle_rate(w, a_cpu, b_cpu, budget, nthreads)
         return r, el, fl, f"{reps} oracle runs on row slices (up to {rows} of {w.M} rows)"
 
@@ -741,13 +953,11 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_name, "data": "synthetic (seeded CPU generator)",
-            "config": dict(config, l2=(f"inputs rotate over {res['rotation_sets']} sets "
-                                       f"({res['rotation_sets'] * w.bytes_moved / 2**20:.0f} MiB "
-                                       "> 2x L2)") if res["rotation_sets"] > 1 else
-                           "operands larger than 2x L2"),
+            "config": config,
             "roofline": roof, "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["launches_per_step"] * args.steps,
-            "clocks": res["clocks"], "plan": res["plan"],
+            "clocks": res["clocks"], "spread": spread_line(res.get("spread"), w.flops),
+            "plan": res["plan"],
             "context": res.get("context"),
             "pct_of_nominal": round(100 * value / world / (2250.0 * tensor_peak_scale(w)), 2),
             "nominal_tflops": 2250.0 * tensor_peak_scale(w)}

@@ -241,7 +241,9 @@ tl_status tl_gemm_fp8(const void* A, const void* B, void* C, int64_t M, int64_t 
  *     Operands that need no copy use no scratch and have no size limit.
  *   - The first call on each device (that passes the argument checks) performs a
  *     one-time set-up: it looks up the array's device address with that device
- *     current.  Make that first call before any stream capture.
+ *     current.  Make that first call before any stream capture.  If that lookup
+ *     failed, later calls on the device that need a copy return TL_ERR_DEVICE; calls
+ *     that need none still run.
  *   - Every call shares the one array, and it keeps whatever the last call left in
  *     it (nothing read from it depends on that).  Calls whose work overlaps on the
  *     GPU (different streams, or host threads enqueueing concurrently) race on the
@@ -266,6 +268,14 @@ const char* tl_status_string(tl_status status);
  * raw status word (role and wait site of the first timeout).
  */
 tl_status tl_device_status(int reset, uint32_t* detail);
+
+/*
+ * The same outcome without reset or detail: synchronises the current device and
+ * returns TL_OK, or the status of the first device-side wait that gave up since the
+ * flag was last cleared (tl_device_status with reset = 1 clears it).  A debugging
+ * aid for use after a sync point; TL_ERR_DEVICE if the device cannot be queried.
+ */
+tl_status tl_last_device_status(void);
 
 /*
  * Limit of every device-side wait for kernels enqueued after this call, in

@@ -126,14 +126,35 @@ def assert_bit_exact(got_bits, ref_bits):
     assert not diff.any(), f"{int(diff.sum())} of {diff.size} elements differ"
 
 
-def sample_indices(M, N, count, rng, bm=128, bn=256):
-    """Random entries plus the tile edges (first/last row and column of every tile)."""
+def sample_indices(M, N, count, rng, bm=128, bn=64, per_edge=16):
+    """Entries to compare with the oracle one by one: `count` random ones; the whole of
+    the first and last row and of the first and last column (the ragged edges, where
+    boxes are zero-filled and stores clipped); and, for every row tile and every column
+    tile, its first and last row (column) at `per_edge` random columns (rows)."""
     rows = list(rng.integers(0, M, count))
     cols = list(rng.integers(0, N, count))
-    edge_r = sorted({0, M - 1} | {min(M - 1, x) for t in range(0, M, bm) for x in (t, t + bm - 1)})
-    edge_c = sorted({0, N - 1} | {min(N - 1, x) for t in range(0, N, 64) for x in (t, t + 63)})
-    for r in edge_r[:64]:
-        for c in rng.choice(edge_c, size=min(8, len(edge_c)), replace=False):
-            rows.append(r)
-            cols.append(c)
+    for r in sorted({0, M - 1}):
+        rows += [r] * N
+        cols += list(range(N))
+    for c in sorted({0, N - 1}):
+        rows += list(range(M))
+        cols += [c] * M
+    edge_r = sorted({min(M - 1, x) for t in range(0, M, bm) for x in (t, t + bm - 1)})
+    edge_c = sorted({min(N - 1, x) for t in range(0, N, bn) for x in (t, t + bn - 1)})
+    for r in edge_r:
+        rows += [r] * per_edge
+        cols += list(rng.integers(0, N, per_edge))
+    for c in edge_c:
+        rows += list(rng.integers(0, M, per_edge))
+        cols += [c] * per_edge
     return np.asarray(rows, np.int64), np.asarray(cols, np.int64)
+
+
+def exact_integer_product(a_cpu, b_cpu, trans_a, trans_b, relu):
+    """The exact product of small-integer operands as float64: every partial sum is an
+    integer far below 2^53, so float64 evaluation is exact in any order (a closed form,
+    not a second implementation of the oracle); ReLU gives +0 for negatives."""
+    a = a_cpu.to(torch.float64).numpy()
+    b = b_cpu.to(torch.float64).numpy()
+    c = (a.T if trans_a else a) @ (b.T if trans_b else b)
+    return np.where(c > 0, c, 0.0) if relu else c

@@ -34,6 +34,7 @@ def test_header_declares_the_expected_entry_points():
     for required in ("tl_gemm", "tl_gemm_plan", "tl_gemm_with_plan", "tl_plan_complete",
                      "tl_gemm_fp8", "tl_gemm_mx", "tl_attention_fwd", "tl_gemm_noalloc",
                      "tl_gemm_noalloc_scratch_bytes", "tl_status_string", "tl_device_status",
+                     "tl_last_device_status",
                      "tl_set_wait_timeout_ns", "tl_version"):
         assert required in names
 

@@ -57,6 +57,51 @@ def test_attention_is_always_a_contraction():
     assert r["bound"] == "tensor" and r["peak"] == 2000.0
 
 
+def test_graph_chunks_cover_every_step_once_and_keep_the_rotation():
+    for steps, rot in [(20, 1), (20, 42), (3, 1), (7, 2), (1000, 42), (333, 1), (5, 5)]:
+        chunks = bench.graph_chunks(steps, rot)
+        covered = [i for first, n, _ in chunks for i in range(first, first + n)]
+        assert covered == list(range(steps)), (steps, rot)
+        assert len(chunks) >= min(steps, 5)
+        for first, n, reuse in chunks:
+            if reuse:                       # a replay of the first graph: same sets in order
+                assert first % rot == 0 and n == chunks[0][1] and chunks[0][0] == 0
+    # few steps: five near-equal chunks of their own
+    assert bench.graph_chunks(20, 1) == [(0, 4, False), (4, 4, False), (8, 4, False),
+                                         (12, 4, False), (16, 4, False)]
+    # many steps: one graph of a whole number of rotations, replayed, then the rest
+    ch = bench.graph_chunks(1000, 42)
+    assert ch[0] == (0, 84, False) and all(c[1] == 84 and c[2] for c in ch[1:-1])
+    assert ch[-1] == (924, 76, False)
+    assert bench.graph_chunks(0, 3) == []
+
+
+def test_spread_takes_percentiles_over_equal_chunks():
+    assert bench.percentile([1.0, 2.0, 3.0, 4.0, 5.0], 50) == 3.0
+    assert bench.percentile([1.0, 2.0, 3.0, 4.0, 5.0], 10) == pytest.approx(1.4)
+    assert bench.percentile([7.0], 90) == 7.0
+    chunks = [(0, 4, False), (4, 4, False), (8, 4, False), (12, 4, False), (16, 4, False),
+              (20, 2, False)]
+    sp = bench.spread_of([4.0, 4.4, 4.0, 3.6, 4.8, 100.0], chunks)
+    # the short remainder chunk is left out; per-call times are ms / 4
+    assert sp["chunks"] == 5 and sp["calls_per_chunk"] == 4
+    m = sp["ms_per_call"]
+    assert m["min"] == pytest.approx(0.9) and m["max"] == pytest.approx(1.2)
+    assert m["p50"] == pytest.approx(1.0) and m["p10"] <= m["p50"] <= m["p90"]
+
+
+def test_nvml_samples_are_summarised_like_the_nvidia_smi_ones():
+    # reason bits of the NVML clock-event mask
+    assert bench.nvml_reason_names(0x4) == {"sw_power_cap"}
+    assert bench.nvml_reason_names(0x1 | 0x8 | 0x40) == {"hw_slowdown", "hw_thermal_slowdown"}
+    assert bench.nvml_reason_names(0x20) == {"sw_thermal_slowdown"}
+    s = bench.summarise_samples([(1500.0, 2070.0, 1390.0, {"sw_power_cap"}),
+                                 (1470.0, 2070.0, 1397.0, set()), (1485.0, None, None, set())])
+    assert s["sm_mhz"] == 1485.0 and s["sm_max_mhz"] == 2070.0 and s["power_w_max"] == 1397.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
+    assert bench.summarise_samples([])["reasons"] == ["no samples"]
+
+
 def _row(sm, power, reasons=()):
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     flags = ["Active" if n in reasons else "Not Active" for n in names]
@@ -116,21 +161,51 @@ def test_json_line_of_the_library_arm(monkeypatch, capsys):
     import torch
     monkeypatch.setattr(torch.cuda, "set_device", lambda *_: None)
     clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    spread = bench.spread_of([0.05, 0.052], [(0, 5, False), (5, 5, False)])
     fake = {"total_ms": 0.1, "rotation_sets": 42, "launches_per_step": 1, "clocks": clocks,
-            "plan": {"bm": 128}, "e2e": {"value": 50.0, "unit": "TFLOP/s",
-                                         "h2d_bytes_per_step": 4 << 20,
-                                         "d2h_bytes_per_step": 2 << 20}}
+            "spread": spread, "plan": {"bm": 128},
+            "e2e": {"value": 50.0, "unit": "TFLOP/s", "h2d_bytes_per_step": 4 << 20,
+                    "d2h_bytes_per_step": 2 << 20}}
     monkeypatch.setattr(bench, "run_tl", lambda *a: fake)
-    d = _main_line(monkeypatch, capsys, ["--steps", "10", "--warmup", "3", "--no-cpu-baseline"])
+    name = "gemm_relu_1024_f16_128x128x64s3"
+    d = _main_line(monkeypatch, capsys, ["--steps", "10", "--warmup", "3", "--no-cpu-baseline",
+                                         "--workload", name])
     assert CONTRACT_KEYS <= set(d)
-    w = workloads.WORKLOADS[workloads.HEADLINE]
-    assert d["config"]["workload"] == workloads.HEADLINE and d["n_gpus"] == 1
+    w = workloads.WORKLOADS[name]
+    assert d["config"]["workload"] == name and d["n_gpus"] == 1
     assert d["value"] == pytest.approx(w.flops * 10 / 1e-4 / 1e12, rel=1e-4)
     assert d["higher_is_better"] is True and d["vs_baseline"] is None and d["dtype"] == "f16"
     assert d["gpu_launches"] == 10 and d["clocks"] == clocks
     assert d["roofline"]["bound"] == "tensor" and d["roofline"]["kernel_ms"] == 0.01
     assert d["roofline"]["algorithmic"]["flops_per_launch"] == w.flops
     assert "42 sets" in d["config"]["l2"]
+    # the spread: per-call time of each chunk, and the rate at each
+    sp = d["spread"]
+    assert sp["chunks"] == 2 and sp["ms_per_call"]["min"] == pytest.approx(0.01)
+    assert sp["ms_per_call"]["max"] == pytest.approx(0.0104)
+    assert sp["tflops"]["min"] == pytest.approx(w.flops / 1e-5 / 1e12, abs=0.1)
+
+
+def test_default_workload_is_the_largest_square_product(monkeypatch, capsys):
+    # the bench's default is 8192^3 bf16 with a column-major B: the workload the
+    # tensor-peak fraction is stated for
+    import torch
+    monkeypatch.setattr(torch.cuda, "set_device", lambda *_: None)
+    assert workloads.HEADLINE == "gemm_8192_bf16_tb"
+    fake = {"total_ms": 14.0, "rotation_sets": 1, "launches_per_step": 1,
+            "clocks": {"sm_mhz": 1500.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]},
+            "plan": {}, "e2e": None}
+    monkeypatch.setattr(bench, "run_tl", lambda *a: fake)
+    d = _main_line(monkeypatch, capsys, ["--steps", "20", "--warmup", "5", "--no-cpu-baseline"])
+    w = workloads.WORKLOADS["gemm_8192_bf16_tb"]
+    assert d["config"]["workload"] == "gemm_8192_bf16_tb" and d["dtype"] == "bf16"
+    assert (w.M, w.N, w.K, w.trans_b) == (8192, 8192, 8192, True)
+    assert d["config"]["l2"] == "operands larger than 2x L2"
+    assert d["value"] == pytest.approx(w.flops * 20 / 14e-3 / 1e12, rel=1e-4)
+    # under the power cap the roofline takes the sustained peak
+    assert d["roofline"]["peak_source"].startswith("measured (sustained")
+    assert d["roofline"]["frac"] == pytest.approx(d["roofline"]["achieved"] /
+                                                  d["roofline"]["peak"], abs=1e-3)
 
 
 def test_cpu_baseline_runs_the_oracle_on_all_cores_and_on_one(monkeypatch, capsys):
@@ -141,14 +216,15 @@ def test_cpu_baseline_runs_the_oracle_on_all_cores_and_on_one(monkeypatch, capsy
             "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
             "plan": {}, "e2e": None}
     monkeypatch.setattr(bench, "run_tl", lambda *a: fake)
+    name = "gemm_relu_1024_f16_128x128x64s3"
     d = _main_line(monkeypatch, capsys, ["--steps", "10", "--warmup", "3",
-                                         "--cpu-budget-s", "0.2"])
+                                         "--cpu-budget-s", "0.2", "--workload", name])
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] == (os.cpu_count() or 1)
     assert cpu["value"] > 0 and "GFLOP" in cpu["sample"]
     one = cpu["single_core"]
     assert one["value"] > 0 and one["unit"] == "TFLOP/s"
-    w = workloads.WORKLOADS[workloads.HEADLINE]
+    w = workloads.WORKLOADS[name]
     # the rate keeps 4 significant figures, the time one decimal
     assert one["workload_s"] == pytest.approx(w.flops / (one["value"] * 1e12), rel=1e-3, abs=0.1)
     assert bench.sig4(4.6449e-05) == 4.645e-05 and bench.sig4(1234.56) == 1235.0
@@ -160,6 +236,8 @@ def test_json_line_of_the_reference_arm(monkeypatch, capsys):
                         lambda w, a, b, budget, threads: (0.004, 0.5, 2e9, 64, 3))
     d = _main_line(monkeypatch, capsys, ["--impl", "reference", "--steps", "2",
                                          "--warmup", "3"])
+    # both arms name the same configuration, rotation note included
+    assert d["config"]["l2"] == "operands larger than 2x L2"
     assert d["impl"] == "reference" and d["value"] == 0.004 and d["dtype"] == "f64"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == 0.004
     assert d["e2e"] == {"value": 0.004, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

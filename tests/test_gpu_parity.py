@@ -4,8 +4,10 @@ Bars:
 * small-integer operands: bit-exact (every fp32 partial sum is an exact integer, so
   the only rounding is the final round-to-nearest-even, identical on both sides);
 * random operands: |C - C_ref| <= 1e-2 + 1e-2 |C_ref| element by element;
-* full-size workloads: every element on the tile edges plus random entries against
-  the oracle computed one by one, and the canary guard band for coverage.
+* full-size workloads: the whole output against the oracle (8192^3: every tile's
+  edge rows and columns, the whole first and last rows and columns, and random
+  entries, computed one by one), their small-integer variants bit for bit in full
+  against the exact integer product, and the canary guard band for coverage.
 """
 import dataclasses
 import itertools
@@ -17,8 +19,9 @@ import torch
 import oracle
 import tiled_gemm_gb300 as tl
 import workloads
-from gpu_helpers import (GuardedC, assert_bit_exact, assert_within_tolerance, oracle_full,
-                         run_tl, sample_indices, to_device_padded)
+from gpu_helpers import (GuardedC, assert_bit_exact, assert_within_tolerance,
+                         exact_integer_product, oracle_full, run_tl, sample_indices,
+                         to_device_padded)
 
 pytestmark = pytest.mark.gpu
 
@@ -265,8 +268,6 @@ def test_offset_operands_and_unaligned_c():
 # ------------------------------------------------------------------ the workloads --
 
 SMALL = ["gemm_relu_256_f16", "gemm_relu_1024_f16_128x128x64s3"]
-LARGE = ["gemm_4096_bf16_tb", "gemm_8192_bf16_tb", "gemm_relu_3000x5000x4100_f16",
-         "gemm_m16_n8192_k8192_bf16", "gemm_m64_n8192_k8192_bf16", "gemm_m128_n8192_k8192_bf16"]
 
 
 def _workload_plan(w):
@@ -283,24 +284,45 @@ def test_small_workloads_full_output(name):
     _check_full(workloads.integer_variant(w), plan=_workload_plan(w), exact=True)
 
 
-@pytest.mark.parametrize("name", LARGE)
-def test_large_workloads_sampled(name):
+# Every output element of these is compared with the oracle (the oracle takes seconds to
+# about half a minute each on 16 host cores); 8192^3 is compared on the sample below.
+FULL = ["gemm_4096_bf16_tb", "gemm_relu_3000x5000x4100_f16", "gemm_m16_n8192_k8192_bf16",
+        "gemm_m64_n8192_k8192_bf16", "gemm_m128_n8192_k8192_bf16"]
+
+
+def _scale_bound(stats, ref_bits, dtype):
+    # a tighter bound that follows from the arithmetic: two roundings of nearly equal
+    # sums differ by at most one unit in the last place of the output format, plus the
+    # fp32 accumulation error; relative to the output's scale this stays near 2^-7
+    scale = np.abs(oracle.decode(ref_bits, dtype)).max()
+    assert stats["max_abs"] <= scale * 2.0 ** -6, (stats, scale)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_large_workloads_full_output(name):
     w = workloads.WORKLOADS[name]
     a, b = workloads.make_inputs(w)
     got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu,
                     plan=_workload_plan(w))
+    c.check_guards()
+    ref = oracle_full(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu)
+    stats = assert_within_tolerance(got, ref, w.dtype)
+    _scale_bound(stats, ref, w.dtype)
+
+
+def test_largest_square_workload_sampled():
+    # 8192^3 (the oracle would take minutes): every row and column tile's first and last
+    # row/column, the whole first and last rows and columns, and random entries
+    w = workloads.WORKLOADS["gemm_8192_bf16_tb"]
+    a, b = workloads.make_inputs(w)
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu)
     c.check_guards()
     rng = np.random.default_rng(7)
     rows, cols = sample_indices(w.M, w.N, 6000, rng)
     ref = oracle.gemm_entries(a, b, w.M, w.N, w.K, rows, cols, dtype=w.dtype,
                               trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu)
     stats = assert_within_tolerance(got[rows, cols], ref, w.dtype)
-    # a tighter bound that follows from the arithmetic: two roundings of nearly equal
-    # sums differ by at most one unit in the last place of the output format, plus the
-    # fp32 accumulation error; relative to the output's scale this stays near 2^-7
-    refv = oracle.decode(ref, w.dtype)
-    scale = np.abs(refv).max()
-    assert stats["max_abs"] <= scale * 2.0 ** -6, (stats, scale)
+    _scale_bound(stats, ref, w.dtype)
 
 
 def test_unit_variance_variant_of_the_square_workload_sampled():
@@ -335,6 +357,21 @@ def test_large_workloads_integer_sampled_bit_exact(name):
     ref = oracle.gemm_entries(a, b, w.M, w.N, w.K, rows, cols, dtype=w.dtype,
                               trans_a=w.trans_a, trans_b=w.trans_b, relu=w.relu)
     assert_bit_exact(got[rows, cols], ref)
+
+
+@pytest.mark.parametrize("name", ["gemm_8192_bf16_tb"] + FULL)
+def test_large_workloads_integer_full_output_bit_exact(name):
+    # small-integer operands: the exact product is an integer matrix (closed form), and
+    # its round-to-nearest-even by the oracle's encoder must equal every output bit for
+    # bit -- the whole of C at the full sizes, 8192^3 included
+    w = workloads.integer_variant(workloads.WORKLOADS[name])
+    a, b = workloads.make_inputs(w)
+    got, c = run_tl(a, b, w.M, w.N, w.K, w.dtype, w.trans_a, w.trans_b, w.relu,
+                    plan=_workload_plan(w))
+    c.check_guards()
+    exact = exact_integer_product(a, b, w.trans_a, w.trans_b, w.relu)
+    assert np.abs(exact).max() < 2 ** 24        # each fp32 partial sum is exact too
+    assert_bit_exact(got, oracle.encode(exact, w.dtype))
 
 
 # ------------------------------------------------------------- streams and graphs --

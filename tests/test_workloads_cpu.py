@@ -42,7 +42,11 @@ def test_every_workload_names_its_shapes_and_seed():
         seeds.add(w.seed)
     assert len(seeds) == len(workloads.WORKLOADS)     # independent draws per workload
     assert workloads.HEADLINE in workloads.WORKLOADS
-    assert workloads.WORKLOADS[workloads.HEADLINE].plan == (128, 128, 64, 3)
+    # the headline: the largest square product, at the planner's own tiling
+    hw = workloads.WORKLOADS[workloads.HEADLINE]
+    assert (hw.M, hw.N, hw.K, hw.trans_b, hw.plan) == (8192, 8192, 8192, True, None)
+    # the quickstart workload keeps the pages' fixed tiling
+    assert workloads.WORKLOADS["gemm_relu_1024_f16_128x128x64s3"].plan == (128, 128, 64, 3)
 
 
 def test_integer_variants_keep_every_fp32_partial_sum_exact():

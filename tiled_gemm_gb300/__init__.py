@@ -7,7 +7,7 @@ binding raises: there is no CPU or PyTorch fallback.
 
 Names follow the C ABI: ``tl_gemm``, ``tl_gemm_with_plan``, ``tl_gemm_noalloc``,
 ``tl_gemm_plan``, ``tl_plan_complete``, ``tl_status_string``, ``tl_device_status``,
-``tl_set_wait_timeout_ns``, ``tl_version``.  ``gemm`` is the tensor-level call.
+``tl_last_device_status``, ``tl_set_wait_timeout_ns``, ``tl_version``.  ``gemm`` is the tensor-level call.
 """
 from __future__ import annotations
 
@@ -94,6 +94,8 @@ def _load() -> ctypes.CDLL:
     lib.tl_status_string.restype = ctypes.c_char_p
     lib.tl_device_status.argtypes = [ci, ctypes.POINTER(u32)]
     lib.tl_device_status.restype = ci
+    lib.tl_last_device_status.argtypes = []
+    lib.tl_last_device_status.restype = ci
     lib.tl_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.tl_set_wait_timeout_ns.restype = None
     lib.tl_attention_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, ci, ci, p]
@@ -187,6 +189,12 @@ def tl_device_status(reset: bool = False) -> tuple[int, int]:
     word = ctypes.c_uint32(0)
     st = _lib.tl_device_status(1 if reset else 0, ctypes.byref(word))
     return st, word.value
+
+
+def tl_last_device_status() -> int:
+    """tl_status of the device-side bounded waits since the flag was last cleared;
+    synchronises the device and clears nothing."""
+    return _lib.tl_last_device_status()
 
 
 def tl_set_wait_timeout_ns(ns: int) -> None:

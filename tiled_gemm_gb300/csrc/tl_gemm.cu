@@ -688,8 +688,10 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   DeviceState* st = device_state(&dev);
   if (st == nullptr) return TL_ERR_DEVICE;
   if (!st->sm103) return TL_ERR_UNSUPPORTED;
-  void* scratch = nullptr;
-  if (no_alloc && (scratch = noalloc_scratch(dev)) == nullptr) return TL_ERR_DEVICE;
+  // The allocation-free variant looks up its scratch array on every device's first call
+  // (so the set-up never falls inside a later stream capture); only calls that need the
+  // array fail if that lookup did.
+  void* scratch = no_alloc ? noalloc_scratch(dev) : nullptr;
   if ((s = check_device_pointer(C, dev)) != TL_OK) return s;
   if (K > 0) {
     if ((s = check_device_pointer(A, dev)) != TL_OK) return s;
@@ -753,6 +755,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     uint8_t* w = nullptr;
     if (no_alloc) {
       if (ws_a_rounded + ws_b > kNoAllocScratchBytes) return TL_ERR_UNSUPPORTED;
+      if (scratch == nullptr) return TL_ERR_DEVICE;
       w = static_cast<uint8_t*>(scratch);
     } else {
       if (cudaMallocAsync(&ws, static_cast<size_t>(ws_a_rounded + ws_b_rounded + ws_split),
@@ -1252,6 +1255,8 @@ tl_status tl_device_status(int reset, uint32_t* detail) {
   }
   return word == 0 ? TL_OK : static_cast<tl_status>(word & 0xFFu);
 }
+
+tl_status tl_last_device_status(void) { return tl_device_status(0, nullptr); }
 
 void tl_set_wait_timeout_ns(uint64_t ns) {
   ns = std::max<uint64_t>(100000ull, std::min<uint64_t>(ns, 60000000000ull));

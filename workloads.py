@@ -321,5 +321,6 @@ for _w in (AttnWorkload("attn_fwd_b1_h8_s1024_d64_causal_f16", 1, 1024, 8, 64, F
                         22, "causal attention 4x32 heads, seq 4096, dim 128, bf16, N(0,1)")):
     ATTN_WORKLOADS[_w.name] = _w
 
-# The benchmark's headline workload: the quickstart GEMM+ReLU.
-HEADLINE = "gemm_relu_1024_f16_128x128x64s3"
+# The benchmark's headline workload: the largest square product, 8192^3 bf16 with a
+# column-major B, where the tensor-peak fraction is stated.
+HEADLINE = "gemm_8192_bf16_tb"
