@@ -327,3 +327,31 @@ def test_import_fails_loudly_without_the_built_library(tmp_path):
                        text=True, timeout=120)
     assert r.returncode != 0
     assert "ImportError" in r.stderr and "not built" in r.stderr
+
+
+def test_odd_width_tiles_need_a_k_major_b_and_fill_whole_waves():
+    # 192- and 224-column tiles are loaded in boxes of whole K-major rows of B; an
+    # N-major B (64-column boxes) cannot tile 96 or 112 columns per CTA
+    for bm, bn in ((256, 224), (256, 192), (128, 224), (128, 192)):
+        st = 3 if bm == 256 else 2            # one CTA holds all bn rows of B per stage
+        p = tl.tl_plan_complete(4096, 4096, 4096, bm, bn, 128, st, dtype=tl.TL_BF16, trans_b=1,
+                                num_sms=152)
+        assert p.tmem_cols == 512 and p.tiles_n == -(-4096 // bn)
+        assert p.tx_bytes == (128 + bn // (bm // 128)) * 128 * 2
+        with pytest.raises(tl.TLError):
+            tl.tl_plan_complete(4096, 4096, 4096, bm, bn, 128, st, dtype=tl.TL_BF16, trans_b=0)
+        with pytest.raises(tl.TLError):       # 128-deep stages only
+            tl.tl_plan_complete(4096, 4096, 4096, bm, bn, 64, st, dtype=tl.TL_BF16, trans_b=1)
+    with pytest.raises(tl.TLError):           # 3 stages of 128 x 224 + 224 x 128 exceed smem
+        tl.tl_plan_complete(4096, 4096, 4096, 128, 224, 128, 3, dtype=tl.TL_BF16, trans_b=1)
+    # 4096^3 with a K-major B: 16 x 19 = 304 pair tiles of 256 x 224 are exactly four waves
+    # of 76 SM pairs, where 256 x 256 tiles leave a last wave 37 % full
+    p = tl.tl_gemm_plan(4096, 4096, 4096, dtype=tl.TL_BF16, trans_b=1, num_sms=152)
+    assert (p.bm, p.bn, p.bk) == (256, 224, 128) and p.tiles == 304 and p.grid == 152
+    assert p.sk_iters == 0
+    # 8192^3 keeps the 256-column tiles (13.5 waves either way); an N-major B never takes
+    # the odd widths
+    p = tl.tl_gemm_plan(8192, 8192, 8192, dtype=tl.TL_BF16, trans_b=1, num_sms=152)
+    assert (p.bm, p.bn) == (256, 256)
+    p = tl.tl_gemm_plan(4096, 4096, 4096, dtype=tl.TL_BF16, trans_b=0, num_sms=152)
+    assert p.bn not in (192, 224)

@@ -64,6 +64,31 @@ def test_random_16bit_cases_bit_exact(seed):
     assert_bit_exact(got, ref)
 
 
+# 192- and 224-column tiles (K-major B): their own seeds, so the cases above keep theirs
+TILINGS_ODD = ((256, 224, 128, 3), (256, 192, 128, 3), (128, 224, 128, 2), (128, 192, 128, 2))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_odd_width_cases_bit_exact(seed):
+    rng = np.random.default_rng(3000 + seed)
+    M, N, K = (int(x) for x in rng.integers(1, 900, 3))
+    ta = bool(rng.integers(2))
+    dtype = workloads.F16 if rng.integers(2) else workloads.BF16
+    relu = bool(rng.integers(2))
+    bm, bn, bk, smax = TILINGS_ODD[rng.integers(len(TILINGS_ODD))]
+    plan = tl.plan_for(0, 0, 0, bm, bn, bk, int(rng.integers(2, smax + 1)),
+                       raster_group=int(rng.integers(1, 9)),
+                       grid=0 if rng.random() < 0.6 else int(rng.integers(1, 9)) * (bm // 128),
+                       stream_k=int(rng.choice([-1, 0, 1])),
+                       tma_store=-1 if rng.random() < 0.15 else 0)
+    dist = "int_small" if dtype == workloads.F16 else "int_unit"
+    w = workloads.Workload("fuzz_odd", M, N, K, dtype, ta, True, relu, dist, dist, seed=seed)
+    a, b = workloads.make_inputs(w)
+    got, c = run_tl(a, b, M, N, K, dtype, ta, True, relu, plan=plan)
+    c.check_guards()
+    assert_bit_exact(got, oracle_full(a, b, M, N, K, dtype, ta, True, relu))
+
+
 @pytest.mark.parametrize("seed", range(40))
 def test_random_fp8_cases_bit_exact(seed):
     from test_gpu_fp8 import TILINGS8, _oracle, run_fp8

@@ -26,6 +26,7 @@ from gpu_helpers import (GuardedC, assert_bit_exact, assert_within_tolerance,
 pytestmark = pytest.mark.gpu
 
 F16, BF16 = workloads.F16, workloads.BF16
+GUARD_ODD = 65            # C one element past a 128-byte boundary: not 16-byte aligned
 
 
 def _w(M, N, K, dtype, ta, tb, relu, dist, seed):
@@ -93,6 +94,48 @@ def test_cta_pairs_all_transposes_random(bn, bk, ta, tb):
     plan = tl.plan_for(0, 0, 0, 256, bn, bk, 3, raster_group=2)
     _check_full(_w(700, 900, 515, BF16, ta, tb, False, "uniform", 70 + bn + bk), plan=plan)
     _check_full(_w(768, 1024, 640, BF16, ta, tb, False, "uniform", 71 + bn + bk), plan=plan)
+
+
+# Tiles of 192 and 224 columns (K-major B only): 64-column epilogue steps, plus, for 224,
+# a last 32-column step written by plain stores; the second accumulator at column 256.
+ODD = [(bm, bn, s) for bm in (128, 256) for bn in (192, 224) for s in (2, 3)
+       if bm == 256 or s == 2]                      # one CTA: 2 stages fit shared memory
+
+
+@pytest.mark.parametrize("bm,bn,stages", ODD)
+@pytest.mark.parametrize("ta", [False, True])
+def test_odd_width_tiles_ragged_integer_bit_exact(bm, bn, stages, ta):
+    # ragged M, N and K (2-D boxes, zero fill), several tiles per CTA on a short grid
+    plan = tl.plan_for(0, 0, 0, bm, bn, 128, stages, raster_group=3, grid=2 * bm // 128)
+    w = _w(bm * 3 + 17, bn * 3 + 40, 64 * 9 + 7, F16, ta, True, True, "int_small",
+           bm + bn + stages + ta)
+    _check_full(w, plan=plan, exact=True)
+
+
+@pytest.mark.parametrize("bm,bn", [(128, 192), (128, 224), (256, 192), (256, 224)])
+@pytest.mark.parametrize("ta", [False, True])
+def test_odd_width_tiles_aligned_and_random(bm, bn, ta):
+    # 3-D one-box-per-stage maps; then random inputs within tolerance
+    plan = tl.plan_for(0, 0, 0, bm, bn, 128, 3 if bm == 256 else 2, raster_group=2)
+    _check_full(_w(bm * 2 + 64, bn * 2, 128 * 5, BF16, ta, True, False, "int_unit",
+                   bm + bn + 5 * ta), plan=plan, exact=True)
+    _check_full(_w(bm * 2 + 5, bn * 3 + 7, 700, BF16, ta, True, True, "uniform", bm + bn + 9),
+                plan=plan)
+
+
+@pytest.mark.parametrize("bm,bn", [(256, 224), (128, 224), (256, 192)])
+def test_odd_width_tiles_stream_k_bit_exact(bm, bn):
+    # the last waves split by k-block: partial sums of the 32-column tail step included
+    plan = tl.plan_for(0, 0, 0, bm, bn, 128, 3 if bm == 256 else 2, stream_k=1)
+    w = _w(1100, 2000, 1536 + 64, F16, False, True, True, "int_small", bm + bn + 11)
+    _check_full(w, plan=plan, exact=True)
+
+
+def test_odd_width_tiles_unaligned_c_plain_stores():
+    # C at an odd element offset: every step, the 64-column ones included, by plain stores
+    plan = tl.plan_for(0, 0, 0, 256, 224, 128, 3)
+    w = _w(600, 500, 384, BF16, False, True, False, "int_unit", 77)
+    _check_full(w, plan=plan, exact=True, ldc=507, c_off=GUARD_ODD)
 
 
 # stream-K: the k-blocks of the last waves split evenly over all units, partial sums

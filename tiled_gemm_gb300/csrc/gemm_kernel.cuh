@@ -234,6 +234,12 @@ struct WorkIter {
   }
 };
 
+// A compile-time integer passed as a value (the width of an epilogue step).
+template <int V>
+struct IntConst {
+  static constexpr int value = V;
+};
+
 template <bool kBf16, bool kRelu>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (kRelu) {
@@ -289,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tl_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
-  static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128 || BN == 256,
-                "BN must be 16, 32, 64, 128 or 256");
+  static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128 || BN == 192 || BN == 224 ||
+                    BN == 256,
+                "BN must be 16, 32, 64, 128, 192, 224 or 256");
   static_assert(CG == 1 || (CG == 2 && BN >= 128), "pairs need BN/2 >= 64");
   constexpr bool kPair = CG == 2;
   static_assert(EB == 1 || EB == 2, "1- or 2-byte elements");
@@ -303,11 +310,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kAStageBytes = a_stage_bytes<BK, EB>();
   constexpr uint32_t kBStage = b_stage_bytes<BN, CG, BK, EB>();
   constexpr uint32_t kMNChunkBytes = 128u * BK;            // one 128-byte(MN) x BK(K) chunk
-  constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;   // two accumulators; the
-                                                               // allocation unit is 32
+  // Two accumulators, kAccStride columns apart.  Widths that are not a power of two
+  // (192, 224: K-major B only) keep the second one at column 256, so that every Tensor
+  // Memory address the kernel forms is a multiple of 32 columns; the allocation is a
+  // power of two of at least 32 columns.
+  constexpr uint32_t kAccStride = (BN == 192 || BN == 224) ? 256u : static_cast<uint32_t>(BN);
+  constexpr uint32_t kTmemCols = 2 * kAccStride < 32 ? 32 : 2 * kAccStride;
   // Epilogue columns per step: one 128-byte staging row, or the whole tile when it is
   // narrower (then K-major B only: a 64-wide M/N-major box would not fit the tile).
+  // A 224-wide tile ends with one 32-column step, written by plain stores.
   constexpr int kEC = BN < kChunk ? BN : kChunk;
+  constexpr int kFull = BN / kEC;                          // full-width epilogue steps
+  constexpr int kTail = BN - kFull * kEC;                  // 0, or 32 for BN 224
+  static_assert(kTail == 0 || kTail == 32, "epilogue tail of 32 columns");
 
   // The next kernel in the stream may start its set-up now (it waits for this grid to
   // complete before it touches global memory, see grid_dependency_wait below).
@@ -515,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * kAccStride;
         for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!wait_bounded<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteMmaFull);
@@ -632,43 +647,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / kEC; ++c) {
-        uint32_t v[kEC];
-        if constexpr (kEC == 16) {
-          tmem_load_16cols(t_row + c * kEC, v);
-        } else {
-#pragma unroll
-          for (int h = 0; h < kEC / 32; ++h)
-            tmem_load_32cols(t_row + c * kEC + 32 * h,
-                             *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
+      // the whole accumulator is in registers: hand the buffer back to the MMA
+      auto release_acc = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+          else mbar_arrive(tempty_bar(acc));
         }
-        tmem_load_wait();
-        if (c == BN / kEC - 1) {
-          // the whole accumulator is in registers: hand the buffer back to the MMA
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
-            else mbar_arrive(tempty_bar(acc));
-          }
-        }
+      };
+      // One epilogue step: W columns starting at column c_col of the tile, in v.
+      auto finish_chunk = [&](auto width, uint32_t* v, int c_col) {
+        constexpr int W = decltype(width)::value;
         if (store_partial) {
           // fp32 partial sum, four columns per 16-byte store
 #pragma unroll
-          for (int j = 0; j < kEC / 4; ++j)
-            __stcg(partial4_at(cluster_id, c * (kEC / 4) + j),
+          for (int j = 0; j < W / 4; ++j)
+            __stcg(partial4_at(cluster_id, c_col / 4 + j),
                    make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
-          continue;
+          return;
         }
         // finisher: add the later k-blocks' partials, in unit order
         for (int u2 = cluster_id + 1; u2 < v_end; ++u2) {
           if (!contributes(u2)) continue;
 #pragma unroll
-          for (int j = 0; j < kEC / 4; ++j) {
-            const float4 t = __ldcg(partial4_at(u2, c * (kEC / 4) + j));
+          for (int j = 0; j < W / 4; ++j) {
+            const float4 t = __ldcg(partial4_at(u2, c_col / 4 + j));
             v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + t.x);
             v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + t.y);
             v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + t.z);
@@ -677,12 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (p.scale) {
 #pragma unroll
-          for (int j = 0; j < kEC; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * p.alpha);
+          for (int j = 0; j < W; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * p.alpha);
         }
-        uint32_t packed[kEC / 2];
-        pack_chunk<kEC / 2>(v, packed, p.bf16, p.relu);
+        uint32_t packed[W / 2];
+        pack_chunk<W / 2>(v, packed, p.bf16, p.relu);
         const int row = m0 + q * 32 + lane;      // this lane's row of the kernel's tile
-        const int col0 = n0 + c * kEC;
+        const int col0 = n0 + c_col;
         if (p.c_trans) {
           // The kernel computed C^T: its row `row` is column `row` of C, and each of
           // its columns is a row of C that the warp's 32 lanes write as 64 contiguous
@@ -690,14 +697,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row < p.M) {
             uint16_t* ccol = reinterpret_cast<uint16_t*>(p.C) + row;
 #pragma unroll
-            for (int j = 0; j < kEC / 2; ++j) {
+            for (int j = 0; j < W / 2; ++j) {
               const int col = col0 + 2 * j;
               if (col < p.N) ccol[static_cast<int64_t>(col) * p.ldc] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
               if (col + 1 < p.N) ccol[static_cast<int64_t>(col + 1) * p.ldc] = static_cast<uint16_t>(packed[j] >> 16);
             }
           }
-        } else if (kEC == kChunk && p.tma_store) {
-          if constexpr (kEC == kChunk) {
+          return;
+        }
+        if constexpr (W == kChunk) {
+          if (p.tma_store) {
             const uint32_t buf = sC + (ew * 2 + sbuf) * 4096u;
             if (lane == 0) bulk_wait_group_read<1>();   // the store two chunks ago has read buf
             __syncwarp();
@@ -719,25 +728,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) bulk_commit_group();   // (an empty group keeps the count uniform)
             sbuf ^= 1u;
+            return;
           }
-        } else if (row < p.M) {
+        }
+        if (row < p.M) {
           uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
-          if (p.c_vec && col0 + kEC <= p.N) {
-            // the lane's kEC values are 2 kEC contiguous bytes of its row of C
+          if (p.c_vec && col0 + W <= p.N) {
+            // the lane's W values are 2 W contiguous bytes of its row of C
             uint4* dst = reinterpret_cast<uint4*>(crow + col0);
 #pragma unroll
-            for (int j = 0; j < kEC / 8; ++j)
+            for (int j = 0; j < W / 8; ++j)
               dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
                                   packed[4 * j + 3]);
           } else {
 #pragma unroll
-            for (int j = 0; j < kEC / 2; ++j) {
+            for (int j = 0; j < W / 2; ++j) {
               const int col = col0 + 2 * j;
               if (col < p.N) crow[col] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
               if (col + 1 < p.N) crow[col + 1] = static_cast<uint16_t>(packed[j] >> 16);
             }
           }
         }
+      };
+#pragma unroll 1
+      for (int c = 0; c < kFull; ++c) {
+        uint32_t v[kEC];
+        if constexpr (kEC == 16) {
+          tmem_load_16cols(t_row + c * kEC, v);
+        } else {
+#pragma unroll
+          for (int h = 0; h < kEC / 32; ++h)
+            tmem_load_32cols(t_row + c * kEC + 32 * h,
+                             *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+        }
+        tmem_load_wait();
+        if (kTail == 0 && c == kFull - 1) release_acc();
+        finish_chunk(IntConst<kEC>{}, v, c * kEC);
+      }
+      if constexpr (kTail > 0) {
+        uint32_t v[32];
+        tmem_load_32cols(t_row + kFull * kEC, v);
+        tmem_load_wait();
+        release_acc();
+        finish_chunk(IntConst<32>{}, v, kFull * kEC);
       }
       if (store_partial) {
         // the warp's partial stores happen before lane 0's fence (warp barrier); the

@@ -52,7 +52,7 @@ struct DeviceState {
   int smem_optin = 0;                        // max dynamic shared memory per CTA
   uint32_t* status = nullptr;
   std::atomic<uint64_t> attr_done{0};        // bit i: smem attribute set for kernel i
-  int max_units[32] = {};                    // resident CTAs (pairs) per kernel
+  int max_units[64] = {};                    // resident CTAs (pairs) per kernel
   std::mutex mu;
 };
 
@@ -153,7 +153,10 @@ bool plan_supported(const tl_plan& pl, int eb = 2) {
            pl.raster_group >= 1 && pl.grid >= 0 && pl.swap_ab == 0;
   }
   const bool narrow = pl.bm == 128 && (pl.bn == 16 || pl.bn == 32) && pl.bk == 128;
-  const bool bn_ok = narrow ||
+  // 192 and 224 columns (not a power of two): 128-deep stages, K-major B (narrow_ok)
+  const bool odd = (pl.bm == 128 || pl.bm == 256) && (pl.bn == 192 || pl.bn == 224) &&
+                   pl.bk == 128;
+  const bool bn_ok = narrow || odd ||
                      (pl.bm == 128 && (pl.bn == 64 || pl.bn == 128 || pl.bn == 256)) ||
                      (pl.bm == 256 && (pl.bn == 128 || pl.bn == 256));
   return bn_ok && (pl.bk == 64 || pl.bk == 128) && pl.stages >= 2 && pl.stages <= 8 &&
@@ -164,14 +167,22 @@ bool plan_supported(const tl_plan& pl, int eb = 2) {
 // be K-major.  With swap_ab the kernel's B is A, K-major when A is not transposed.
 // 8-bit operands: an N-major B is read in boxes 128 elements wide, so each CTA's share
 // of the tile's columns (bn / cg) must be a multiple of 128.
+// Tiles of 192 or 224 columns also need a K-major B: an N-major B is loaded in boxes of
+// 64 columns, which must tile each CTA's share of the tile.
 bool narrow_ok(const tl_plan& pl, int trans_a, int trans_b, int eb = 2) {
   if (eb == 1) return trans_b == 1 || (pl.bn / (pl.bm / 128)) % 128 == 0;
-  if (pl.bn >= 64) return true;
+  if (pl.bn >= 64 && pl.bn != 192 && pl.bn != 224) return true;
   return pl.swap_ab ? trans_a == 0 : trans_b == 1;
 }
 
 template <int BK, int EB>
 uint32_t smem_for_bk(int bm, int bn, int stages) {
+  if constexpr (BK == 128 && EB == 2) {
+    if (bn == 192) return bm == 256 ? tl::smem_bytes_for<192, 2, BK>(stages)
+                                    : tl::smem_bytes_for<192, 1, BK>(stages);
+    if (bn == 224) return bm == 256 ? tl::smem_bytes_for<224, 2, BK>(stages)
+                                    : tl::smem_bytes_for<224, 1, BK>(stages);
+  }
   if (bm == 256) {
     return bn == 128 ? tl::smem_bytes_for<128, 2, BK, EB>(stages)
                      : tl::smem_bytes_for<256, 2, BK, EB>(stages);
@@ -273,7 +284,8 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_
       static_cast<int64_t>(pl->stages) * (128 * pl->bk + (pl->bn / cg) * pl->bk) * eb;
   pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages, eb);
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
-  pl->tmem_cols = std::max(32, 2 * pl->bn);
+  // two accumulators; 192- and 224-column tiles keep the second at column 256
+  pl->tmem_cols = (pl->bn == 192 || pl->bn == 224) ? 512 : std::max(32, 2 * pl->bn);
   pl->tma_store = (!pl->swap_ab && pl->bn >= 64) ? 1 : 0;   // for a 16-byte aligned C
   pl->repack_a = pl->repack_b = 0;                            // ditto for A and B
   pl->tx_bytes = (128 + pl->bn / cg) * pl->bk * eb;
@@ -344,7 +356,11 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, in
   // that model, calibrated on GB300 (a 1-CTA 128-wide tile runs at ~0.64 of the
   // per-SM rate of a 256-wide one).
   struct Cand { int bm, bn, bk, stages; double tile_cost; };
+  // The 224- and 192-column pair tiles (K-major B only) fill whole waves where the
+  // 256-column ones leave a short last wave, e.g. 4096^3: 16 x 19 = 304 tiles of
+  // 256 x 224 are 4 waves of 76 SM pairs, against 3.4 waves of 256 x 256.
   const Cand cands[] = {{256, 256, 128, 3, 128.0}, {256, 256, 64, 6, 135.0},
+                        {256, 224, 128, 3, 116.5}, {256, 192, 128, 3, 103.0},
                         {256, 128, 128, 4, 100.0}, {128, 256, 64, 4, 192.0},
                         {128, 128, 64, 6, 150.0},  {128, 64, 128, 4, 110.0},
                         {128, 64, 64, 8, 115.0}};
@@ -358,6 +374,7 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, in
     const int cg = cands[i].bm / 128;
     if (cg == 2 && M <= 128) continue;            // the odd CTA would hold no rows of A
     if (eb == 1 && !trans_b && (cands[i].bn / cg) % 128 != 0) continue;   // 128-wide N boxes
+    if ((cands[i].bn == 192 || cands[i].bn == 224) && (eb != 2 || !trans_b)) continue;
     const int64_t tiles = ceil_div(M, cands[i].bm) * ceil_div(N, cands[i].bn);
     const int64_t waves = ceil_div(tiles, std::max(1, sms / cg));
     const double cost = static_cast<double>(waves) * cands[i].tile_cost;
@@ -408,11 +425,13 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
 template <int BN, int CG, int BK, int EB = 2>
 int prepare_kernel(DeviceState* st) {
   // slot of this kernel in the per-device caches: 0-11 the 16-bit tilings, 12-13 the
-  // narrow ones, 16-27 the 8-bit ones (28-31: attention, 32-35: the block-scaled kernel)
-  constexpr int kIdx = BN < 64 ? 12 + (BN == 32)
-                               : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) +
-                                     6 * (BK * EB == 256) + 16 * (EB == 1);
-  constexpr uint32_t bit = 1u << kIdx;
+  // narrow ones, 16-27 the 8-bit ones (28-31: attention, 32-35: the block-scaled kernel),
+  // 36-39 the 192- and 224-column ones
+  constexpr int kIdx = (BN == 192 || BN == 224) ? 36 + (BN == 224) + 2 * (CG - 1)
+                       : BN < 64 ? 12 + (BN == 32)
+                                 : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) +
+                                       6 * (BK * EB == 256) + 16 * (EB == 1);
+  constexpr uint64_t bit = 1ull << kIdx;
   if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
   std::lock_guard<std::mutex> lock(st->mu);
   if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
@@ -442,6 +461,10 @@ int prepare_kernel(DeviceState* st) {
 
 template <int BK, int EB>
 int resident_units_bk(DeviceState* st, int bm, int bn) {
+  if constexpr (BK == 128 && EB == 2) {
+    if (bn == 192) return bm == 256 ? prepare_kernel<192, 2, BK>(st) : prepare_kernel<192, 1, BK>(st);
+    if (bn == 224) return bm == 256 ? prepare_kernel<224, 2, BK>(st) : prepare_kernel<224, 1, BK>(st);
+  }
   if (bm == 256) {
     return bn == 128 ? prepare_kernel<128, 2, BK, EB>(st) : prepare_kernel<256, 2, BK, EB>(st);
   }
@@ -487,6 +510,14 @@ template <int BK, int EB>
 tl_status launch_tiling(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
                         const CUtensorMap& tb, const CUtensorMap& tc, const tl::GemmParams& prm,
                         cudaStream_t stream) {
+  if constexpr (BK == 128 && EB == 2) {
+    if (pl.bn == 192)
+      return pl.bm == 256 ? launch_bn<192, 2, BK>(st, pl, ta, tb, tc, prm, stream)
+                          : launch_bn<192, 1, BK>(st, pl, ta, tb, tc, prm, stream);
+    if (pl.bn == 224)
+      return pl.bm == 256 ? launch_bn<224, 2, BK>(st, pl, ta, tb, tc, prm, stream)
+                          : launch_bn<224, 1, BK>(st, pl, ta, tb, tc, prm, stream);
+  }
   if (pl.bm == 256) {
     return pl.bn == 128 ? launch_bn<128, 2, BK, EB>(st, pl, ta, tb, tc, prm, stream)
                         : launch_bn<256, 2, BK, EB>(st, pl, ta, tb, tc, prm, stream);
