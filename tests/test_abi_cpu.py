@@ -78,9 +78,10 @@ def test_plan_tiles_cover_the_output_exactly_once(M, N, K):
     assert p.k_blocks * p.bk >= K > (p.k_blocks - 1) * p.bk
     assert p.tiles == p.tiles_m * p.tiles_n
     cg = p.bm // 128                       # CTAs per tile
-    assert p.grid % cg == 0
+    per_unit = cg * p.ksplit               # cluster split-K: two CTAs share a tile
+    assert p.grid % per_unit == 0
     if p.sk_iters == 0:                    # whole tiles only: one unit per tile at most
-        assert 1 <= p.grid <= cg * min(148 // cg, p.tiles)
+        assert 1 <= p.grid <= per_unit * min(148 // per_unit, p.tiles)
         assert p.dp_tiles == p.tiles
     else:                                  # split: every unit takes a share
         assert p.grid == cg * (148 // cg)
@@ -115,7 +116,7 @@ def test_every_supported_tiling_fits_shared_memory_and_others_are_rejected():
 def test_stream_k_split_choices():
     # short tiles stay whole (the fix-up would cost more than it saves), whole waves are
     # never split, the ragged 3.2-wave shape is split, forcing works both ways
-    p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152)
+    p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, ksplit=1)
     assert (p.dp_tiles, p.sk_iters, p.grid) == (64, 0, 64)
     p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, stream_k=1)
     assert (p.dp_tiles, p.sk_iters, p.grid) == (0, 64 * 16, 152)
@@ -355,3 +356,30 @@ def test_odd_width_tiles_need_a_k_major_b_and_fill_whole_waves():
     assert (p.bm, p.bn) == (256, 256)
     p = tl.tl_gemm_plan(4096, 4096, 4096, dtype=tl.TL_BF16, trans_b=0, num_sms=152)
     assert p.bn not in (192, 224)
+
+
+def test_cluster_split_k_plans():
+    # the quickstart tiling (64 tiles of 128 x 128, 16 k-blocks): two CTAs per tile
+    p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152)
+    assert p.ksplit == 2 and p.grid == 128 and p.sk_iters == 0
+    # its receive buffer (128 x 128 fp32) is part of each CTA's shared memory
+    off = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, ksplit=1)
+    assert off.ksplit == 1 and off.grid == 64
+    assert p.smem_bytes == off.smem_bytes + 128 * 128 * 4
+    # more tiles than half the SMs, or a short k-loop: no split
+    assert tl.tl_plan_complete(2048, 2048, 1024, 128, 128, 64, 3, num_sms=152).ksplit == 1
+    assert tl.tl_plan_complete(1024, 1024, 192, 128, 128, 64, 3, num_sms=152).ksplit == 1
+    # pairs never split; a forced split that cannot apply is an error
+    assert tl.tl_plan_complete(1024, 1024, 1024, 256, 256, 128, 3, num_sms=152).ksplit == 1
+    for kw in ({"bm": 256, "bn": 256, "bk": 128, "stages": 3},
+               {"bm": 128, "bn": 256, "bk": 64, "stages": 4}):        # buffer does not fit
+        with pytest.raises(tl.TLError):
+            tl.tl_plan_complete(1024, 1024, 1024, num_sms=152, ksplit=2, **kw)
+    with pytest.raises(tl.TLError):                                     # one k-block
+        tl.tl_plan_complete(1024, 1024, 64, 128, 128, 64, 3, num_sms=152, ksplit=2)
+    with pytest.raises(tl.TLError):                                     # with stream-K
+        tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, ksplit=2,
+                            stream_k=1)
+    # a forced grid counts CTAs: 6 CTAs are 3 clusters
+    g = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, ksplit=2, grid=6)
+    assert g.grid == 6

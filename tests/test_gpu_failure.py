@@ -34,14 +34,17 @@ def short_limit():
         tl.tl_device_status(reset=True)
 
 
-@pytest.mark.parametrize("bm,bn,bk,stages", [(128, 128, 64, 3), (256, 256, 128, 3)])
+@pytest.mark.parametrize("bm,bn,bk,stages,ksplit", [(128, 128, 64, 3, 1), (128, 128, 64, 3, 2),
+                                                    (256, 256, 128, 3, 0)])
 def test_a_wait_that_nothing_ends_times_out_and_the_context_survives(short_limit, bm, bn, bk,
-                                                                     stages):
+                                                                     stages, ksplit):
+    # ksplit 2: two CTAs of a cluster per tile, both stalled, their partial-sum hand-over
+    # never reached
     w = workloads.Workload("stall", 600, 700, 1000, workloads.F16, False, False, True,
                            "int_small", "int_small", seed=bm + bn)
     a, b = workloads.make_inputs(w)
     ad, bd = a.cuda(), b.cuda()
-    plan = tl.plan_for(0, 0, 0, bm, bn, bk, stages)
+    plan = tl.plan_for(0, 0, 0, bm, bn, bk, stages, ksplit=ksplit)
     out = torch.full((w.M, w.N), 3.0, dtype=torch.float16, device="cuda")
 
     tl.tl_debug_set_stall(1)

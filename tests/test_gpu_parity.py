@@ -138,6 +138,59 @@ def test_odd_width_tiles_unaligned_c_plain_stores():
     _check_full(w, plan=plan, exact=True, ldc=507, c_off=GUARD_ODD)
 
 
+# Cluster split-K: two CTAs of a cluster share each tile's k-blocks; the second hands its
+# fp32 partial sum to the first through distributed shared memory.
+KSPLIT_CASES = [
+    # bn, bk, stages, M, N, K, grid (0: one cluster per tile), trans_a, trans_b
+    (128, 64, 3, 1024, 1024, 1024, 0, False, False),   # the quickstart tiling
+    (128, 64, 3, 1000, 900, 777, 0, True, False),      # ragged K: 13 k-blocks, 6 + 7
+    (64, 128, 3, 300, 520, 1000, 0, False, True),      # 8 k-blocks of 128
+    (128, 128, 2, 400, 384, 2048, 0, True, True),
+    (128, 64, 3, 700, 900, 515, 4, False, True),       # 2 clusters walking 48 tiles
+    (64, 64, 4, 257, 333, 128, 6, True, True),         # 2 k-blocks: one each; 3 clusters
+    (64, 64, 4, 129, 200, 320, 0, False, False),       # 5 k-blocks: 2 + 3
+]
+
+
+@pytest.mark.parametrize("bn,bk,stages,M,N,K,grid,ta,tb", KSPLIT_CASES)
+def test_cluster_split_k_bit_exact(bn, bk, stages, M, N, K, grid, ta, tb):
+    plan = tl.plan_for(0, 0, 0, 128, bn, bk, stages, raster_group=3, grid=grid, ksplit=2)
+    p = tl.tl_plan_complete(M, N, K, 128, bn, bk, stages, trans_a=int(ta), trans_b=int(tb),
+                            num_sms=152, raster_group=3, grid=grid, ksplit=2)
+    assert p.ksplit == 2 and p.grid % 2 == 0 and p.sk_iters == 0
+    w = _w(M, N, K, F16, ta, tb, True, "int_small", bn + bk + M + K)
+    _check_full(w, plan=plan, exact=True)
+    _check_full(_w(M, N, K, BF16, ta, tb, False, "uniform", bn + K), plan=plan)
+
+
+@pytest.mark.parametrize("bn,stages,M", [(16, 6, 16), (32, 5, 30)])
+def test_cluster_split_k_with_the_operand_swap_bit_exact(bn, stages, M):
+    # skinny products: C^T tiles of 128 x bn, k-blocks shared by a cluster of two
+    plan = tl.plan_for(0, 0, 0, 128, bn, 128, stages, swap_ab=1, ksplit=2)
+    w = _w(M, 2000, 1536 + 40, BF16, False, True, False, "int_unit", bn + M)
+    _check_full(w, plan=plan, exact=True)
+
+
+def test_cluster_split_k_deterministic_over_repeats_and_graph_replay():
+    w = _w(640, 768, 1000, BF16, False, True, True, "normal_over_sqrtk", 52)
+    plan = tl.plan_for(0, 0, 0, 128, 128, 64, 3, ksplit=2)
+    a, b = workloads.make_inputs(w)
+    got1, _ = run_tl(a, b, w.M, w.N, w.K, w.dtype, False, True, True, plan=plan)
+    got2, _ = run_tl(a, b, w.M, w.N, w.K, w.dtype, False, True, True, plan=plan)
+    assert np.array_equal(got1, got2)
+    ad, bd = a.cuda(), b.cuda()
+    out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tl.gemm(ad, bd, trans_b=True, relu=True, out=out, plan=plan, stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), got1)
+
+
 # stream-K: the k-blocks of the last waves split evenly over all units, partial sums
 # added by each split tile's finisher
 SPLIT_CASES = [

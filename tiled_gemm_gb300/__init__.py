@@ -57,7 +57,7 @@ class Plan(ctypes.Structure):
         ("l2_prefetch", ctypes.c_int32), ("producers", ctypes.c_int32),
         ("stream_k", ctypes.c_int32), ("dp_tiles", ctypes.c_int32),
         ("swap_ab", ctypes.c_int32), ("sk_iters", ctypes.c_int64),
-        ("workspace_bytes", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64), ("ksplit", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -171,9 +171,10 @@ def tl_plan_complete(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: 
                      dtype: int = TL_F16, trans_a: int = 0, trans_b: int = 0,
                      num_sms: int = 0, raster_group: int = 16, grid: int = 0,
                      l2_prefetch: int = -1, producers: int = 0, stream_k: int = 0,
-                     swap_ab: int = 0) -> Plan:
+                     swap_ab: int = 0, ksplit: int = 0) -> Plan:
     pl = Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
-              l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k, swap_ab=swap_ab)
+              l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k, swap_ab=swap_ab,
+              ksplit=ksplit)
     st = _lib.tl_plan_complete(M, N, K, dtype, trans_a, trans_b, num_sms, ctypes.byref(pl))
     if st != TL_OK:
         raise TLError(st, "tl_plan_complete")
@@ -282,15 +283,16 @@ def gemm(a, b, *, trans_a: bool = False, trans_b: bool = False, relu: bool = Fal
 def plan_for(M: int, N: int, K: int, bm: int, bn: int, bk: int, stages: int,
              raster_group: int = 16, grid: int = 0, l2_prefetch: int = -1,
              producers: int = 0, stream_k: int = 0, swap_ab: int = 0,
-             tma_store: int = 0) -> Plan:
+             tma_store: int = 0, ksplit: int = 0) -> Plan:
     """A plan with a fixed tiling, to pass as ``gemm(..., plan=...)``; l2_prefetch < 0,
     producers <= 0 and stream_k = 0 take the library's defaults for the problem
     (stream_k -1 forces whole tiles only, 1 forces the split of the last waves);
     swap_ab = 1 runs the kernel on C^T = op(B)^T op(A)^T (bm x bn tiles of C^T);
-    tma_store = -1 writes C with plain stores instead of TMA bulk stores."""
+    tma_store = -1 writes C with plain stores instead of TMA bulk stores; ksplit 0 is
+    automatic, 1 off, 2 two CTAs of a cluster per tile (cluster split-K)."""
     return Plan(bm=bm, bn=bn, bk=bk, stages=stages, raster_group=raster_group, grid=grid,
                 l2_prefetch=l2_prefetch, producers=producers, stream_k=stream_k,
-                swap_ab=swap_ab, tma_store=tma_store)
+                swap_ab=swap_ab, tma_store=tma_store, ksplit=ksplit)
 
 
 def _fp8_code(t) -> int:

@@ -81,6 +81,7 @@ enum WaitSite : uint32_t {
   kSiteDrain = 5,
   kSiteStreamK = 6,
   kSiteInjected = 7,    // the test hook's wait that nothing ends (GemmParams::stall)
+  kSiteClusterSplit = 8,  // cluster split-K hand-over of a partial accumulator
 };
 
 struct GemmParams {
@@ -109,6 +110,10 @@ struct GemmParams {
   // holds the tile's first k-block adds the partials in order and writes C.
   int32_t dp_tiles;
   int64_t sk_iters;
+  // Cluster split-K (one-CTA tiles only): 1, or 2 CTAs of a cluster on each tile, CTA r
+  // taking k-blocks [r kb / 2, (r + 1) kb / 2).  CTA 1 sends its fp32 accumulator into
+  // CTA 0's shared memory (distributed shared memory); CTA 0 adds it and writes C.
+  int32_t ksplit;
   float* sk_partials;                 // [unit][cta][4 warps][BN/4 col groups][32 lanes][4]
   unsigned long long* sk_flags;       // [unit][cta][4 warps]
   unsigned long long sk_token;        // unique to this launch, never 0
@@ -134,17 +139,25 @@ __host__ __device__ constexpr uint32_t b_stage_bytes() {
 }
 
 // Barrier block: full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done,
-// then the 4-byte Tensor Memory base slot, the 4-byte abort flag and, per stage, the
-// last lap at which a producer armed that stage (int32 x 8, -1 = never).
+// red_full[4], red_empty[4] (cluster split-K, one per epilogue warp), then the 4-byte
+// Tensor Memory base slot, the 4-byte abort flag and, per stage, the last lap at which a
+// producer armed that stage (int32 x 8, -1 = never).
 __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
-  return static_cast<uint32_t>(8 * (2 * stages + 5) + 8 + 32);
+  return static_cast<uint32_t>(8 * (2 * stages + 5 + 8) + 8 + 32);
+}
+
+// Cluster split-K receive buffer: one 128 x BN fp32 accumulator, per epilogue warp BN
+// columns x 32 lanes, four columns per 16-byte entry, lane-major.
+template <int BN>
+__host__ __device__ constexpr uint32_t red_bytes(int ksplit) {
+  return ksplit > 1 ? static_cast<uint32_t>(128 * BN * 4) : 0u;
 }
 
 template <int BN, int CG, int BK, int EB = 2>
-__host__ __device__ constexpr uint32_t smem_bytes_for(int stages) {
+__host__ __device__ constexpr uint32_t smem_bytes_for(int stages, int ksplit = 1) {
   // +1024: the dynamic shared memory base is rounded up to 1024 B in the kernel
   return 1024u + stages * (a_stage_bytes<BK, EB>() + b_stage_bytes<BN, CG, BK, EB>()) +
-         staging_bytes<BN>() + barrier_bytes(stages);
+         staging_bytes<BN>() + red_bytes<BN>(ksplit) + barrier_bytes(stages);
 }
 
 // Grouped raster order: walk `group` tile-rows top to bottom, then the next column.
@@ -210,14 +223,17 @@ __device__ __forceinline__ int64_t sk_begin(const GemmParams& p, int unit, int u
 }
 
 struct WorkIter {
-  int next_dp, step, dp_end, kb;
+  int next_dp, step, dp_end, kb, kr0, kr1;
   int64_t it, it_end;
-  __device__ __forceinline__ WorkIter(const GemmParams& p, int unit, int units)
+  // krank / ksplit: this CTA's part of each whole tile's k-blocks (cluster split-K)
+  __device__ __forceinline__ WorkIter(const GemmParams& p, int unit, int units, int krank = 0)
       : next_dp(unit), step(units), dp_end(p.dp_tiles), kb(p.k_blocks),
+        kr0(krank * p.k_blocks / max(1, p.ksplit)),
+        kr1((krank + 1) * p.k_blocks / max(1, p.ksplit)),
         it(sk_begin(p, unit, units)), it_end(sk_begin(p, unit + 1, units)) {}
   __device__ __forceinline__ bool next(WorkItem& w) {
     if (next_dp < dp_end) {
-      w = {next_dp, 0, kb};
+      w = {next_dp, kr0, kr1};
       next_dp += step;
       return true;
     }
@@ -339,16 +355,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const int S = p.stages;
 
+  const bool ksplit = !kPair && p.ksplit > 1;
   const uint32_t sA = base;
   const uint32_t sB = sA + S * kAStageBytes;
   const uint32_t sC = sB + S * kBStage;
-  const uint32_t sBar = sC + staging_bytes<BN>();
+  const uint32_t sRed = sC + staging_bytes<BN>();
+  const uint32_t sBar = sRed + red_bytes<BN>(ksplit ? 2 : 1);
   auto full_bar = [&](int s) { return sBar + 8u * s; };
   auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
   auto tfull_bar = [&](int a) { return sBar + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return sBar + 8u * (2 * S + 2 + a); };
   const uint32_t done_bar = sBar + 8u * (2 * S + 4);
-  const uint32_t slot = sBar + 8u * (2 * S + 5);
+  auto red_full_bar = [&](int q) { return sBar + 8u * (2 * S + 5 + q); };
+  auto red_empty_bar = [&](int q) { return sBar + 8u * (2 * S + 9 + q); };
+  const uint32_t slot = sBar + 8u * (2 * S + 13);
   volatile uint32_t* const tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
@@ -358,8 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // position in the CTA pair
   const bool leader = rank == 0;
-  const int cluster_id = static_cast<int>(blockIdx.x) / CG;
-  const int n_clusters = static_cast<int>(gridDim.x) / CG;
+  // cluster split-K: krank 0 finishes each tile, krank 1 contributes its partial sum
+  const int krank = ksplit ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cta_per_unit = CG * (ksplit ? 2 : 1);
+  const int cluster_id = static_cast<int>(blockIdx.x) / cta_per_unit;
+  const int n_clusters = static_cast<int>(gridDim.x) / cta_per_unit;
 
   // TMA boxes of one stage in this CTA (a chunk is kChunkElems = 128 bytes wide).
   // A: K-major, one 2-D box {chunk K, 128 M} per K chunk, or M-major, one 2-D box
@@ -381,6 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), kEpiWarps * CG);   // every epilogue warp of the pair
     }
     mbar_init(done_bar, 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(red_full_bar(q), 32);    // the 32 lanes of the contributor's warp q
+      mbar_init(red_empty_bar(q), 32);   // the 32 lanes of the finisher's warp q
+    }
     *abort_flag = 0u;
     for (int s = 0; s < 8; ++s) lap_armed[s] = -1;
     fence_barrier_init();
@@ -396,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (kPair) cluster_sync_all();   // the peer's barriers exist before any use
+  if (kPair || ksplit) cluster_sync_all();   // the peer's barriers exist before any use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot_ptr;
   // Everything above touched only this CTA's shared and Tensor Memory.  The operands,
@@ -461,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // walk this unit's (tile, k-block) iterations g = 0, 1, ...; issue g = pi, pi + P, ...
-      WorkIter work(p, cluster_id, n_clusters);
+      WorkIter work(p, cluster_id, n_clusters, krank);
       WorkItem w;
       int g = 0;
       while (ok && work.next(w)) {
@@ -522,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_timeout(p.status, abort_flag, kSiteInjected);
         ok = false;
       }
-      WorkIter work(p, cluster_id, n_clusters);
+      WorkIter work(p, cluster_id, n_clusters, krank);
       WorkItem w;
       while (ok && work.next(w)) {
         if (!wait_bounded<kPair>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -587,7 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;               // staging-buffer owner index
     uint32_t acc = 0, acc_phase = 0;
     uint32_t sbuf = 0;
-    WorkIter work(p, cluster_id, n_clusters);
+    uint32_t red_phase = 0;                // tiles exchanged so far, mod 2
+    WorkIter work(p, cluster_id, n_clusters, krank);
     WorkItem w;
     while (work.next(w)) {
       int mb, nb;
@@ -597,9 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Stream-K roles: a partial item that starts mid-tile stores its sum for the
       // tile's finisher; an item that starts at k-block 0 but ends early is the
       // finisher and adds the partials of units cluster_id + 1 .. v_end - 1.
-      const bool store_partial = w.k0 > 0;
+      const bool store_partial = !ksplit && w.k0 > 0;
       int v_end = cluster_id + 1;
-      if (w.k0 == 0 && w.k1 < p.k_blocks) {
+      if (!ksplit && w.k0 == 0 && w.k1 < p.k_blocks) {
         const int64_t tile_end = static_cast<int64_t>(w.tile - p.dp_tiles + 1) * p.k_blocks;
         while (v_end < n_clusters && sk_begin(p, v_end, n_clusters) < tile_end) ++v_end;
       }
@@ -646,6 +674,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
         break;
       }
+      // Cluster split-K: CTA 1 writes its accumulator into CTA 0's receive buffer once
+      // CTA 0 has read the previous tile's; CTA 0 waits for it to arrive.  Every lane
+      // waits (and later arrives) itself, so each one orders its own accesses.
+      const bool red_send = ksplit && krank == 1;
+      const bool red_recv = ksplit && krank == 0;
+      if (red_send || red_recv) {
+        const bool got = wait_bounded<true>(red_send ? red_empty_bar(q) : red_full_bar(q),
+                                            red_send ? (red_phase ^ 1u) : red_phase,
+                                            abort_flag, p.timeout_ns);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteClusterSplit);
+          break;
+        }
+      }
+      const uint32_t red_entry = sRed + static_cast<uint32_t>(q * (BN / 4) * 32 + lane) * 16u;
+      const uint32_t red_remote = red_send ? mapa_shared(red_entry, 0) : 0u;
       tc_fence_after_sync();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
@@ -661,6 +705,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // One epilogue step: W columns starting at column c_col of the tile, in v.
       auto finish_chunk = [&](auto width, uint32_t* v, int c_col) {
         constexpr int W = decltype(width)::value;
+        if (red_send) {
+          // entry (column group, lane) of this warp's part of CTA 0's receive buffer
+#pragma unroll
+          for (int j = 0; j < W / 4; ++j)
+            st_cluster_v4(red_remote + static_cast<uint32_t>(c_col / 4 + j) * 512u, v[4 * j],
+                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          return;
+        }
+        if (red_recv) {
+          // own k-blocks first, then CTA 1's: a fixed order
+#pragma unroll
+          for (int j = 0; j < W / 4; ++j) {
+            const float4 t = ld_shared_f4(red_entry + static_cast<uint32_t>(c_col / 4 + j) * 512u);
+            v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + t.x);
+            v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + t.y);
+            v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + t.z);
+            v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + t.w);
+          }
+        }
         if (store_partial) {
           // fp32 partial sum, four columns per 16-byte store
 #pragma unroll
@@ -772,6 +835,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_acc();
         finish_chunk(IntConst<32>{}, v, kFull * kEC);
       }
+      if (red_send) {
+        // the partial is in CTA 0's buffer (release: the stores come first)
+        mbar_arrive_cluster(mapa_shared(red_full_bar(q), 0));
+        red_phase ^= 1u;
+      } else if (red_recv) {
+        // the buffer is read: CTA 1 may write the next tile's partial
+        mbar_arrive_cluster(mapa_shared(red_empty_bar(q), 1));
+        red_phase ^= 1u;
+      }
       if (store_partial) {
         // the warp's partial stores happen before lane 0's fence (warp barrier); the
         // GPU-scope fence and release store make all of them visible before the flag
@@ -820,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if constexpr (kPair) cluster_sync_all();   // no CTA leaves while its peer may touch it
+  if (kPair || ksplit) cluster_sync_all();   // no CTA leaves while its peer may touch it
   tc_fence_after_sync();
   if (warp == 1) {
     __syncwarp();

@@ -53,6 +53,7 @@ struct DeviceState {
   uint32_t* status = nullptr;
   std::atomic<uint64_t> attr_done{0};        // bit i: smem attribute set for kernel i
   int max_units[64] = {};                    // resident CTAs (pairs) per kernel
+  int max_clusters2[64] = {};                // resident clusters of two per kernel
   std::mutex mu;
 };
 
@@ -176,33 +177,36 @@ bool narrow_ok(const tl_plan& pl, int trans_a, int trans_b, int eb = 2) {
 }
 
 template <int BK, int EB>
-uint32_t smem_for_bk(int bm, int bn, int stages) {
+uint32_t smem_for_bk(int bm, int bn, int stages, int ks) {
   if constexpr (BK == 128 && EB == 2) {
     if (bn == 192) return bm == 256 ? tl::smem_bytes_for<192, 2, BK>(stages)
-                                    : tl::smem_bytes_for<192, 1, BK>(stages);
+                                    : tl::smem_bytes_for<192, 1, BK>(stages, ks);
     if (bn == 224) return bm == 256 ? tl::smem_bytes_for<224, 2, BK>(stages)
-                                    : tl::smem_bytes_for<224, 1, BK>(stages);
+                                    : tl::smem_bytes_for<224, 1, BK>(stages, ks);
   }
   if (bm == 256) {
     return bn == 128 ? tl::smem_bytes_for<128, 2, BK, EB>(stages)
                      : tl::smem_bytes_for<256, 2, BK, EB>(stages);
   }
   if constexpr (BK == 128 && EB == 2) {
-    if (bn == 16) return tl::smem_bytes_for<16, 1, BK>(stages);
-    if (bn == 32) return tl::smem_bytes_for<32, 1, BK>(stages);
+    if (bn == 16) return tl::smem_bytes_for<16, 1, BK>(stages, ks);
+    if (bn == 32) return tl::smem_bytes_for<32, 1, BK>(stages, ks);
   }
   switch (bn) {
-    case 64: return tl::smem_bytes_for<64, 1, BK, EB>(stages);
-    case 128: return tl::smem_bytes_for<128, 1, BK, EB>(stages);
-    default: return tl::smem_bytes_for<256, 1, BK, EB>(stages);
+    case 64: return tl::smem_bytes_for<64, 1, BK, EB>(stages, ks);
+    case 128: return tl::smem_bytes_for<128, 1, BK, EB>(stages, ks);
+    default: return tl::smem_bytes_for<256, 1, BK, EB>(stages, ks);
   }
 }
 
-uint32_t smem_for(int bm, int bn, int bk, int stages, int eb = 2) {
+// Dynamic shared memory of one CTA; ks = 2 adds cluster split-K's receive buffer.
+uint32_t smem_for(int bm, int bn, int bk, int stages, int eb = 2, int ks = 1) {
   if (eb == 1) {
-    return bk == 256 ? smem_for_bk<256, 1>(bm, bn, stages) : smem_for_bk<128, 1>(bm, bn, stages);
+    return bk == 256 ? smem_for_bk<256, 1>(bm, bn, stages, ks)
+                     : smem_for_bk<128, 1>(bm, bn, stages, ks);
   }
-  return bk == 128 ? smem_for_bk<128, 2>(bm, bn, stages) : smem_for_bk<64, 2>(bm, bn, stages);
+  return bk == 128 ? smem_for_bk<128, 2>(bm, bn, stages, ks)
+                   : smem_for_bk<64, 2>(bm, bn, stages, ks);
 }
 
 tl_status validate_common(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
@@ -235,12 +239,16 @@ int default_prefetch(const tl_plan& pl) {
 // costs ~6,000 SM cycles, i.e. fixup_kb k-blocks of about max(600, MMA cycles) each --
 // so short tiles stay whole.  Under the power cap the split also raises the clock-
 // limited work, hence the 0.87 margin.
+//
+// With cluster split-K (ksplit = 2) a unit is a cluster of two CTAs that share each of its
+// whole tiles' k-blocks; nothing else is split.
 void schedule(tl_plan* pl, int64_t units_avail, bool allow_split, int eb = 2) {
   const int cg = pl->bm / 128;
+  const int ks = std::max(1, pl->ksplit);
   const int64_t units = std::max<int64_t>(1, units_avail);
   const int64_t T = pl->tiles, KI = pl->k_blocks;
   int64_t dp = T, iters = 0;
-  if (allow_split && pl->stream_k >= 0 && units > 1 && KI >= 2) {
+  if (ks == 1 && allow_split && pl->stream_k >= 0 && units > 1 && KI >= 2) {
     const int64_t full = T / units, rem = T % units;
     if (rem != 0 || pl->stream_k == 1) {
       const int64_t dp_try = full >= 1 ? (full - 1) * units : 0;
@@ -259,7 +267,19 @@ void schedule(tl_plan* pl, int64_t units_avail, bool allow_split, int eb = 2) {
   }
   pl->dp_tiles = static_cast<int32_t>(dp);
   pl->sk_iters = iters;
-  pl->grid = static_cast<int32_t>(cg * (iters > 0 ? units : std::min<int64_t>(units, T)));
+  pl->grid = static_cast<int32_t>(cg * ks * (iters > 0 ? units : std::min<int64_t>(units, T)));
+}
+
+// Cluster split-K for one-CTA tiles: when at most half the SMs would hold a tile and the
+// k-loop is long enough to halve, two CTAs of a cluster share each tile's k-blocks.  The
+// quickstart 1024^3 tiling (64 tiles of 128 x 128, 16 k-blocks of 64) is bound by the
+// latency of its 3-stage ring refills from DRAM: split, each tile has two rings' loads
+// in flight, and the partial-sum hand-over costs one Tensor Memory read and a 64 KB
+// write into the peer's shared memory.
+int auto_ksplit(const tl_plan& pl, int sms, int eb) {
+  if (pl.bm != 128 || pl.stream_k == 1 || 2 * pl.tiles > sms || pl.k_blocks < 4) return 1;
+  // the receive buffer (128 x bn fp32) must fit beside the ring
+  return smem_for(pl.bm, pl.bn, pl.bk, pl.stages, eb, 2) <= kMaxSmemPerCta ? 2 : 1;
 }
 
 // fp32 partial-sum slots (one 128 x bn tile per CTA) and ready flags (one per epilogue
@@ -282,7 +302,13 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_
   // per CTA: 128 rows of A and bn/cg columns of B per stage
   pl->ring_bytes =
       static_cast<int64_t>(pl->stages) * (128 * pl->bk + (pl->bn / cg) * pl->bk) * eb;
-  pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages, eb);
+  // cluster split-K: 0 automatic, 1 off, 2 on (one-CTA tiles, at least 2 k-blocks, and
+  // not with a forced stream-K split)
+  if (pl->ksplit < 0 || pl->ksplit > 2) return TL_ERR_INVALID_ARG;
+  if (pl->ksplit == 0) pl->ksplit = auto_ksplit(*pl, sms, eb);
+  if (pl->ksplit == 2 && (pl->bm != 128 || pl->k_blocks < 2 || pl->stream_k == 1))
+    return TL_ERR_INVALID_ARG;
+  pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages, eb, pl->ksplit);
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
   // two accumulators; 192- and 224-column tiles keep the second at column 256
   pl->tmem_cols = (pl->bn == 192 || pl->bn == 224) ? 512 : std::max(32, 2 * pl->bn);
@@ -291,8 +317,11 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_
   pl->tx_bytes = (128 + pl->bn / cg) * pl->bk * eb;
   if (pl->tiles > (int64_t{1} << 31) - 1) return TL_ERR_UNSUPPORTED;
   if (pl->stream_k < -1 || pl->stream_k > 1) return TL_ERR_INVALID_ARG;
-  // grid in CTAs: a multiple of cg; one persistent unit (CTA or pair) per SM (pair)
-  const int64_t want_units = pl->grid > 0 ? std::max<int64_t>(1, pl->grid / cg) : sms / cg;
+  // grid in CTAs: a multiple of cg * ksplit; one persistent unit (CTA, pair or split
+  // cluster) per SM or SM pair
+  const int per_unit = cg * pl->ksplit;
+  const int64_t want_units =
+      pl->grid > 0 ? std::max<int64_t>(1, pl->grid / per_unit) : sms / per_unit;
   schedule(pl, want_units, true, eb);
   if (pl->l2_prefetch < 0) pl->l2_prefetch = default_prefetch(*pl);
   if (pl->l2_prefetch > 1024) return TL_ERR_INVALID_ARG;
@@ -327,6 +356,7 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, in
     pl->bk = 128;
     pl->stages = pl->bn == 16 ? 6 : 5;
     pl->swap_ab = 1;
+    pl->ksplit = 1;                // the stream-K split below, over all SMs
     return;
   }
   // One wave of narrow tiles.  When every 128 x 64 tile of C gets an SM of its own, the
@@ -398,7 +428,7 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, in
 // writes global memory.  attr must hold 2 entries.
 template <int BN, int CG, int BK, int EB>
 void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t smem,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, int ks = 1) {
   *cfg = cudaLaunchConfig_t{};
   cfg->blockDim = dim3(tl::kThreads);
   cfg->dynamicSmemBytes = smem;
@@ -407,9 +437,9 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[n].val.programmaticStreamSerializationAllowed = 1;
   ++n;
-  if (CG == 2) {
+  if (CG * ks > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(CG * ks);
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -419,11 +449,11 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t sm
 }
 
 // Once per device and kernel: allow the large dynamic shared memory, and find how many
-// units (CTAs, or CTA pairs) the device keeps resident at once -- the persistent grid
-// must not exceed it (pairs sit on SM pairs within one GPC).  Returns that count, or
-// -1 if the attribute could not be set.
+// units (CTAs, CTA pairs, or with ks = 2 clusters of two one-CTA units) the device keeps
+// resident at once -- the persistent grid must not exceed it (pairs sit on SM pairs
+// within one GPC).  Returns that count, or -1 if the attribute could not be set.
 template <int BN, int CG, int BK, int EB = 2>
-int prepare_kernel(DeviceState* st) {
+int prepare_kernel(DeviceState* st, int ks = 1) {
   // slot of this kernel in the per-device caches: 0-11 the 16-bit tilings, 12-13 the
   // narrow ones, 16-27 the 8-bit ones (28-31: attention, 32-35: the block-scaled kernel),
   // 36-39 the 192- and 224-column ones
@@ -432,60 +462,65 @@ int prepare_kernel(DeviceState* st) {
                                  : (BN == 64 ? 0 : (BN == 128 ? 1 : 2)) + 3 * (CG - 1) +
                                        6 * (BK * EB == 256) + 16 * (EB == 1);
   constexpr uint64_t bit = 1ull << kIdx;
-  if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
+  auto units_for = [&] { return ks == 2 ? st->max_clusters2[kIdx] : st->max_units[kIdx]; };
+  if (st->attr_done.load(std::memory_order_acquire) & bit) return units_for();
   std::lock_guard<std::mutex> lock(st->mu);
-  if (st->attr_done.load(std::memory_order_acquire) & bit) return st->max_units[kIdx];
+  if (st->attr_done.load(std::memory_order_acquire) & bit) return units_for();
   auto kern = tl::tl_gemm_kernel<BN, CG, BK, EB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            st->smem_optin) != cudaSuccess) {
     (void)cudaGetLastError();
     return -1;
   }
-  int units = st->sms / CG;
-  if (CG == 2) {
+  // resident clusters of two: the CTA pairs of CG = 2, or cluster split-K's pairs of
+  // one-CTA units
+  int pairs = st->sms / 2;
+  {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    launch_config<BN, CG, BK, EB>(&cfg, attr, static_cast<size_t>(st->smem_optin), nullptr);
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * units));
+    launch_config<BN, CG, BK, EB>(&cfg, attr, static_cast<size_t>(st->smem_optin), nullptr,
+                                  CG == 2 ? 1 : 2);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
-      units = n;
+      pairs = n;
     } else {
       (void)cudaGetLastError();
     }
   }
-  st->max_units[kIdx] = units;
+  st->max_units[kIdx] = CG == 2 ? pairs : st->sms;
+  st->max_clusters2[kIdx] = pairs;
   st->attr_done.fetch_or(bit, std::memory_order_acq_rel);
-  return units;
+  return units_for();
 }
 
 template <int BK, int EB>
-int resident_units_bk(DeviceState* st, int bm, int bn) {
+int resident_units_bk(DeviceState* st, int bm, int bn, int ks) {
   if constexpr (BK == 128 && EB == 2) {
-    if (bn == 192) return bm == 256 ? prepare_kernel<192, 2, BK>(st) : prepare_kernel<192, 1, BK>(st);
-    if (bn == 224) return bm == 256 ? prepare_kernel<224, 2, BK>(st) : prepare_kernel<224, 1, BK>(st);
+    if (bn == 192) return bm == 256 ? prepare_kernel<192, 2, BK>(st, ks) : prepare_kernel<192, 1, BK>(st, ks);
+    if (bn == 224) return bm == 256 ? prepare_kernel<224, 2, BK>(st, ks) : prepare_kernel<224, 1, BK>(st, ks);
   }
   if (bm == 256) {
-    return bn == 128 ? prepare_kernel<128, 2, BK, EB>(st) : prepare_kernel<256, 2, BK, EB>(st);
+    return bn == 128 ? prepare_kernel<128, 2, BK, EB>(st, ks) : prepare_kernel<256, 2, BK, EB>(st, ks);
   }
   if constexpr (BK == 128 && EB == 2) {
-    if (bn == 16) return prepare_kernel<16, 1, BK>(st);
-    if (bn == 32) return prepare_kernel<32, 1, BK>(st);
+    if (bn == 16) return prepare_kernel<16, 1, BK>(st, ks);
+    if (bn == 32) return prepare_kernel<32, 1, BK>(st, ks);
   }
   switch (bn) {
-    case 64: return prepare_kernel<64, 1, BK, EB>(st);
-    case 128: return prepare_kernel<128, 1, BK, EB>(st);
-    default: return prepare_kernel<256, 1, BK, EB>(st);
+    case 64: return prepare_kernel<64, 1, BK, EB>(st, ks);
+    case 128: return prepare_kernel<128, 1, BK, EB>(st, ks);
+    default: return prepare_kernel<256, 1, BK, EB>(st, ks);
   }
 }
 
 int resident_units(DeviceState* st, const tl_plan& pl, int eb) {
   if (eb == 1) {
-    return pl.bk == 256 ? resident_units_bk<256, 1>(st, pl.bm, pl.bn)
-                        : resident_units_bk<128, 1>(st, pl.bm, pl.bn);
+    return pl.bk == 256 ? resident_units_bk<256, 1>(st, pl.bm, pl.bn, pl.ksplit)
+                        : resident_units_bk<128, 1>(st, pl.bm, pl.bn, pl.ksplit);
   }
-  return pl.bk == 128 ? resident_units_bk<128, 2>(st, pl.bm, pl.bn)
-                      : resident_units_bk<64, 2>(st, pl.bm, pl.bn);
+  return pl.bk == 128 ? resident_units_bk<128, 2>(st, pl.bm, pl.bn, pl.ksplit)
+                      : resident_units_bk<64, 2>(st, pl.bm, pl.bn, pl.ksplit);
 }
 
 // Launch with exactly pl.grid CTAs: the work split in `prm` was computed for that grid.
@@ -497,7 +532,8 @@ tl_status launch_bn(DeviceState* st, const tl_plan& pl, const CUtensorMap& ta,
   auto kern = tl::tl_gemm_kernel<BN, CG, BK, EB>;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  launch_config<BN, CG, BK, EB>(&cfg, attr, static_cast<size_t>(pl.smem_bytes), stream);
+  launch_config<BN, CG, BK, EB>(&cfg, attr, static_cast<size_t>(pl.smem_bytes), stream,
+                                std::max(1, pl.ksplit));
   cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -748,6 +784,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     pl.producers = forced->producers;
     pl.stream_k = forced->stream_k;
     pl.swap_ab = forced->swap_ab;
+    pl.ksplit = forced->ksplit;
   } else {
     choose_tiling(M, N, K, trans_a, trans_b, st->sms, &pl, eb);
   }
@@ -759,9 +796,10 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   const int resident = resident_units(st, pl, eb);
   if (resident <= 0) return TL_ERR_LAUNCH;
   {
-    const int cg = pl.bm / 128;
-    const int64_t want_units = forced && forced->grid > 0 ? std::max(1, forced->grid / cg)
-                                                           : st->sms / cg;
+    const int per_unit = (pl.bm / 128) * pl.ksplit;
+    const int64_t want_units = forced && forced->grid > 0
+                                   ? std::max(1, forced->grid / per_unit)
+                                   : st->sms / per_unit;
     schedule(&pl, std::min<int64_t>(want_units, resident), !no_alloc, eb);
   }
   const int64_t ws_split = split_workspace_bytes(pl);
@@ -904,6 +942,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.producers = pl.producers;
   prm.dp_tiles = pl.dp_tiles;
   prm.sk_iters = pl.sk_iters;
+  prm.ksplit = pl.ksplit;
   prm.sk_partials = sk_partials;
   prm.sk_flags = sk_flags;
   prm.sk_token = next_split_token();
@@ -1241,11 +1280,13 @@ tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int 
   const int32_t prod = plan->producers;
   const int32_t sk = plan->stream_k;
   const int32_t swap = plan->swap_ab;
+  const int32_t ks = plan->ksplit;
   std::memset(&plan->tiles_m, 0, sizeof(tl_plan) - offsetof(tl_plan, tiles_m));
   plan->l2_prefetch = pf;
   plan->producers = prod;
   plan->stream_k = sk;
   plan->swap_ab = swap;
+  plan->ksplit = ks;
   return complete_plan(M, N, K, trans_a, trans_b, num_sms, plan, elem_bytes(dtype));
 }
 
