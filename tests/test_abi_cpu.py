@@ -150,16 +150,18 @@ def test_one_wave_of_narrow_tiles():
 
 
 def test_skinny_products_swap_operands():
-    # M <= 32 against long N and K: the kernel runs on C^T with M as the MMA's N,
-    # the 64 tiles of 128 rows of C^T split by k-block over all SMs
-    for M, bn, stages in ((1, 16, 6), (16, 16, 6), (17, 32, 5), (32, 32, 5)):
+    # M <= 64 against long N and K: the kernel runs on C^T with M as the MMA's N, the 64
+    # tiles of 128 rows of C^T each shared by the two CTAs of a cluster (cluster split-K)
+    for M, bn, stages in ((1, 16, 6), (16, 16, 6), (17, 32, 5), (32, 32, 5), (33, 64, 3),
+                          (64, 64, 3)):
         p = tl.tl_gemm_plan(M, 8192, 8192, dtype=tl.TL_BF16, trans_b=1, num_sms=152)
         assert p.swap_ab == 1 and (p.bm, p.bn, p.bk, p.stages) == (128, bn, 128, stages)
         assert (p.tiles_m, p.tiles_n, p.k_blocks) == (64, 1, 64)
-        assert p.dp_tiles == 0 and p.sk_iters == 64 * 64 and p.grid == 152
-        assert p.tma_store == 0 and p.tx_bytes == (128 + bn) * 128 * 2
+        assert p.ksplit == 2 and p.grid == 128 and p.dp_tiles == 64 and p.sk_iters == 0
+        assert p.tma_store == 0 and p.tx_bytes == (128 + bn) * 128 * 2   # C^T: plain stores
+        assert p.smem_bytes <= 232448
     # wider M, an M-major A, short N or K: the direct form
-    assert tl.tl_gemm_plan(64, 8192, 8192, trans_b=1).swap_ab == 0
+    assert tl.tl_gemm_plan(128, 8192, 8192, trans_b=1).swap_ab == 0
     assert tl.tl_gemm_plan(16, 8192, 8192, trans_a=1).swap_ab == 0
     assert tl.tl_gemm_plan(16, 1024, 8192).swap_ab == 0
     assert tl.tl_gemm_plan(16, 8192, 512).swap_ab == 0
@@ -362,17 +364,18 @@ def test_cluster_split_k_plans():
     # the quickstart tiling (64 tiles of 128 x 128, 16 k-blocks): two CTAs per tile
     p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152)
     assert p.ksplit == 2 and p.grid == 128 and p.sk_iters == 0
-    # its receive buffer (128 x 128 fp32) is part of each CTA's shared memory
+    # its receive buffer (the peer's partial sums of 64 rows x 128 fp32) is part of each
+    # CTA's shared memory
     off = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, ksplit=1)
     assert off.ksplit == 1 and off.grid == 64
-    assert p.smem_bytes == off.smem_bytes + 128 * 128 * 4
+    assert p.smem_bytes == off.smem_bytes + 64 * 128 * 4
     # more tiles than half the SMs, or a short k-loop: no split
     assert tl.tl_plan_complete(2048, 2048, 1024, 128, 128, 64, 3, num_sms=152).ksplit == 1
     assert tl.tl_plan_complete(1024, 1024, 192, 128, 128, 64, 3, num_sms=152).ksplit == 1
     # pairs never split; a forced split that cannot apply is an error
     assert tl.tl_plan_complete(1024, 1024, 1024, 256, 256, 128, 3, num_sms=152).ksplit == 1
     for kw in ({"bm": 256, "bn": 256, "bk": 128, "stages": 3},
-               {"bm": 128, "bn": 256, "bk": 64, "stages": 4}):        # buffer does not fit
+               {"bm": 128, "bn": 256, "bk": 64, "stages": 4}):        # smem does not fit
         with pytest.raises(tl.TLError):
             tl.tl_plan_complete(1024, 1024, 1024, num_sms=152, ksplit=2, **kw)
     with pytest.raises(tl.TLError):                                     # one k-block

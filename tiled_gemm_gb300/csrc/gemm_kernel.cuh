@@ -111,8 +111,9 @@ struct GemmParams {
   int32_t dp_tiles;
   int64_t sk_iters;
   // Cluster split-K (one-CTA tiles only): 1, or 2 CTAs of a cluster on each tile, CTA r
-  // taking k-blocks [r kb / 2, (r + 1) kb / 2).  CTA 1 sends its fp32 accumulator into
-  // CTA 0's shared memory (distributed shared memory); CTA 0 adds it and writes C.
+  // taking k-blocks [r kb / 2, (r + 1) kb / 2).  CTA r finishes rows [64 r, 64 r + 64) of
+  // the tile: each CTA sends the fp32 partial sums of the other 64 rows into its peer's
+  // shared memory (distributed shared memory), adds the peer's for its own and writes C.
   int32_t ksplit;
   float* sk_partials;                 // [unit][cta][4 warps][BN/4 col groups][32 lanes][4]
   unsigned long long* sk_flags;       // [unit][cta][4 warps]
@@ -146,11 +147,12 @@ __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
   return static_cast<uint32_t>(8 * (2 * stages + 5 + 8) + 8 + 32);
 }
 
-// Cluster split-K receive buffer: one 128 x BN fp32 accumulator, per epilogue warp BN
-// columns x 32 lanes, four columns per 16-byte entry, lane-major.
+// Cluster split-K receive buffer: the peer's partial sums of the 64 rows this CTA
+// finishes, per finishing epilogue warp BN columns x 32 lanes, four columns per 16-byte
+// entry, lane-major.
 template <int BN>
 __host__ __device__ constexpr uint32_t red_bytes(int ksplit) {
-  return ksplit > 1 ? static_cast<uint32_t>(128 * BN * 4) : 0u;
+  return ksplit > 1 ? static_cast<uint32_t>(64 * BN * 4) : 0u;
 }
 
 template <int BN, int CG, int BK, int EB = 2>
@@ -674,11 +676,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
         break;
       }
-      // Cluster split-K: CTA 1 writes its accumulator into CTA 0's receive buffer once
-      // CTA 0 has read the previous tile's; CTA 0 waits for it to arrive.  Every lane
-      // waits (and later arrives) itself, so each one orders its own accesses.
-      const bool red_send = ksplit && krank == 1;
-      const bool red_recv = ksplit && krank == 0;
+      // Cluster split-K: the warp of lane quadrant q finishes its 32 rows in CTA q / 2.
+      // There it waits for the peer's partial sums of those rows; in the other CTA it
+      // writes them into the peer's receive buffer once the peer has read the previous
+      // tile's.  Every lane waits (and later arrives) itself, so each one orders its own
+      // accesses.
+      const bool red_send = ksplit && (q >> 1) != krank;
+      const bool red_recv = ksplit && (q >> 1) == krank;
       if (red_send || red_recv) {
         const bool got = wait_bounded<true>(red_send ? red_empty_bar(q) : red_full_bar(q),
                                             red_send ? (red_phase ^ 1u) : red_phase,
@@ -688,8 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      const uint32_t red_entry = sRed + static_cast<uint32_t>(q * (BN / 4) * 32 + lane) * 16u;
-      const uint32_t red_remote = red_send ? mapa_shared(red_entry, 0) : 0u;
+      const uint32_t red_entry =
+          sRed + static_cast<uint32_t>((q & 1) * (BN / 4) * 32 + lane) * 16u;
+      const uint32_t red_remote = red_send ? mapa_shared(red_entry, krank ^ 1) : 0u;
       tc_fence_after_sync();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
@@ -706,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto finish_chunk = [&](auto width, uint32_t* v, int c_col) {
         constexpr int W = decltype(width)::value;
         if (red_send) {
-          // entry (column group, lane) of this warp's part of CTA 0's receive buffer
+          // entry (column group, lane) of this warp's part of the peer's receive buffer
 #pragma unroll
           for (int j = 0; j < W / 4; ++j)
             st_cluster_v4(red_remote + static_cast<uint32_t>(c_col / 4 + j) * 512u, v[4 * j],
@@ -714,7 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           return;
         }
         if (red_recv) {
-          // own k-blocks first, then CTA 1's: a fixed order
+          // own partial + the peer's: one addition per element, the same in either CTA
+          // (IEEE addition is commutative), so the result does not depend on the rows
 #pragma unroll
           for (int j = 0; j < W / 4; ++j) {
             const float4 t = ld_shared_f4(red_entry + static_cast<uint32_t>(c_col / 4 + j) * 512u);
@@ -836,12 +842,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         finish_chunk(IntConst<32>{}, v, kFull * kEC);
       }
       if (red_send) {
-        // the partial is in CTA 0's buffer (release: the stores come first)
-        mbar_arrive_cluster(mapa_shared(red_full_bar(q), 0));
+        // the partial is in the peer's buffer (release: the stores come first)
+        mbar_arrive_cluster(mapa_shared(red_full_bar(q), krank ^ 1));
         red_phase ^= 1u;
       } else if (red_recv) {
-        // the buffer is read: CTA 1 may write the next tile's partial
-        mbar_arrive_cluster(mapa_shared(red_empty_bar(q), 1));
+        // the buffer is read: the peer may write the next tile's partial
+        mbar_arrive_cluster(mapa_shared(red_empty_bar(q), krank ^ 1));
         red_phase ^= 1u;
       }
       if (store_partial) {

@@ -273,9 +273,9 @@ void schedule(tl_plan* pl, int64_t units_avail, bool allow_split, int eb = 2) {
 // Cluster split-K for one-CTA tiles: when at most half the SMs would hold a tile and the
 // k-loop is long enough to halve, two CTAs of a cluster share each tile's k-blocks.  The
 // quickstart 1024^3 tiling (64 tiles of 128 x 128, 16 k-blocks of 64) is bound by the
-// latency of its 3-stage ring refills from DRAM: split, each tile has two rings' loads
-// in flight, and the partial-sum hand-over costs one Tensor Memory read and a 64 KB
-// write into the peer's shared memory.
+// latency of its 3-stage ring refills: split, each tile has two rings' loads in flight,
+// and each CTA finishes half the tile's rows after a 32 KB exchange of partial sums
+// with its peer through distributed shared memory.
 int auto_ksplit(const tl_plan& pl, int sms, int eb) {
   if (pl.bm != 128 || pl.stream_k == 1 || 2 * pl.tiles > sms || pl.k_blocks < 4) return 1;
   // the receive buffer (128 x bn fp32) must fit beside the ring
@@ -341,22 +341,22 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, in
   pl->grid = 0;
   pl->l2_prefetch = -1;
   pl->swap_ab = 0;
-  // Very skinny products (M <= 32 rows against a long N and K) stream B from memory
-  // once and are bound by that stream.  Computing C^T = op(B)^T op(A)^T puts N on
-  // the MMA's 128 rows and M on its narrow N side, so each stage carries 32 KB of B
-  // instead of 16 KB beside a mostly empty 128-row tile of A; the 128-row tiles of
-  // C^T are then split by k-block over all SMs (stream-K), with small fp32 partials.
-  // Measured on GB300 at N = K = 8192 this gains ~7 % at M = 16, while at M = 64 and
-  // 128 the split's fix-up costs more than it saves (128 x 64 tiles stay faster).
-  // An M-major A (trans_a) cannot feed boxes narrower than 64, so it keeps the
-  // direct form.
-  if (eb == 2 && M <= 32 && !trans_a && N >= 2048 && K >= 1024) {
+  // Skinny products (M <= 64 rows against a long N and K) stream B from memory once and
+  // are bound by that stream.  Computing C^T = op(B)^T op(A)^T puts N on the MMA's 128
+  // rows and M on its narrow N side (16-, 32- or 64-column tiles), so each stage carries
+  // 32 KB of B beside a small tile of A, instead of a mostly empty 128-row tile of A.
+  // The 128-row tiles of C^T (64 at N = 8192) then share each tile's k-blocks between
+  // the two CTAs of a cluster (cluster split-K), so that 128 SMs stream B.  Measured on
+  // GB300 at N = K = 8192 (us per call): M = 16: 33.8 with a stream-K split over all SMs,
+  // 27.1 with the cluster split; M = 64: 34.2 with direct 128 x 64 tiles, 30.4 with the
+  // cluster split.  M = 128 keeps the direct tiles (34.7, against 38.2 split).  An
+  // M-major A (trans_a) cannot feed these boxes, so it keeps the direct form.
+  if (eb == 2 && M <= 64 && !trans_a && N >= 2048 && K >= 1024) {
     pl->bm = 128;
-    pl->bn = M <= 16 ? 16 : 32;
+    pl->bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     pl->bk = 128;
-    pl->stages = pl->bn == 16 ? 6 : 5;
+    pl->stages = pl->bn == 16 ? 6 : (pl->bn == 32 ? 5 : 3);
     pl->swap_ab = 1;
-    pl->ksplit = 1;                // the stream-K split below, over all SMs
     return;
   }
   // One wave of narrow tiles.  When every 128 x 64 tile of C gets an SM of its own, the
