@@ -498,6 +498,8 @@ def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl, preheat_s: fl
     torch.cuda.synchronize()
     # pre-heat: untimed replays, back to back with the timed ones
     reps = int(min(100000, max(1, math.ceil(preheat_s * 1e3 / (step_ms * G)))))
+    if preheat_s <= 0:
+        reps = 1
 
     clocks = clock_sampler(torch.cuda.current_device())
     clocks.start()
@@ -699,7 +701,8 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
         a, b, c = sets[i % rot]
         gemm_call(a, b, c)
 
-    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl,
+                                            preheat_s=args.preheat_s)
     e2e = None
     if not args.no_e2e:
         e2e = e2e_pipeline(args, [a_cpu, b_cpu], (w.M, w.N), w.torch_dtype,
@@ -742,7 +745,8 @@ def run_mx(args, w: workloads.MxWorkload, rank: int, world: int, dist) -> dict:
         st = sets[i % rot]
         call(st[:4], st[4])
 
-    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl,
+                                            preheat_s=args.preheat_s)
     e2e = None
     if not args.no_e2e:
         e2e = e2e_pipeline(args, list(ins_cpu), (w.M, w.N), w.c_torch_dtype, call, w.flops,
@@ -770,7 +774,8 @@ def run_attn(args, w: workloads.AttnWorkload, rank: int, world: int, dist) -> di
         q, k, v, o = sets[i % rot]
         tl.attention(q, k, v, causal=w.causal, out=o, stream=stream)
 
-    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl)
+    max_ms, clk, spread = timed_graph_steps(args, step, rot, stream, dist, dev, tl,
+                                            preheat_s=args.preheat_s)
 
     def lib_step(i):
         q, k, v, _ = sets[i % rot]
@@ -829,6 +834,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--preheat-s", type=float, default=2.0,
+                    help="untimed replays before the timed region, in seconds (0: one round)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -152,16 +152,19 @@ def test_one_wave_of_narrow_tiles():
 def test_skinny_products_swap_operands():
     # M <= 64 against long N and K: the kernel runs on C^T with M as the MMA's N, the 64
     # tiles of 128 rows of C^T each shared by the two CTAs of a cluster (cluster split-K)
-    for M, bn, stages in ((1, 16, 6), (16, 16, 6), (17, 32, 5), (32, 32, 5), (33, 64, 3),
-                          (64, 64, 3)):
+    for M, bn, stages in ((1, 16, 6), (16, 16, 6), (17, 32, 5), (32, 32, 5), (33, 64, 4),
+                          (64, 64, 4), (65, 128, 3), (128, 128, 3)):
         p = tl.tl_gemm_plan(M, 8192, 8192, dtype=tl.TL_BF16, trans_b=1, num_sms=152)
         assert p.swap_ab == 1 and (p.bm, p.bn, p.bk, p.stages) == (128, bn, 128, stages)
         assert (p.tiles_m, p.tiles_n, p.k_blocks) == (64, 1, 64)
         assert p.ksplit == 2 and p.grid == 128 and p.dp_tiles == 64 and p.sk_iters == 0
         assert p.tma_store == 0 and p.tx_bytes == (128 + bn) * 128 * 2   # C^T: plain stores
         assert p.smem_bytes <= 232448
-    # wider M, an M-major A, short N or K: the direct form
-    assert tl.tl_gemm_plan(128, 8192, 8192, trans_b=1).swap_ab == 0
+    # wider M, an M-major A, short N or K, or an N too long for the split at M > 64: the
+    # direct form
+    assert tl.tl_gemm_plan(129, 8192, 8192, trans_b=1, num_sms=152).swap_ab == 0
+    assert tl.tl_gemm_plan(128, 16384, 8192, trans_b=1, num_sms=152).swap_ab == 0
+    assert tl.tl_gemm_plan(64, 16384, 8192, trans_b=1, num_sms=152).swap_ab == 1
     assert tl.tl_gemm_plan(16, 8192, 8192, trans_a=1).swap_ab == 0
     assert tl.tl_gemm_plan(16, 1024, 8192).swap_ab == 0
     assert tl.tl_gemm_plan(16, 8192, 512).swap_ab == 0

@@ -155,11 +155,13 @@ __host__ __device__ constexpr uint32_t red_bytes(int ksplit) {
   return ksplit > 1 ? static_cast<uint32_t>(64 * BN * 4) : 0u;
 }
 
+// `staging`: the TMA-store staging of C; a kernel that computes C^T (plain stores) has none.
 template <int BN, int CG, int BK, int EB = 2>
-__host__ __device__ constexpr uint32_t smem_bytes_for(int stages, int ksplit = 1) {
+__host__ __device__ constexpr uint32_t smem_bytes_for(int stages, int ksplit = 1,
+                                                      bool staging = true) {
   // +1024: the dynamic shared memory base is rounded up to 1024 B in the kernel
   return 1024u + stages * (a_stage_bytes<BK, EB>() + b_stage_bytes<BN, CG, BK, EB>()) +
-         staging_bytes<BN>() + red_bytes<BN>(ksplit) + barrier_bytes(stages);
+         (staging ? staging_bytes<BN>() : 0u) + red_bytes<BN>(ksplit) + barrier_bytes(stages);
 }
 
 // Grouped raster order: walk `group` tile-rows top to bottom, then the next column.
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sA = base;
   const uint32_t sB = sA + S * kAStageBytes;
   const uint32_t sC = sB + S * kBStage;
-  const uint32_t sRed = sC + staging_bytes<BN>();
+  const uint32_t sRed = sC + (p.c_trans ? 0u : staging_bytes<BN>());   // C^T: no staging
   const uint32_t sBar = sRed + red_bytes<BN>(ksplit ? 2 : 1);
   auto full_bar = [&](int s) { return sBar + 8u * s; };
   auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
@@ -407,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(done_bar, 1);
     for (int q = 0; q < 4; ++q) {
-      mbar_init(red_full_bar(q), 32);    // the 32 lanes of the contributor's warp q
-      mbar_init(red_empty_bar(q), 32);   // the 32 lanes of the finisher's warp q
+      mbar_init(red_full_bar(q), 32);    // the 32 lanes of the sending warp q
+      mbar_init(red_empty_bar(q), 1);    // one lane of the finishing warp q
     }
     *abort_flag = 0u;
     for (int s = 0; s < 8; ++s) lap_armed[s] = -1;
@@ -698,11 +700,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
-      // the whole accumulator is in registers: hand the buffer back to the MMA
+      // The whole accumulator is in registers: hand the buffer back to the MMA.  Lane 31
+      // arrives: lane 0 issues the warp's bulk stores, and an arrive with release
+      // semantics from it was measured to wait ~2,400 cycles behind them (CTA pairs).
       auto release_acc = [&]() {
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 31) {
           if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
           else mbar_arrive(tempty_bar(acc));
         }
@@ -846,8 +850,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_cluster(mapa_shared(red_full_bar(q), krank ^ 1));
         red_phase ^= 1u;
       } else if (red_recv) {
-        // the buffer is read: the peer may write the next tile's partial
-        mbar_arrive_cluster(mapa_shared(red_empty_bar(q), krank ^ 1));
+        // the buffer is read (every lane has added its entries, then the warp barrier):
+        // the peer may write the next tile's partial.  Lane 31 arrives, as above.
+        __syncwarp();
+        if (lane == 31) mbar_arrive_cluster(mapa_shared(red_empty_bar(q), krank ^ 1));
         red_phase ^= 1u;
       }
       if (store_partial) {

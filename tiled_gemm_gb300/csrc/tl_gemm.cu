@@ -177,36 +177,37 @@ bool narrow_ok(const tl_plan& pl, int trans_a, int trans_b, int eb = 2) {
 }
 
 template <int BK, int EB>
-uint32_t smem_for_bk(int bm, int bn, int stages, int ks) {
+uint32_t smem_for_bk(int bm, int bn, int stages, int ks, bool stg) {
   if constexpr (BK == 128 && EB == 2) {
-    if (bn == 192) return bm == 256 ? tl::smem_bytes_for<192, 2, BK>(stages)
-                                    : tl::smem_bytes_for<192, 1, BK>(stages, ks);
-    if (bn == 224) return bm == 256 ? tl::smem_bytes_for<224, 2, BK>(stages)
-                                    : tl::smem_bytes_for<224, 1, BK>(stages, ks);
+    if (bn == 192) return bm == 256 ? tl::smem_bytes_for<192, 2, BK>(stages, 1, stg)
+                                    : tl::smem_bytes_for<192, 1, BK>(stages, ks, stg);
+    if (bn == 224) return bm == 256 ? tl::smem_bytes_for<224, 2, BK>(stages, 1, stg)
+                                    : tl::smem_bytes_for<224, 1, BK>(stages, ks, stg);
   }
   if (bm == 256) {
-    return bn == 128 ? tl::smem_bytes_for<128, 2, BK, EB>(stages)
-                     : tl::smem_bytes_for<256, 2, BK, EB>(stages);
+    return bn == 128 ? tl::smem_bytes_for<128, 2, BK, EB>(stages, 1, stg)
+                     : tl::smem_bytes_for<256, 2, BK, EB>(stages, 1, stg);
   }
   if constexpr (BK == 128 && EB == 2) {
-    if (bn == 16) return tl::smem_bytes_for<16, 1, BK>(stages, ks);
-    if (bn == 32) return tl::smem_bytes_for<32, 1, BK>(stages, ks);
+    if (bn == 16) return tl::smem_bytes_for<16, 1, BK>(stages, ks, stg);
+    if (bn == 32) return tl::smem_bytes_for<32, 1, BK>(stages, ks, stg);
   }
   switch (bn) {
-    case 64: return tl::smem_bytes_for<64, 1, BK, EB>(stages, ks);
-    case 128: return tl::smem_bytes_for<128, 1, BK, EB>(stages, ks);
-    default: return tl::smem_bytes_for<256, 1, BK, EB>(stages, ks);
+    case 64: return tl::smem_bytes_for<64, 1, BK, EB>(stages, ks, stg);
+    case 128: return tl::smem_bytes_for<128, 1, BK, EB>(stages, ks, stg);
+    default: return tl::smem_bytes_for<256, 1, BK, EB>(stages, ks, stg);
   }
 }
 
-// Dynamic shared memory of one CTA; ks = 2 adds cluster split-K's receive buffer.
-uint32_t smem_for(int bm, int bn, int bk, int stages, int eb = 2, int ks = 1) {
+// Dynamic shared memory of one CTA; ks = 2 adds cluster split-K's receive buffer, and a
+// plan that computes C^T (swap_ab, plain stores of C) has no TMA-store staging.
+uint32_t smem_for(int bm, int bn, int bk, int stages, int eb = 2, int ks = 1, bool stg = true) {
   if (eb == 1) {
-    return bk == 256 ? smem_for_bk<256, 1>(bm, bn, stages, ks)
-                     : smem_for_bk<128, 1>(bm, bn, stages, ks);
+    return bk == 256 ? smem_for_bk<256, 1>(bm, bn, stages, ks, stg)
+                     : smem_for_bk<128, 1>(bm, bn, stages, ks, stg);
   }
-  return bk == 128 ? smem_for_bk<128, 2>(bm, bn, stages, ks)
-                   : smem_for_bk<64, 2>(bm, bn, stages, ks);
+  return bk == 128 ? smem_for_bk<128, 2>(bm, bn, stages, ks, stg)
+                   : smem_for_bk<64, 2>(bm, bn, stages, ks, stg);
 }
 
 tl_status validate_common(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
@@ -279,7 +280,7 @@ void schedule(tl_plan* pl, int64_t units_avail, bool allow_split, int eb = 2) {
 int auto_ksplit(const tl_plan& pl, int sms, int eb) {
   if (pl.bm != 128 || pl.stream_k == 1 || 2 * pl.tiles > sms || pl.k_blocks < 4) return 1;
   // the receive buffer (128 x bn fp32) must fit beside the ring
-  return smem_for(pl.bm, pl.bn, pl.bk, pl.stages, eb, 2) <= kMaxSmemPerCta ? 2 : 1;
+  return smem_for(pl.bm, pl.bn, pl.bk, pl.stages, eb, 2, !pl.swap_ab) <= kMaxSmemPerCta ? 2 : 1;
 }
 
 // fp32 partial-sum slots (one 128 x bn tile per CTA) and ready flags (one per epilogue
@@ -308,7 +309,7 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_
   if (pl->ksplit == 0) pl->ksplit = auto_ksplit(*pl, sms, eb);
   if (pl->ksplit == 2 && (pl->bm != 128 || pl->k_blocks < 2 || pl->stream_k == 1))
     return TL_ERR_INVALID_ARG;
-  pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages, eb, pl->ksplit);
+  pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages, eb, pl->ksplit, !pl->swap_ab);
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
   // two accumulators; 192- and 224-column tiles keep the second at column 256
   pl->tmem_cols = (pl->bn == 192 || pl->bn == 224) ? 512 : std::max(32, 2 * pl->bn);
@@ -341,21 +342,25 @@ void choose_tiling(int64_t M, int64_t N, int64_t K, int trans_a, int trans_b, in
   pl->grid = 0;
   pl->l2_prefetch = -1;
   pl->swap_ab = 0;
-  // Skinny products (M <= 64 rows against a long N and K) stream B from memory once and
+  // Skinny products (M <= 128 rows against a long N and K) stream B from memory once and
   // are bound by that stream.  Computing C^T = op(B)^T op(A)^T puts N on the MMA's 128
-  // rows and M on its narrow N side (16-, 32- or 64-column tiles), so each stage carries
-  // 32 KB of B beside a small tile of A, instead of a mostly empty 128-row tile of A.
-  // The 128-row tiles of C^T (64 at N = 8192) then share each tile's k-blocks between
-  // the two CTAs of a cluster (cluster split-K), so that 128 SMs stream B.  Measured on
-  // GB300 at N = K = 8192 (us per call): M = 16: 33.8 with a stream-K split over all SMs,
-  // 27.1 with the cluster split; M = 64: 34.2 with direct 128 x 64 tiles, 30.4 with the
-  // cluster split.  M = 128 keeps the direct tiles (34.7, against 38.2 split).  An
-  // M-major A (trans_a) cannot feed these boxes, so it keeps the direct form.
-  if (eb == 2 && M <= 64 && !trans_a && N >= 2048 && K >= 1024) {
+  // rows and M on its narrow N side (16-, 32-, 64- or 128-column tiles), so each stage
+  // carries 32 KB of B beside a small tile of A, instead of a mostly empty 128-row tile of
+  // A (and A is read from L2 once per 128 rows of N, not once per 64 columns of C).  The
+  // 128-row tiles of C^T (64 at N = 8192) then share each tile's k-blocks between the two
+  // CTAs of a cluster (cluster split-K), so that 128 SMs stream B; C^T is written by plain
+  // stores, so these plans carry no store staging and fit deeper rings.  Measured on GB300
+  // at N = K = 8192 (us per call): M = 16: 33.8 with a stream-K split over all SMs, 27.1
+  // with the cluster split; M = 64: 34.2 with direct 128 x 64 tiles, 29.3 swapped and split
+  // with 4 stages; M = 128: 34.5 direct, 33.3 swapped and split with 3 stages.  Wider M,
+  // or an N too long for the split at M > 64, keeps the direct form, and so does an
+  // M-major A (trans_a), which cannot feed these boxes.
+  const bool split_fits = 2 * ceil_div(N, 128) <= sms;
+  if (eb == 2 && !trans_a && N >= 2048 && K >= 1024 && (M <= 64 || (M <= 128 && split_fits))) {
     pl->bm = 128;
-    pl->bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    pl->bn = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
     pl->bk = 128;
-    pl->stages = pl->bn == 16 ? 6 : (pl->bn == 32 ? 5 : 3);
+    pl->stages = pl->bn == 16 ? 6 : (pl->bn == 32 ? 5 : (pl->bn == 64 ? 4 : 3));
     pl->swap_ab = 1;
     return;
   }
