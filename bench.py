@@ -389,27 +389,24 @@ def oracle_rate_mx(w: workloads.MxWorkload, a_cpu, b_cpu, sa_cpu, budget_s: floa
 
 # ------------------------------------------------------------------ GPU arm ----
 
-def graph_chunks(steps: int, rot: int, max_calls: int = 64, min_chunks: int = 5):
+def graph_chunks(steps: int, rot: int, max_calls: int = 64, one_graph_max: int = 4096):
     """Split `steps` consecutive calls into the CUDA graphs of the timed region.
 
-    Returns [(first step, calls, reuse)]: chunks of calls replayed back to back, at
-    least `min_chunks` of them when steps allow, so that the per-chunk times give a
-    spread.  Many steps: one graph of G calls (G a multiple of the rotation, so every
-    replay walks the same input sets in order) replayed steps // G times, then the
-    remainder (reuse = True marks replays of that first graph).  Few steps: near-equal
-    consecutive chunks, each captured with its own step indices."""
+    Returns [(first step, calls, reuse)].  Up to one_graph_max steps: one graph of all of
+    them (no graph boundary between calls).  More steps: one graph of G calls (G a
+    multiple of the rotation, so every replay walks the same input sets in order)
+    replayed steps // G times (reuse = True marks replays of that first graph), then the
+    remainder."""
     if steps <= 0:
         return []
+    if steps <= one_graph_max:
+        return [(0, steps, False)]
     G = rot * max(1, math.ceil(max_calls / rot))
-    if steps >= min_chunks * G:
-        n_full, rem = divmod(steps, G)
-        chunks = [(i * G, G, i > 0) for i in range(n_full)]
-        if rem:
-            chunks.append((n_full * G, rem, False))
-        return chunks
-    n = min(steps, min_chunks)
-    bounds = [steps * j // n for j in range(n + 1)]
-    return [(bounds[j], bounds[j + 1] - bounds[j], False) for j in range(n)]
+    n_full, rem = divmod(steps, G)
+    chunks = [(i * G, G, i > 0) for i in range(n_full)]
+    if rem:
+        chunks.append((n_full * G, rem, False))
+    return chunks
 
 
 def percentile(xs, q: float) -> float:
@@ -422,9 +419,9 @@ def percentile(xs, q: float) -> float:
 
 
 def spread_of(chunk_ms, chunks) -> dict:
-    """Per-call time of each chunk (its events' interval over its calls): min, p10, p50,
-    p90 and max over the chunks of the largest size (a shorter remainder chunk is left
-    out, so that every figure averages the same number of calls)."""
+    """Per-call time of each timed sequence (its events' interval over its calls): min,
+    p10, p50, p90 and max over the sequences of the largest size (a shorter remainder is
+    left out, so that every figure averages the same number of calls)."""
     size = max(c[1] for c in chunks)
     per_call = [ms / c[1] for ms, c in zip(chunk_ms, chunks) if c[1] == size]
     return {"chunks": len(per_call), "calls_per_chunk": size,
@@ -529,12 +526,25 @@ def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl, preheat_s: fl
     status, word = tl.tl_device_status(reset=True)
     if status != tl.TL_OK:
         raise RuntimeError(f"device-side wait gave up in the timed region: {word:#x}")
+    if len(chunks) == 1:
+        # one graph: the spread comes from five more replays of the timed sequence, each
+        # between its own events, after the timed region (nothing is added inside it)
+        rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        with torch.cuda.stream(stream):
+            rep_ev[0].record(stream)
+            for j in range(5):
+                graphs[0].replay()
+                rep_ev[j + 1].record(stream)
+        torch.cuda.synchronize()
+        chunk_ms = [rep_ev[j].elapsed_time(rep_ev[j + 1]) for j in range(5)]
+        chunks = chunks * 5
     spread = spread_of(chunk_ms, chunks)
     spread["preheat_ms"] = round(reps * step_ms * G, 1)
     return max_over_ranks(total_ms, dist, dev), clk, spread
 
 
-def library_context(name: str, step, rot: int, stream, steps: int, flops: int) -> dict:
+def library_context(name: str, step, rot: int, stream, steps: int, flops: int,
+                    preheat_s: float = 2.0) -> dict:
     """The same workload through a vendor library (a library run, never inspected), timed
     as the kernel is: CUDA-graph replays of consecutive calls on the rotating inputs.
     Context for the reader only; any failure is reported, never raised."""
@@ -552,6 +562,13 @@ def library_context(name: str, step, rot: int, stream, steps: int, flops: int) -
         with torch.cuda.stream(stream):
             g.replay()
         torch.cuda.synchronize()
+        # the same pre-heat as the library's own timed steps, so both run at the clock
+        # the load sustains
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < preheat_s:
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize()
         reps = max(2, steps // (4 * G))
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -716,7 +733,7 @@ def run_tl(args, w: workloads.Workload, rank: int, world: int, dist) -> dict:
             if w.relu:
                 c.relu_()
         context = library_context("torch.matmul (cuBLAS)" + (" + relu_" if w.relu else ""),
-                                  lib_step, rot, stream, args.steps, w.flops)
+                                  lib_step, rot, stream, args.steps, w.flops, args.preheat_s)
     return {"total_ms": max_ms, "clocks": clk, "spread": spread, "e2e": e2e, "context": context,
             "rotation_sets": rot, "launches_per_step": launches_per_step,
             "plan": tl.tl_gemm_plan(w.M, w.N, w.K, w.dtype, int(w.trans_a), int(w.trans_b),
@@ -783,7 +800,7 @@ def run_attn(args, w: workloads.AttnWorkload, rank: int, world: int, dist) -> di
             q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2), is_causal=w.causal)
 
     context = library_context("torch scaled_dot_product_attention", lib_step, rot, stream,
-                              args.steps, w.flops)
+                              args.steps, w.flops, args.preheat_s)
     e2e = None
     if not args.no_e2e:
         e2e = e2e_pipeline(args, [q_cpu, k_cpu, v_cpu], tuple(q_cpu.shape), w.torch_dtype,

@@ -115,6 +115,7 @@ struct GemmParams {
   // the tile: each CTA sends the fp32 partial sums of the other 64 rows into its peer's
   // shared memory (distributed shared memory), adds the peer's for its own and writes C.
   int32_t ksplit;
+  int32_t serpentine;       // 1: odd-numbered whole tiles of each unit walk K backwards
   float* sk_partials;                 // [unit][cta][4 warps][BN/4 col groups][32 lanes][4]
   unsigned long long* sk_flags;       // [unit][cta][4 warps]
   unsigned long long sk_token;        // unique to this launch, never 0
@@ -141,10 +142,11 @@ __host__ __device__ constexpr uint32_t b_stage_bytes() {
 
 // Barrier block: full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done,
 // red_full[4], red_empty[4] (cluster split-K, one per epilogue warp), then the 4-byte
-// Tensor Memory base slot, the 4-byte abort flag and, per stage, the last lap at which a
-// producer armed that stage (int32 x 8, -1 = never).
+// Tensor Memory base slot, the 4-byte abort flag, per stage the last lap at which a
+// producer armed that stage (int32 x 8, -1 = never), and the peer CTA's abort flag as the
+// peer wrote it at teardown (4 bytes, 8 reserved).
 __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
-  return static_cast<uint32_t>(8 * (2 * stages + 5 + 8) + 8 + 32);
+  return static_cast<uint32_t>(8 * (2 * stages + 5 + 8) + 8 + 32 + 8);
 }
 
 // Cluster split-K receive buffer: the peer's partial sums of the 64 rows this CTA
@@ -220,6 +222,8 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 // role of the unit walks the same sequence.
 struct WorkItem {
   int tile, k0, k1;   // k-blocks [k0, k1) of tile `tile`
+  bool rev;           // walk them from k1 - 1 down to k0
+  __device__ __forceinline__ int kb_at(int i) const { return rev ? k1 - 1 - i : k0 + i; }
 };
 
 __device__ __forceinline__ int64_t sk_begin(const GemmParams& p, int unit, int units) {
@@ -227,18 +231,22 @@ __device__ __forceinline__ int64_t sk_begin(const GemmParams& p, int unit, int u
 }
 
 struct WorkIter {
-  int next_dp, step, dp_end, kb, kr0, kr1;
+  int next_dp, step, dp_end, kb, kr0, kr1, n_dp, serp;
   int64_t it, it_end;
   // krank / ksplit: this CTA's part of each whole tile's k-blocks (cluster split-K)
   __device__ __forceinline__ WorkIter(const GemmParams& p, int unit, int units, int krank = 0)
       : next_dp(unit), step(units), dp_end(p.dp_tiles), kb(p.k_blocks),
         kr0(krank * p.k_blocks / max(1, p.ksplit)),
-        kr1((krank + 1) * p.k_blocks / max(1, p.ksplit)),
+        kr1((krank + 1) * p.k_blocks / max(1, p.ksplit)), n_dp(0), serp(p.serpentine),
         it(sk_begin(p, unit, units)), it_end(sk_begin(p, unit + 1, units)) {}
   __device__ __forceinline__ bool next(WorkItem& w) {
     if (next_dp < dp_end) {
-      w = {next_dp, kr0, kr1};
+      // serpentine: every other whole tile walks K backwards, so that it starts on the
+      // k-slices the previous wave of tiles (which shares its A or B panels) read last,
+      // still in L2
+      w = {next_dp, kr0, kr1, serp != 0 && (n_dp & 1) != 0};
       next_dp += step;
+      ++n_dp;
       return true;
     }
     if (it < it_end) {
@@ -246,7 +254,7 @@ struct WorkIter {
       const int k0 = static_cast<int>(it - static_cast<int64_t>(t) * kb);
       const int64_t left = it_end - it;
       const int k1 = left < static_cast<int64_t>(kb - k0) ? k0 + static_cast<int>(left) : kb;
-      w = {dp_end + t, k0, k1};
+      w = {dp_end + t, k0, k1, false};
       it += k1 - k0;
       return true;
     }
@@ -377,6 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<volatile uint32_t*>(base_ptr + (slot - base));
   volatile uint32_t* const abort_flag = tmem_slot_ptr + 1;
   volatile int32_t* const lap_armed = reinterpret_cast<volatile int32_t*>(tmem_slot_ptr + 2);
+  volatile uint32_t* const peer_abort = tmem_slot_ptr + 10;   // written by the peer CTA
+  const uint32_t peer_abort_addr = slot + 40u;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -413,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(red_empty_bar(q), 1);    // one lane of the finishing warp q
     }
     *abort_flag = 0u;
+    *peer_abort = 0u;
     for (int s = 0; s < 8; ++s) lap_armed[s] = -1;
     fence_barrier_init();
   }
@@ -501,8 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;    // this CTA's A rows
         const int nb0 = nb * BN + static_cast<int>(rank) * kBnCta;      // this CTA's B columns
         if (g == 0) grid_dependency_wait();
-        for (int kb = w.k0; kb < w.k1; ++kb, ++g) {
+        for (int i = 0; i < w.k1 - w.k0; ++i, ++g) {
           if (g % n_producers != pi) continue;
+          const int kb = w.kb_at(i);
           const int stage = g % S;
           const uint32_t phase = static_cast<uint32_t>(g / S) & 1u;
           if (!wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -518,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < n_boxes; ++j) issue_box(j, kb, m0, nb0, a_dst, b_dst, fb, false);
           if (leader) lap_armed[stage] = g / S;   // stage laps are armed in order
           // optional L2 prefetch of the k-block l2_prefetch iterations ahead (same item)
-          if (p.l2_prefetch > 0 && kb + p.l2_prefetch < w.k1) {
+          if (p.l2_prefetch > 0 && i + p.l2_prefetch < w.k1 - w.k0) {
             for (int j = 0; j < n_boxes; ++j)
-              issue_box(j, kb + p.l2_prefetch, m0, nb0, 0, 0, 0, true);
+              issue_box(j, w.kb_at(i + p.l2_prefetch), m0, nb0, 0, 0, 0, true);
           }
         }
       }
@@ -562,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccStride;
-        for (int kb = w.k0; kb < w.k1; ++kb) {
+        for (int i = 0; i < w.k1 - w.k0; ++i) {
           if (!wait_bounded<kPair>(full_bar(stage), phase, abort_flag, p.timeout_ns)) {
             record_timeout(p.status, abort_flag, kSiteMmaFull);
             ok = false;
@@ -573,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b_desc = b_desc0 + ((stage * kBStage) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / kMmaK; ++k) {
-            const uint32_t acc_in = (kb != w.k0 || k != 0) ? 1u : 0u;
+            const uint32_t acc_in = (i != 0 || k != 0) ? 1u : 0u;   // the first overwrites
             const uint64_t ad = a_desc + k_off(p.trans_a, kBM, k);
             const uint64_t bd = b_desc + k_off(!p.trans_b, kBnCta, k);
             if constexpr (EB == 1) {
@@ -880,14 +892,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------------ teardown --
   __syncwarp();
-  if constexpr (kPair) {
-    // After a timeout the odd CTA cannot observe its own loads landing (they complete
-    // on the even CTA's barriers): give any copy still in flight time to finish.
-    if (*abort_flag) {
-      const uint64_t t0 = clock_cycles();
-      while (clock_cycles() - t0 < 800000ull) __nanosleep(1000);   // >= 200 us
-    }
-  }
   tc_fence_before_sync();
   __syncthreads();
   // Every load a producer issued must have landed before the CTA may exit.  All roles
@@ -904,7 +908,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if (kPair || ksplit) cluster_sync_all();   // no CTA leaves while its peer may touch it
+  if (kPair || ksplit) {
+    // No CTA leaves while its peer may still touch it.  After a timeout in either CTA
+    // (any role, or the drain above) copies still in flight may complete on the other
+    // CTA's barriers or in its shared memory, and the odd CTA of a pair cannot see its
+    // own loads land: each CTA tells the other whether it gave up, and if either did,
+    // both wait out a grace period before they exit.  (The output is then undefined.)
+    // (Both CTAs read the same "either gave up" after the barrier, so both or neither
+    // take the pause and its second barrier.)
+    if (threadIdx.x == 0)
+      st_cluster_u32(mapa_shared(peer_abort_addr, cluster_ctarank() ^ 1u), *abort_flag);
+    cluster_sync_all();
+    if (*abort_flag != 0u || *peer_abort != 0u) {
+      if (threadIdx.x == 0) {
+        const uint64_t t0 = clock_cycles();
+        while (clock_cycles() - t0 < 800000ull) __nanosleep(1000);   // >= 200 us
+      }
+      __syncthreads();
+      cluster_sync_all();
+    }
+  }
   tc_fence_after_sync();
   if (warp == 1) {
     __syncwarp();

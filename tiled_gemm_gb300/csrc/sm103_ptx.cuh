@@ -358,6 +358,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a,
                : "memory");
 }
 
+// 4-byte store into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // 16-byte load of four floats from this CTA's shared memory.
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   float4 v;

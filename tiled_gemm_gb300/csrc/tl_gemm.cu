@@ -948,6 +948,7 @@ tl_status run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   prm.dp_tiles = pl.dp_tiles;
   prm.sk_iters = pl.sk_iters;
   prm.ksplit = pl.ksplit;
+  prm.serpentine = 1;
   prm.sk_partials = sk_partials;
   prm.sk_flags = sk_flags;
   prm.sk_token = next_split_token();
