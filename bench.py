@@ -529,8 +529,11 @@ def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl, preheat_s: fl
     if len(chunks) == 1:
         # one graph: the spread comes from five more replays of the timed sequence, each
         # between its own events, after the timed region (nothing is added inside it)
+        # (behind one untimed replay, so that the GPU is busy while the first timed
+        # replay is submitted, as in the timed region, which follows the pre-heat)
         rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         with torch.cuda.stream(stream):
+            pre.replay()
             rep_ev[0].record(stream)
             for j in range(5):
                 graphs[0].replay()
