@@ -176,7 +176,8 @@ class ClockSampler:
         time.sleep(0.3)
 
     def mark(self, which: str) -> None:
-        """Start or end of the timed region (the nvidia-smi record keeps every sample)."""
+        """Start of the pre-heat, start or end of the timed region (the nvidia-smi record
+        keeps every sample)."""
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -205,18 +206,21 @@ def nvml_reason_names(mask: int) -> set:
 class NvmlClockSampler:
     """SM clock, power and clock-event reasons read in-process through NVML every
     `period_s` (read-only queries: nothing on the GPU is changed).  Samples are kept
-    between mark("start") and mark("end"), so that even a timed region of a few
-    milliseconds has a record of its own."""
+    between mark("start") and mark("end"); a timed region too short for `min_samples`
+    samples takes, in addition, the last samples of the pre-heat replays that run back to
+    back before it (from mark("preheat") on: the same graphs, the GPU never idle)."""
 
     def __init__(self, uuid: str | None, pci_bus_id: str | None, index: int,
-                 period_s: float = 0.002):
+                 period_s: float = 0.001, min_samples: int = 5):
         import ctypes
         import threading
         self._ct = ctypes
         self._threading = threading
         self.period_s = period_s
+        self.min_samples = min_samples
         self.samples = []            # (host time, sm MHz, power W, reason mask)
         self.window = [None, None]
+        self.preheat = None
         self.lib = ctypes.CDLL("libnvidia-ml.so.1")
         if self.lib.nvmlInit_v2() != 0:
             raise OSError("nvmlInit failed")
@@ -264,20 +268,43 @@ class NvmlClockSampler:
         self._thread.start()
 
     def mark(self, which: str) -> None:
-        self.window[0 if which == "start" else 1] = time.perf_counter()
+        now = time.perf_counter()
+        if which == "preheat":
+            self.preheat = now
+        else:
+            self.window[0 if which == "start" else 1] = now
 
     def stop(self) -> dict:
         self._stop.set()
         if self._thread is not None:
             self._thread.join(timeout=5)
         self.lib.nvmlShutdown()
-        t0, t1 = self.window
-        inside = [s for s in self.samples
-                  if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
-        rec = summarise_samples([(s[1], self.max_mhz, s[2], nvml_reason_names(s[3]))
-                                 for s in inside])
+        picked, n_timed, lead_ms = clock_window([s[0] for s in self.samples], self.preheat,
+                                                self.window[0], self.window[1],
+                                                self.min_samples)
+        rec = summarise_samples([(self.samples[i][1], self.max_mhz, self.samples[i][2],
+                                  nvml_reason_names(self.samples[i][3])) for i in picked])
+        rec["timed_samples"] = n_timed
         rec["source"] = f"NVML every {self.period_s * 1e3:.0f} ms ({self.matched})"
+        if lead_ms > 0:
+            rec["source"] += (f"; timed region plus the last {lead_ms:.1f} ms of the "
+                              "pre-heat replays right before it")
         return rec
+
+
+def clock_window(times, t_pre, t0, t1, min_samples: int):
+    """Indices of the clock samples that describe the timed region [t0, t1]: the samples
+    inside it, and, if they are fewer than min_samples, as many of the latest samples
+    taken since t_pre (the start of the back-to-back pre-heat) as make up the count.
+    Returns (indices, samples inside the region, ms of pre-heat taken before t0)."""
+    inside = [i for i, t in enumerate(times)
+              if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+    lead = []
+    if len(inside) < min_samples and t0 is not None and t_pre is not None:
+        before = [i for i, t in enumerate(times) if t_pre <= t < t0]
+        lead = before[max(0, len(before) - (min_samples - len(inside))):]
+    lead_ms = (t0 - times[lead[0]]) * 1e3 if lead else 0.0
+    return lead + inside, len(inside), lead_ms
 
 
 def clock_sampler(dev_index: int):
@@ -504,7 +531,9 @@ def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl, preheat_s: fl
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    pre_ev = torch.cuda.Event()
     with torch.cuda.stream(stream):
+        pre_ev.record(stream)
         for _ in range(reps):
             pre.replay()
         events[0].record(stream)
@@ -512,7 +541,11 @@ def timed_graph_steps(args, step, rot: int, stream, dist, dev, tl, preheat_s: fl
             g.replay()
             events[j + 1].record(stream)
     # the clock record covers the device's timed region: from when the first event
-    # completes (polled) to the end of the last replay
+    # completes (polled) to the end of the last replay (and, for a short region, the end
+    # of the pre-heat that runs back to back before it)
+    while not pre_ev.query():
+        time.sleep(0.0002)
+    clocks.mark("preheat")
     while not events[0].query():
         time.sleep(0.0002)
     clocks.mark("start")

@@ -101,6 +101,22 @@ def test_nvml_samples_are_summarised_like_the_nvidia_smi_ones():
     assert bench.summarise_samples([])["reasons"] == ["no samples"]
 
 
+def test_short_timed_regions_borrow_the_last_pre_heat_samples():
+    times = [0.0, 1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0]      # seconds
+    # a long region keeps its own samples only
+    idx, n, lead = bench.clock_window(times, 0.5, 2.5, 7.5, 5)
+    assert idx == [3, 4, 5, 6, 7] and n == 5 and lead == 0.0
+    # a short one is made up to five samples from the pre-heat right before it
+    idx, n, lead = bench.clock_window(times, 0.5, 5.5, 6.5, 5)
+    assert idx == [2, 3, 4, 5, 6] and n == 1 and lead == pytest.approx(3500.0)
+    # never from before the pre-heat started
+    idx, n, lead = bench.clock_window(times, 3.5, 5.5, 6.5, 5)
+    assert idx == [4, 5, 6] and n == 1
+    # no pre-heat mark: the region alone, however short
+    idx, n, lead = bench.clock_window(times, None, 5.5, 6.5, 5)
+    assert idx == [6] and n == 1 and lead == 0.0
+
+
 def _row(sm, power, reasons=()):
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     flags = ["Active" if n in reasons else "Not Active" for n in names]
