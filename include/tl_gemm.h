@@ -117,11 +117,12 @@ typedef struct {
   int64_t sk_iters;      /* k-block iterations split evenly (0: no split)           */
   int64_t workspace_bytes; /* bytes of the stream-ordered workspace (repacked       */
                          /* operands, stream-K partial sums and flags)              */
-  int32_t ksplit;        /* cluster split-K, bm = 128 only: 2 = two CTAs of a cluster */
-                         /* share each tile's k-blocks, the second handing its fp32 */
-                         /* partial sum to the first through distributed shared     */
-                         /* memory; 1 = off; 0 (input) = automatic (when the tiles  */
-                         /* fill at most half the SMs and k_blocks >= 4)            */
+  int32_t ksplit;        /* cluster split-K, bm = 128 and bn a power of two only:   */
+                         /* 2 = two CTAs of a cluster share each tile's k-blocks,   */
+                         /* each handing the fp32 partial sums of half the tile's   */
+                         /* columns to the other through distributed shared memory; */
+                         /* 1 = off; 0 (input) = automatic (when the tiles fill at  */
+                         /* most half the SMs and k_blocks >= 4)                    */
 } tl_plan;
 
 /*

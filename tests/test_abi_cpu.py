@@ -367,8 +367,8 @@ def test_cluster_split_k_plans():
     # the quickstart tiling (64 tiles of 128 x 128, 16 k-blocks): two CTAs per tile
     p = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152)
     assert p.ksplit == 2 and p.grid == 128 and p.sk_iters == 0
-    # its receive buffer (the peer's partial sums of 64 rows x 128 fp32) is part of each
-    # CTA's shared memory
+    # its receive buffer (the peer's partial sums of 128 rows x 64 columns, fp32) is part
+    # of each CTA's shared memory
     off = tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, ksplit=1)
     assert off.ksplit == 1 and off.grid == 64
     assert p.smem_bytes == off.smem_bytes + 64 * 128 * 4
@@ -383,6 +383,12 @@ def test_cluster_split_k_plans():
             tl.tl_plan_complete(1024, 1024, 1024, num_sms=152, ksplit=2, **kw)
     with pytest.raises(tl.TLError):                                     # one k-block
         tl.tl_plan_complete(1024, 1024, 64, 128, 128, 64, 3, num_sms=152, ksplit=2)
+    # each CTA finishes half the tile's columns: power-of-two widths only
+    with pytest.raises(tl.TLError):
+        tl.tl_plan_complete(1024, 1024, 1024, 128, 224, 128, 2, trans_b=1, num_sms=152,
+                            ksplit=2)
+    assert tl.tl_plan_complete(1024, 1024, 1024, 128, 224, 128, 2, trans_b=1,
+                               num_sms=152).ksplit == 1
     with pytest.raises(tl.TLError):                                     # with stream-K
         tl.tl_plan_complete(1024, 1024, 1024, 128, 128, 64, 3, num_sms=152, ksplit=2,
                             stream_k=1)

@@ -237,6 +237,29 @@ def test_swapped_operands_for_skinny_products(bn, stages, M, N, K, ta, tb, sk):
     _check_full(_w(M, N, K, BF16, ta, tb, False, "uniform", M + N + K + 3), plan=plan)
 
 
+# C^T with C's pitch a multiple of 8 elements goes out by 16-byte stores after an 8 x 8
+# transpose across lanes: a ragged N (the kernel's rows) ends inside a vector, a ragged
+# M inside a transposed block; the guards also cover the pitch padding
+SWAP_VEC_CASES = [
+    # bn, stages, M, N, K, ldc, ksplit
+    (16, 6, 13, 1003, 900, 1008, 1),
+    (16, 6, 16, 2048, 1536, 2048, 2),
+    (32, 5, 30, 2001, 1536, 2008, 2),
+    (64, 4, 61, 517, 640, 520, 2),
+    (128, 3, 100, 333, 1000, 336, 1),
+    (128, 3, 128, 1030, 1024, 1040, 2),
+]
+
+
+@pytest.mark.parametrize("bn,stages,M,N,K,ldc,ks", SWAP_VEC_CASES)
+def test_swapped_operands_vector_stores(bn, stages, M, N, K, ldc, ks):
+    plan = tl.plan_for(0, 0, 0, 128, bn, 128, stages, raster_group=4, swap_ab=1, ksplit=ks)
+    _check_full(_w(M, N, K, F16, False, True, True, "int_small", M + N + bn), plan=plan,
+                exact=True, ldc=ldc)
+    _check_full(_w(M, N, K, BF16, False, True, False, "uniform", M + K + bn), plan=plan,
+                ldc=ldc)
+
+
 @pytest.mark.parametrize("bn,stages", [(16, 6), (32, 5)])
 def test_narrow_tiles_without_swap(bn, stages):
     # N itself narrow: bn 16/32 tiles of C with a K-major B (trans_b)

@@ -110,10 +110,11 @@ struct GemmParams {
   // holds the tile's first k-block adds the partials in order and writes C.
   int32_t dp_tiles;
   int64_t sk_iters;
-  // Cluster split-K (one-CTA tiles only): 1, or 2 CTAs of a cluster on each tile, CTA r
-  // taking k-blocks [r kb / 2, (r + 1) kb / 2).  CTA r finishes rows [64 r, 64 r + 64) of
-  // the tile: each CTA sends the fp32 partial sums of the other 64 rows into its peer's
-  // shared memory (distributed shared memory), adds the peer's for its own and writes C.
+  // Cluster split-K (one-CTA tiles of a power-of-two width only): 1, or 2 CTAs of a
+  // cluster on each tile, CTA r taking k-blocks [r kb / 2, (r + 1) kb / 2).  CTA r
+  // finishes columns [r BN / 2, (r + 1) BN / 2) of the tile: each CTA sends the fp32
+  // partial sums of the other half into its peer's shared memory (distributed shared
+  // memory), adds the peer's to its own half and writes C.
   int32_t ksplit;
   int32_t serpentine;       // 1: odd-numbered whole tiles of each unit walk K backwards
   float* sk_partials;                 // [unit][cta][4 warps][BN/4 col groups][32 lanes][4]
@@ -271,6 +272,48 @@ struct IntConst {
   static constexpr int value = V;
 };
 
+// W consecutive accumulator columns of the warp's 32 lanes into v (W = 8, 16 or a
+// multiple of 32); tmem_load_wait() before use.
+template <int W>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* v) {
+  if constexpr (W == 8) {
+    tmem_load_8cols(taddr, *reinterpret_cast<uint32_t(*)[8]>(v));
+  } else if constexpr (W == 16) {
+    tmem_load_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
+  } else {
+    static_assert(W % 32 == 0, "accumulator loads of 8, 16 or 32k columns");
+#pragma unroll
+    for (int h = 0; h < W / 32; ++h)
+      tmem_load_32cols(taddr + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * h));
+  }
+}
+
+// Transpose of an 8 x 8 matrix of 16-bit elements held by 8 consecutive lanes: lane r
+// (r = lane % 8) enters with row r as four words (word k = elements 2k, 2k + 1, the
+// lower in the low half) and leaves with column r in the same form.  Three rounds of
+// exchanges between lanes 4, 2 and 1 apart, each swapping the off-diagonal blocks of
+// the next-smaller block size (4 x 4, 2 x 2, then single elements within a word).
+// All 32 lanes of the warp take part.
+__device__ __forceinline__ void transpose8x8_u16(uint32_t& w0, uint32_t& w1, uint32_t& w2,
+                                                 uint32_t& w3, int r) {
+  constexpr uint32_t kAll = 0xFFFFFFFFu;
+  const bool h4 = (r & 4) != 0, h2 = (r & 2) != 0, h1 = (r & 1) != 0;
+  uint32_t s0 = __shfl_xor_sync(kAll, h4 ? w0 : w2, 4);
+  uint32_t s1 = __shfl_xor_sync(kAll, h4 ? w1 : w3, 4);
+  if (h4) { w0 = s0; w1 = s1; } else { w2 = s0; w3 = s1; }
+  s0 = __shfl_xor_sync(kAll, h2 ? w0 : w1, 2);
+  s1 = __shfl_xor_sync(kAll, h2 ? w2 : w3, 2);
+  if (h2) { w0 = s0; w2 = s1; } else { w1 = s0; w3 = s1; }
+  auto swap_halves = [&](uint32_t& w) {
+    const uint32_t got = __shfl_xor_sync(kAll, h1 ? (w & 0xFFFFu) : (w >> 16), 1);
+    w = h1 ? ((w & 0xFFFF0000u) | got) : ((w & 0xFFFFu) | (got << 16));
+  };
+  swap_halves(w0);
+  swap_halves(w1);
+  swap_halves(w2);
+  swap_halves(w3);
+}
+
 template <bool kBf16, bool kRelu>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (kRelu) {
@@ -353,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kEC = BN < kChunk ? BN : kChunk;
   constexpr int kFull = BN / kEC;                          // full-width epilogue steps
   constexpr int kTail = BN - kFull * kEC;                  // 0, or 32 for BN 224
+  // the cluster split-K halves the columns: power-of-two widths only
+  constexpr bool kColumnSplit = CG == 1 && (BN & (BN - 1)) == 0;
   static_assert(kTail == 0 || kTail == 32, "epilogue tail of 32 columns");
 
   // The next kernel in the stream may start its set-up now (it waits for this grid to
@@ -693,25 +738,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
         break;
       }
-      // Cluster split-K: the warp of lane quadrant q finishes its 32 rows in CTA q / 2.
-      // There it waits for the peer's partial sums of those rows; in the other CTA it
-      // writes them into the peer's receive buffer once the peer has read the previous
-      // tile's.  Every lane waits (and later arrives) itself, so each one orders its own
-      // accesses.
-      const bool red_send = ksplit && (q >> 1) != krank;
-      const bool red_recv = ksplit && (q >> 1) == krank;
-      if (red_send || red_recv) {
-        const bool got = wait_bounded<true>(red_send ? red_empty_bar(q) : red_full_bar(q),
-                                            red_send ? (red_phase ^ 1u) : red_phase,
-                                            abort_flag, p.timeout_ns);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
-          if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteClusterSplit);
-          break;
-        }
-      }
-      const uint32_t red_entry =
-          sRed + static_cast<uint32_t>((q & 1) * (BN / 4) * 32 + lane) * 16u;
-      const uint32_t red_remote = red_send ? mapa_shared(red_entry, krank ^ 1) : 0u;
       tc_fence_after_sync();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
@@ -729,26 +755,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // One epilogue step: W columns starting at column c_col of the tile, in v.
       auto finish_chunk = [&](auto width, uint32_t* v, int c_col) {
         constexpr int W = decltype(width)::value;
-        if (red_send) {
-          // entry (column group, lane) of this warp's part of the peer's receive buffer
-#pragma unroll
-          for (int j = 0; j < W / 4; ++j)
-            st_cluster_v4(red_remote + static_cast<uint32_t>(c_col / 4 + j) * 512u, v[4 * j],
-                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          return;
-        }
-        if (red_recv) {
-          // own partial + the peer's: one addition per element, the same in either CTA
-          // (IEEE addition is commutative), so the result does not depend on the rows
-#pragma unroll
-          for (int j = 0; j < W / 4; ++j) {
-            const float4 t = ld_shared_f4(red_entry + static_cast<uint32_t>(c_col / 4 + j) * 512u);
-            v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + t.x);
-            v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + t.y);
-            v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + t.z);
-            v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + t.w);
-          }
-        }
         if (store_partial) {
           // fp32 partial sum, four columns per 16-byte store
 #pragma unroll
@@ -778,6 +784,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         pack_chunk<W / 2>(v, packed, p.bf16, p.relu);
         const int row = m0 + q * 32 + lane;      // this lane's row of the kernel's tile
         const int col0 = n0 + c_col;
+        if (p.c_trans && p.c_vec) {
+          // The kernel computed C^T: its row `row` is column `row` of C, and each of its
+          // columns is a row of C.  Each 8 x 8 block (8 lanes x 8 columns) is transposed
+          // across its lanes by shuffles, so that lane 8g + r then holds 8 consecutive
+          // columns of C row col0 + 8b + r and writes them as one 16-byte store (one
+          // 2-byte store per element was measured ~100 cycles per warp instruction).
+          const int r = lane & 7;
+          const int cn = m0 + q * 32 + 8 * (lane >> 3);       // first C column of the lane
+#pragma unroll
+          for (int b = 0; b < W / 8; ++b) {
+            uint32_t w0 = packed[4 * b], w1 = packed[4 * b + 1];
+            uint32_t w2 = packed[4 * b + 2], w3 = packed[4 * b + 3];
+            transpose8x8_u16(w0, w1, w2, w3, r);
+            const int cm = col0 + 8 * b + r;                    // C row
+            if (cm < p.N && cn < p.M) {
+              uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(cm) * p.ldc + cn;
+              if (cn + 8 <= p.M) {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w0, w1, w2, w3);
+              } else {
+                const uint32_t wv[4] = {w0, w1, w2, w3};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (cn + e < p.M) dst[e] = static_cast<uint16_t>(wv[e >> 1] >> (16 * (e & 1)));
+              }
+            }
+          }
+          return;
+        }
         if (p.c_trans) {
           // The kernel computed C^T: its row `row` is column `row` of C, and each of
           // its columns is a row of C that the warp's 32 lanes write as 64 contiguous
@@ -838,8 +872,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      if constexpr (kColumnSplit) {
+        if (ksplit) {
+          // Cluster split-K: CTA r finishes columns [r H, (r + 1) H) of every row of the
+          // tile (H = BN / 2).  Each warp first writes its rows' partial sums of the
+          // peer's columns into the peer's receive buffer (once the peer has read the
+          // previous tile's) and announces them; then it waits for the peer's partial
+          // sums of its own columns, adds them to its own and finishes those columns.
+          // All four warps of both CTAs share the work.  Every lane waits and arrives
+          // itself where it orders its own accesses.
+          constexpr int kHW = BN / 2;
+          constexpr int kHC = kHW < kChunk ? kHW : kChunk;   // columns per step
+          constexpr int kHN = kHW / kHC;
+          const uint32_t peer = krank ^ 1u;
+          // entry (column group j of the warp's half, lane): 16 bytes, lane-major, so a
+          // warp's access covers 512 contiguous bytes
+          const uint32_t my_entry = sRed + static_cast<uint32_t>(q * (kHW / 4) * 32 + lane) * 16u;
+          const uint32_t peer_entry = mapa_shared(my_entry, peer);
+          bool split_ok = wait_bounded<true>(red_empty_bar(q), red_phase ^ 1u, abort_flag, p.timeout_ns);
+          if (__all_sync(0xFFFFFFFFu, split_ok)) {
 #pragma unroll 1
-      for (int c = 0; c < kFull; ++c) {
+            for (int h = 0; h < kHN; ++h) {
+              uint32_t v[kHC];
+              tmem_load_cols<kHC>(t_row + peer * kHW + h * kHC, v);
+              tmem_load_wait();
+#pragma unroll
+              for (int j = 0; j < kHC / 4; ++j)
+                st_cluster_v4(peer_entry + static_cast<uint32_t>(h * (kHC / 4) + j) * 512u,
+                              v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+            // release: this lane's stores into the peer come first
+            mbar_arrive_cluster(mapa_shared(red_full_bar(q), peer));
+            split_ok = wait_bounded<true>(red_full_bar(q), red_phase, abort_flag, p.timeout_ns);
+          }
+          if (!__all_sync(0xFFFFFFFFu, split_ok)) {
+            if (lane == 0 && !*abort_flag) record_timeout(p.status, abort_flag, kSiteClusterSplit);
+            break;
+          }
+#pragma unroll 1
+          for (int h = 0; h < kHN; ++h) {
+            uint32_t v[kHC];
+            tmem_load_cols<kHC>(t_row + krank * kHW + h * kHC, v);
+            tmem_load_wait();
+            if (h == kHN - 1) release_acc();
+            // own partial + the peer's: one IEEE addition per element, so the sum does
+            // not depend on which CTA finishes the column
+#pragma unroll
+            for (int j = 0; j < kHC / 4; ++j) {
+              const float4 t = ld_shared_f4(my_entry + static_cast<uint32_t>(h * (kHC / 4) + j) * 512u);
+              v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + t.x);
+              v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + t.y);
+              v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + t.z);
+              v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + t.w);
+            }
+            finish_chunk(IntConst<kHC>{}, v, static_cast<int>(krank) * kHW + h * kHC);
+          }
+          // the buffer is read (every lane, then the warp barrier): the peer may write
+          // the next tile's partial sums.  Lane 31 arrives, as for the accumulator.
+          __syncwarp();
+          if (lane == 31) mbar_arrive_cluster(mapa_shared(red_empty_bar(q), peer));
+          red_phase ^= 1u;
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < kFull && !(kColumnSplit && ksplit); ++c) {
         uint32_t v[kEC];
         if constexpr (kEC == 16) {
           tmem_load_16cols(t_row + c * kEC, v);
@@ -859,17 +955,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_load_wait();
         release_acc();
         finish_chunk(IntConst<32>{}, v, kFull * kEC);
-      }
-      if (red_send) {
-        // the partial is in the peer's buffer (release: the stores come first)
-        mbar_arrive_cluster(mapa_shared(red_full_bar(q), krank ^ 1));
-        red_phase ^= 1u;
-      } else if (red_recv) {
-        // the buffer is read (every lane has added its entries, then the warp barrier):
-        // the peer may write the next tile's partial.  Lane 31 arrives, as above.
-        __syncwarp();
-        if (lane == 31) mbar_arrive_cluster(mapa_shared(red_empty_bar(q), krank ^ 1));
-        red_phase ^= 1u;
       }
       if (store_partial) {
         // the warp's partial stores happen before lane 0's fence (warp barrier); the

@@ -275,10 +275,15 @@ void schedule(tl_plan* pl, int64_t units_avail, bool allow_split, int eb = 2) {
 // k-loop is long enough to halve, two CTAs of a cluster share each tile's k-blocks.  The
 // quickstart 1024^3 tiling (64 tiles of 128 x 128, 16 k-blocks of 64) is bound by the
 // latency of its 3-stage ring refills: split, each tile has two rings' loads in flight,
-// and each CTA finishes half the tile's rows after a 32 KB exchange of partial sums
-// with its peer through distributed shared memory.
+// and each CTA finishes half the tile's columns after a 32 KB exchange of partial sums
+// with its peer through distributed shared memory.  The halves need a power-of-two
+// tile width.
+bool pow2_width(int bn) { return (bn & (bn - 1)) == 0; }
+
 int auto_ksplit(const tl_plan& pl, int sms, int eb) {
-  if (pl.bm != 128 || pl.stream_k == 1 || 2 * pl.tiles > sms || pl.k_blocks < 4) return 1;
+  if (pl.bm != 128 || !pow2_width(pl.bn) || pl.stream_k == 1 || 2 * pl.tiles > sms ||
+      pl.k_blocks < 4)
+    return 1;
   // the receive buffer (128 x bn fp32) must fit beside the ring
   return smem_for(pl.bm, pl.bn, pl.bk, pl.stages, eb, 2, !pl.swap_ab) <= kMaxSmemPerCta ? 2 : 1;
 }
@@ -303,11 +308,12 @@ tl_status complete_plan(int64_t M, int64_t N, int64_t K, int trans_a, int trans_
   // per CTA: 128 rows of A and bn/cg columns of B per stage
   pl->ring_bytes =
       static_cast<int64_t>(pl->stages) * (128 * pl->bk + (pl->bn / cg) * pl->bk) * eb;
-  // cluster split-K: 0 automatic, 1 off, 2 on (one-CTA tiles, at least 2 k-blocks, and
-  // not with a forced stream-K split)
+  // cluster split-K: 0 automatic, 1 off, 2 on (one-CTA tiles of a power-of-two width,
+  // at least 2 k-blocks, and not with a forced stream-K split)
   if (pl->ksplit < 0 || pl->ksplit > 2) return TL_ERR_INVALID_ARG;
   if (pl->ksplit == 0) pl->ksplit = auto_ksplit(*pl, sms, eb);
-  if (pl->ksplit == 2 && (pl->bm != 128 || pl->k_blocks < 2 || pl->stream_k == 1))
+  if (pl->ksplit == 2 &&
+      (pl->bm != 128 || !pow2_width(pl->bn) || pl->k_blocks < 2 || pl->stream_k == 1))
     return TL_ERR_INVALID_ARG;
   pl->smem_bytes = smem_for(pl->bm, pl->bn, pl->bk, pl->stages, eb, pl->ksplit, !pl->swap_ab);
   if (pl->smem_bytes > kMaxSmemPerCta) return TL_ERR_INVALID_ARG;
