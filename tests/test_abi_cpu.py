@@ -355,10 +355,11 @@ def test_odd_width_tiles_need_a_k_major_b_and_fill_whole_waves():
     p = tl.tl_gemm_plan(4096, 4096, 4096, dtype=tl.TL_BF16, trans_b=1, num_sms=152)
     assert (p.bm, p.bn, p.bk) == (256, 224, 128) and p.tiles == 304 and p.grid == 152
     assert p.sk_iters == 0
+    assert p.raster_group == 16                 # one group spans all 16 tile rows
     # 8192^3 keeps the 256-column tiles (13.5 waves either way); an N-major B never takes
     # the odd widths
     p = tl.tl_gemm_plan(8192, 8192, 8192, dtype=tl.TL_BF16, trans_b=1, num_sms=152)
-    assert (p.bm, p.bn) == (256, 256)
+    assert (p.bm, p.bn) == (256, 256) and p.raster_group == 12
     p = tl.tl_gemm_plan(4096, 4096, 4096, dtype=tl.TL_BF16, trans_b=0, num_sms=152)
     assert p.bn not in (192, 224)
 

