@@ -159,7 +159,7 @@ tl_status tl_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, i
 
 /*
  * The plan tl_gemm() would run for this problem.  Host only: touches no GPU (the
- * SM count is taken as `num_sms`, or 148 when num_sms <= 0).  Returns
+ * SM count is taken as `num_sms`, or 152 (GB300) when num_sms <= 0).  Returns
  * TL_ERR_INVALID_ARG for negative sizes or bad enums.  The resource figures follow
  * the pages' shared-memory model S = stages * (BM*BK*s_A + BK*BN*s_B) + S_other
  * ("TileLang: from tile dataflow to controllable AI kernels", section "more

@@ -314,6 +314,31 @@ __device__ __forceinline__ void transpose8x8_u16(uint32_t& w0, uint32_t& w1, uin
   swap_halves(w3);
 }
 
+// One 32-row x 64-column chunk of C (a warp's rows, packed 16-bit pairs) through a
+// staging buffer in the TMA store's 128-byte swizzle and one bulk store at (x, y) of C.
+// Two buffers per warp alternate: before writing `buf`, the store issued two chunks ago
+// (which read it) must have read it.  `store` false issues an empty group (the counts
+// stay uniform across lanes and chunks).
+__device__ __forceinline__ void stage_and_store_chunk(const CUtensorMap* map, uint32_t buf,
+                                                      const uint32_t* packed, int lane, int x,
+                                                      int y, bool store) {
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  // row `lane` of the 32 x 64 staging box: 16-byte chunk j lands at chunk j ^ (row % 8)
+  const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * j]),
+                 "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]), "r"(packed[4 * j + 3])
+                 : "memory");
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0 && store) tma_store_2d(map, buf, x, y);   // clipped at M, N
+  if (lane == 0) bulk_commit_group();
+}
+
 template <bool kBf16, bool kRelu>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (kRelu) {
@@ -399,6 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the cluster split-K halves the columns: power-of-two widths only
   constexpr bool kColumnSplit = CG == 1 && (BN & (BN - 1)) == 0;
   static_assert(kTail == 0 || kTail == 32, "epilogue tail of 32 columns");
+  // A CTA pair's last whole tile (TMA stores of C) is finished by all eight warps: the
+  // four epilogue warps take its first kHelpC 64-column steps, warps 0, 1, 6 and 7 (idle
+  // by then; warp w reads the Tensor Memory lanes of quadrant w % 4) the rest.  (2048^3:
+  // 18.0 -> 17.1 us.  Compiled into the one-CTA kernels, where the planner's tilings
+  // leave it idle, the code alone cost the quickstart tiling 0.4 us per call.)
+  constexpr bool kHelpable = kPair && kEC == kChunk && kFull >= 2;
+  constexpr int kHelpC = kHelpable ? (kFull + 1) / 2 : kFull;
 
   // The next kernel in the stream may start its set-up now (it waits for this grid to
   // complete before it touches global memory, see grid_dependency_wait below).
@@ -686,6 +718,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(w.tile, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
       const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;
       const int n0 = nb * BN;
+      WorkIter peek = work;
+      WorkItem w_next;
+      const bool last_item = !peek.next(w_next);
+      const bool helped = kHelpable && last_item && !ksplit && !p.c_trans && p.tma_store &&
+                          w.k0 == 0 && w.k1 == p.k_blocks;
       // Stream-K roles: a partial item that starts mid-tile stores its sum for the
       // tile's finisher; an item that starts at k-block 0 but ends early is the
       // finisher and adds the partials of units cluster_id + 1 .. v_end - 1.
@@ -829,26 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (W == kChunk) {
           if (p.tma_store) {
-            const uint32_t buf = sC + (ew * 2 + sbuf) * 4096u;
-            if (lane == 0) bulk_wait_group_read<1>();   // the store two chunks ago has read buf
-            __syncwarp();
-            // row `lane` of the 32 x 64 staging box, 128-byte swizzle: 16-byte chunk j
-            // lands at chunk j ^ (row % 8)
-            const uint32_t row_addr = buf + lane * 128u;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t dst = row_addr + ((j ^ (lane & 7)) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                           "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
-                           "r"(packed[4 * j + 3])
-                           : "memory");
-            }
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0 && m0 + q * 32 < p.M && col0 < p.N) {
-              tma_store_2d(&tmap_c, buf, col0, m0 + q * 32);   // clipped at M, N
-            }
-            if (lane == 0) bulk_commit_group();   // (an empty group keeps the count uniform)
+            stage_and_store_chunk(&tmap_c, sC + (ew * 2 + sbuf) * 4096u, packed, lane, col0,
+                                  m0 + q * 32, m0 + q * 32 < p.M && col0 < p.N);
             sbuf ^= 1u;
             return;
           }
@@ -932,9 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // After the pair's last tile nothing more is sent, and the hand-back (whose
           // release waits for this warp's stores of C) is left out: 1 % per call on
           // the skinny products.
-          WorkIter peek = work;
-          WorkItem w_next;
-          if (peek.next(w_next)) {
+          if (!last_item) {
             __syncwarp();
             if (lane == 31) mbar_arrive_cluster(mapa_shared(red_empty_bar(q), peer));
           }
@@ -942,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int c = 0; c < kFull && !(kColumnSplit && ksplit); ++c) {
+      for (int c = 0; c < (helped ? kHelpC : kFull) && !(kColumnSplit && ksplit); ++c) {
         uint32_t v[kEC];
         if constexpr (kEC == 16) {
           tmem_load_16cols(t_row + c * kEC, v);
@@ -957,11 +974,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         finish_chunk(IntConst<kEC>{}, v, c * kEC);
       }
       if constexpr (kTail > 0) {
-        uint32_t v[32];
-        tmem_load_32cols(t_row + kFull * kEC, v);
-        tmem_load_wait();
-        release_acc();
-        finish_chunk(IntConst<32>{}, v, kFull * kEC);
+        if (!helped) {
+          uint32_t v[32];
+          tmem_load_32cols(t_row + kFull * kEC, v);
+          tmem_load_wait();
+          release_acc();
+          finish_chunk(IntConst<32>{}, v, kFull * kEC);
+        }
       }
       if (store_partial) {
         // the warp's partial stores happen before lane 0's fence (warp barrier); the
@@ -983,6 +1002,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the staging buffers must stay valid until the bulk stores have read them; the
     // global writes themselves complete before the grid is reported finished
     if (p.tma_store && lane == 0) bulk_wait_group_read<0>();
+  }
+
+  if constexpr (kHelpable) {
+    if ((warp <= 1 || warp >= 6) && !ksplit && !p.c_trans && p.tma_store) {
+      // ------------------------------------------- the last tile's other half --
+      // The same walk as every role: the CTA's last item and its accumulator.  This warp
+      // waits for the MMA thread's final commit ("done", one phase only: a parity wait
+      // on the accumulator's own barrier could match an earlier tile's phase when the
+      // warp gets here early).  Every MMA is then done, so the ring is idle and its first
+      // 32 KB hold this warp's two staging buffers.
+      WorkIter it(p, cluster_id, n_clusters, krank);
+      WorkItem wl;
+      int n_items = 0;
+      while (it.next(wl)) ++n_items;
+      if (n_items > 0 && wl.k0 == 0 && wl.k1 == p.k_blocks) {
+        const uint32_t acc = static_cast<uint32_t>(n_items - 1) & 1u;
+        bool ready = true;
+        if (lane == 0)
+          ready = wait_bounded<kPair>(done_bar, 0, abort_flag, p.timeout_ns) && !*abort_flag;
+        __syncwarp();
+        if (__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) {
+          tc_fence_after_sync();
+          int mb, nb;
+          tile_coords(wl.tile, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
+          const int q = warp & 3;
+          const int m0 = mb * kBM * CG + static_cast<int>(rank) * kBM;
+          const int n0 = nb * BN;
+          const int hw = warp <= 1 ? warp : warp - 4;        // 0..3: staging owner
+          const uint32_t t_row =
+              tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
+          uint32_t sbuf = 0;
+#pragma unroll 1
+          for (int c = kHelpC; c < kFull; ++c) {
+            uint32_t v[kChunk];
+#pragma unroll
+            for (int h = 0; h < kChunk / 32; ++h)
+              tmem_load_32cols(t_row + c * kChunk + 32 * h,
+                               *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+            tmem_load_wait();
+            if (p.scale) {
+#pragma unroll
+              for (int j = 0; j < kChunk; ++j)
+                v[j] = __float_as_uint(__uint_as_float(v[j]) * p.alpha);
+            }
+            uint32_t packed[kChunk / 2];
+            pack_chunk<kChunk / 2>(v, packed, p.bf16, p.relu);
+            const int col0 = n0 + c * kChunk;
+            stage_and_store_chunk(&tmap_c, sA + static_cast<uint32_t>(hw * 2 + sbuf) * 4096u,
+                                  packed, lane, col0, m0 + q * 32,
+                                  m0 + q * 32 < p.M && col0 < p.N);
+            sbuf ^= 1u;
+          }
+          if constexpr (kTail > 0) {
+            // the 32-column tail by plain stores, as in the epilogue warps
+            uint32_t v[32];
+            tmem_load_32cols(t_row + kFull * kChunk, v);
+            tmem_load_wait();
+            if (p.scale) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] = __float_as_uint(__uint_as_float(v[j]) * p.alpha);
+            }
+            uint32_t packed[16];
+            pack_chunk<16>(v, packed, p.bf16, p.relu);
+            const int row = m0 + q * 32 + lane;
+            const int col0 = n0 + kFull * kChunk;
+            if (row < p.M) {
+              uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
+              if (p.c_vec && col0 + 32 <= p.N) {
+                uint4* dst = reinterpret_cast<uint4*>(crow + col0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                      packed[4 * j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const int col = col0 + 2 * j;
+                  if (col < p.N) crow[col] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
+                  if (col + 1 < p.N) crow[col + 1] = static_cast<uint16_t>(packed[j] >> 16);
+                }
+              }
+            }
+          }
+          if (lane == 0) bulk_wait_group_read<0>();   // the staging is read before exit
+        } else if (lane == 0 && !*abort_flag) {
+          record_timeout(p.status, abort_flag, kSiteEpiTmemFull);
+        }
+      }
+    }
   }
 
   // ------------------------------------------------------------------ teardown --

@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxSmemPerCta = 232448;   // 227 KB opt-in per CTA on sm_100-class parts
-constexpr int kDefaultSms = 148;
+constexpr int kDefaultSms = 152;         // GB300 (two dies of 76), when no device is asked
 
 __device__ uint32_t g_status_word;           // bounded-wait outcome, see tl_device_status
 
