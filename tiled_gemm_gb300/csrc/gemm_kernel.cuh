@@ -721,8 +721,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       WorkIter peek = work;
       WorkItem w_next;
       const bool last_item = !peek.next(w_next);
-      const bool helped = kHelpable && last_item && !ksplit && !p.c_trans && p.tma_store &&
-                          w.k0 == 0 && w.k1 == p.k_blocks;
+      const bool helped = kHelpable && n_producers == kProducers && last_item && !ksplit &&
+                          !p.c_trans && p.tma_store && w.k0 == 0 && w.k1 == p.k_blocks;
       // Stream-K roles: a partial item that starts mid-tile stores its sum for the
       // tile's finisher; an item that starts at k-block 0 but ends early is the
       // finisher and adds the partials of units cluster_id + 1 .. v_end - 1.
@@ -1005,7 +1005,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if constexpr (kHelpable) {
-    if ((warp <= 1 || warp >= 6) && !ksplit && !p.c_trans && p.tma_store) {
+    // (only when warps 6 and 7 are producers too: then every helping warp reaches this
+    // point within a few stages of the last MMA, and the wait below stays short)
+    if ((warp <= 1 || warp >= 6) && n_producers == kProducers && !ksplit && !p.c_trans &&
+        p.tma_store) {
       // ------------------------------------------- the last tile's other half --
       // The same walk as every role: the CTA's last item and its accumulator.  This warp
       // waits for the MMA thread's final commit ("done", one phase only: a parity wait
