@@ -29,6 +29,8 @@
 //                        (max(x, 0), "TileLang core primitives" page, section 3.8),
 //                        cast with round-to-nearest-even, swizzled shared staging,
 //                        then TMA bulk stores that skip rows/columns outside C.
+//                        (C^T plans: 16-byte stores after a transpose across lanes.
+//                        CTA pairs: warps 0, 1, 6, 7 also finish half of the last tile.)
 //
 // The accumulator is double-buffered in Tensor Memory (2 x BN columns), so the
 // epilogue of one tile overlaps the main loop of the next.  CTAs are persistent:
@@ -150,9 +152,9 @@ __host__ __device__ constexpr uint32_t barrier_bytes(int stages) {
   return static_cast<uint32_t>(8 * (2 * stages + 5 + 8) + 8 + 32 + 8);
 }
 
-// Cluster split-K receive buffer: the peer's partial sums of the 64 rows this CTA
-// finishes, per finishing epilogue warp BN columns x 32 lanes, four columns per 16-byte
-// entry, lane-major.
+// Cluster split-K receive buffer: the peer's partial sums of the BN / 2 columns this CTA
+// finishes, per epilogue warp BN / 2 columns x 32 lanes, four columns per 16-byte entry,
+// lane-major.
 template <int BN>
 __host__ __device__ constexpr uint32_t red_bytes(int ksplit) {
   return ksplit > 1 ? static_cast<uint32_t>(64 * BN * 4) : 0u;
