@@ -171,9 +171,15 @@ tl_status tl_gemm_plan(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int tran
 /*
  * Fill the derived fields of `plan` (tiles, k-blocks, ring/smem bytes, TMEM
  * columns, tx bytes) from its bm/bn/bk/stages and the problem size.  Host only.
- * Returns TL_ERR_INVALID_ARG when the tiling is not one the kernel supports
- * (bm = 128 with bn in {64,128,256}, or bm = 256 with bn in {128,256}; bk = 64
- * or 128; stages 2..8; shared memory within the per-CTA limit).
+ * Returns TL_ERR_INVALID_ARG when the tiling is not one the kernel supports:
+ *   16-bit operands: bm = 128 with bn in {64,128,256}, or bm = 256 with bn in
+ *     {128,256}, bk = 64 or 128; bm = 128 with bn in {16,32} (skinny plans) or
+ *     bm in {128,256} with bn in {192,224}, bk = 128 only, and for those a
+ *     K-major B (trans_b = 1; with swap_ab, an A that is not transposed);
+ *   8-bit operands (tl_gemm_fp8): bm = 128 with bn in {64,128,256}, or bm = 256
+ *     with bn in {128,256}, bk = 128 or 256, no swap_ab;
+ *   stages 2..8 and shared memory within the per-CTA limit;
+ *   ksplit = 2 only with bm = 128 and a power-of-two bn.
  */
 tl_status tl_plan_complete(int64_t M, int64_t N, int64_t K, tl_dtype dtype, int trans_a,
                            int trans_b, int num_sms, tl_plan* plan);
